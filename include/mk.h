@@ -1,0 +1,178 @@
+/*
+ * mk.h -- C ABI of the single-launch MoE decode megakernel for GB300 (sm_103a).
+ *
+ * One call of mk_decode_step runs one decode step (T = 1) or one speculative
+ * verify step (T > 1) of a Mixture-of-Experts (or dense) transformer: every
+ * layer -- RMSNorm, GQA or MLA attention over a paged bf16 KV cache, output
+ * projection, softmax/top-k router, shared and routed SwiGLU experts,
+ * residual updates -- then the final norm and the LM head, in ONE persistent
+ * kernel launch. While one stage computes, a producer warp in every CTA keeps
+ * streaming the weight tiles of the following stages (and layers) into a
+ * shared-memory ring with TMA bulk copies, so HBM stays busy across layer
+ * boundaries.
+ *
+ * Sources (the pages describe the method, not an interface; the interface is
+ * this library's own):
+ *  - all MoE layers of the model in a single kernel, no per-layer launches:
+ *    "TPU Megakernel Achieves 709 tokens/s on Kimi K3" (kongchang.com),
+ *    section "The Key Innovation: 92 MoE Layers in a Single Pallas Kernel";
+ *  - weights of the next layer move while the current layer computes:
+ *    same page, section "Cross-Layer Weight Prefetching"; the myzaker article,
+ *    section on fusing hundreds of small kernels ("attention weights of layer
+ *    N+1 already move while layer N runs its MoE");
+ *  - decode is bound by moving weights from HBM, every token re-reads them:
+ *    myzaker article, same section; tanhow.com translation of the Inferact
+ *    blog, paragraph on the memory-bandwidth limit;
+ *  - router picks a few experts per token, per layer: kongchang.com, MoE
+ *    explainer after "Cross-Layer Weight Prefetching";
+ *  - MLA KV cache: tanhow.com translation, paragraph on VMEM lifetimes;
+ *  - speculative verification of draft tokens in one batch: myzaker article,
+ *    DSpark paragraphs; paged KV (PagedAttention): myzaker article, section
+ *    on the vLLM founders.
+ *
+ * Conventions for every entry point:
+ *  - returns MK_OK (0) or a negative mk_status; the thread-local message of
+ *    the last failure is available from mk_last_error();
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream);
+ *  - pointers documented as "device" must be device (or managed) memory of
+ *    the current device; "host or device" accepts either (copied with
+ *    cudaMemcpyDefault);
+ *  - the library never exits the process and never traps on the device.
+ */
+#ifndef MK_H
+#define MK_H
+#include <stdint.h>
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MK_ABI_VERSION 1
+
+typedef enum mk_status {
+    MK_OK = 0,
+    MK_ERR_INVALID_ARG = -1, /* bad pointer, size, shape, position or token id */
+    MK_ERR_OOM = -2,         /* device allocation failed */
+    MK_ERR_CUDA = -3,        /* a CUDA runtime call failed */
+    MK_ERR_UNSUPPORTED = -4, /* configuration outside what the kernel implements */
+    MK_ERR_TIMEOUT = -5,     /* a device-side wait exceeded its time limit; the step was abandoned */
+    MK_ERR_STATE = -6        /* call out of order (e.g. kv from another model) */
+} mk_status;
+
+enum { MK_ATTN_GQA = 0, MK_ATTN_MLA = 1 };
+
+/* Model shape. GQA uses n_q_heads/n_kv_heads/head_dim; MLA uses n_q_heads
+ * plus the *_rank/*_dim fields. n_routed_experts = 0 gives a dense model whose
+ * MLP is the shared expert (n_shared_experts = 1, shared_ffn_dim wide). */
+typedef struct mk_config {
+    int32_t n_layers, d_model, vocab, attn_kind;
+    int32_t n_q_heads, n_kv_heads, head_dim;
+    int32_t q_lora_rank, kv_lora_rank, qk_nope_dim, qk_rope_dim, v_head_dim;
+    int32_t n_routed_experts, top_k, n_shared_experts, ffn_dim, shared_ffn_dim;
+    int32_t max_batch, max_tokens_per_seq, max_ctx, kv_page_size;
+    float rms_eps, rope_theta;
+} mk_config;
+
+/* Weight kinds. Canonical layouts are row-major [rows, cols] bf16:
+ *  EMBED, LM_HEAD [vocab, d]; *_NORM gains [n];
+ *  GQA: WQ [Hq*hd, d], WK/WV [Hkv*hd, d], WO [d, Hq*hd];
+ *  MLA: WDQ [q_lora, d], Q_NORM [q_lora], WUQ [H*(nope+rope), q_lora] (per
+ *       head: nope rows then rope rows), WDKV [kv_lora+rope, d] (latent rows
+ *       then k_rope rows), KV_NORM [kv_lora], WUKV [H*(nope+v), kv_lora]
+ *       (per head: W_uk rows then W_uv rows), WO [d, H*v];
+ *  MoE: ROUTER [E, d]; per expert GATE/UP [ffn, d], DOWN [d, ffn];
+ *  shared expert: SH_GATE/SH_UP [sffn, d], SH_DOWN [d, sffn]. */
+enum mk_weight_kind {
+    MK_W_EMBED = 1, MK_W_LM_HEAD = 2, MK_W_FINAL_NORM = 3, MK_W_ATTN_NORM = 4, MK_W_FFN_NORM = 5,
+    MK_W_WQ = 6, MK_W_WK = 7, MK_W_WV = 8, MK_W_WO = 9,
+    MK_W_WDQ = 10, MK_W_Q_NORM = 11, MK_W_WUQ = 12, MK_W_WDKV = 13, MK_W_KV_NORM = 14, MK_W_WUKV = 15,
+    MK_W_ROUTER = 16, MK_W_GATE = 17, MK_W_UP = 18, MK_W_DOWN = 19,
+    MK_W_SH_GATE = 20, MK_W_SH_UP = 21, MK_W_SH_DOWN = 22
+};
+
+/* One entry of the weight table: layer = -1 for EMBED/LM_HEAD/FINAL_NORM,
+ * expert = routed expert index (0 otherwise); data = bf16 bits in the
+ * canonical layout, host or device memory, only read during the call. */
+typedef struct mk_weight {
+    int32_t kind, layer, expert, reserved;
+    const void* data;
+} mk_weight;
+
+typedef struct mk_model mk_model;
+typedef struct mk_kv mk_kv;
+
+/* Static facts about a loaded model (sizes in bytes). */
+typedef struct mk_info {
+    int64_t weight_bytes;      /* packed weights resident in HBM */
+    int64_t scratch_bytes;     /* activations, partials, counters */
+    int32_t grid_ctas;         /* persistent CTAs (one per SM) */
+    int32_t threads_per_cta;
+    int32_t smem_bytes;        /* dynamic shared memory per CTA */
+    int32_t ring_slots, slot_bytes;
+    int32_t sm_count;
+} mk_info;
+
+/* Validate `cfg`, allocate device memory for all weights and per-step
+ * scratch, and copy every tensor of `table` (n entries; each required tensor
+ * exactly once) into the library's packed layout. The caller keeps ownership
+ * of its buffers. Errors: INVALID_ARG (bad/missing/duplicate tensor),
+ * UNSUPPORTED (shape the kernel does not implement), OOM, CUDA.
+ * Synchronises `stream` before returning. */
+int mk_load_weights(const mk_config* cfg, const mk_weight* table, int32_t n, void* stream, mk_model** out);
+
+/* Paged KV cache for `batch` sequences of up to `max_ctx` positions each
+ * (must be <= cfg.max_ctx, batch <= cfg.max_batch). Pages hold
+ * cfg.kv_page_size positions. The default block table interleaves the
+ * sequences' pages (page j of sequence b is physical page j*batch + b).
+ * Contents start as zeros. */
+int mk_alloc_kv(const mk_model* m, int32_t batch, int32_t max_ctx, mk_kv** out);
+
+/* Replace the block table: host array [batch][pages_per_seq] of distinct
+ * physical page ids in [0, batch*pages_per_seq). Synchronous. */
+int mk_kv_set_block_table(mk_kv* kv, const int32_t* table);
+int32_t mk_kv_pages_per_seq(const mk_kv* kv);
+
+/* Copy n positions [pos0, pos0+n) of sequence `seq`, layer `layer` between
+ * the cache and `rows` (host or device; bf16 [n][row], row = [K heads | V
+ * heads] (2*Hkv*hd) for GQA, [latent | k_rope] (kv_lora+rope) for MLA). The
+ * row layout is the logical one; pages and the block table are hidden.
+ * Asynchronous on `stream` when `rows` is device memory. */
+int mk_kv_write(mk_kv* kv, int32_t layer, int32_t seq, int32_t pos0, int32_t n, const void* rows, void* stream);
+int mk_kv_read(const mk_kv* kv, int32_t layer, int32_t seq, int32_t pos0, int32_t n, void* rows, void* stream);
+
+/* One decode (T = 1) or verify (T > 1) step of `batch` sequences.
+ *  tokens    device int32 [batch*T], token t of sequence b at b*T + t;
+ *  positions device int32 [batch], position of each sequence's first token
+ *            in this step; positions [0, positions[b]) of the cache must
+ *            hold that sequence's context; the step writes K/V (or latents)
+ *            for positions [positions[b], positions[b]+T);
+ *  logits    device float [batch*T, vocab] (written);
+ *  accept    device int32 [batch] or NULL: greedy acceptance length (1 + the
+ *            number of leading draft tokens t+1 that equal the argmax of the
+ *            logits at t; argmax ties go to the lower id). Needs T > 1.
+ * Asynchronous: argument errors are returned immediately; errors found on
+ * the device (token or position out of range, timeouts) are reported by the
+ * next mk_step_status. */
+int mk_decode_step(mk_model* m, mk_kv* kv, const int32_t* tokens, const int32_t* positions, int32_t batch,
+                   int32_t T, float* logits, int32_t* accept, void* stream);
+
+/* Synchronise `stream` and return the device status of the last step
+ * (MK_OK, MK_ERR_TIMEOUT, MK_ERR_INVALID_ARG). A failed status resets the
+ * model's device state so the next step can run. */
+int mk_step_status(mk_model* m, void* stream);
+
+/* Routing of the last step: host arrays idx [L][batch*T][k] (int32) and
+ * w [L][batch*T][k] (float). Synchronises `stream`. MoE models only. */
+int mk_debug_routing(mk_model* m, int32_t* idx_out, float* w_out, void* stream);
+
+int mk_model_info(const mk_model* m, mk_info* out);
+
+/* Free a model or a KV cache (NULL is a no-op). A KV cache must be freed
+ * before its model. */
+void mk_free(void* handle);
+
+const char* mk_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

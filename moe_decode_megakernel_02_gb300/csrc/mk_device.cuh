@@ -1,0 +1,378 @@
+// mk_device.cuh -- the persistent decode megakernel (sm_103a).
+//
+// One cooperative launch, one CTA per SM. Each CTA = 8 consumer warps + 1
+// producer warp. The whole step (all layers, the LM head, verify acceptance)
+// is a fixed program of stages; the work items of every stage are spread
+// over the CTAs. Every CTA's producer warp walks the same program as its
+// consumers and streams each weight tile / KV chunk its consumers will need
+// into a 4-slot shared-memory ring with TMA bulk copies
+// (cp.async.bulk + mbarrier complete_tx). Weight tiles depend on no
+// activation, so the producer runs ahead across stage and layer boundaries
+// while the consumers wait for their inputs: this is the GPU form of the
+// cross-layer weight prefetch ("TPU Megakernel Achieves 709 tokens/s on Kimi
+// K3", section "Cross-Layer Weight Prefetching"; myzaker article: layer N+1's
+// attention weights move while layer N computes its MoE). The only tiles that
+// must wait are the routed experts', which are known once the router is done.
+//
+// Dependencies between stages are release/acquire counters in global memory
+// (one per layer and stage, double-buffered by step parity); every wait gives
+// up after a time limit, records MK_ERR_TIMEOUT and makes every CTA leave.
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+
+namespace mk {
+
+// ---------------------------------------------------------------- shape ----
+constexpr int NCW = 8;                    // consumer warps
+constexpr int NCT = NCW * 32;             // consumer threads
+constexpr int NTHREADS = NCT + 32;        // + one producer warp
+constexpr int NSLOT = 4;                  // ring slots
+constexpr int SLOT_BYTES = 37888;         // one MLA chunk (32 padded latent rows + rope rows)
+constexpr int TILE_MAX = 32768;           // GEMV weight tile
+constexpr int STAGE_BYTES = 65536;        // activation / query staging
+constexpr int STAGE_FLOATS = STAGE_BYTES / 4;
+constexpr int RED_FLOATS = 1024;
+constexpr int MT = 4;                     // tokens per register group in the GEMV
+constexpr int MAX_M = 64;                 // batch * tokens per step
+constexpr int MAX_E = 256;
+constexpr int MAX_K = 8;
+constexpr int GQA_CH = 64;                // positions per GQA chunk (= one page)
+constexpr int MLA_CH = 32;                // positions per MLA chunk (half a page)
+constexpr int PAGE = 64;
+// MLA: 16 heads, latent 512, rope 64 (checked on the host)
+constexpr int MLA_H = 16, MLA_KL = 512, MLA_RD = 64, MLA_D = MLA_KL + MLA_RD;
+constexpr int MLA_QS = 584;               // padded smem row strides (bf16 elements)
+constexpr int MLA_CS = 520;
+constexpr int MLA_RS = 72;
+constexpr int MLA_CHUNK_BYTES = MLA_CH * MLA_CS * 2 + MLA_CH * MLA_RS * 2;
+static_assert(MLA_CHUNK_BYTES <= SLOT_BYTES, "MLA chunk must fit a slot");
+
+enum InKind { IN_COPY = 0, IN_RMS = 1, IN_SWIGLU = 2 };
+enum OutKind { OUT_STORE = 0, OUT_RESID = 1, OUT_SCALED = 2 };
+enum StatusCode { ST_OK = 0, ST_INVALID = 1, ST_TIMEOUT = 5 };
+
+// A matrix-vector stage: out[m][row] (+)= W[row, :] . f(in)[m, :]
+// W is packed [n_kc][N][Kc] (K-panels; n_kc == 1 is plain row-major).
+struct Gemv {
+    const uint16_t* W;
+    long long w_estride;          // elements between routed experts
+    int N, K, Kc, R, n_kc, n_rb;  // rows, reduction length, panel width, rows per tile
+    int in_kind;
+    const float* src;             // input rows [M][src_stride]
+    int src_stride;
+    long long src_sstride;        // per routed slot (gate/up output of the slot)
+    const uint16_t* gain;         // IN_RMS gain [K]
+    int grp_rows, grp_stride;     // grouped input: rows [i*grp_rows, ...) read src + i*grp_stride
+    int sw_off;                   // IN_SWIGLU: up values at +sw_off
+    int out_kind;
+    float* dst;
+    int dst_stride;
+    long long dst_sstride;        // per routed slot
+    float* dst2;                  // OUT_RESID: next layer's residual
+};
+
+enum { G_A = 0, G_QB, G_QLAT, G_UV, G_O, G_ROUTER, G_SHGU, G_SHDOWN, G_GU, G_DOWN, NG };
+
+struct Layer {
+    Gemv g[NG];
+    const uint16_t* kv_norm;  // MLA latent RMSNorm gain
+    const float* a;           // GQA: q|k|v   MLA: c_q | latent | k_rope   [M][a_stride]
+    const float* q;           // MLA: q_b output [M][H*(nope+rope)]
+    const float* qlat;        // MLA: absorbed queries [M][H*kl]
+    float* olat;              // MLA: combined latent attention output [M][H*kl]
+    float* o;                 // attention output [M][Hq*hd | H*vd]
+    const float* rlog;        // router logits [M][E]
+    float* x;                 // residual entering the layer [M][d]
+    float* xn;                // residual leaving the layer [M][d]
+    int a_stride;
+};
+
+// counters per layer (and one extra "layer" L for the head)
+enum { C_A = 0, C_QB, C_APP, C_QLAT, C_ATTN, C_COMB, C_UV, C_O, C_ROUTER, C_SHGU, C_CARRY, C_SHDOWN, C_DOWN,
+       C_INIT, C_LM, C_AMAX, C_GU0, NCTR = C_GU0 + MAX_E };
+
+struct Params {
+    int L, d, V, attn, Hq, Hkv, hd, ql, kl, nope, rd, vd, E, topk, has_sh, ffn, sffn;
+    float eps, attn_scale;
+    int G;                          // CTAs in the grid
+    const Layer* layers;
+    Gemv lm;
+    const uint16_t* embed;
+    const float2* rope;             // [npos][rope_half] (cos, sin)
+    int rope_half, rope_npos;
+    uint16_t* kv_pool;              // [L][pages][page_elems]
+    long long kv_layer_elems;
+    long long page_elems;           // elements of one page (per layer pool)
+    int pps;                        // pages per sequence
+    const int* btab;                // [kv_batch][pps]
+    int kv_cap, kv_batch;           // positions per sequence, sequences in the cache
+    const uint16_t* zeros;          // >= 2 KB of zero bytes (fills unused chunk rows)
+    uint16_t* newlat;               // MLA new latents [MAX_M][576] bf16
+    float* part;                    // attention partials
+    int s_max;
+    const int* tokens;
+    const int* pos;
+    int B, T, M;
+    float* logits;
+    int* accept;
+    int* amax;
+    float* zptr[6];
+    long long zn[6];                // floats to zero at the start of the step
+    int nz, carry;                  // carry: residual copied by items (split-K output projection)
+    unsigned* ctr;                  // [2][L+1][NCTR]
+    int parity;
+    unsigned* status;               // [0] code [1] abort [2] where [3] cta
+    long long timeout_ns;
+    int* dbg_idx;
+    float* dbg_w;
+};
+
+// ----------------------------------------------------------- smem layout ----
+struct Misc {
+    unsigned long long full[NSLOT];
+    unsigned long long empty[NSLOT];
+    int abort;
+    int n_slots, p_nslots;
+    float rms[MAX_M];
+    uint8_t slot_e[MAX_E];          // consumer: routed slot -> expert
+    uint8_t p_slot_e[MAX_E];        // producer copy
+    uint8_t used[MAX_E];
+    uint8_t p_used[MAX_E];
+    uint8_t ridx[MAX_M][MAX_K];
+    float rw[MAX_M][MAX_K];
+    float cw[256];                  // combine weights
+};
+constexpr int SMEM_RING = 0;
+constexpr int SMEM_STAGE = NSLOT * SLOT_BYTES;
+constexpr int SMEM_RED = SMEM_STAGE + STAGE_BYTES;
+constexpr int SMEM_MISC = SMEM_RED + RED_FLOATS * 4;
+constexpr int SMEM_TOTAL = SMEM_MISC + (int)sizeof(Misc);
+
+// ------------------------------------------------------------------ PTX ----
+__device__ __forceinline__ uint32_t su32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+__device__ __forceinline__ long long gtimer() {
+    long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+__device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ unsigned ld_relaxed(const unsigned* p) {
+    unsigned v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void red_release(unsigned* p, unsigned v) {
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ void mbar_init(unsigned long long* b, unsigned n) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(su32(b)), "r"(n));
+}
+__device__ __forceinline__ void mbar_expect_tx(unsigned long long* b, unsigned bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(su32(b)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(unsigned long long* b) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(su32(b)) : "memory");
+}
+__device__ __forceinline__ bool mbar_test(unsigned long long* b, unsigned parity) {
+    unsigned ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(su32(b)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, unsigned bytes, unsigned long long* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(su32(dst)),
+        "l"(src), "r"(bytes), "r"(su32(bar))
+        : "memory");
+}
+__device__ __forceinline__ void cbar() { asm volatile("bar.sync 1, %0;" ::"n"(NCT) : "memory"); }
+
+__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};\n"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], const void* p) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(su32(p)));
+}
+
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+__device__ __forceinline__ float bf2f(uint16_t h) { return __uint_as_float((uint32_t)h << 16); }
+__device__ __forceinline__ uint16_t f2bf(float f) { return __bfloat16_as_ushort(__float2bfloat16_rn(f)); }
+__device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
+
+// ------------------------------------------------------------- status ----
+__device__ __noinline__ void raise_status(const Params& p, unsigned code, unsigned where) {
+    if (atomicCAS(&p.status[0], 0u, code) == 0u) {
+        p.status[2] = where;
+        p.status[3] = blockIdx.x;
+    }
+    atomicExch(&p.status[1], 1u);
+    __threadfence();
+}
+
+// one thread: wait until *c >= target (acquire); false on abort / timeout
+__device__ __noinline__ bool wait_ge(const Params& p, const unsigned* c, unsigned target, unsigned where) {
+    if (ld_acquire(c) >= target) return true;
+    const long long t0 = gtimer();
+    for (unsigned it = 0;; ++it) {
+        if (ld_acquire(c) >= target) return true;
+        if ((it & 31) == 31) {
+            if (ld_relaxed(&p.status[1])) return false;
+            if (gtimer() - t0 > p.timeout_ns) {
+                raise_status(p, ST_TIMEOUT, where);
+                return false;
+            }
+        }
+    }
+}
+
+// a lane: wait for mbarrier phase `parity`; false on abort / timeout
+__device__ __noinline__ bool mbar_wait(const Params& p, unsigned long long* b, unsigned parity, unsigned where) {
+    if (mbar_test(b, parity)) return true;
+    const long long t0 = gtimer();
+    for (unsigned it = 0;; ++it) {
+        if (mbar_test(b, parity)) return true;
+        if ((it & 15) == 15) {
+            if (ld_relaxed(&p.status[1])) return false;
+            if (gtimer() - t0 > p.timeout_ns) {
+                raise_status(p, ST_TIMEOUT, where);
+                return false;
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ unsigned* ctr_of(const Params& p, int layer, int which) {
+    return p.ctr + ((size_t)p.parity * (p.L + 1) + layer) * NCTR + which;
+}
+
+// ------------------------------------------------------------ schedule ----
+// items [lo, hi) of a stage with n items for this CTA; `off` rotates which
+// CTAs take the extra items from stage to stage.
+__device__ __forceinline__ void my_range(const Params& p, int n, int off, int& lo, int& hi) {
+    int v = (int)blockIdx.x + off;
+    if (v >= p.G) v -= p.G;
+    lo = (int)((long long)v * n / p.G);
+    hi = (int)((long long)(v + 1) * n / p.G);
+}
+
+__device__ __forceinline__ int gemv_items(const Gemv& g) { return g.n_rb * g.n_kc; }
+
+// attention splits: units = prefix chunks + 1 tail unit (the new positions)
+__device__ __forceinline__ int gqa_target(const Params& p) {
+    int t = p.G / (p.B * p.Hkv);
+    return t < 1 ? 1 : t;
+}
+__device__ __forceinline__ int mla_target(const Params& p) {
+    int t = p.G / (p.B * p.T);
+    return t < 1 ? 1 : t;
+}
+__device__ __forceinline__ int nch_of(const Params& p, int b, int ch) { return (p.pos[b] + ch - 1) / ch; }
+
+__device__ int attn_items(const Params& p) {
+    int n = 0;
+    if (p.attn == 0) {
+        const int tg = gqa_target(p);
+        for (int b = 0; b < p.B; ++b) {
+            int u = nch_of(p, b, GQA_CH) + 1;
+            n += p.Hkv * (u < tg ? u : tg);
+        }
+    } else {
+        const int tg = mla_target(p);
+        for (int b = 0; b < p.B; ++b) {
+            int u = nch_of(p, b, MLA_CH) + 1;
+            n += p.T * (u < tg ? u : tg);
+        }
+    }
+    return n;
+}
+
+struct AttnItem {
+    int b, g, s, S, u_lo, u_hi, nch;
+};
+// decode item index -> (sequence, head group or token, split, unit range)
+__device__ AttnItem attn_item(const Params& p, int i) {
+    AttnItem it;
+    const bool gqa = p.attn == 0;
+    const int tg = gqa ? gqa_target(p) : mla_target(p);
+    const int per = gqa ? p.Hkv : p.T;
+    const int ch = gqa ? GQA_CH : MLA_CH;
+    for (int b = 0; b < p.B; ++b) {
+        int nch = nch_of(p, b, ch);
+        int u = nch + 1;
+        int S = u < tg ? u : tg;
+        if (i < per * S) {
+            it.b = b;
+            it.g = i / S;
+            it.s = i % S;
+            it.S = S;
+            it.nch = nch;
+            it.u_lo = (int)((long long)it.s * u / S);
+            it.u_hi = (int)((long long)(it.s + 1) * u / S);
+            return it;
+        }
+        i -= per * S;
+    }
+    it.b = it.g = it.s = it.S = it.u_lo = it.u_hi = it.nch = 0;
+    return it;
+}
+
+__device__ __forceinline__ const uint16_t* page_ptr(const Params& p, const uint16_t* pool, int b, int page_idx) {
+    return pool + (size_t)p.btab[b * p.pps + page_idx] * p.page_elems;
+}
+
+// --------------------------------------------------------- producer ring ----
+struct PRing {
+    unsigned slot, phase;
+};
+
+// lane 0 acquires the next slot (waits for the consumers to free it) and
+// announces `bytes`; returns the slot pointer (lane 0 only), or nullptr on abort
+__device__ __forceinline__ uint8_t* prod_begin(const Params& p, uint8_t* smem, Misc& ms, PRing& r, unsigned bytes) {
+    if (!mbar_wait(p, &ms.empty[r.slot], r.phase ^ 1u, 0x100u)) return nullptr;
+    mbar_expect_tx(&ms.full[r.slot], bytes);
+    return smem + SMEM_RING + r.slot * SLOT_BYTES;
+}
+__device__ __forceinline__ void prod_next(PRing& r) {
+    if (++r.slot == NSLOT) {
+        r.slot = 0;
+        r.phase ^= 1u;
+    }
+}
+
+// consumer ring state (identical in every consumer thread)
+struct CRing {
+    unsigned slot, phase;
+};
+__device__ __forceinline__ const uint8_t* cons_wait(const Params& p, uint8_t* smem, Misc& ms, CRing& r) {
+    if (!mbar_wait(p, &ms.full[r.slot], r.phase, 0x200u)) {
+        ms.abort = 1;
+        return nullptr;
+    }
+    return smem + SMEM_RING + r.slot * SLOT_BYTES;
+}
+__device__ __forceinline__ void cons_release(Misc& ms, CRing& r) {
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(&ms.empty[r.slot]);
+    if (++r.slot == NSLOT) {
+        r.slot = 0;
+        r.phase ^= 1u;
+    }
+}
+
+}  // namespace mk

@@ -1,0 +1,764 @@
+// mk_host.cu -- C ABI of the decode megakernel (include/mk.h): validation,
+// weight packing, scratch layout, paged KV cache and the cooperative launch.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <map>
+#include <string>
+#include <tuple>
+#include <vector>
+
+#include "../../include/mk.h"
+#include "mk_kernel.cuh"
+
+namespace {
+
+thread_local std::string g_err;
+
+int fail(int code, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_err = buf;
+    return code;
+}
+
+#define CK(call)                                                                                        \
+    do {                                                                                                \
+        cudaError_t e_ = (call);                                                                        \
+        if (e_ != cudaSuccess)                                                                          \
+            return fail(e_ == cudaErrorMemoryAllocation ? MK_ERR_OOM : MK_ERR_CUDA, "%s: %s (%s:%d)", #call, \
+                        cudaGetErrorString(e_), __FILE__, __LINE__);                                    \
+    } while (0)
+
+constexpr uint32_t MODEL_MAGIC = 0x4d4b4d44u;  // "MKMD"
+constexpr uint32_t KV_MAGIC = 0x4d4b4b56u;     // "MKKV"
+
+size_t align256(size_t n) { return (n + 255) & ~(size_t)255; }
+
+}  // namespace
+
+struct mk_model {
+    uint32_t magic;
+    mk_config cfg;
+    int dev, sms, G;
+    uint16_t* wblob = nullptr;
+    size_t wbytes = 0;
+    uint8_t* sblob = nullptr;
+    size_t sbytes = 0;
+    std::vector<mk::Layer> layers;
+    mk::Layer* d_layers = nullptr;
+    mk::Params base;  // everything except the per-step fields
+    unsigned* ctr = nullptr;
+    size_t ctr_n = 0;
+    unsigned* status = nullptr;
+    int* dbg_idx = nullptr;
+    float* dbg_w = nullptr;
+    int last_M = 0;
+    uint64_t steps = 0;
+    int live_kv = 0;
+};
+
+struct mk_kv {
+    uint32_t magic;
+    mk_model* m;
+    int batch, max_ctx, pps;
+    size_t page_elems, layer_elems;
+    uint16_t* pool = nullptr;
+    int* btab = nullptr;
+    std::vector<int> h_btab;
+};
+
+namespace {
+
+struct Dims {
+    int L, d, V, gqa, Hq, Hkv, hd, ql, kl, nope, rd, vd, E, k, sh, ffn, sffn, Mx;
+    int a_rows, o_in, qh;
+};
+
+Dims dims_of(const mk_config& c) {
+    Dims d;
+    d.L = c.n_layers; d.d = c.d_model; d.V = c.vocab; d.gqa = c.attn_kind == MK_ATTN_GQA;
+    d.Hq = c.n_q_heads; d.Hkv = c.n_kv_heads; d.hd = c.head_dim;
+    d.ql = c.q_lora_rank; d.kl = c.kv_lora_rank; d.nope = c.qk_nope_dim; d.rd = c.qk_rope_dim; d.vd = c.v_head_dim;
+    d.E = c.n_routed_experts; d.k = c.top_k; d.sh = c.n_shared_experts; d.ffn = c.ffn_dim; d.sffn = c.shared_ffn_dim;
+    d.Mx = c.max_batch * c.max_tokens_per_seq;
+    d.qh = d.nope + d.rd;
+    d.a_rows = d.gqa ? (d.Hq + 2 * d.Hkv) * d.hd : d.ql + d.kl + d.rd;
+    d.o_in = d.gqa ? d.Hq * d.hd : d.Hq * d.vd;
+    return d;
+}
+
+bool k_ok(int K) { return K == 128 || (K > 0 && K % 256 == 0 && (K <= 2048 || K % 1024 == 0 || K % 512 == 0)); }
+
+int validate(const mk_config* c) {
+    if (!c) return fail(MK_ERR_INVALID_ARG, "cfg is NULL");
+    if (c->n_layers < 1 || c->d_model < 1 || c->vocab < 1 || c->max_batch < 1 || c->max_tokens_per_seq < 1 ||
+        c->max_ctx < 1)
+        return fail(MK_ERR_INVALID_ARG, "non-positive dimension");
+    if (c->kv_page_size != mk::PAGE) return fail(MK_ERR_UNSUPPORTED, "kv_page_size must be %d", mk::PAGE);
+    if (!(c->rms_eps > 0.f) || !(c->rope_theta > 0.f)) return fail(MK_ERR_INVALID_ARG, "rms_eps/rope_theta");
+    const Dims d = dims_of(*c);
+    if (d.Mx > mk::MAX_M) return fail(MK_ERR_UNSUPPORTED, "max_batch*max_tokens_per_seq > %d", mk::MAX_M);
+    if (c->max_tokens_per_seq > 16) return fail(MK_ERR_UNSUPPORTED, "max_tokens_per_seq > 16");
+    if (!k_ok(d.d) || d.d % 8) return fail(MK_ERR_UNSUPPORTED, "d_model must be 128 or a multiple of 256");
+    if (c->attn_kind == MK_ATTN_GQA) {
+        if (d.Hq < 1 || d.Hkv < 1 || d.Hq % d.Hkv) return fail(MK_ERR_INVALID_ARG, "GQA heads");
+        if (d.hd != 64 && d.hd != 128) return fail(MK_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
+        if (d.Hq / d.Hkv * c->max_tokens_per_seq > 8)
+            return fail(MK_ERR_UNSUPPORTED, "GQA: (q heads per kv head) * tokens per step must be <= 8");
+        if (!k_ok(d.o_in)) return fail(MK_ERR_UNSUPPORTED, "n_q_heads*head_dim");
+    } else if (c->attn_kind == MK_ATTN_MLA) {
+        if (d.Hq != mk::MLA_H || d.kl != mk::MLA_KL || d.rd != mk::MLA_RD || d.nope != 128)
+            return fail(MK_ERR_UNSUPPORTED, "MLA kernel implements 16 heads, kv_lora 512, rope 64, nope 128");
+        if (d.vd < 8 || d.vd % 8 || !k_ok(d.ql) || !k_ok(d.o_in)) return fail(MK_ERR_UNSUPPORTED, "MLA dims");
+    } else {
+        return fail(MK_ERR_INVALID_ARG, "attn_kind");
+    }
+    if (d.E < 0 || d.E > mk::MAX_E) return fail(MK_ERR_UNSUPPORTED, "n_routed_experts > %d", mk::MAX_E);
+    if (d.E > 0) {
+        if (d.k < 1 || d.k > mk::MAX_K || d.k > d.E) return fail(MK_ERR_UNSUPPORTED, "top_k");
+        if (d.ffn < 8 || d.ffn % 8 || !k_ok(d.ffn) || d.E % 8) return fail(MK_ERR_UNSUPPORTED, "expert ffn / count");
+    }
+    if (d.sh < 0 || d.sh > 1) return fail(MK_ERR_UNSUPPORTED, "n_shared_experts must be 0 or 1");
+    if (d.sh && (d.sffn % 8 || !k_ok(d.sffn))) return fail(MK_ERR_UNSUPPORTED, "shared_ffn_dim");
+    if (d.E == 0 && !d.sh) return fail(MK_ERR_UNSUPPORTED, "model needs routed or shared experts");
+    if (d.V % 8) return fail(MK_ERR_UNSUPPORTED, "vocab must be a multiple of 8");
+    return MK_OK;
+}
+
+void make_gemv(mk::Gemv& g, const uint16_t* W, int N, int K, int in_kind, const float* src, int src_stride,
+               const uint16_t* gain, int out_kind, float* dst, int dst_stride, float* dst2 = nullptr) {
+    std::memset(&g, 0, sizeof g);
+    int Kc = K;
+    if (K > 2048) Kc = K % 1024 == 0 ? 1024 : (K % 512 == 0 ? 512 : 256);
+    int R = (mk::TILE_MAX / (2 * Kc)) / 8 * 8;
+    if (R > N) R = N;
+    g.W = W;
+    g.N = N;
+    g.K = K;
+    g.Kc = Kc;
+    g.R = R;
+    g.n_kc = K / Kc;
+    g.n_rb = (N + R - 1) / R;
+    g.in_kind = in_kind;
+    g.src = src;
+    g.src_stride = src_stride;
+    g.gain = gain;
+    g.out_kind = out_kind;
+    g.dst = dst;
+    g.dst_stride = dst_stride;
+    g.dst2 = dst2;
+}
+
+// canonical [rows][K] block -> rows [row0, row0+rows) of a packed [n_kc][N][Kc] matrix
+int pack_rows(uint16_t* dst, int N, int K, int Kc, int row0, const void* src, int rows, size_t src_row_pitch,
+              cudaStream_t s) {
+    const int n_kc = K / Kc;
+    for (int kc = 0; kc < n_kc; ++kc) {
+        CK(cudaMemcpy2DAsync(dst + (size_t)kc * N * Kc + (size_t)row0 * Kc, (size_t)Kc * 2,
+                             static_cast<const uint16_t*>(src) + (size_t)kc * Kc, src_row_pitch, (size_t)Kc * 2,
+                             rows, cudaMemcpyDefault, s));
+    }
+    return MK_OK;
+}
+
+__global__ void transpose_heads(const uint16_t* __restrict__ in, uint16_t* __restrict__ out, int H, int rows_in,
+                                int head_stride_rows, int cols) {
+    // in: per head h, a [rows_in][cols] block starting at row h*head_stride_rows
+    // out: per head h, [cols][rows_in]
+    const size_t n = (size_t)H * rows_in * cols;
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+        const int h = (int)(i / ((size_t)rows_in * cols));
+        const size_t r = i - (size_t)h * rows_in * cols;
+        const int c = (int)(r / rows_in), q = (int)(r - (size_t)c * rows_in);
+        out[i] = in[((size_t)h * head_stride_rows + q) * cols + c];
+    }
+}
+
+__global__ void kv_scatter(uint16_t* pool, const int* btab, int pps, size_t page_elems, int gqa, int Hkv, int hd,
+                           int kl, int rd, int seq, int pos0, int n, int row, uint16_t* rows, int to_cache) {
+    const size_t total = (size_t)n * row;
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
+        const int p = (int)(i / row), j = (int)(i - (size_t)p * row);
+        const int pos = pos0 + p;
+        uint16_t* pg = pool + (size_t)btab[seq * pps + pos / mk::PAGE] * page_elems;
+        const int pr = pos % mk::PAGE;
+        size_t off;
+        if (gqa) {
+            const int isv = j >= Hkv * hd;
+            const int jj = isv ? j - Hkv * hd : j;
+            const int g = jj / hd, e = jj - g * hd;
+            off = (size_t)g * 2 * mk::PAGE * hd + (size_t)isv * mk::PAGE * hd + (size_t)pr * hd + e;
+        } else {
+            off = j < kl ? (size_t)pr * kl + j : (size_t)mk::PAGE * kl + (size_t)pr * rd + (j - kl);
+        }
+        if (to_cache)
+            pg[off] = rows[i];
+        else
+            rows[i] = pg[off];
+    }
+}
+
+bool is_device_ptr(const void* p) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged;
+}
+
+long long wait_ns() {
+    const char* e = getenv("MK_WAIT_NS");
+    long long v = e ? atoll(e) : 0;
+    return v > 0 ? v : 2000000000LL;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* mk_last_error(void) { return g_err.c_str(); }
+
+int mk_load_weights(const mk_config* cfg, const mk_weight* table, int32_t n, void* stream, mk_model** out) {
+    if (!out) return fail(MK_ERR_INVALID_ARG, "out is NULL");
+    *out = nullptr;
+    int rc = validate(cfg);
+    if (rc) return rc;
+    if (!table || n < 1) return fail(MK_ERR_INVALID_ARG, "empty weight table");
+    cudaStream_t s = (cudaStream_t)stream;
+    const Dims D = dims_of(*cfg);
+
+    // ---- index the table ----
+    std::map<std::tuple<int, int, int>, const void*> T;
+    for (int i = 0; i < n; ++i) {
+        const mk_weight& w = table[i];
+        if (!w.data) return fail(MK_ERR_INVALID_ARG, "table[%d].data is NULL", i);
+        auto key = std::make_tuple(w.kind, w.layer, w.expert);
+        if (T.count(key)) return fail(MK_ERR_INVALID_ARG, "duplicate tensor kind %d layer %d expert %d", w.kind, w.layer, w.expert);
+        T[key] = w.data;
+    }
+    auto need = [&](int kind, int layer, int expert, const void** p) -> int {
+        auto it = T.find(std::make_tuple(kind, layer, expert));
+        if (it == T.end()) return fail(MK_ERR_INVALID_ARG, "missing tensor kind %d layer %d expert %d", kind, layer, expert);
+        *p = it->second;
+        return MK_OK;
+    };
+
+    mk_model* m = new mk_model();
+    m->magic = MODEL_MAGIC;
+    m->cfg = *cfg;
+    auto bail = [&](int code) {
+        if (m->wblob) cudaFree(m->wblob);
+        if (m->sblob) cudaFree(m->sblob);
+        if (m->d_layers) cudaFree(m->d_layers);
+        delete m;
+        return code;
+    };
+    CK(cudaGetDevice(&m->dev));
+    CK(cudaDeviceGetAttribute(&m->sms, cudaDevAttrMultiProcessorCount, m->dev));
+    CK(cudaFuncSetAttribute(mk::megakernel, cudaFuncAttributeMaxDynamicSharedMemorySize, mk::SMEM_TOTAL));
+    int per_sm = 0;
+    CK(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, mk::megakernel, mk::NTHREADS, mk::SMEM_TOTAL));
+    if (per_sm < 1) return bail(fail(MK_ERR_UNSUPPORTED, "megakernel does not fit on an SM"));
+    m->G = m->sms < 255 ? m->sms : 255;
+
+    // ---- packed weight layout ----
+    const int L = D.L, d = D.d;
+    struct Off { size_t a, qn, kvn, uq, ukT, uv, o, router, gu, down, shgu, shdown, an, fn; };
+    std::vector<Off> lo(L);
+    size_t cur = 0;
+    auto take = [&](size_t elems) { size_t o = cur; cur += align256(elems * 2) / 2; return o; };
+    const size_t off_embed = take((size_t)D.V * d), off_lm = take((size_t)D.V * d), off_fn = take(d);
+    for (int l = 0; l < L; ++l) {
+        Off& o = lo[l];
+        o.an = take(d);
+        o.fn = take(d);
+        o.a = take((size_t)D.a_rows * d);
+        if (!D.gqa) {
+            o.qn = take(D.ql);
+            o.kvn = take(D.kl);
+            o.uq = take((size_t)D.Hq * D.qh * D.ql);
+            o.ukT = take((size_t)D.Hq * D.kl * D.nope);
+            o.uv = take((size_t)D.Hq * D.vd * D.kl);
+        }
+        o.o = take((size_t)d * D.o_in);
+        if (D.E) {
+            o.router = take((size_t)D.E * d);
+            o.gu = take((size_t)D.E * 2 * D.ffn * d);
+            o.down = take((size_t)D.E * d * D.ffn);
+        }
+        if (D.sh) {
+            o.shgu = take((size_t)2 * D.sffn * d);
+            o.shdown = take((size_t)d * D.sffn);
+        }
+    }
+    m->wbytes = cur * 2;
+    {
+        cudaError_t e = cudaMalloc(&m->wblob, m->wbytes);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            return bail(fail(MK_ERR_OOM, "weights: cudaMalloc(%zu) failed", m->wbytes));
+        }
+    }
+    uint16_t* W = m->wblob;
+
+    // ---- scratch layout (floats unless noted) ----
+    const size_t Mx = D.Mx;
+    const int Q8 = 8;
+    size_t scur = 0;
+    auto stake = [&](size_t bytes) { size_t o = scur; scur += align256(bytes); return o; };
+    const size_t s_x = stake((size_t)(L + 1) * Mx * d * 4);
+    const size_t s_a = stake((size_t)L * Mx * D.a_rows * 4);
+    const size_t s_q = D.gqa ? 0 : stake((size_t)L * Mx * D.Hq * D.qh * 4);
+    const size_t s_qlat = D.gqa ? 0 : stake((size_t)L * Mx * D.Hq * D.kl * 4);
+    const size_t s_olat = D.gqa ? 0 : stake((size_t)L * Mx * D.Hq * D.kl * 4);
+    const size_t s_o = stake((size_t)L * Mx * D.o_in * 4);
+    const int nsl = D.E ? (int)std::min<size_t>((size_t)D.E, Mx * D.k) : 0;
+    const size_t s_rlog = D.E ? stake((size_t)L * Mx * D.E * 4) : 0;
+    const size_t s_gu = D.E ? stake((size_t)L * nsl * Mx * 2 * D.ffn * 4) : 0;
+    const size_t s_shgu = D.sh ? stake((size_t)L * Mx * 2 * D.sffn * 4) : 0;
+    const size_t part_floats = D.gqa ? (size_t)cfg->max_batch * D.Hkv * m->G * Q8 * (D.hd + 2)
+                                     : (size_t)Mx * m->G * mk::MLA_H * (mk::MLA_KL + 2);
+    const size_t s_part = stake(part_floats * 4);
+    const size_t s_newlat = stake(Mx * mk::MLA_D * 2);
+    const size_t s_amax = stake(Mx * 4);
+    const size_t s_zero = stake(4096);
+    const size_t ctr_n = (size_t)2 * (L + 1) * mk::NCTR;
+    const size_t s_ctr = stake(ctr_n * 4);
+    const size_t s_status = stake(64);
+    const size_t s_dbgi = D.E ? stake((size_t)L * Mx * D.k * 4) : 0;
+    const size_t s_dbgw = D.E ? stake((size_t)L * Mx * D.k * 4) : 0;
+    const int rope_dim = D.gqa ? D.hd : D.rd;
+    const int npos = cfg->max_ctx + cfg->max_tokens_per_seq;
+    const size_t s_rope = stake((size_t)npos * (rope_dim / 2) * 8);
+    m->sbytes = scur;
+    {
+        cudaError_t e = cudaMalloc(&m->sblob, m->sbytes);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            return bail(fail(MK_ERR_OOM, "scratch: cudaMalloc(%zu) failed", m->sbytes));
+        }
+    }
+    CK(cudaMemsetAsync(m->sblob, 0, m->sbytes, s));
+    uint8_t* S = m->sblob;
+    auto F = [&](size_t off) { return reinterpret_cast<float*>(S + off); };
+
+    // ---- copy / pack every tensor ----
+    const void* p;
+    int r;
+#define NEED(kind, layer, expert)                      \
+    do {                                               \
+        if ((r = need(kind, layer, expert, &p))) return bail(r); \
+    } while (0)
+#define PACK(dst, N, K, row0, src, rows)                                                              \
+    do {                                                                                              \
+        const int Kc_ = (K) > 2048 ? ((K) % 1024 == 0 ? 1024 : ((K) % 512 == 0 ? 512 : 256)) : (K); \
+        if ((r = pack_rows(dst, N, K, Kc_, row0, src, rows, (size_t)(K) * 2, s))) return bail(r);     \
+    } while (0)
+    NEED(MK_W_EMBED, -1, 0);
+    CK(cudaMemcpyAsync(W + off_embed, p, (size_t)D.V * d * 2, cudaMemcpyDefault, s));
+    NEED(MK_W_LM_HEAD, -1, 0);
+    PACK(W + off_lm, D.V, d, 0, p, D.V);
+    NEED(MK_W_FINAL_NORM, -1, 0);
+    CK(cudaMemcpyAsync(W + off_fn, p, (size_t)d * 2, cudaMemcpyDefault, s));
+    uint16_t* tmp = nullptr;  // device staging for the MLA W_uk transpose
+    if (!D.gqa) CK(cudaMalloc(&tmp, (size_t)D.Hq * (D.nope + D.vd) * D.kl * 2));
+    for (int l = 0; l < L; ++l) {
+        const Off& o = lo[l];
+        NEED(MK_W_ATTN_NORM, l, 0);
+        CK(cudaMemcpyAsync(W + o.an, p, (size_t)d * 2, cudaMemcpyDefault, s));
+        NEED(MK_W_FFN_NORM, l, 0);
+        CK(cudaMemcpyAsync(W + o.fn, p, (size_t)d * 2, cudaMemcpyDefault, s));
+        if (D.gqa) {
+            NEED(MK_W_WQ, l, 0);
+            PACK(W + o.a, D.a_rows, d, 0, p, D.Hq * D.hd);
+            NEED(MK_W_WK, l, 0);
+            PACK(W + o.a, D.a_rows, d, D.Hq * D.hd, p, D.Hkv * D.hd);
+            NEED(MK_W_WV, l, 0);
+            PACK(W + o.a, D.a_rows, d, (D.Hq + D.Hkv) * D.hd, p, D.Hkv * D.hd);
+        } else {
+            NEED(MK_W_WDQ, l, 0);
+            PACK(W + o.a, D.a_rows, d, 0, p, D.ql);
+            NEED(MK_W_WDKV, l, 0);
+            PACK(W + o.a, D.a_rows, d, D.ql, p, D.kl + D.rd);
+            NEED(MK_W_Q_NORM, l, 0);
+            CK(cudaMemcpyAsync(W + o.qn, p, (size_t)D.ql * 2, cudaMemcpyDefault, s));
+            NEED(MK_W_KV_NORM, l, 0);
+            CK(cudaMemcpyAsync(W + o.kvn, p, (size_t)D.kl * 2, cudaMemcpyDefault, s));
+            NEED(MK_W_WUQ, l, 0);
+            PACK(W + o.uq, D.Hq * D.qh, D.ql, 0, p, D.Hq * D.qh);
+            NEED(MK_W_WUKV, l, 0);
+            CK(cudaMemcpyAsync(tmp, p, (size_t)D.Hq * (D.nope + D.vd) * D.kl * 2, cudaMemcpyDefault, s));
+            transpose_heads<<<512, 256, 0, s>>>(tmp, W + o.ukT, D.Hq, D.nope, D.nope + D.vd, D.kl);
+            CK(cudaGetLastError());
+            CK(cudaMemcpy2DAsync(W + o.uv, (size_t)D.vd * D.kl * 2, tmp + (size_t)D.nope * D.kl,
+                                 (size_t)(D.nope + D.vd) * D.kl * 2, (size_t)D.vd * D.kl * 2, D.Hq,
+                                 cudaMemcpyDeviceToDevice, s));
+        }
+        NEED(MK_W_WO, l, 0);
+        PACK(W + o.o, d, D.o_in, 0, p, d);
+        if (D.E) {
+            NEED(MK_W_ROUTER, l, 0);
+            PACK(W + o.router, D.E, d, 0, p, D.E);
+            for (int e = 0; e < D.E; ++e) {
+                uint16_t* gu = W + o.gu + (size_t)e * 2 * D.ffn * d;
+                NEED(MK_W_GATE, l, e);
+                PACK(gu, 2 * D.ffn, d, 0, p, D.ffn);
+                NEED(MK_W_UP, l, e);
+                PACK(gu, 2 * D.ffn, d, D.ffn, p, D.ffn);
+                NEED(MK_W_DOWN, l, e);
+                PACK(W + o.down + (size_t)e * d * D.ffn, d, D.ffn, 0, p, d);
+            }
+        }
+        if (D.sh) {
+            NEED(MK_W_SH_GATE, l, 0);
+            PACK(W + o.shgu, 2 * D.sffn, d, 0, p, D.sffn);
+            NEED(MK_W_SH_UP, l, 0);
+            PACK(W + o.shgu, 2 * D.sffn, d, D.sffn, p, D.sffn);
+            NEED(MK_W_SH_DOWN, l, 0);
+            PACK(W + o.shdown, d, D.sffn, 0, p, d);
+        }
+    }
+#undef NEED
+#undef PACK
+
+    // ---- RoPE table (fp64 frequency, angle, cos, sin; stored fp32) ----
+    {
+        const int half = rope_dim / 2;
+        std::vector<float2> rt((size_t)npos * half);
+        for (int pos = 0; pos < npos; ++pos)
+            for (int i = 0; i < half; ++i) {
+                const double inv = std::pow((double)cfg->rope_theta, -2.0 * (double)i / (double)rope_dim);
+                const double ang = (double)pos * inv;
+                rt[(size_t)pos * half + i] = make_float2((float)std::cos(ang), (float)std::sin(ang));
+            }
+        CK(cudaMemcpyAsync(S + s_rope, rt.data(), rt.size() * sizeof(float2), cudaMemcpyHostToDevice, s));
+        CK(cudaStreamSynchronize(s));  // rt and tmp go out of scope
+    }
+    if (tmp) CK(cudaFree(tmp));
+
+    // ---- stage descriptors ----
+    m->layers.resize(L);
+    const int Mxi = (int)Mx;
+    for (int l = 0; l < L; ++l) {
+        const Off& o = lo[l];
+        mk::Layer& Ld = m->layers[l];
+        std::memset(&Ld, 0, sizeof Ld);
+        float* x = F(s_x) + (size_t)l * Mx * d;
+        float* xn = F(s_x) + (size_t)(l + 1) * Mx * d;
+        float* a = F(s_a) + (size_t)l * Mx * D.a_rows;
+        float* ob = F(s_o) + (size_t)l * Mx * D.o_in;
+        Ld.x = x;
+        Ld.xn = xn;
+        Ld.a = a;
+        Ld.a_stride = D.a_rows;
+        Ld.o = ob;
+        make_gemv(Ld.g[mk::G_A], W + o.a, D.a_rows, d, mk::IN_RMS, x, d, W + o.an, mk::OUT_STORE, a, D.a_rows);
+        if (!D.gqa) {
+            float* q = F(s_q) + (size_t)l * Mx * D.Hq * D.qh;
+            float* qlat = F(s_qlat) + (size_t)l * Mx * D.Hq * D.kl;
+            float* olat = F(s_olat) + (size_t)l * Mx * D.Hq * D.kl;
+            Ld.q = q;
+            Ld.qlat = qlat;
+            Ld.olat = olat;
+            Ld.kv_norm = W + o.kvn;
+            make_gemv(Ld.g[mk::G_QB], W + o.uq, D.Hq * D.qh, D.ql, mk::IN_RMS, a, D.a_rows, W + o.qn, mk::OUT_STORE,
+                      q, D.Hq * D.qh);
+            make_gemv(Ld.g[mk::G_QLAT], W + o.ukT, D.Hq * D.kl, D.nope, mk::IN_COPY, q, D.Hq * D.qh, nullptr,
+                      mk::OUT_STORE, qlat, D.Hq * D.kl);
+            Ld.g[mk::G_QLAT].grp_rows = D.kl;
+            Ld.g[mk::G_QLAT].grp_stride = D.qh;
+            make_gemv(Ld.g[mk::G_UV], W + o.uv, D.Hq * D.vd, D.kl, mk::IN_COPY, olat, D.Hq * D.kl, nullptr,
+                      mk::OUT_STORE, ob, D.Hq * D.vd);
+            Ld.g[mk::G_UV].grp_rows = D.vd;
+            Ld.g[mk::G_UV].grp_stride = D.kl;
+        }
+        make_gemv(Ld.g[mk::G_O], W + o.o, d, D.o_in, mk::IN_COPY, ob, D.o_in, nullptr, mk::OUT_RESID, x, d, xn);
+        if (D.E) {
+            float* rlog = F(s_rlog) + (size_t)l * Mx * D.E;
+            float* gu = F(s_gu) + (size_t)l * nsl * Mx * 2 * D.ffn;
+            Ld.rlog = rlog;
+            make_gemv(Ld.g[mk::G_ROUTER], W + o.router, D.E, d, mk::IN_RMS, x, d, W + o.fn, mk::OUT_STORE, rlog, D.E);
+            make_gemv(Ld.g[mk::G_GU], W + o.gu, 2 * D.ffn, d, mk::IN_RMS, x, d, W + o.fn, mk::OUT_STORE, gu,
+                      2 * D.ffn);
+            Ld.g[mk::G_GU].w_estride = (long long)2 * D.ffn * d;
+            Ld.g[mk::G_GU].dst_sstride = (long long)Mx * 2 * D.ffn;
+            make_gemv(Ld.g[mk::G_DOWN], W + o.down, d, D.ffn, mk::IN_SWIGLU, gu, 2 * D.ffn, nullptr, mk::OUT_SCALED,
+                      xn, d);
+            Ld.g[mk::G_DOWN].w_estride = (long long)d * D.ffn;
+            Ld.g[mk::G_DOWN].src_sstride = (long long)Mx * 2 * D.ffn;
+            Ld.g[mk::G_DOWN].sw_off = D.ffn;
+        }
+        if (D.sh) {
+            float* shgu = F(s_shgu) + (size_t)l * Mx * 2 * D.sffn;
+            make_gemv(Ld.g[mk::G_SHGU], W + o.shgu, 2 * D.sffn, d, mk::IN_RMS, x, d, W + o.fn, mk::OUT_STORE, shgu,
+                      2 * D.sffn);
+            make_gemv(Ld.g[mk::G_SHDOWN], W + o.shdown, d, D.sffn, mk::IN_SWIGLU, shgu, 2 * D.sffn, nullptr,
+                      mk::OUT_SCALED, xn, d);
+            Ld.g[mk::G_SHDOWN].sw_off = D.sffn;
+        }
+    }
+    (void)Mxi;
+    CK(cudaMalloc(&m->d_layers, sizeof(mk::Layer) * L));
+    CK(cudaMemcpyAsync(m->d_layers, m->layers.data(), sizeof(mk::Layer) * L, cudaMemcpyHostToDevice, s));
+
+    mk::Params& P = m->base;
+    std::memset(&P, 0, sizeof P);
+    P.L = L; P.d = d; P.V = D.V; P.attn = D.gqa ? 0 : 1; P.Hq = D.Hq; P.Hkv = D.Hkv; P.hd = D.hd;
+    P.ql = D.ql; P.kl = D.kl; P.nope = D.nope; P.rd = D.rd; P.vd = D.vd; P.E = D.E; P.topk = D.k;
+    P.has_sh = D.sh; P.ffn = D.ffn; P.sffn = D.sffn;
+    P.eps = cfg->rms_eps;
+    P.attn_scale = D.gqa ? (float)(1.0 / std::sqrt((double)D.hd)) : (float)(1.0 / std::sqrt((double)D.qh));
+    P.G = m->G;
+    P.layers = m->d_layers;
+    P.embed = W + off_embed;
+    make_gemv(P.lm, W + off_lm, D.V, d, mk::IN_RMS, F(s_x) + (size_t)L * Mx * d, d, W + off_fn, mk::OUT_STORE,
+              nullptr, D.V);
+    P.rope = reinterpret_cast<const float2*>(S + s_rope);
+    P.rope_half = rope_dim / 2;
+    P.rope_npos = npos;
+    P.zeros = reinterpret_cast<const uint16_t*>(S + s_zero);
+    P.newlat = reinterpret_cast<uint16_t*>(S + s_newlat);
+    P.part = F(s_part);
+    P.s_max = m->G;
+    P.amax = reinterpret_cast<int*>(S + s_amax);
+    // buffers accumulated with atomics (K split into panels) are cleared at the start of each step
+    P.carry = m->layers[0].g[mk::G_O].n_kc > 1;
+    int nz = 0;
+    if (m->layers[0].g[mk::G_A].n_kc > 1) {
+        P.zptr[nz] = F(s_a);
+        P.zn[nz++] = (long long)L * Mx * D.a_rows;
+    }
+    if (D.sh && m->layers[0].g[mk::G_SHGU].n_kc > 1) {
+        P.zptr[nz] = F(s_shgu);
+        P.zn[nz++] = (long long)L * Mx * 2 * D.sffn;
+    }
+    if (D.E && m->layers[0].g[mk::G_GU].n_kc > 1) {
+        P.zptr[nz] = F(s_gu);
+        P.zn[nz++] = (long long)L * nsl * Mx * 2 * D.ffn;
+    }
+    if (P.carry) {
+        P.zptr[nz] = F(s_x) + (size_t)Mx * d;
+        P.zn[nz++] = (long long)L * Mx * d;
+    }
+    P.nz = nz;  // logits (split-K head) are added per step in mk_decode_step
+    m->ctr = reinterpret_cast<unsigned*>(S + s_ctr);
+    m->ctr_n = ctr_n;
+    m->status = reinterpret_cast<unsigned*>(S + s_status);
+    P.ctr = m->ctr;
+    P.status = m->status;
+    P.timeout_ns = wait_ns();
+    if (D.E) {
+        m->dbg_idx = reinterpret_cast<int*>(S + s_dbgi);
+        m->dbg_w = reinterpret_cast<float*>(S + s_dbgw);
+    }
+    CK(cudaStreamSynchronize(s));
+    *out = m;
+    return MK_OK;
+}
+
+int mk_model_info(const mk_model* m, mk_info* out) {
+    if (!m || m->magic != MODEL_MAGIC || !out) return fail(MK_ERR_INVALID_ARG, "bad model or out");
+    out->weight_bytes = (int64_t)m->wbytes;
+    out->scratch_bytes = (int64_t)m->sbytes;
+    out->grid_ctas = m->G;
+    out->threads_per_cta = mk::NTHREADS;
+    out->smem_bytes = mk::SMEM_TOTAL;
+    out->ring_slots = mk::NSLOT;
+    out->slot_bytes = mk::SLOT_BYTES;
+    out->sm_count = m->sms;
+    return MK_OK;
+}
+
+int mk_alloc_kv(const mk_model* m, int32_t batch, int32_t max_ctx, mk_kv** out) {
+    if (!out) return fail(MK_ERR_INVALID_ARG, "out is NULL");
+    *out = nullptr;
+    if (!m || m->magic != MODEL_MAGIC) return fail(MK_ERR_INVALID_ARG, "bad model handle");
+    if (batch < 1 || batch > m->cfg.max_batch) return fail(MK_ERR_INVALID_ARG, "batch out of range");
+    if (max_ctx < 1 || max_ctx > m->cfg.max_ctx + m->cfg.max_tokens_per_seq)
+        return fail(MK_ERR_INVALID_ARG, "max_ctx out of range");
+    const Dims D = dims_of(m->cfg);
+    mk_kv* kv = new mk_kv();
+    kv->magic = KV_MAGIC;
+    kv->m = const_cast<mk_model*>(m);
+    kv->batch = batch;
+    kv->max_ctx = max_ctx;
+    kv->pps = (max_ctx + mk::PAGE - 1) / mk::PAGE;
+    kv->page_elems = D.gqa ? (size_t)D.Hkv * 2 * mk::PAGE * D.hd : (size_t)mk::PAGE * mk::MLA_D;
+    const size_t pages = (size_t)batch * kv->pps;
+    kv->layer_elems = pages * kv->page_elems;
+    const size_t bytes = kv->layer_elems * D.L * 2;
+    cudaError_t e = cudaMalloc(&kv->pool, bytes);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        delete kv;
+        return fail(MK_ERR_OOM, "kv: cudaMalloc(%zu) failed", bytes);
+    }
+    e = cudaMalloc(&kv->btab, pages * sizeof(int));
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        cudaFree(kv->pool);
+        delete kv;
+        return fail(MK_ERR_OOM, "kv block table");
+    }
+    CK(cudaMemset(kv->pool, 0, bytes));
+    kv->h_btab.resize(pages);
+    for (int b = 0; b < batch; ++b)
+        for (int j = 0; j < kv->pps; ++j) kv->h_btab[(size_t)b * kv->pps + j] = j * batch + b;
+    CK(cudaMemcpy(kv->btab, kv->h_btab.data(), pages * sizeof(int), cudaMemcpyHostToDevice));
+    kv->m->live_kv++;
+    *out = kv;
+    return MK_OK;
+}
+
+int32_t mk_kv_pages_per_seq(const mk_kv* kv) { return (kv && kv->magic == KV_MAGIC) ? kv->pps : -1; }
+
+int mk_kv_set_block_table(mk_kv* kv, const int32_t* table) {
+    if (!kv || kv->magic != KV_MAGIC || !table) return fail(MK_ERR_INVALID_ARG, "bad kv or table");
+    const size_t pages = (size_t)kv->batch * kv->pps;
+    std::vector<char> seen(pages, 0);
+    for (size_t i = 0; i < pages; ++i) {
+        if (table[i] < 0 || (size_t)table[i] >= pages || seen[table[i]])
+            return fail(MK_ERR_INVALID_ARG, "block table entry %zu invalid or repeated", i);
+        seen[table[i]] = 1;
+    }
+    std::memcpy(kv->h_btab.data(), table, pages * sizeof(int));
+    CK(cudaMemcpy(kv->btab, table, pages * sizeof(int), cudaMemcpyHostToDevice));
+    return MK_OK;
+}
+
+static int kv_copy(const mk_kv* kv, int32_t layer, int32_t seq, int32_t pos0, int32_t n, void* rows, void* stream,
+                   int to_cache) {
+    if (!kv || kv->magic != KV_MAGIC || !rows) return fail(MK_ERR_INVALID_ARG, "bad kv or rows");
+    const Dims D = dims_of(kv->m->cfg);
+    if (layer < 0 || layer >= D.L || seq < 0 || seq >= kv->batch || pos0 < 0 || n < 0 || pos0 + n > kv->max_ctx)
+        return fail(MK_ERR_INVALID_ARG, "kv range out of bounds");
+    if (n == 0) return MK_OK;
+    const int row = D.gqa ? 2 * D.Hkv * D.hd : mk::MLA_D;
+    const size_t bytes = (size_t)n * row * 2;
+    cudaStream_t s = (cudaStream_t)stream;
+    uint16_t* dev = static_cast<uint16_t*>(rows);
+    const bool host = !is_device_ptr(rows);
+    if (host) {
+        CK(cudaMalloc(&dev, bytes));
+        if (to_cache) CK(cudaMemcpyAsync(dev, rows, bytes, cudaMemcpyHostToDevice, s));
+    }
+    kv_scatter<<<256, 256, 0, s>>>(kv->pool + (size_t)layer * kv->layer_elems, kv->btab, kv->pps, kv->page_elems,
+                                   D.gqa, D.Hkv, D.hd, D.kl, D.rd, seq, pos0, n, row, dev, to_cache);
+    CK(cudaGetLastError());
+    if (host) {
+        if (!to_cache) CK(cudaMemcpyAsync(rows, dev, bytes, cudaMemcpyDeviceToHost, s));
+        CK(cudaStreamSynchronize(s));
+        CK(cudaFree(dev));
+    }
+    return MK_OK;
+}
+
+int mk_kv_write(mk_kv* kv, int32_t layer, int32_t seq, int32_t pos0, int32_t n, const void* rows, void* stream) {
+    return kv_copy(kv, layer, seq, pos0, n, const_cast<void*>(rows), stream, 1);
+}
+
+int mk_kv_read(const mk_kv* kv, int32_t layer, int32_t seq, int32_t pos0, int32_t n, void* rows, void* stream) {
+    return kv_copy(kv, layer, seq, pos0, n, rows, stream, 0);
+}
+
+int mk_decode_step(mk_model* m, mk_kv* kv, const int32_t* tokens, const int32_t* positions, int32_t batch,
+                   int32_t T, float* logits, int32_t* accept, void* stream) {
+    if (!m || m->magic != MODEL_MAGIC) return fail(MK_ERR_INVALID_ARG, "bad model handle");
+    if (!kv || kv->magic != KV_MAGIC) return fail(MK_ERR_INVALID_ARG, "bad kv handle");
+    if (kv->m != m) return fail(MK_ERR_STATE, "kv cache belongs to another model");
+    if (!tokens || !positions || !logits) return fail(MK_ERR_INVALID_ARG, "NULL tokens/positions/logits");
+    if (batch < 1 || batch > kv->batch) return fail(MK_ERR_INVALID_ARG, "batch %d out of range", batch);
+    if (T < 1 || T > m->cfg.max_tokens_per_seq) return fail(MK_ERR_INVALID_ARG, "T %d out of range", T);
+    if (accept && T < 2) return fail(MK_ERR_INVALID_ARG, "accept needs T > 1");
+    mk::Params P = m->base;
+    P.page_elems = (long long)kv->page_elems;
+    P.pps = kv->pps;
+    P.btab = kv->btab;
+    P.kv_cap = kv->max_ctx;
+    P.kv_batch = kv->batch;
+    P.kv_pool = kv->pool;
+    P.kv_layer_elems = (long long)kv->layer_elems;
+    P.tokens = tokens;
+    P.pos = positions;
+    P.B = batch;
+    P.T = T;
+    P.M = batch * T;
+    P.logits = logits;
+    P.accept = accept;
+    P.lm.dst = logits;
+    if (P.lm.n_kc > 1) {
+        P.zptr[P.nz] = logits;
+        P.zn[P.nz++] = (long long)P.M * P.V;
+    }
+    P.parity = (int)(m->steps & 1);
+    P.dbg_idx = m->dbg_idx;
+    P.dbg_w = m->dbg_w;
+    cudaStream_t s = (cudaStream_t)stream;
+    void* args[] = {&P};
+    CK(cudaLaunchCooperativeKernel((const void*)mk::megakernel, dim3(m->G), dim3(mk::NTHREADS), args,
+                                   mk::SMEM_TOTAL, s));
+    m->steps++;
+    m->last_M = P.M;
+    return MK_OK;
+}
+
+int mk_step_status(mk_model* m, void* stream) {
+    if (!m || m->magic != MODEL_MAGIC) return fail(MK_ERR_INVALID_ARG, "bad model handle");
+    cudaStream_t s = (cudaStream_t)stream;
+    CK(cudaStreamSynchronize(s));
+    unsigned st[4];
+    CK(cudaMemcpy(st, m->status, sizeof st, cudaMemcpyDeviceToHost));
+    if (st[0] == 0 && st[1] == 0) return MK_OK;
+    // reset device state so the next step starts clean
+    CK(cudaMemset(m->ctr, 0, m->ctr_n * sizeof(unsigned)));
+    CK(cudaMemset(m->status, 0, 64));
+    CK(cudaDeviceSynchronize());
+    m->steps = 0;
+    if (st[0] == mk::ST_TIMEOUT)
+        return fail(MK_ERR_TIMEOUT, "device wait timed out (where=0x%x, cta=%u)", st[2], st[3]);
+    if (st[0] == mk::ST_INVALID)
+        return fail(MK_ERR_INVALID_ARG, "token id or position out of range for this step");
+    return fail(MK_ERR_CUDA, "device status %u", st[0]);
+}
+
+int mk_debug_routing(mk_model* m, int32_t* idx_out, float* w_out, void* stream) {
+    if (!m || m->magic != MODEL_MAGIC || !idx_out || !w_out) return fail(MK_ERR_INVALID_ARG, "bad arguments");
+    if (!m->dbg_idx) return fail(MK_ERR_STATE, "model has no router");
+    CK(cudaStreamSynchronize((cudaStream_t)stream));
+    const size_t n = (size_t)m->cfg.n_layers * m->last_M * m->cfg.top_k;
+    // the device buffers are laid out [L][M][k] for the last step's M
+    CK(cudaMemcpy(idx_out, m->dbg_idx, n * 4, cudaMemcpyDeviceToHost));
+    CK(cudaMemcpy(w_out, m->dbg_w, n * 4, cudaMemcpyDeviceToHost));
+    return MK_OK;
+}
+
+void mk_free(void* h) {
+    if (!h) return;
+    const uint32_t magic = *static_cast<uint32_t*>(h);
+    if (magic == KV_MAGIC) {
+        mk_kv* kv = static_cast<mk_kv*>(h);
+        kv->magic = 0;
+        cudaFree(kv->pool);
+        cudaFree(kv->btab);
+        if (kv->m) kv->m->live_kv--;
+        delete kv;
+    } else if (magic == MODEL_MAGIC) {
+        mk_model* m = static_cast<mk_model*>(h);
+        m->magic = 0;
+        cudaFree(m->wblob);
+        cudaFree(m->sblob);
+        cudaFree(m->d_layers);
+        delete m;
+    }
+}
+
+}  // extern "C"

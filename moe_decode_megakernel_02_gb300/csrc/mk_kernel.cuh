@@ -1,0 +1,1416 @@
+// mk_kernel.cuh -- stage program of the decode megakernel (producer + consumers).
+#pragma once
+#include "mk_device.cuh"
+
+namespace mk {
+
+struct Dep {
+    int layer, which;
+    unsigned target;
+};
+struct Deps {
+    Dep d[3];
+    int n;
+};
+__device__ __forceinline__ Deps deps0() {
+    Deps d;
+    d.n = 0;
+    return d;
+}
+__device__ __forceinline__ Deps deps1(int l, int w, unsigned t) {
+    Deps d;
+    d.n = 1;
+    d.d[0] = {l, w, t};
+    return d;
+}
+
+// per-thread view of the run (consumer threads and the producer warp each
+// keep an identical copy of the schedule state)
+struct Ctx {
+    const Params& p;
+    uint8_t* smem;
+    Misc& ms;
+    int off;
+    bool dead;
+    CRing cr;
+    PRing pr;
+    // what the staging buffer currently holds
+    const void* sk_src;
+    int sk_off, sk_kc, sk_m0, sk_kind;
+    int issued;  // producer: ring fills issued
+    __device__ Ctx(const Params& pp, uint8_t* s)
+        : p(pp), smem(s), ms(*reinterpret_cast<Misc*>(s + SMEM_MISC)), off(0), dead(false) {
+        cr.slot = 0;
+        cr.phase = 0;
+        pr.slot = 0;
+        pr.phase = 0;
+        sk_src = nullptr;
+        sk_off = sk_kc = sk_m0 = sk_kind = -1;
+        issued = 0;
+    }
+    __device__ float* stage() { return reinterpret_cast<float*>(smem + SMEM_STAGE); }
+    __device__ float* red() { return reinterpret_cast<float*>(smem + SMEM_RED); }
+    __device__ void advance(int n) { off = (int)((off + (long long)n) % p.G); }
+};
+
+__device__ __forceinline__ int ctid() { return threadIdx.x; }
+
+// consumer: thread 0 waits for all deps, then every consumer thread passes a
+// barrier (so their later reads of other CTAs' data are ordered after it)
+__device__ bool cwait(Ctx& c, const Deps& ds, unsigned where) {
+    if (threadIdx.x == 0 && !c.dead) {
+        bool ok = true;
+        for (int i = 0; i < ds.n && ok; ++i)
+            if (ds.d[i].target > 0) ok = wait_ge(c.p, ctr_of(c.p, ds.d[i].layer, ds.d[i].which), ds.d[i].target, where);
+        if (!ok) c.ms.abort = 1;
+        __threadfence();
+    }
+    cbar();
+    if (*(volatile int*)&c.ms.abort) c.dead = true;
+    return !c.dead;
+}
+
+// consumer: all consumer threads' global writes done -> release `n` to a counter
+__device__ void csignal(Ctx& c, int layer, int which, unsigned n) {
+    cbar();
+    if (threadIdx.x == 0 && n) {
+        __threadfence();
+        red_release(ctr_of(c.p, layer, which), n);
+    }
+    if (*(volatile int*)&c.ms.abort) c.dead = true;
+}
+
+// =============================================================== GEMV ====
+
+// fill stage[t][0..Kc) with f(input) for tokens m0 .. m0+ms-1
+__device__ void stage_input(Ctx& c, const Gemv& g, const float* src, int grp_off, int kc, int m0, int ms) {
+    const Params& p = c.p;
+    float* xs = c.stage();
+    const int Kc = g.Kc, k0 = kc * Kc, tid = ctid(), lane = tid & 31, warp = tid >> 5;
+    const int total = ms * Kc;
+    if (g.in_kind == IN_RMS) {
+        for (int t = warp; t < ms; t += NCW) {
+            const float* row = src + (size_t)(m0 + t) * g.src_stride;
+            float ss = 0.f;
+            for (int k = lane * 4; k < g.K; k += 128) {
+                float4 v = __ldcg(reinterpret_cast<const float4*>(row + k));
+                ss = fmaf(v.x, v.x, ss);
+                ss = fmaf(v.y, v.y, ss);
+                ss = fmaf(v.z, v.z, ss);
+                ss = fmaf(v.w, v.w, ss);
+            }
+#pragma unroll
+            for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+            if (lane == 0) c.ms.rms[t] = 1.0f / sqrtf(ss / (float)g.K + p.eps);
+        }
+        cbar();
+        for (int i = tid * 4; i < total; i += NCT * 4) {
+            const int t = i / Kc, k = i - t * Kc;
+            float4 v = __ldcg(reinterpret_cast<const float4*>(src + (size_t)(m0 + t) * g.src_stride + k0 + k));
+            uint2 gw = *reinterpret_cast<const uint2*>(g.gain + k0 + k);
+            const float r = c.ms.rms[t];
+            float4 o;
+            o.x = v.x * r * bf_lo(gw.x);
+            o.y = v.y * r * bf_hi(gw.x);
+            o.z = v.z * r * bf_lo(gw.y);
+            o.w = v.w * r * bf_hi(gw.y);
+            *reinterpret_cast<float4*>(xs + i) = o;
+        }
+    } else if (g.in_kind == IN_COPY) {
+        for (int i = tid * 4; i < total; i += NCT * 4) {
+            const int t = i / Kc, k = i - t * Kc;
+            *reinterpret_cast<float4*>(xs + i) =
+                __ldcg(reinterpret_cast<const float4*>(src + (size_t)(m0 + t) * g.src_stride + grp_off + k0 + k));
+        }
+    } else {  // IN_SWIGLU: h = silu(gate) * up
+        for (int i = tid * 4; i < total; i += NCT * 4) {
+            const int t = i / Kc, k = i - t * Kc;
+            const float* r = src + (size_t)(m0 + t) * g.src_stride + k0 + k;
+            float4 gv = __ldcg(reinterpret_cast<const float4*>(r));
+            float4 uv = __ldcg(reinterpret_cast<const float4*>(r + g.sw_off));
+            float4 o;
+            o.x = silu(gv.x) * uv.x;
+            o.y = silu(gv.y) * uv.y;
+            o.z = silu(gv.z) * uv.z;
+            o.w = silu(gv.w) * uv.w;
+            *reinterpret_cast<float4*>(xs + i) = o;
+        }
+    }
+}
+
+// one lane: 8 rows x 8 k of the tile against MTc staged tokens, then a
+// reduction over the lanes that share the 8 rows; per-warp sums go to red[]
+template <int MTc>
+__device__ void gemv_compute(const uint8_t* tile, int nr, int Kc, const float* xs, int mt0, float* red) {
+    const int tid = ctid(), lane = tid & 31, warp = tid >> 5;
+    const int NC = Kc >> 3;
+    const int pairs = (nr >> 3) * NC;
+    float acc[8][MTc];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int m = 0; m < MTc; ++m) acc[i][m] = 0.f;
+    int rg = 0;
+    if (tid < pairs) {
+        rg = tid / NC;
+        const int ch = tid - rg * NC;
+        float xv[MTc][8];
+#pragma unroll
+        for (int m = 0; m < MTc; ++m) {
+            const float4 a = *reinterpret_cast<const float4*>(xs + (size_t)(mt0 + m) * Kc + ch * 8);
+            const float4 b = *reinterpret_cast<const float4*>(xs + (size_t)(mt0 + m) * Kc + ch * 8 + 4);
+            xv[m][0] = a.x; xv[m][1] = a.y; xv[m][2] = a.z; xv[m][3] = a.w;
+            xv[m][4] = b.x; xv[m][5] = b.y; xv[m][6] = b.z; xv[m][7] = b.w;
+        }
+        const uint4* wp = reinterpret_cast<const uint4*>(tile) + (size_t)rg * 8 * NC + ch;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint4 w = wp[(size_t)i * NC];
+            const float wf[8] = {bf_lo(w.x), bf_hi(w.x), bf_lo(w.y), bf_hi(w.y),
+                                 bf_lo(w.z), bf_hi(w.z), bf_lo(w.w), bf_hi(w.w)};
+#pragma unroll
+            for (int m = 0; m < MTc; ++m) {
+                float a = acc[i][m];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) a = fmaf(wf[e], xv[m][e], a);
+                acc[i][m] = a;
+            }
+        }
+    }
+    const int span = NC < 32 ? NC : 32;
+    for (int o = span >> 1; o > 0; o >>= 1)
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+#pragma unroll
+            for (int m = 0; m < MTc; ++m) acc[i][m] += __shfl_xor_sync(0xffffffffu, acc[i][m], o);
+    if (tid < pairs) {
+        const int WPR = NC >= 32 ? (NC >> 5) : 1;
+        const bool writer = NC >= 32 ? (lane == 0) : ((lane % NC) == 0);
+        if (writer) {
+            const int wr = NC >= 32 ? (warp % WPR) : 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+#pragma unroll
+                for (int m = 0; m < MTc; ++m) red[((rg * WPR + wr) * 8 + i) * MTc + m] = acc[i][m];
+        }
+    }
+}
+
+__device__ __forceinline__ float route_weight(const Misc& ms, int m, int expert, int k) {
+    for (int j = 0; j < k; ++j)
+        if (ms.ridx[m][j] == expert) return ms.rw[m][j];
+    return 0.f;
+}
+
+__device__ void gemv_epilogue(Ctx& c, const Gemv& g, int slot, int expert, int r0, int nr, int mbase, int mcount,
+                              int MTc) {
+    const float* red = c.red();
+    const int NC = g.Kc >> 3;
+    const int WPR = NC >= 32 ? (NC >> 5) : 1;
+    for (int idx = ctid(); idx < nr * MTc; idx += NCT) {
+        const int r = idx / MTc, mt = idx - r * MTc;
+        if (mt >= mcount) continue;
+        const int rg = r >> 3, i = r & 7;
+        float y = 0.f;
+        for (int wr = 0; wr < WPR; ++wr) y += red[((rg * WPR + wr) * 8 + i) * MTc + mt];
+        const int m = mbase + mt, row = r0 + r;
+        if (g.out_kind == OUT_STORE) {
+            float* d = g.dst + (size_t)slot * g.dst_sstride + (size_t)m * g.dst_stride + row;
+            if (g.n_kc == 1)
+                *d = y;
+            else
+                atomicAdd(d, y);
+        } else if (g.out_kind == OUT_RESID) {
+            float* d = g.dst + (size_t)m * g.dst_stride + row;
+            if (g.n_kc == 1) {
+                const float v = __ldcg(d) + y;
+                *d = v;
+                g.dst2[(size_t)m * g.dst_stride + row] = v;
+            } else {
+                atomicAdd(d, y);
+            }
+        } else {  // OUT_SCALED: routed expert down projection into the next residual
+            const float w = expert < 0 ? 1.0f : route_weight(c.ms, m, expert, c.p.topk);
+            if (w != 0.f) atomicAdd(g.dst + (size_t)m * g.dst_stride + row, w * y);
+        }
+    }
+}
+
+// consumer: one GEMV work item
+__device__ void cons_gemv(Ctx& c, const Gemv& g, int slot, int expert, int j) {
+    const Params& p = c.p;
+    const int kc = j / g.n_rb, rb = j - kc * g.n_rb;
+    const int r0 = rb * g.R, nr = min(g.R, g.N - r0);
+    const float* src = g.src + (size_t)slot * g.src_sstride;
+    const int grp_off = g.grp_rows ? (r0 / g.grp_rows) * g.grp_stride : 0;
+    const int cap = STAGE_FLOATS / g.Kc;
+    const int M = p.M;
+    const uint8_t* tile = nullptr;
+    for (int m0 = 0; m0 < M; m0 += cap) {
+        const int ms = min(cap, M - m0);
+        if (c.sk_src != src || c.sk_off != grp_off || c.sk_kc != kc || c.sk_m0 != m0 || c.sk_kind != g.in_kind) {
+            cbar();  // everyone is done with the previous contents
+            stage_input(c, g, src, grp_off, kc, m0, ms);
+            cbar();
+            c.sk_src = src;
+            c.sk_off = grp_off;
+            c.sk_kc = kc;
+            c.sk_m0 = m0;
+            c.sk_kind = g.in_kind;
+        }
+        if (!tile && !c.dead) tile = cons_wait(p, c.smem, c.ms, c.cr);
+        for (int mt0 = 0; mt0 < ms; mt0 += MT) {
+            const int cnt = min(MT, ms - mt0);
+            const int MTc = cnt == 1 ? 1 : (cnt == 2 ? 2 : 4);
+            if (tile) {
+                if (MTc == 1)
+                    gemv_compute<1>(tile, nr, g.Kc, c.stage(), mt0, c.red());
+                else if (MTc == 2)
+                    gemv_compute<2>(tile, nr, g.Kc, c.stage(), mt0, c.red());
+                else
+                    gemv_compute<4>(tile, nr, g.Kc, c.stage(), mt0, c.red());
+            }
+            if (m0 + mt0 + cnt >= M) cons_release(c.ms, c.cr);  // last use of the tile
+            cbar();
+            if (tile) gemv_epilogue(c, g, slot, expert, r0, nr, m0 + mt0, cnt, MTc);
+            cbar();
+        }
+    }
+    if (*(volatile int*)&c.ms.abort) c.dead = true;
+}
+
+// producer: bulk-load the weight tile of one GEMV item
+__device__ void prod_gemv(Ctx& c, const Gemv& g, int expert, int j) {
+    const int kc = j / g.n_rb, rb = j - kc * g.n_rb;
+    const int r0 = rb * g.R, nr = min(g.R, g.N - r0);
+    const unsigned bytes = (unsigned)nr * g.Kc * 2u;
+    const uint16_t* src =
+        g.W + (expert >= 0 ? (size_t)expert * g.w_estride : 0) + (size_t)kc * g.N * g.Kc + (size_t)r0 * g.Kc;
+    int ok = 1;
+    if ((threadIdx.x & 31) == 0) {
+        uint8_t* dst = prod_begin(c.p, c.smem, c.ms, c.pr, bytes);
+        if (dst)
+            bulk_g2s(dst, src, bytes, &c.ms.full[c.pr.slot]);
+        else
+            ok = 0;
+    }
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (!ok) {
+        c.dead = true;
+        return;
+    }
+    ++c.issued;
+    prod_next(c.pr);
+}
+
+template <bool PROD>
+__device__ void stage_gemv(Ctx& c, int l, const Gemv& g, const Deps& deps, int sig) {
+    const int n = gemv_items(g);
+    int lo, hi;
+    my_range(c.p, n, c.off, lo, hi);
+    c.advance(n);
+    if (lo >= hi) return;
+    c.sk_src = nullptr;  // a new stage: the input contents may have changed
+    if constexpr (PROD) {
+        for (int j = lo; j < hi && !c.dead; ++j) prod_gemv(c, g, -1, j);
+    } else {
+        cwait(c, deps, 0x1000u | (unsigned)(l << 16) | (unsigned)sig);
+        for (int j = lo; j < hi; ++j) cons_gemv(c, g, 0, -1, j);
+        csignal(c, l, sig, (unsigned)(hi - lo));
+    }
+}
+
+// ============================================================ routing ====
+// softmax / top-k of the router logits of every token (ties -> lower id),
+// union of the selected experts (sorted by id) -> routed slots.
+// consumers: full routing into Misc; producer warp: slot list only.
+template <bool PROD>
+__device__ bool route(Ctx& c, int l) {
+    const Params& p = c.p;
+    const Layer& Ld = p.layers[l];
+    const int E = p.E, k = p.topk;
+    const int tid = threadIdx.x, lane = tid & 31;
+    uint8_t* used = PROD ? c.ms.p_used : c.ms.used;
+    uint8_t* slot_e = PROD ? c.ms.p_slot_e : c.ms.slot_e;
+    if constexpr (PROD) {
+        int ok = 1;
+        if (lane == 0) {
+            ok = wait_ge(p, ctr_of(p, l, C_ROUTER), (unsigned)gemv_items(Ld.g[G_ROUTER]), 0x300u);
+            __threadfence();
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        __syncwarp();
+        if (!ok) {
+            c.dead = true;
+            return false;
+        }
+        for (int e = lane; e < E; e += 32) used[e] = 0;
+        __syncwarp();
+    } else {
+        cwait(c, deps1(l, C_ROUTER, (unsigned)gemv_items(Ld.g[G_ROUTER])), 0x400u);
+        for (int e = tid; e < E; e += NCT) used[e] = 0;
+        cbar();
+    }
+    const int warp = PROD ? 0 : (tid >> 5);
+    const int nw = PROD ? 1 : NCW;
+    for (int m = warp; m < p.M; m += nw) {
+        float v[MAX_E / 32];
+        const float* lg = Ld.rlog + (size_t)m * E;
+#pragma unroll
+        for (int i = 0; i < MAX_E / 32; ++i) {
+            const int e = lane + 32 * i;
+            v[i] = e < E ? __ldcg(lg + e) : -INFINITY;
+        }
+        float sel[MAX_K];
+        int sid[MAX_K];
+        for (int j = 0; j < k; ++j) {
+            float bv = -INFINITY;
+            int bi = 0x7fffffff;
+#pragma unroll
+            for (int i = 0; i < MAX_E / 32; ++i) {
+                const int e = lane + 32 * i;
+                if (e < E && (v[i] > bv || (v[i] == bv && e < bi))) {
+                    bv = v[i];
+                    bi = e;
+                }
+            }
+#pragma unroll
+            for (int o = 16; o; o >>= 1) {
+                const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+                const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+                if (ov > bv || (ov == bv && oi < bi)) {
+                    bv = ov;
+                    bi = oi;
+                }
+            }
+            if (bi >= E) {  // NaN logits (only after a failed step): keep ids in range
+                bi = j;
+                bv = 0.f;
+            }
+            sel[j] = bv;
+            sid[j] = bi;
+#pragma unroll
+            for (int i = 0; i < MAX_E / 32; ++i)
+                if (lane + 32 * i == bi) v[i] = -INFINITY;
+        }
+        if (lane == 0) {
+            // renormalised top-k probabilities = softmax over the selected logits
+            float den = 0.f, w[MAX_K];
+            for (int j = 0; j < k; ++j) {
+                w[j] = expf(sel[j] - sel[0]);
+                den += w[j];
+            }
+            for (int j = 0; j < k; ++j) {
+                used[sid[j]] = 1;
+                if constexpr (!PROD) {
+                    c.ms.ridx[m][j] = (uint8_t)sid[j];
+                    c.ms.rw[m][j] = w[j] / den;
+                    if (blockIdx.x == 0 && p.dbg_idx) {
+                        const size_t o = ((size_t)l * p.M + m) * k + j;
+                        p.dbg_idx[o] = sid[j];
+                        p.dbg_w[o] = w[j] / den;
+                    }
+                }
+            }
+        }
+    }
+    if constexpr (PROD) {
+        __syncwarp();
+    } else {
+        cbar();
+    }
+    if (PROD || tid < 32) {
+        int n = 0;
+        for (int e0 = 0; e0 < E; e0 += 32) {
+            const int e = e0 + lane;
+            const bool u = e < E && used[e];
+            const unsigned b = __ballot_sync(0xffffffffu, u);
+            if (u) slot_e[n + __popc(b & ((1u << lane) - 1u))] = (uint8_t)e;
+            n += __popc(b);
+        }
+        if (lane == 0) {
+            if (PROD)
+                c.ms.p_nslots = n;
+            else
+                c.ms.n_slots = n;
+        }
+    }
+    if constexpr (PROD) {
+        __syncwarp();
+    } else {
+        cbar();
+    }
+    return true;
+}
+
+// routed-expert stage: items = slots x (row blocks x k panels), slot-major
+template <bool PROD>
+__device__ void stage_experts(Ctx& c, int l, const Gemv& g, bool down) {
+    const Params& p = c.p;
+    const int nslots = PROD ? c.ms.p_nslots : c.ms.n_slots;
+    const uint8_t* slot_e = PROD ? c.ms.p_slot_e : c.ms.slot_e;
+    const int per = gemv_items(g);
+    const int n = nslots * per;
+    int lo, hi;
+    my_range(p, n, c.off, lo, hi);
+    c.advance(n);
+    if (lo >= hi) return;
+    c.sk_src = nullptr;
+    if constexpr (PROD) {
+        for (int i = lo; i < hi && !c.dead; ++i) prod_gemv(c, g, slot_e[i / per], i % per);
+    } else {
+        const Layer& Ld = p.layers[l];
+        int cur = -1;
+        unsigned cnt = 0;
+        for (int i = lo; i < hi; ++i) {
+            const int s = i / per;
+            if (s != cur) {
+                if (!down && cur >= 0) csignal(c, l, C_GU0 + cur, cnt);
+                cur = s;
+                cnt = 0;
+                // gate/up inputs were ready before routing (the router waited for
+                // the output projection); each down slot waits for its gate/up
+                if (down) cwait(c, deps1(l, C_GU0 + s, (unsigned)gemv_items(Ld.g[G_GU])), 0x500u);
+            }
+            cons_gemv(c, g, s, slot_e[s], i % per);
+            ++cnt;
+        }
+        if (down)
+            csignal(c, l, C_DOWN, (unsigned)(hi - lo));
+        else if (cur >= 0)
+            csignal(c, l, C_GU0 + cur, cnt);
+    }
+}
+
+// ====================================================== GQA attention ====
+// item (sequence b, kv head g, split s) over units [u_lo, u_hi): prefix
+// chunks of 64 cached positions (from the ring) and, in the last split, the T
+// new positions (computed here, appended to the cache, read from smem).
+// Output: unnormalised partial (max, sum, o[hd]) per query row t*Gq + hh.
+
+// reduce 32 values across the warp: lane i returns the sum of value i
+__device__ __forceinline__ float reduce_scatter32(float (&v)[32]) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int step = 0; step < 5; ++step) {
+        const int o = 16 >> step;
+        const int n = 16 >> step;
+        const bool up = lane & o;
+#pragma unroll
+        for (int i = 0; i < n; ++i) {
+            const float send = up ? v[i] : v[i + n];
+            const float keep = up ? v[i + n] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
+    }
+    return v[0];
+}
+
+template <int DPL>
+struct GqaState {
+    float m[8], l[8], o[8][DPL];
+};
+
+// one warp's share (rows [base, base+8)) of a block of K/V rows
+template <int DPL, bool TAIL>
+__device__ void gqa_rows(const Params& p, GqaState<DPL>& st, const float (&q)[8][DPL], int Q, const void* Kp,
+                         const void* Vp, int base, int nvalid, int tailT, float* sc) {
+    const int lane = threadIdx.x & 31, hd = p.hd, Gq = p.Hq / p.Hkv;
+    // partial dot products of this lane's DPL dims for rows base..base+7
+    for (int half = 0; half < (Q > 4 ? 2 : 1); ++half) {
+        float v[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = 0.f;
+        const int r0 = half * 4;  // query rows r0..r0+3 (Q > 4) or all rows (Q <= 4)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int row = base + j;
+            if (row < nvalid) {
+                float kv[DPL];
+                if (TAIL) {
+                    const float* K = reinterpret_cast<const float*>(Kp) + (size_t)row * hd + lane * DPL;
+#pragma unroll
+                    for (int e = 0; e < DPL; ++e) kv[e] = K[e];
+                } else {
+                    const uint16_t* K = reinterpret_cast<const uint16_t*>(Kp) + (size_t)row * hd + lane * DPL;
+#pragma unroll
+                    for (int e = 0; e < DPL; ++e) kv[e] = bf2f(K[e]);
+                }
+                if (Q <= 4) {
+#pragma unroll
+                    for (int qq = 0; qq < 4; ++qq) {
+                        float a = 0.f;
+#pragma unroll
+                        for (int e = 0; e < DPL; ++e) a = fmaf(q[qq][e], kv[e], a);
+                        v[j * 4 + qq] = a;
+                    }
+                } else {
+#pragma unroll
+                    for (int qq = 0; qq < 4; ++qq) {
+                        float a = 0.f;
+#pragma unroll
+                        for (int e = 0; e < DPL; ++e) a = fmaf(q[r0 + qq][e], kv[e], a);
+                        v[j * 4 + qq] = a;
+                    }
+                }
+            }
+        }
+        const float s = reduce_scatter32(v);
+        sc[half * 32 + lane] = s;
+    }
+    __syncwarp();
+    // online softmax per query row over this warp's rows
+    for (int qr = 0; qr < Q; ++qr) {
+        const int t = qr / Gq;
+        float sv[8];
+        float mc = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int row = base + j;
+            bool ok = row < nvalid && (!TAIL || row <= t);
+            const int idx = Q <= 4 ? (j * 4 + qr) : ((qr >> 2) * 32 + j * 4 + (qr & 3));
+            sv[j] = ok ? sc[idx] : -INFINITY;
+            mc = fmaxf(mc, sv[j]);
+        }
+        if (mc == -INFINITY) continue;
+        const float mn = fmaxf(st.m[qr], mc);
+        const float corr = st.m[qr] == -INFINITY ? 0.f : expf(st.m[qr] - mn);
+        float ps = 0.f;
+        float acc[DPL];
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) acc[e] = st.o[qr][e] * corr;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            if (sv[j] == -INFINITY) continue;
+            const float pj = expf(sv[j] - mn);
+            ps += pj;
+            const int row = base + j;
+            if (TAIL) {
+                const float* V = reinterpret_cast<const float*>(Vp) + (size_t)row * hd + lane * DPL;
+#pragma unroll
+                for (int e = 0; e < DPL; ++e) acc[e] = fmaf(pj, V[e], acc[e]);
+            } else {
+                const uint16_t* V = reinterpret_cast<const uint16_t*>(Vp) + (size_t)row * hd + lane * DPL;
+#pragma unroll
+                for (int e = 0; e < DPL; ++e) acc[e] = fmaf(pj, bf2f(V[e]), acc[e]);
+            }
+        }
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) st.o[qr][e] = acc[e];
+        st.l[qr] = st.l[qr] * corr + ps;
+        st.m[qr] = mn;
+    }
+    __syncwarp();
+}
+
+template <int DPL>
+__device__ void cons_attn_gqa(Ctx& c, int l, const AttnItem& it) {
+    const Params& p = c.p;
+    const Layer& Ld = p.layers[l];
+    const int hd = p.hd, Gq = p.Hq / p.Hkv, T = p.T, Q = T * Gq, half = hd / 2;
+    const int tid = ctid(), lane = tid & 31, warp = tid >> 5;
+    const int b = it.b, g = it.g, pos0 = p.pos[b];
+    const bool tail = it.u_hi == it.nch + 1;
+    float* qs = c.stage();             // [Q][hd]
+    float* tk = qs + Q * hd;           // [T][hd] new keys (bf16-rounded)
+    float* tv = tk + T * hd;           // [T][hd]
+    float* sc = tv + T * hd;           // [NCW][64]
+    float* ws = sc + NCW * 64;         // [NCW][Q][2 + hd]
+    cbar();
+    c.sk_src = nullptr;
+    const int a_stride = Ld.a_stride;
+    for (int i = tid; i < Q * half; i += NCT) {
+        const int qr = i / half, e = i - qr * half;
+        const int t = qr / Gq, h = g * Gq + (qr - t * Gq);
+        const float* qa = Ld.a + (size_t)(b * T + t) * a_stride + h * hd;
+        const float2 cs = p.rope[(size_t)(pos0 + t) * p.rope_half + e];
+        const float x0 = __ldcg(qa + e), x1 = __ldcg(qa + e + half);
+        qs[qr * hd + e] = (x0 * cs.x - x1 * cs.y) * p.attn_scale;
+        qs[qr * hd + e + half] = (x1 * cs.x + x0 * cs.y) * p.attn_scale;
+    }
+    if (tail) {
+        uint16_t* pool = p.kv_pool + (size_t)l * p.kv_layer_elems;
+        for (int i = tid; i < T * half; i += NCT) {
+            const int t = i / half, e = i - t * half;
+            const int pos = pos0 + t;
+            const float* ka = Ld.a + (size_t)(b * T + t) * a_stride + p.Hq * hd + g * hd;
+            const float* va = ka + p.Hkv * hd;
+            const float2 cs = p.rope[(size_t)pos * p.rope_half + e];
+            const float x0 = __ldcg(ka + e), x1 = __ldcg(ka + e + half);
+            const uint16_t k0 = f2bf(x0 * cs.x - x1 * cs.y), k1 = f2bf(x1 * cs.x + x0 * cs.y);
+            const uint16_t v0 = f2bf(__ldcg(va + e)), v1 = f2bf(__ldcg(va + e + half));
+            tk[t * hd + e] = bf2f(k0);
+            tk[t * hd + e + half] = bf2f(k1);
+            tv[t * hd + e] = bf2f(v0);
+            tv[t * hd + e + half] = bf2f(v1);
+            // append to the page: [Hkv][K|V][64][hd]
+            uint16_t* pg = pool + (size_t)p.btab[b * p.pps + pos / PAGE] * p.page_elems +
+                           (size_t)g * 2 * PAGE * hd + (size_t)(pos % PAGE) * hd;
+            pg[e] = k0;
+            pg[e + half] = k1;
+            pg[(size_t)PAGE * hd + e] = v0;
+            pg[(size_t)PAGE * hd + e + half] = v1;
+        }
+    }
+    cbar();
+    float qreg[8][DPL];
+#pragma unroll
+    for (int qr = 0; qr < 8; ++qr)
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) qreg[qr][e] = qr < Q ? qs[qr * hd + lane * DPL + e] : 0.f;
+    GqaState<DPL> st;
+#pragma unroll
+    for (int qr = 0; qr < 8; ++qr) {
+        st.m[qr] = -INFINITY;
+        st.l[qr] = 0.f;
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) st.o[qr][e] = 0.f;
+    }
+    for (int u = it.u_lo; u < it.u_hi; ++u) {
+        if (u < it.nch) {
+            const uint8_t* tile = c.dead ? nullptr : cons_wait(p, c.smem, c.ms, c.cr);
+            if (tile) {
+                const int nvalid = min(GQA_CH, pos0 - u * GQA_CH);
+                gqa_rows<DPL, false>(p, st, qreg, Q, tile, tile + (size_t)GQA_CH * hd * 2, warp * 8, nvalid, 0,
+                                     sc + warp * 64);
+            }
+            cons_release(c.ms, c.cr);
+        } else if (warp == 0) {
+            gqa_rows<DPL, true>(p, st, qreg, Q, tk, tv, 0, T, T, sc);
+        }
+    }
+    // merge the 8 warps' states
+    const int W = 2 + hd;
+    for (int qr = 0; qr < Q; ++qr) {
+        float* w = ws + ((size_t)warp * Q + qr) * W;
+        if (lane == 0) {
+            w[0] = st.m[qr];
+            w[1] = st.l[qr];
+        }
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) w[2 + lane * DPL + e] = st.o[qr][e];
+    }
+    cbar();
+    float* out = p.part + ((((size_t)b * p.Hkv + g) * p.s_max + it.s) * Q) * W;
+    for (int i = tid; i < Q * W; i += NCT) {
+        const int qr = i / W, e = i - qr * W;
+        float mx = -INFINITY;
+        for (int w = 0; w < NCW; ++w) mx = fmaxf(mx, ws[((size_t)w * Q + qr) * W]);
+        float v = 0.f;
+        if (e == 0) {
+            v = mx;
+        } else if (mx != -INFINITY) {
+            for (int w = 0; w < NCW; ++w) {
+                const float mw = ws[((size_t)w * Q + qr) * W];
+                if (mw != -INFINITY) v += ws[((size_t)w * Q + qr) * W + e] * expf(mw - mx);
+            }
+        }
+        out[(size_t)qr * W + e] = v;
+    }
+    cbar();
+}
+
+// ======================================================= MLA attention ====
+// item (sequence b, token t, split s): 16 heads x (latent 512 + rope 64)
+// against 32-position chunks of the latent cache. Scores and P.V run on the
+// tensor cores (mma.sync m16n8k16, bf16 in, fp32 accumulate); the queries and
+// probabilities are split into bf16 hi + lo parts so the products keep ~16
+// mantissa bits (the cache values are exact bf16 already).
+struct MlaSmem {
+    uint16_t* qhi;   // [16][MLA_QS]
+    uint16_t* qlo;
+    float* spart;    // [KS][16][NR]
+    uint16_t* phi;   // [16][40]
+    uint16_t* plo;
+    float* mst;      // [16] running max
+    float* lst;      // [16] running sum
+    float* cst;      // [16] correction of this chunk
+    uint16_t* tc;    // tail latent rows [16][MLA_CS]
+    uint16_t* tr;    // tail rope rows [16][MLA_RS]
+};
+__device__ __forceinline__ MlaSmem mla_smem(float* stage) {
+    MlaSmem s;
+    uint8_t* b = reinterpret_cast<uint8_t*>(stage);
+    s.qhi = reinterpret_cast<uint16_t*>(b);
+    s.qlo = reinterpret_cast<uint16_t*>(b + 16 * MLA_QS * 2);
+    s.spart = reinterpret_cast<float*>(b + 2 * 16 * MLA_QS * 2);                 // 37376
+    s.phi = reinterpret_cast<uint16_t*>(b + 37376 + 4096);                        // 41472
+    s.plo = reinterpret_cast<uint16_t*>(b + 41472 + 16 * 40 * 2);                 // 42752
+    s.mst = reinterpret_cast<float*>(b + 42752 + 16 * 40 * 2);                    // 44032
+    s.lst = s.mst + 16;
+    s.cst = s.lst + 16;
+    s.tc = reinterpret_cast<uint16_t*>(b + 44032 + 192);                          // 44224
+    s.tr = reinterpret_cast<uint16_t*>(b + 44224 + 16 * MLA_CS * 2);              // 60864
+    return s;
+}
+
+__device__ __forceinline__ uint32_t lds32(const uint16_t* p) { return *reinterpret_cast<const uint32_t*>(p); }
+
+__device__ void mla_chunk(const MlaSmem& S, const uint16_t* ck, const uint16_t* kr, int NR, int nvalid,
+                          float (&acc)[8][4]) {
+    const int tid = ctid(), lane = tid & 31, warp = tid >> 5, g = lane >> 2, t4 = lane & 3;
+    // ---- scores S[16][NR] = Q . KV^T ----
+    const int NT = NR / 8, KS = 8 / NT, nt = warp % NT, ks = warp / NT;
+    const int steps = 36 / KS;
+    float sacc[4] = {0.f, 0.f, 0.f, 0.f};
+    const int n = nt * 8 + g;
+    for (int kk = ks * steps; kk < (ks + 1) * steps; ++kk) {
+        const int k0 = kk * 16;
+        uint32_t ah[4], al[4];
+        ah[0] = lds32(S.qhi + g * MLA_QS + k0 + 2 * t4);
+        ah[1] = lds32(S.qhi + (g + 8) * MLA_QS + k0 + 2 * t4);
+        ah[2] = lds32(S.qhi + g * MLA_QS + k0 + 8 + 2 * t4);
+        ah[3] = lds32(S.qhi + (g + 8) * MLA_QS + k0 + 8 + 2 * t4);
+        al[0] = lds32(S.qlo + g * MLA_QS + k0 + 2 * t4);
+        al[1] = lds32(S.qlo + (g + 8) * MLA_QS + k0 + 2 * t4);
+        al[2] = lds32(S.qlo + g * MLA_QS + k0 + 8 + 2 * t4);
+        al[3] = lds32(S.qlo + (g + 8) * MLA_QS + k0 + 8 + 2 * t4);
+        const uint16_t* br = k0 < MLA_KL ? (ck + n * MLA_CS + k0) : (kr + n * MLA_RS + (k0 - MLA_KL));
+        const uint32_t b0 = lds32(br + 2 * t4), b1 = lds32(br + 8 + 2 * t4);
+        mma_bf16(sacc, ah, b0, b1);
+        mma_bf16(sacc, al, b0, b1);
+    }
+    {
+        float* sp = S.spart + (size_t)ks * 16 * NR;
+        sp[g * NR + nt * 8 + 2 * t4] = sacc[0];
+        sp[g * NR + nt * 8 + 2 * t4 + 1] = sacc[1];
+        sp[(g + 8) * NR + nt * 8 + 2 * t4] = sacc[2];
+        sp[(g + 8) * NR + nt * 8 + 2 * t4 + 1] = sacc[3];
+    }
+    cbar();
+    // ---- online softmax: warp w owns heads 2w, 2w+1; 16 lanes per head ----
+    {
+        const int h = 2 * warp + (lane >> 4), l16 = lane & 15;
+        float s0 = -INFINITY, s1 = -INFINITY;
+        if (l16 < nvalid) {
+            s0 = 0.f;
+            for (int q = 0; q < KS; ++q) s0 += S.spart[((size_t)q * 16 + h) * NR + l16];
+        }
+        if (NR == 32 && l16 + 16 < nvalid) {
+            s1 = 0.f;
+            for (int q = 0; q < KS; ++q) s1 += S.spart[((size_t)q * 16 + h) * NR + l16 + 16];
+        }
+        float mc = fmaxf(s0, s1);
+#pragma unroll
+        for (int o = 8; o; o >>= 1) mc = fmaxf(mc, __shfl_xor_sync(0xffffffffu, mc, o));
+        const float mold = S.mst[h];
+        const float mn = fmaxf(mold, mc);
+        float corr = 1.f, p0 = 0.f, p1 = 0.f;
+        if (mn != -INFINITY) {
+            corr = mold == -INFINITY ? 0.f : expf(mold - mn);
+            p0 = s0 == -INFINITY ? 0.f : expf(s0 - mn);
+            p1 = s1 == -INFINITY ? 0.f : expf(s1 - mn);
+        }
+        float ps = p0 + p1;
+#pragma unroll
+        for (int o = 8; o; o >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o);
+        __syncwarp();
+        if (l16 == 0) {
+            S.mst[h] = mn;
+            S.lst[h] = S.lst[h] * corr + ps;
+            S.cst[h] = corr;
+        }
+        const uint16_t h0 = f2bf(p0), h1 = f2bf(p1);
+        S.phi[h * 40 + l16] = h0;
+        S.plo[h * 40 + l16] = f2bf(p0 - bf2f(h0));
+        if (NR == 32) {
+            S.phi[h * 40 + l16 + 16] = h1;
+            S.plo[h * 40 + l16 + 16] = f2bf(p1 - bf2f(h1));
+        }
+    }
+    cbar();
+    // ---- O[16][512] = O * corr + P . V ; warp w owns dims [64w, 64w+64) ----
+    {
+        const float c0 = S.cst[g], c1 = S.cst[g + 8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            acc[j][0] *= c0;
+            acc[j][1] *= c0;
+            acc[j][2] *= c1;
+            acc[j][3] *= c1;
+        }
+        for (int kp = 0; kp < NR; kp += 16) {
+            uint32_t ah[4], al[4];
+            ah[0] = lds32(S.phi + g * 40 + kp + 2 * t4);
+            ah[1] = lds32(S.phi + (g + 8) * 40 + kp + 2 * t4);
+            ah[2] = lds32(S.phi + g * 40 + kp + 8 + 2 * t4);
+            ah[3] = lds32(S.phi + (g + 8) * 40 + kp + 8 + 2 * t4);
+            al[0] = lds32(S.plo + g * 40 + kp + 2 * t4);
+            al[1] = lds32(S.plo + (g + 8) * 40 + kp + 2 * t4);
+            al[2] = lds32(S.plo + g * 40 + kp + 8 + 2 * t4);
+            al[3] = lds32(S.plo + (g + 8) * 40 + kp + 8 + 2 * t4);
+#pragma unroll
+            for (int np = 0; np < 4; ++np) {
+                const int n0 = warp * 64 + np * 16;
+                uint32_t r[4];
+                ldsm_x4_t(r, ck + (size_t)(kp + (lane & 15)) * MLA_CS + n0 + (lane >> 4) * 8);
+                mma_bf16(acc[2 * np], ah, r[0], r[1]);
+                mma_bf16(acc[2 * np], al, r[0], r[1]);
+                mma_bf16(acc[2 * np + 1], ah, r[2], r[3]);
+                mma_bf16(acc[2 * np + 1], al, r[2], r[3]);
+            }
+        }
+    }
+}
+
+__device__ void cons_attn_mla(Ctx& c, int l, const AttnItem& it) {
+    const Params& p = c.p;
+    const Layer& Ld = p.layers[l];
+    const int tid = ctid(), lane = tid & 31, warp = tid >> 5, g = lane >> 2, t4 = lane & 3;
+    const int b = it.b, t = it.g, m = b * p.T + t, pos = p.pos[b] + t;
+    const bool tail = it.u_hi == it.nch + 1;
+    MlaSmem S = mla_smem(c.stage());
+    cbar();
+    c.sk_src = nullptr;
+    // queries: [absorbed latent query (512) | roped rope query (64)] * scale, split hi/lo
+    const int qh = p.nope + p.rd;
+    for (int i = tid; i < MLA_H * MLA_D; i += NCT) {
+        const int h = i / MLA_D, e = i - h * MLA_D;
+        float v;
+        if (e < MLA_KL) {
+            v = __ldcg(Ld.qlat + (size_t)m * MLA_H * MLA_KL + h * MLA_KL + e);
+        } else {
+            const int r = e - MLA_KL, hr = MLA_RD / 2, ri = r < hr ? r : r - hr;
+            const float* qr = Ld.q + (size_t)m * MLA_H * qh + h * qh + p.nope;
+            const float2 cs = p.rope[(size_t)pos * p.rope_half + ri];
+            const float x0 = __ldcg(qr + ri), x1 = __ldcg(qr + ri + hr);
+            v = r < hr ? (x0 * cs.x - x1 * cs.y) : (x1 * cs.x + x0 * cs.y);
+        }
+        v *= p.attn_scale;
+        const uint16_t hi = f2bf(v);
+        S.qhi[h * MLA_QS + e] = hi;
+        S.qlo[h * MLA_QS + e] = f2bf(v - bf2f(hi));
+    }
+    if (tid < 16) {
+        S.mst[tid] = -INFINITY;
+        S.lst[tid] = 0.f;
+    }
+    if (tail) {
+        // the new positions 0..T-1 of this step; token t sees 0..t
+        for (int i = tid; i < 16 * MLA_D; i += NCT) {
+            const int r = i / MLA_D, e = i - r * MLA_D;
+            const uint16_t v = r <= t ? p.newlat[(size_t)(b * p.T + r) * MLA_D + e] : (uint16_t)0;
+            if (e < MLA_KL)
+                S.tc[r * MLA_CS + e] = v;
+            else
+                S.tr[r * MLA_RS + (e - MLA_KL)] = v;
+        }
+    }
+    cbar();
+    float acc[8][4];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+    for (int u = it.u_lo; u < it.u_hi; ++u) {
+        if (u < it.nch) {
+            const uint8_t* tile = c.dead ? nullptr : cons_wait(p, c.smem, c.ms, c.cr);
+            const int nvalid = min(MLA_CH, p.pos[b] - u * MLA_CH);
+            if (tile) {
+                mla_chunk(S, reinterpret_cast<const uint16_t*>(tile),
+                          reinterpret_cast<const uint16_t*>(tile + MLA_CH * MLA_CS * 2), MLA_CH, nvalid, acc);
+            } else {
+                cbar();
+                cbar();
+            }
+            cons_release(c.ms, c.cr);
+        } else {
+            mla_chunk(S, S.tc, S.tr, 16, t + 1, acc);
+        }
+    }
+    // partial: (max, sum) per head and the unnormalised O rows
+    const size_t base = ((size_t)m * p.s_max + it.s) * MLA_H;
+    float* po = p.part + base * (MLA_KL + 2);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const int dim = warp * 64 + j * 8 + 2 * t4;
+        float* r0 = po + (size_t)g * (MLA_KL + 2) + 2 + dim;
+        float* r1 = po + (size_t)(g + 8) * (MLA_KL + 2) + 2 + dim;
+        r0[0] = acc[j][0];
+        r0[1] = acc[j][1];
+        r1[0] = acc[j][2];
+        r1[1] = acc[j][3];
+    }
+    cbar();
+    if (tid < 16) {
+        po[(size_t)tid * (MLA_KL + 2)] = S.mst[tid];
+        po[(size_t)tid * (MLA_KL + 2) + 1] = S.lst[tid];
+    }
+    cbar();
+}
+
+// producer: bulk-load one MLA chunk (32 positions) into padded smem rows;
+// rows past the valid positions are filled from a zero buffer
+__device__ void prod_mla_chunk(Ctx& c, int l, int b, int u) {
+    const Params& p = c.p;
+    const int lane = threadIdx.x & 31;
+    const int nvalid = min(MLA_CH, p.pos[b] - u * MLA_CH);
+    const unsigned bytes = MLA_CH * (MLA_KL * 2 + MLA_RD * 2);
+    uint8_t* dst = nullptr;
+    unsigned long long dptr = 0;
+    if (lane == 0) {
+        dst = prod_begin(p, c.smem, c.ms, c.pr, bytes);
+        dptr = (unsigned long long)dst;
+    }
+    dptr = __shfl_sync(0xffffffffu, dptr, 0);
+    if (!dptr) {
+        c.dead = true;
+        return;
+    }
+    dst = reinterpret_cast<uint8_t*>(dptr);
+    const uint16_t* pg = page_ptr(p, (p.kv_pool + (size_t)l * p.kv_layer_elems), b, (u * MLA_CH) / PAGE);
+    const int r0 = (u * MLA_CH) % PAGE;
+    // lane r copies latent row r and rope row r
+    const int r = lane;
+    const uint16_t* srcc = r < nvalid ? pg + (size_t)(r0 + r) * MLA_KL : p.zeros;
+    const uint16_t* srcr = r < nvalid ? pg + (size_t)PAGE * MLA_KL + (size_t)(r0 + r) * MLA_RD : p.zeros;
+    bulk_g2s(dst + (size_t)r * MLA_CS * 2, srcc, MLA_KL * 2, &c.ms.full[c.pr.slot]);
+    bulk_g2s(dst + (size_t)MLA_CH * MLA_CS * 2 + (size_t)r * MLA_RS * 2, srcr, MLA_RD * 2, &c.ms.full[c.pr.slot]);
+    __syncwarp();
+    ++c.issued;
+    prod_next(c.pr);
+}
+
+__device__ void prod_gqa_chunk(Ctx& c, int l, int b, int g, int u) {
+    const Params& p = c.p;
+    const int hd = p.hd;
+    const int nvalid = min(GQA_CH, p.pos[b] - u * GQA_CH);
+    const unsigned bytes = 2u * nvalid * hd * 2u;
+    int ok = 1;
+    if ((threadIdx.x & 31) == 0) {
+        uint8_t* dst = prod_begin(p, c.smem, c.ms, c.pr, bytes);
+        if (dst) {
+            const uint16_t* pg = page_ptr(p, (p.kv_pool + (size_t)l * p.kv_layer_elems), b, u) + (size_t)g * 2 * PAGE * hd;
+            bulk_g2s(dst, pg, nvalid * hd * 2u, &c.ms.full[c.pr.slot]);
+            bulk_g2s(dst + (size_t)GQA_CH * hd * 2, pg + (size_t)PAGE * hd, nvalid * hd * 2u, &c.ms.full[c.pr.slot]);
+        } else {
+            ok = 0;
+        }
+    }
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (!ok) {
+        c.dead = true;
+        return;
+    }
+    ++c.issued;
+    prod_next(c.pr);
+}
+
+template <bool PROD>
+__device__ void stage_attn(Ctx& c, int l, const Deps& deps) {
+    const Params& p = c.p;
+    const int n = attn_items(p);
+    int lo, hi;
+    my_range(p, n, c.off, lo, hi);
+    c.advance(n);
+    if (lo >= hi) return;
+    if constexpr (PROD) {
+        for (int i = lo; i < hi && !c.dead; ++i) {
+            const AttnItem it = attn_item(p, i);
+            for (int u = it.u_lo; u < min(it.u_hi, it.nch) && !c.dead; ++u) {
+                if (p.attn == 0)
+                    prod_gqa_chunk(c, l, it.b, it.g, u);
+                else
+                    prod_mla_chunk(c, l, it.b, u);
+            }
+        }
+    } else {
+        cwait(c, deps, 0x600u | (unsigned)(l << 16));
+        for (int i = lo; i < hi; ++i) {
+            const AttnItem it = attn_item(p, i);
+            if (p.attn == 0) {
+                if (p.hd == 128)
+                    cons_attn_gqa<4>(c, l, it);
+                else
+                    cons_attn_gqa<2>(c, l, it);
+            } else {
+                cons_attn_mla(c, l, it);
+            }
+        }
+        csignal(c, l, C_ATTN, (unsigned)(hi - lo));
+    }
+}
+
+// ======================================================== combine ====
+// GQA: item (token, q head) -> o[m][h*hd ...]
+// MLA: item (token, head, 128-dim chunk) -> olat[m][h*512 ...]
+__device__ int comb_items(const Params& p) { return p.attn == 0 ? p.M * p.Hq : p.M * MLA_H * 4; }
+
+__device__ void cons_comb(Ctx& c, int l, int i) {
+    const Params& p = c.p;
+    const Layer& Ld = p.layers[l];
+    const int tid = ctid();
+    cbar();
+    if (p.attn == 0) {
+        const int Gq = p.Hq / p.Hkv, Q = p.T * Gq, hd = p.hd, W = 2 + hd;
+        const int m = i / p.Hq, h = i - m * p.Hq, b = m / p.T, t = m - b * p.T;
+        const int g = h / Gq, qr = t * Gq + (h - g * Gq);
+        const int units = nch_of(p, b, GQA_CH) + 1, tg = gqa_target(p), S = units < tg ? units : tg;
+        const float* base = p.part + (((size_t)b * p.Hkv + g) * p.s_max) * Q * W + (size_t)qr * W;
+        if (tid == 0) {
+            float mx = -INFINITY;
+            for (int s = 0; s < S; ++s) mx = fmaxf(mx, __ldcg(base + (size_t)s * Q * W));
+            float L = 0.f;
+            for (int s = 0; s < S; ++s) {
+                const float ms = __ldcg(base + (size_t)s * Q * W);
+                const float w = ms == -INFINITY ? 0.f : expf(ms - mx);
+                c.ms.cw[s] = w;
+                L += w * __ldcg(base + (size_t)s * Q * W + 1);
+            }
+            c.ms.cw[255] = 1.0f / L;
+        }
+        cbar();
+        for (int e = tid; e < hd; e += NCT) {
+            float v = 0.f;
+            for (int s = 0; s < S; ++s) v = fmaf(c.ms.cw[s], __ldcg(base + (size_t)s * Q * W + 2 + e), v);
+            Ld.o[(size_t)m * p.Hq * hd + h * hd + e] = v * c.ms.cw[255];
+        }
+    } else {
+        const int W = MLA_KL + 2;
+        const int m = i / (MLA_H * 4), r = i - m * MLA_H * 4, h = r >> 2, dc = r & 3;
+        const int b = m / p.T;
+        const int units = nch_of(p, b, MLA_CH) + 1, tg = mla_target(p), S = units < tg ? units : tg;
+        const float* base = p.part + ((size_t)m * p.s_max * MLA_H + h) * W;
+        const size_t sstride = (size_t)MLA_H * W;
+        if (tid == 0) {
+            float mx = -INFINITY;
+            for (int s = 0; s < S; ++s) mx = fmaxf(mx, __ldcg(base + s * sstride));
+            float L = 0.f;
+            for (int s = 0; s < S; ++s) {
+                const float ms = __ldcg(base + s * sstride);
+                const float w = ms == -INFINITY ? 0.f : expf(ms - mx);
+                c.ms.cw[s] = w;
+                L += w * __ldcg(base + s * sstride + 1);
+            }
+            c.ms.cw[255] = 1.0f / L;
+        }
+        cbar();
+        for (int e = tid; e < 128; e += NCT) {
+            const int dim = dc * 128 + e;
+            float v = 0.f;
+            for (int s = 0; s < S; ++s) v = fmaf(c.ms.cw[s], __ldcg(base + s * sstride + 2 + dim), v);
+            Ld.olat[(size_t)m * MLA_H * MLA_KL + h * MLA_KL + dim] = v * c.ms.cw[255];
+        }
+    }
+}
+
+template <bool PROD>
+__device__ void stage_comb(Ctx& c, int l, const Deps& deps) {
+    const int n = comb_items(c.p);
+    int lo, hi;
+    my_range(c.p, n, c.off, lo, hi);
+    c.advance(n);
+    if constexpr (!PROD) {
+        if (lo >= hi) return;
+        cwait(c, deps, 0x700u | (unsigned)(l << 16));
+        for (int i = lo; i < hi; ++i) cons_comb(c, l, i);
+        csignal(c, l, C_COMB, (unsigned)(hi - lo));
+    }
+}
+
+// ========================================================= MLA append ====
+// item = token: latent = RMSNorm(kv_a latent part) * gain, k_rope = RoPE(kv_a
+// rope part); both rounded to bf16, written to the page and to newlat.
+template <bool PROD>
+__device__ void stage_append(Ctx& c, int l, const Deps& deps) {
+    const Params& p = c.p;
+    const int n = p.M;
+    int lo, hi;
+    my_range(p, n, c.off, lo, hi);
+    c.advance(n);
+    if constexpr (!PROD) {
+        if (lo >= hi) return;
+        cwait(c, deps, 0x800u | (unsigned)(l << 16));
+        const Layer& Ld = p.layers[l];
+        const int tid = ctid(), lane = tid & 31, warp = tid >> 5;
+        for (int m = lo; m < hi; ++m) {
+            const int b = m / p.T, t = m - b * p.T, pos = p.pos[b] + t;
+            const float* a = Ld.a + (size_t)m * Ld.a_stride + p.ql;
+            cbar();
+            if (warp == 0) {
+                float ss = 0.f;
+                for (int e = lane; e < MLA_KL; e += 32) {
+                    const float v = __ldcg(a + e);
+                    ss = fmaf(v, v, ss);
+                }
+#pragma unroll
+                for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+                if (lane == 0) c.ms.rms[0] = 1.0f / sqrtf(ss / (float)MLA_KL + p.eps);
+            }
+            cbar();
+            uint16_t* pg = const_cast<uint16_t*>(page_ptr(p, p.kv_pool + (size_t)l * p.kv_layer_elems, b, pos / PAGE));
+            const int pr = pos % PAGE;
+            uint16_t* nl = p.newlat + (size_t)m * MLA_D;
+            for (int e = tid; e < MLA_D; e += NCT) {
+                uint16_t v;
+                if (e < MLA_KL) {
+                    v = f2bf(__ldcg(a + e) * c.ms.rms[0] * bf2f(Ld.kv_norm[e]));
+                    pg[(size_t)pr * MLA_KL + e] = v;
+                } else {
+                    const int r = e - MLA_KL, hr = MLA_RD / 2, ri = r < hr ? r : r - hr;
+                    const float2 cs = p.rope[(size_t)pos * p.rope_half + ri];
+                    const float x0 = __ldcg(a + MLA_KL + ri), x1 = __ldcg(a + MLA_KL + ri + hr);
+                    v = f2bf(r < hr ? (x0 * cs.x - x1 * cs.y) : (x1 * cs.x + x0 * cs.y));
+                    pg[(size_t)PAGE * MLA_KL + (size_t)pr * MLA_RD + r] = v;
+                }
+                nl[e] = v;
+            }
+        }
+        csignal(c, l, C_APP, (unsigned)(hi - lo));
+    }
+}
+
+// ===================================================== residual carry ====
+// (only when the output projection is split over K: x_{l+1} += x_l)
+template <bool PROD>
+__device__ void stage_carry(Ctx& c, int l, const Deps& deps) {
+    const Params& p = c.p;
+    const int chunk = 2048;
+    const int n = (p.M * p.d + chunk - 1) / chunk;
+    int lo, hi;
+    my_range(p, n, c.off, lo, hi);
+    c.advance(n);
+    if constexpr (!PROD) {
+        if (lo >= hi) return;
+        cwait(c, deps, 0x900u | (unsigned)(l << 16));
+        const Layer& Ld = p.layers[l];
+        const int total = p.M * p.d;
+        for (int i = lo * chunk + ctid(); i < min(hi * chunk, total); i += NCT) {
+            const int m = i / p.d, e = i - m * p.d;
+            atomicAdd(Ld.xn + (size_t)m * p.d + e, __ldcg(Ld.x + (size_t)m * p.d + e));
+        }
+        csignal(c, l, C_CARRY, (unsigned)(hi - lo));
+    }
+}
+
+// ===================================================== head / verify ====
+template <bool PROD>
+__device__ void stage_argmax(Ctx& c, const Deps& deps) {
+    const Params& p = c.p;
+    const int n = p.M;
+    int lo, hi;
+    my_range(p, n, c.off, lo, hi);
+    c.advance(n);
+    if constexpr (!PROD) {
+        if (lo >= hi) return;
+        cwait(c, deps, 0xa00u);
+        const int tid = ctid(), lane = tid & 31, warp = tid >> 5;
+        float* bv = c.red();
+        int* bi = reinterpret_cast<int*>(c.red() + NCW);
+        for (int m = lo; m < hi; ++m) {
+            const float* lg = p.logits + (size_t)m * p.V;
+            float v = -INFINITY;
+            int id = 0x7fffffff;
+            for (int e = tid; e < p.V; e += NCT) {
+                const float x = __ldcg(lg + e);
+                if (x > v || (x == v && e < id)) {
+                    v = x;
+                    id = e;
+                }
+            }
+#pragma unroll
+            for (int o = 16; o; o >>= 1) {
+                const float ov = __shfl_xor_sync(0xffffffffu, v, o);
+                const int oi = __shfl_xor_sync(0xffffffffu, id, o);
+                if (ov > v || (ov == v && oi < id)) {
+                    v = ov;
+                    id = oi;
+                }
+            }
+            cbar();
+            if (lane == 0) {
+                bv[warp] = v;
+                bi[warp] = id;
+            }
+            cbar();
+            if (tid == 0) {
+                for (int w = 1; w < NCW; ++w)
+                    if (bv[w] > v || (bv[w] == v && bi[w] < id)) {
+                        v = bv[w];
+                        id = bi[w];
+                    }
+                p.amax[m] = id;
+            }
+        }
+        csignal(c, p.L, C_AMAX, (unsigned)(hi - lo));
+    }
+}
+
+// ====================================================== init (consumers) ====
+__device__ bool init_phase(Ctx& c) {
+    const Params& p = c.p;
+    const int tid = ctid();
+    // every CTA checks the step's inputs itself (all reach the same verdict)
+    if (tid == 0) {
+        int bad = 0;
+        for (int m = 0; m < p.M; ++m)
+            if (p.tokens[m] < 0 || p.tokens[m] >= p.V) bad = 1;
+        for (int b = 0; b < p.B; ++b)
+            if (p.pos[b] < 0 || p.pos[b] + p.T > p.kv_cap || p.pos[b] + p.T > p.rope_npos) bad = 1;
+        c.ms.abort = bad;
+        if (bad && blockIdx.x == 0) raise_status(p, ST_INVALID, 0x10u);
+    }
+    cbar();
+    if (c.ms.abort) {
+        c.dead = true;
+        return false;
+    }
+    const size_t gtid = (size_t)blockIdx.x * NCT + tid, gstride = (size_t)p.G * NCT;
+    // counters of the other parity are used by the next step: clear them now
+    unsigned* other = p.ctr + (size_t)(p.parity ^ 1) * (p.L + 1) * NCTR;
+    for (size_t i = gtid; i < (size_t)(p.L + 1) * NCTR; i += gstride) other[i] = 0u;
+    for (int z = 0; z < p.nz; ++z)
+        for (size_t i = gtid; i < (size_t)p.zn[z]; i += gstride) p.zptr[z][i] = 0.f;
+    float* x0 = p.layers[0].x;
+    for (size_t i = gtid; i < (size_t)p.M * p.d; i += gstride) {
+        const int m = (int)(i / p.d), e = (int)(i - (size_t)m * p.d);
+        x0[i] = bf2f(p.embed[(size_t)p.tokens[m] * p.d + e]);
+    }
+    csignal(c, p.L, C_INIT, 1u);
+    return !c.dead;
+}
+
+__device__ bool prod_check(const Params& p) {
+    for (int b = 0; b < p.B; ++b)
+        if (p.pos[b] < 0 || p.pos[b] + p.T > p.kv_cap || p.pos[b] + p.T > p.rope_npos) return false;
+    for (int m = 0; m < p.M; ++m)
+        if (p.tokens[m] < 0 || p.tokens[m] >= p.V) return false;
+    return true;
+}
+
+// ============================================================ program ====
+template <bool PROD>
+__device__ void program(Ctx& c) {
+    const Params& p = c.p;
+    if constexpr (PROD) {
+        if (!prod_check(p)) return;
+    } else {
+        if (!init_phase(c)) return;
+    }
+    int n_down = 0, n_shdown = 0, n_carry = 0;
+    for (int l = 0; l < p.L; ++l) {
+        if constexpr (PROD) {
+            if (c.dead) return;
+        }
+        const Layer& Ld = p.layers[l];
+        Deps prev;
+        if (l == 0) {
+            prev = deps1(p.L, C_INIT, (unsigned)p.G);
+        } else {
+            prev.n = 3;
+            prev.d[0] = {l - 1, C_DOWN, (unsigned)n_down};
+            prev.d[1] = {l - 1, C_SHDOWN, (unsigned)n_shdown};
+            prev.d[2] = {l - 1, C_CARRY, (unsigned)n_carry};
+        }
+        const unsigned nA = (unsigned)gemv_items(Ld.g[G_A]);
+        if (p.attn == 1) {
+            stage_gemv<PROD>(c, l, Ld.g[G_A], prev, C_A);
+            stage_gemv<PROD>(c, l, Ld.g[G_QB], deps1(l, C_A, nA), C_QB);
+            stage_append<PROD>(c, l, deps1(l, C_A, nA));
+            stage_gemv<PROD>(c, l, Ld.g[G_QLAT], deps1(l, C_QB, (unsigned)gemv_items(Ld.g[G_QB])), C_QLAT);
+            Deps da;
+            da.n = 2;
+            da.d[0] = {l, C_QLAT, (unsigned)gemv_items(Ld.g[G_QLAT])};
+            da.d[1] = {l, C_APP, (unsigned)p.M};
+            stage_attn<PROD>(c, l, da);
+            stage_comb<PROD>(c, l, deps1(l, C_ATTN, (unsigned)attn_items(p)));
+            stage_gemv<PROD>(c, l, Ld.g[G_UV], deps1(l, C_COMB, (unsigned)comb_items(p)), C_UV);
+            stage_gemv<PROD>(c, l, Ld.g[G_O], deps1(l, C_UV, (unsigned)gemv_items(Ld.g[G_UV])), C_O);
+        } else {
+            stage_gemv<PROD>(c, l, Ld.g[G_A], prev, C_A);
+            stage_attn<PROD>(c, l, deps1(l, C_A, nA));
+            stage_comb<PROD>(c, l, deps1(l, C_ATTN, (unsigned)attn_items(p)));
+            stage_gemv<PROD>(c, l, Ld.g[G_O], deps1(l, C_COMB, (unsigned)comb_items(p)), C_O);
+        }
+        const unsigned nO = (unsigned)gemv_items(Ld.g[G_O]);
+        if (p.E > 0) stage_gemv<PROD>(c, l, Ld.g[G_ROUTER], deps1(l, C_O, nO), C_ROUTER);
+        if (p.has_sh) stage_gemv<PROD>(c, l, Ld.g[G_SHGU], deps1(l, C_O, nO), C_SHGU);
+        n_carry = 0;
+        if (p.carry) {
+            stage_carry<PROD>(c, l, deps1(l, C_O, nO));
+            n_carry = (p.M * p.d + 2047) / 2048;
+        }
+        n_shdown = 0;
+        if (p.has_sh) {
+            stage_gemv<PROD>(c, l, Ld.g[G_SHDOWN], deps1(l, C_SHGU, (unsigned)gemv_items(Ld.g[G_SHGU])), C_SHDOWN);
+            n_shdown = gemv_items(Ld.g[G_SHDOWN]);
+        }
+        n_down = 0;
+        if (p.E > 0) {
+            if (!route<PROD>(c, l) && PROD) return;
+            stage_experts<PROD>(c, l, Ld.g[G_GU], false);
+            stage_experts<PROD>(c, l, Ld.g[G_DOWN], true);
+            n_down = (PROD ? c.ms.p_nslots : c.ms.n_slots) * gemv_items(Ld.g[G_DOWN]);
+        }
+    }
+    if constexpr (PROD) {
+        if (c.dead) return;
+    }
+    Deps last;
+    last.n = 3;
+    last.d[0] = {p.L - 1, C_DOWN, (unsigned)n_down};
+    last.d[1] = {p.L - 1, C_SHDOWN, (unsigned)n_shdown};
+    last.d[2] = {p.L - 1, C_CARRY, (unsigned)n_carry};
+    stage_gemv<PROD>(c, p.L, p.lm, last, C_LM);
+    if (p.accept) {
+        stage_argmax<PROD>(c, deps1(p.L, C_LM, (unsigned)gemv_items(p.lm)));
+        if constexpr (!PROD) {
+            if (blockIdx.x == 0) {
+                cwait(c, deps1(p.L, C_AMAX, (unsigned)p.M), 0xb00u);
+                const int b = ctid();
+                if (b < p.B && !c.dead) {
+                    int a = 0;
+                    while (a < p.T - 1 && __ldcg(p.amax + b * p.T + a) == p.tokens[b * p.T + a + 1]) ++a;
+                    p.accept[b] = a + 1;
+                }
+            }
+        }
+    }
+}
+
+// producer epilogue after an abort: wait (bounded) for the bulk copies it
+// issued so none lands in shared memory after the CTA has exited
+__device__ void prod_drain(Ctx& c) {
+    if ((threadIdx.x & 31) != 0) return;
+    // slots filled but possibly not yet consumed are the last NSLOT ones
+    PRing r = c.pr;
+    const int n = c.issued < NSLOT ? c.issued : NSLOT;
+    for (int i = 0; i < n; ++i) {
+        if (r.slot == 0) {
+            r.slot = NSLOT - 1;
+            r.phase ^= 1u;
+        } else {
+            --r.slot;
+        }
+        // the fill of this slot completed phase `r.phase`; wait for it
+        const long long t0 = gtimer();
+        while (!mbar_test(&c.ms.full[r.slot], r.phase)) {
+            if (gtimer() - t0 > c.p.timeout_ns) break;
+        }
+    }
+}
+
+__global__ void __launch_bounds__(NTHREADS, 1) megakernel(const __grid_constant__ Params p) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    Misc& ms = *reinterpret_cast<Misc*>(smem + SMEM_MISC);
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < NSLOT; ++i) {
+            mbar_init(&ms.full[i], 1);
+            mbar_init(&ms.empty[i], NCW);
+        }
+        // a step that failed earlier leaves the abort flag set until the host
+        // resets it (mk_step_status): refuse to run on stale state
+        ms.abort = ld_relaxed(&p.status[1]) ? 1 : 0;
+        ms.n_slots = ms.p_nslots = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    if (ms.abort) return;
+    Ctx c(p, smem);
+    if (threadIdx.x >= NCT) {
+        program<true>(c);
+        if (c.dead) prod_drain(c);
+    } else {
+        program<false>(c);
+    }
+}
+
+}  // namespace mk
