@@ -158,45 +158,46 @@ def allmax(ws, v):
     return float(t.item())
 
 
-def cpu_baseline(cfg, B, T, ctx, sample_layers=2):
+def cpu_baseline(cfg, B, T, ctx, sample_layers=23, steps=1, warmup=0):
     """Time the oracle (single thread, fp32 accumulation as the reference step
-    is defined) on `sample_layers` layers of the workload; scale to a step."""
+    is defined) on `sample_layers` layers of the workload and scale to the
+    full layer count. Weights and cache are generated before timing; each
+    timed step decodes the next position."""
     import oracle
     import synth
-    sub = configs.scaled(cfg, n_layers=sample_layers)
+    sub = configs.scaled(cfg, n_layers=min(sample_layers, cfg["n_layers"]))
+    nl = sub["n_layers"]
     m = oracle.Model(sub)
-    kv = oracle.KV(m, B, ctx + T + 1)
-    # inputs (weights, cache) are generated before timing; only the step is timed
+    kv = oracle.KV(m, B, ctx + (steps + warmup + 1) * T + 1)
     kv.prefill(cfg["seed"], ctx)
     tok = synth.tokens(cfg["seed"], 0, B, T, cfg["vocab"])
-    oracle.decode(m, kv, tok, [ctx] * B, precision=32)  # touches (generates) every tensor the step uses
-    kv2 = oracle.KV(m, B, ctx + T + 1)
-    kv2.prefill(cfg["seed"], ctx)
-    t0 = time.perf_counter()
-    oracle.decode(m, kv2, tok, [ctx] * B, precision=32)
-    dt = time.perf_counter() - t0
-    step_s = dt * cfg["n_layers"] / sample_layers
+    # generate every tensor the step touches (untimed), then time whole steps
+    for _ in range(max(1, warmup)):
+        oracle.decode(m, kv, tok, [ctx] * B, precision=32)
+    times = []
+    for i in range(steps):
+        t0 = time.perf_counter()
+        oracle.decode(m, kv, tok, [ctx + (i + 1) * T] * B, precision=32)
+        times.append(time.perf_counter() - t0)
+    dt = statistics.median(times)
+    step_s = dt * cfg["n_layers"] / nl
     return {"value": B * T / step_s, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"one decode step of {sample_layers} of {cfg['n_layers']} layers (batch {B}, ctx {ctx}), "
-                      f"scaled x{cfg['n_layers'] / sample_layers:g}; {dt:.1f} s measured",
+            "sample": f"decode step of {nl} of {cfg['n_layers']} layers (batch {B}, ctx {ctx}) timed "
+                      f"{steps}x, median {dt:.2f} s, scaled x{cfg['n_layers'] / nl:g}",
             "seconds_per_step": step_s}
 
 
 def run_reference(args, cfg, B, T, ctx, ws, rank):
     if rank != 0:
         return
-    vals = []
-    for _ in range(args.warmup if args.warmup < 1 else 1):
-        pass
-    for _ in range(max(1, args.steps)):
-        vals.append(cpu_baseline(cfg, B, T, ctx, sample_layers=1))
-    v = statistics.median([x["value"] for x in vals])
+    cb = cpu_baseline(cfg, B, T, ctx, sample_layers=8, steps=max(1, args.steps), warmup=1)
+    v = cb["value"]
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 / v * B * T,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic",
             "config": {"workload": workload_name(cfg, B, T, ctx), "batch": B, "tokens_per_seq": T, "ctx": ctx},
-            "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": vals[0]["sample"]},
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": cb["sample"]},
             "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 

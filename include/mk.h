@@ -166,6 +166,16 @@ int mk_debug_routing(mk_model* m, int32_t* idx_out, float* w_out, void* stream);
 
 int mk_model_info(const mk_model* m, mk_info* out);
 
+/* Stage trace of the last step, recorded when the environment variable
+ * MK_TRACE=1 was set at mk_load_weights. For each CTA (grid_ctas of them)
+ * up to 8192 records of 32 bytes: {uint32 code = stage << 16 | layer,
+ * uint32 items, int64 t_wait, int64 t_ready, int64 t_end} (device
+ * %globaltimer ns: the CTA started waiting for the stage's inputs, they were
+ * ready, its items were done). recs_out: host buffer of grid_ctas*8192*32
+ * bytes; counts_out: host int32 [grid_ctas] records written. Synchronises
+ * `stream`. Errors: STATE when tracing is off. */
+int mk_trace_read(mk_model* m, void* recs_out, int64_t bytes, int32_t* counts_out, void* stream);
+
 /* Free a model or a KV cache (NULL is a no-op). A KV cache must be freed
  * before its model. */
 void mk_free(void* handle);

@@ -19,8 +19,9 @@ HEADER = os.path.join(_ROOT, "include", "mk.h")
 OK, ERR_INVALID_ARG, ERR_OOM, ERR_CUDA, ERR_UNSUPPORTED, ERR_TIMEOUT, ERR_STATE = 0, -1, -2, -3, -4, -5, -6
 ATTN_GQA, ATTN_MLA = 0, 1
 EXPORTS = ("mk_load_weights", "mk_alloc_kv", "mk_kv_set_block_table", "mk_kv_pages_per_seq", "mk_kv_write",
-           "mk_kv_read", "mk_decode_step", "mk_step_status", "mk_debug_routing", "mk_model_info", "mk_free",
-           "mk_last_error")
+           "mk_kv_read", "mk_decode_step", "mk_step_status", "mk_debug_routing", "mk_model_info", "mk_trace_read",
+           "mk_free", "mk_last_error")
+TRACE_CAP = 8192
 
 
 def build_cmds() -> list:
@@ -77,11 +78,12 @@ def lib():
         L.mk_step_status.argtypes = [P, P]
         L.mk_debug_routing.argtypes = [P, P, P, P]
         L.mk_model_info.argtypes = [P, ctypes.POINTER(Info)]
+        L.mk_trace_read.argtypes = [P, P, ctypes.c_int64, P, P]
         L.mk_free.argtypes = [P]
         L.mk_free.restype = None
         L.mk_last_error.restype = ctypes.c_char_p
         for f in ("mk_load_weights", "mk_alloc_kv", "mk_kv_set_block_table", "mk_kv_write", "mk_kv_read",
-                  "mk_decode_step", "mk_step_status", "mk_debug_routing", "mk_model_info"):
+                  "mk_decode_step", "mk_step_status", "mk_debug_routing", "mk_model_info", "mk_trace_read"):
             getattr(L, f).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -142,6 +144,17 @@ class Model:
         w = np.zeros((L, M, k), dtype=np.float32)
         _check(lib().mk_debug_routing(self.h, idx.ctypes.data, w.ctypes.data, _stream(stream)))
         return idx, w
+
+    def trace(self, stream=None):
+        """Stage trace of the last step (needs MK_TRACE=1 at load): structured numpy array per record."""
+        import numpy as np
+        G = self.info().grid_ctas
+        dt = np.dtype([("code", "<u4"), ("n", "<u4"), ("t_wait", "<i8"), ("t_ready", "<i8"), ("t_end", "<i8")])
+        recs = np.zeros(G * TRACE_CAP, dtype=dt)
+        counts = np.zeros(G, dtype=np.int32)
+        _check(lib().mk_trace_read(self.h, recs.ctypes.data, recs.nbytes, counts.ctypes.data, _stream(stream)))
+        recs = recs.reshape(G, TRACE_CAP)
+        return [recs[g, :counts[g]] for g in range(G)]
 
     def close(self):
         if getattr(self, "h", None):

@@ -28,10 +28,16 @@ namespace mk {
 constexpr int NCW = 8;                    // consumer warps
 constexpr int NCT = NCW * 32;             // consumer threads
 constexpr int NTHREADS = NCT + 32;        // + one producer warp
-constexpr int NSLOT = 4;                  // ring slots
+#ifndef MK_NSLOT
+#define MK_NSLOT 4
+#endif
+#ifndef MK_STAGE_BYTES
+#define MK_STAGE_BYTES 65536
+#endif
+constexpr int NSLOT = MK_NSLOT;           // ring slots
 constexpr int SLOT_BYTES = 37888;         // one MLA chunk (32 padded latent rows + rope rows)
 constexpr int TILE_MAX = 32768;           // GEMV weight tile
-constexpr int STAGE_BYTES = 65536;        // activation / query staging
+constexpr int STAGE_BYTES = MK_STAGE_BYTES;  // activation / query staging
 constexpr int STAGE_FLOATS = STAGE_BYTES / 4;
 constexpr int RED_FLOATS = 1024;
 constexpr int MT = 4;                     // tokens per register group in the GEMV
@@ -110,7 +116,8 @@ struct Params {
     int kv_cap, kv_batch;           // positions per sequence, sequences in the cache
     const uint16_t* zeros;          // >= 2 KB of zero bytes (fills unused chunk rows)
     uint16_t* newlat;               // MLA new latents [MAX_M][576] bf16
-    float* part;                    // attention partials
+    float* part;                    // attention partials: unnormalised O rows
+    float* part_ml;                 // attention partials: (running max, sum) per row
     int s_max;
     const int* tokens;
     const int* pos;
@@ -127,6 +134,18 @@ struct Params {
     long long timeout_ns;
     int* dbg_idx;
     float* dbg_w;
+    struct TraceRec* trace;         // optional stage trace [G][trace_cap]
+    unsigned* trace_n;              // records written per CTA
+    int trace_cap;
+    int trace_items;                // also one record per GEMV work item
+};
+
+// one traced stage of one CTA (consumer side): when the CTA started waiting
+// for the stage's inputs, when they were ready, when its items were done
+struct TraceRec {
+    unsigned code;  // stage << 16 | layer
+    unsigned n;     // items this CTA processed
+    long long t_wait, t_ready, t_end;
 };
 
 // ----------------------------------------------------------- smem layout ----
@@ -143,12 +162,15 @@ struct Misc {
     uint8_t ridx[MAX_M][MAX_K];
     float rw[MAX_M][MAX_K];
     float cw[256];                  // combine weights
+    float bred[NCW];                // block reductions
 };
 constexpr int SMEM_RING = 0;
 constexpr int SMEM_STAGE = NSLOT * SLOT_BYTES;
 constexpr int SMEM_RED = SMEM_STAGE + STAGE_BYTES;
 constexpr int SMEM_MISC = SMEM_RED + RED_FLOATS * 4;
-constexpr int SMEM_TOTAL = SMEM_MISC + (int)sizeof(Misc);
+constexpr int SMEM_CTX = (SMEM_MISC + (int)sizeof(Misc) + 15) & ~15;
+constexpr int CTX_BYTES = 128;  // per warp (checked against sizeof(Ctx))
+constexpr int SMEM_TOTAL = SMEM_CTX + (NCW + 1) * CTX_BYTES;
 
 // ------------------------------------------------------------------ PTX ----
 __device__ __forceinline__ uint32_t su32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -188,10 +210,26 @@ __device__ __forceinline__ bool mbar_test(unsigned long long* b, unsigned parity
         : "memory");
     return ok != 0;
 }
+// streamed data (weights, cached KV) is read once per step: load it with an
+// evict-first L2 policy so it does not push code and activations out of L2
+__device__ __forceinline__ unsigned long long l2_evict_first() {
+    unsigned long long pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+__device__ __forceinline__ void bulk_g2s_pol(void* dst, const void* src, unsigned bytes, unsigned long long* bar,
+                                             unsigned long long pol) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+            su32(dst)),
+        "l"(src), "r"(bytes), "r"(su32(bar)), "l"(pol)
+        : "memory");
+}
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, unsigned bytes, unsigned long long* bar) {
     asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(su32(dst)),
-        "l"(src), "r"(bytes), "r"(su32(bar))
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+            su32(dst)),
+        "l"(src), "r"(bytes), "r"(su32(bar)), "l"(l2_evict_first())
         : "memory");
 }
 __device__ __forceinline__ void cbar() { asm volatile("bar.sync 1, %0;" ::"n"(NCT) : "memory"); }
@@ -348,11 +386,17 @@ __device__ __forceinline__ uint8_t* prod_begin(const Params& p, uint8_t* smem, M
     mbar_expect_tx(&ms.full[r.slot], bytes);
     return smem + SMEM_RING + r.slot * SLOT_BYTES;
 }
+// ring states are shared by the lanes of a warp (they live in shared memory):
+// every lane reads the old value before any lane writes the new one
 __device__ __forceinline__ void prod_next(PRing& r) {
-    if (++r.slot == NSLOT) {
-        r.slot = 0;
-        r.phase ^= 1u;
+    PRing n = r;
+    if (++n.slot == NSLOT) {
+        n.slot = 0;
+        n.phase ^= 1u;
     }
+    __syncwarp();
+    r = n;
+    __syncwarp();
 }
 
 // consumer ring state (identical in every consumer thread)
@@ -360,6 +404,7 @@ struct CRing {
     unsigned slot, phase;
 };
 __device__ __forceinline__ const uint8_t* cons_wait(const Params& p, uint8_t* smem, Misc& ms, CRing& r) {
+    if (mbar_test(&ms.full[r.slot], r.phase)) return smem + SMEM_RING + r.slot * SLOT_BYTES;  // fast path
     if (!mbar_wait(p, &ms.full[r.slot], r.phase, 0x200u)) {
         ms.abort = 1;
         return nullptr;
@@ -367,12 +412,16 @@ __device__ __forceinline__ const uint8_t* cons_wait(const Params& p, uint8_t* sm
     return smem + SMEM_RING + r.slot * SLOT_BYTES;
 }
 __device__ __forceinline__ void cons_release(Misc& ms, CRing& r) {
+    CRing n = r;
     __syncwarp();
-    if ((threadIdx.x & 31) == 0) mbar_arrive(&ms.empty[r.slot]);
-    if (++r.slot == NSLOT) {
-        r.slot = 0;
-        r.phase ^= 1u;
+    if ((threadIdx.x & 31) == 0) mbar_arrive(&ms.empty[n.slot]);
+    if (++n.slot == NSLOT) {
+        n.slot = 0;
+        n.phase ^= 1u;
     }
+    __syncwarp();
+    r = n;
+    __syncwarp();
 }
 
 }  // namespace mk

@@ -325,9 +325,13 @@ int mk_load_weights(const mk_config* cfg, const mk_weight* table, int32_t n, voi
     const size_t s_rlog = D.E ? stake((size_t)L * Mx * D.E * 4) : 0;
     const size_t s_gu = D.E ? stake((size_t)L * nsl * Mx * 2 * D.ffn * 4) : 0;
     const size_t s_shgu = D.sh ? stake((size_t)L * Mx * 2 * D.sffn * 4) : 0;
-    const size_t part_floats = D.gqa ? (size_t)cfg->max_batch * D.Hkv * m->G * Q8 * (D.hd + 2)
-                                     : (size_t)Mx * m->G * mk::MLA_H * (mk::MLA_KL + 2);
-    const size_t s_part = stake(part_floats * 4);
+    const size_t part_rows = D.gqa ? (size_t)cfg->max_batch * D.Hkv * m->G * Q8 : (size_t)Mx * m->G * mk::MLA_H;
+    const size_t s_part = stake(part_rows * (D.gqa ? D.hd : mk::MLA_KL) * 4);
+    const size_t s_part_ml = stake(part_rows * 2 * 4);
+    const int trace_cap = 8192;
+    const bool tracing = getenv("MK_TRACE") && atoi(getenv("MK_TRACE")) > 0;
+    const size_t s_trace = tracing ? stake((size_t)m->G * trace_cap * sizeof(mk::TraceRec)) : 0;
+    const size_t s_trace_n = tracing ? stake((size_t)m->G * 4) : 0;
     const size_t s_newlat = stake(Mx * mk::MLA_D * 2);
     const size_t s_amax = stake(Mx * 4);
     const size_t s_zero = stake(4096);
@@ -528,7 +532,14 @@ int mk_load_weights(const mk_config* cfg, const mk_weight* table, int32_t n, voi
     P.zeros = reinterpret_cast<const uint16_t*>(S + s_zero);
     P.newlat = reinterpret_cast<uint16_t*>(S + s_newlat);
     P.part = F(s_part);
+    P.part_ml = F(s_part_ml);
     P.s_max = m->G;
+    if (tracing) {
+        P.trace = reinterpret_cast<mk::TraceRec*>(S + s_trace);
+        P.trace_n = reinterpret_cast<unsigned*>(S + s_trace_n);
+        P.trace_cap = trace_cap;
+        P.trace_items = atoi(getenv("MK_TRACE")) > 1;
+    }
     P.amax = reinterpret_cast<int*>(S + s_amax);
     // buffers accumulated with atomics (K split into panels) are cleared at the start of each step
     P.carry = m->layers[0].g[mk::G_O].n_kc > 1;
@@ -728,6 +739,17 @@ int mk_step_status(mk_model* m, void* stream) {
     if (st[0] == mk::ST_INVALID)
         return fail(MK_ERR_INVALID_ARG, "token id or position out of range for this step");
     return fail(MK_ERR_CUDA, "device status %u", st[0]);
+}
+
+int mk_trace_read(mk_model* m, void* recs_out, int64_t bytes, int32_t* counts_out, void* stream) {
+    if (!m || m->magic != MODEL_MAGIC || !counts_out) return fail(MK_ERR_INVALID_ARG, "bad arguments");
+    if (!m->base.trace) return fail(MK_ERR_STATE, "tracing is off (set MK_TRACE=1 before mk_load_weights)");
+    const size_t need = (size_t)m->G * m->base.trace_cap * sizeof(mk::TraceRec);
+    if (!recs_out || bytes < (int64_t)need) return fail(MK_ERR_INVALID_ARG, "trace buffer needs %zu bytes", need);
+    CK(cudaStreamSynchronize((cudaStream_t)stream));
+    CK(cudaMemcpy(recs_out, m->base.trace, need, cudaMemcpyDeviceToHost));
+    CK(cudaMemcpy(counts_out, m->base.trace_n, (size_t)m->G * 4, cudaMemcpyDeviceToHost));
+    return MK_OK;
 }
 
 int mk_debug_routing(mk_model* m, int32_t* idx_out, float* w_out, void* stream) {

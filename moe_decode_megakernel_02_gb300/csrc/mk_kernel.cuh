@@ -1,5 +1,7 @@
 // mk_kernel.cuh -- stage program of the decode megakernel (producer + consumers).
 #pragma once
+#include <new>
+
 #include "mk_device.cuh"
 
 namespace mk {
@@ -26,7 +28,7 @@ __device__ __forceinline__ Deps deps1(int l, int w, unsigned t) {
 
 // per-thread view of the run (consumer threads and the producer warp each
 // keep an identical copy of the schedule state)
-struct Ctx {
+struct alignas(16) Ctx {
     const Params& p;
     uint8_t* smem;
     Misc& ms;
@@ -36,8 +38,11 @@ struct Ctx {
     PRing pr;
     // what the staging buffer currently holds
     const void* sk_src;
+    const void* sk_gain;
     int sk_off, sk_kc, sk_m0, sk_kind;
     int issued;  // producer: ring fills issued
+    long long t_start;
+    unsigned cur_code;  // trace: stage being run
     __device__ Ctx(const Params& pp, uint8_t* s)
         : p(pp), smem(s), ms(*reinterpret_cast<Misc*>(s + SMEM_MISC)), off(0), dead(false) {
         cr.slot = 0;
@@ -45,13 +50,40 @@ struct Ctx {
         pr.slot = 0;
         pr.phase = 0;
         sk_src = nullptr;
+        sk_gain = nullptr;
         sk_off = sk_kc = sk_m0 = sk_kind = -1;
         issued = 0;
+        t_start = gtimer();
+        if (pp.trace && threadIdx.x == 0) pp.trace_n[blockIdx.x] = 0;
     }
     __device__ float* stage() { return reinterpret_cast<float*>(smem + SMEM_STAGE); }
     __device__ float* red() { return reinterpret_cast<float*>(smem + SMEM_RED); }
-    __device__ void advance(int n) { off = (int)((off + (long long)n) % p.G); }
+    __device__ void advance(int n) {
+        const int o = (int)((off + (long long)n) % p.G);
+        __syncwarp();
+        off = o;
+        __syncwarp();
+    }
+    __device__ void bump_issued() {
+        const int v = issued + 1;
+        __syncwarp();
+        issued = v;
+        __syncwarp();
+    }
+    __device__ void set_ring(const CRing& v) {
+        __syncwarp();
+        cr = v;
+        __syncwarp();
+    }
+    __device__ void set_pring(const PRing& v, int iss) {
+        __syncwarp();
+        pr = v;
+        issued = iss;
+        __syncwarp();
+    }
 };
+
+static_assert(sizeof(Ctx) <= CTX_BYTES, "Ctx must fit its shared-memory slot");
 
 __device__ __forceinline__ int ctid() { return threadIdx.x; }
 
@@ -80,35 +112,101 @@ __device__ void csignal(Ctx& c, int layer, int which, unsigned n) {
     if (*(volatile int*)&c.ms.abort) c.dead = true;
 }
 
+// consumer-wide reductions (all 256 consumer threads call; uses Misc.bred)
+__device__ float cblock_sum(Ctx& c, float v) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    cbar();
+    if (lane == 0) c.ms.bred[warp] = v;
+    cbar();
+    float t = 0.f;
+#pragma unroll
+    for (int w = 0; w < NCW; ++w) t += c.ms.bred[w];
+    return t;
+}
+__device__ float cblock_max(Ctx& c, float v) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    cbar();
+    if (lane == 0) c.ms.bred[warp] = v;
+    cbar();
+    float t = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < NCW; ++w) t = fmaxf(t, c.ms.bred[w]);
+    return t;
+}
+
+// stage trace (consumer thread 0): wait start, inputs ready, stage done
+__device__ __forceinline__ void trace_rec(Ctx& c, unsigned code, unsigned n, long long t0, long long t1) {
+    if (!c.p.trace || threadIdx.x != 0) return;
+    unsigned* cnt = c.p.trace_n + blockIdx.x;
+    const unsigned i = *cnt;
+    if (i >= (unsigned)c.p.trace_cap) return;
+    TraceRec* r = c.p.trace + (size_t)blockIdx.x * c.p.trace_cap + i;
+    r->code = code;
+    r->n = n;
+    r->t_wait = t0;
+    r->t_ready = t1;
+    r->t_end = gtimer();
+    *cnt = i + 1;
+}
+
 // =============================================================== GEMV ====
 
 // fill stage[t][0..Kc) with f(input) for tokens m0 .. m0+ms-1
-__device__ void stage_input(Ctx& c, const Gemv& g, const float* src, int grp_off, int kc, int m0, int ms) {
+__device__ __noinline__ void stage_input(Ctx& c, const Gemv& g, const float* src, int grp_off, int kc, int m0, int ms) {
     const Params& p = c.p;
     float* xs = c.stage();
     const int Kc = g.Kc, k0 = kc * Kc, tid = ctid(), lane = tid & 31, warp = tid >> 5;
     const int total = ms * Kc;
     if (g.in_kind == IN_RMS) {
-        for (int t = warp; t < ms; t += NCW) {
-            const float* row = src + (size_t)(m0 + t) * g.src_stride;
-            float ss = 0.f;
-            for (int k = lane * 4; k < g.K; k += 128) {
-                float4 v = __ldcg(reinterpret_cast<const float4*>(row + k));
-                ss = fmaf(v.x, v.x, ss);
-                ss = fmaf(v.y, v.y, ss);
-                ss = fmaf(v.z, v.z, ss);
-                ss = fmaf(v.w, v.w, ss);
-            }
+        // pass 1: per-token sum of squares over the whole row (all threads);
+        // when the staged chunk is the whole row its raw values land in xs
+        float* acc = c.ms.rms;
+        for (int t = tid; t < ms; t += NCT) acc[t] = 0.f;
+        cbar();
+        const bool whole = g.n_kc == 1;
+        const int rowlen = g.K, tot = ms * rowlen;
+        float part = 0.f;
+        int cur = -1;
+#pragma unroll 4
+        for (int i = tid * 4; i < tot; i += NCT * 4) {
+            const int t = i / rowlen, k = i - t * rowlen;
+            const float4 v = __ldcg(reinterpret_cast<const float4*>(src + (size_t)(m0 + t) * g.src_stride + k));
+            if (whole) *reinterpret_cast<float4*>(xs + i) = v;
+            // a warp's 128 consecutive floats never straddle a row (rows are
+            // multiples of 128 floats), so `t` changes uniformly in the warp
+            if (t != cur) {
+                if (cur >= 0) {
 #pragma unroll
-            for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-            if (lane == 0) c.ms.rms[t] = 1.0f / sqrtf(ss / (float)g.K + p.eps);
+                    for (int o = 16; o; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+                    if (lane == 0) atomicAdd(&acc[cur], part);
+                }
+                part = 0.f;
+                cur = t;
+            }
+            part = fmaf(v.x, v.x, part);
+            part = fmaf(v.y, v.y, part);
+            part = fmaf(v.z, v.z, part);
+            part = fmaf(v.w, v.w, part);
+        }
+        if (cur >= 0) {
+#pragma unroll
+            for (int o = 16; o; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+            if (lane == 0) atomicAdd(&acc[cur], part);
         }
         cbar();
+        if (tid < ms) acc[tid] = 1.0f / sqrtf(acc[tid] / (float)g.K + p.eps);
+        cbar();
+#pragma unroll 4
         for (int i = tid * 4; i < total; i += NCT * 4) {
             const int t = i / Kc, k = i - t * Kc;
-            float4 v = __ldcg(reinterpret_cast<const float4*>(src + (size_t)(m0 + t) * g.src_stride + k0 + k));
+            const float4 v = whole ? *reinterpret_cast<const float4*>(xs + i)
+                                   : __ldcg(reinterpret_cast<const float4*>(src + (size_t)(m0 + t) * g.src_stride + k0 + k));
             uint2 gw = *reinterpret_cast<const uint2*>(g.gain + k0 + k);
-            const float r = c.ms.rms[t];
+            const float r = acc[t];
             float4 o;
             o.x = v.x * r * bf_lo(gw.x);
             o.y = v.y * r * bf_hi(gw.x);
@@ -117,12 +215,14 @@ __device__ void stage_input(Ctx& c, const Gemv& g, const float* src, int grp_off
             *reinterpret_cast<float4*>(xs + i) = o;
         }
     } else if (g.in_kind == IN_COPY) {
+#pragma unroll 4
         for (int i = tid * 4; i < total; i += NCT * 4) {
             const int t = i / Kc, k = i - t * Kc;
             *reinterpret_cast<float4*>(xs + i) =
                 __ldcg(reinterpret_cast<const float4*>(src + (size_t)(m0 + t) * g.src_stride + grp_off + k0 + k));
         }
     } else {  // IN_SWIGLU: h = silu(gate) * up
+#pragma unroll 4
         for (int i = tid * 4; i < total; i += NCT * 4) {
             const int t = i / Kc, k = i - t * Kc;
             const float* r = src + (size_t)(m0 + t) * g.src_stride + k0 + k;
@@ -138,185 +238,386 @@ __device__ void stage_input(Ctx& c, const Gemv& g, const float* src, int grp_off
     }
 }
 
-// one lane: 8 rows x 8 k of the tile against MTc staged tokens, then a
-// reduction over the lanes that share the 8 rows; per-warp sums go to red[]
-template <int MTc>
-__device__ void gemv_compute(const uint8_t* tile, int nr, int Kc, const float* xs, int mt0, float* red) {
-    const int tid = ctid(), lane = tid & 31, warp = tid >> 5;
-    const int NC = Kc >> 3;
-    const int pairs = (nr >> 3) * NC;
-    float acc[8][MTc];
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-#pragma unroll
-        for (int m = 0; m < MTc; ++m) acc[i][m] = 0.f;
-    int rg = 0;
-    if (tid < pairs) {
-        rg = tid / NC;
-        const int ch = tid - rg * NC;
-        float xv[MTc][8];
-#pragma unroll
-        for (int m = 0; m < MTc; ++m) {
-            const float4 a = *reinterpret_cast<const float4*>(xs + (size_t)(mt0 + m) * Kc + ch * 8);
-            const float4 b = *reinterpret_cast<const float4*>(xs + (size_t)(mt0 + m) * Kc + ch * 8 + 4);
-            xv[m][0] = a.x; xv[m][1] = a.y; xv[m][2] = a.z; xv[m][3] = a.w;
-            xv[m][4] = b.x; xv[m][5] = b.y; xv[m][6] = b.z; xv[m][7] = b.w;
-        }
-        const uint4* wp = reinterpret_cast<const uint4*>(tile) + (size_t)rg * 8 * NC + ch;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const uint4 w = wp[(size_t)i * NC];
-            const float wf[8] = {bf_lo(w.x), bf_hi(w.x), bf_lo(w.y), bf_hi(w.y),
-                                 bf_lo(w.z), bf_hi(w.z), bf_lo(w.w), bf_hi(w.w)};
-#pragma unroll
-            for (int m = 0; m < MTc; ++m) {
-                float a = acc[i][m];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) a = fmaf(wf[e], xv[m][e], a);
-                acc[i][m] = a;
-            }
-        }
-    }
-    const int span = NC < 32 ? NC : 32;
-    for (int o = span >> 1; o > 0; o >>= 1)
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-#pragma unroll
-            for (int m = 0; m < MTc; ++m) acc[i][m] += __shfl_xor_sync(0xffffffffu, acc[i][m], o);
-    if (tid < pairs) {
-        const int WPR = NC >= 32 ? (NC >> 5) : 1;
-        const bool writer = NC >= 32 ? (lane == 0) : ((lane % NC) == 0);
-        if (writer) {
-            const int wr = NC >= 32 ? (warp % WPR) : 0;
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-#pragma unroll
-                for (int m = 0; m < MTc; ++m) red[((rg * WPR + wr) * 8 + i) * MTc + m] = acc[i][m];
-        }
-    }
-}
-
 __device__ __forceinline__ float route_weight(const Misc& ms, int m, int expert, int k) {
     for (int j = 0; j < k; ++j)
         if (ms.ridx[m][j] == expert) return ms.rw[m][j];
     return 0.f;
 }
 
-__device__ void gemv_epilogue(Ctx& c, const Gemv& g, int slot, int expert, int r0, int nr, int mbase, int mcount,
-                              int MTc) {
-    const float* red = c.red();
-    const int NC = g.Kc >> 3;
-    const int WPR = NC >= 32 ? (NC >> 5) : 1;
-    for (int idx = ctid(); idx < nr * MTc; idx += NCT) {
-        const int r = idx / MTc, mt = idx - r * MTc;
-        if (mt >= mcount) continue;
-        const int rg = r >> 3, i = r & 7;
-        float y = 0.f;
-        for (int wr = 0; wr < WPR; ++wr) y += red[((rg * WPR + wr) * 8 + i) * MTc + mt];
-        const int m = mbase + mt, row = r0 + r;
-        if (g.out_kind == OUT_STORE) {
-            float* d = g.dst + (size_t)slot * g.dst_sstride + (size_t)m * g.dst_stride + row;
-            if (g.n_kc == 1)
-                *d = y;
-            else
-                atomicAdd(d, y);
-        } else if (g.out_kind == OUT_RESID) {
-            float* d = g.dst + (size_t)m * g.dst_stride + row;
-            if (g.n_kc == 1) {
-                const float v = __ldcg(d) + y;
-                *d = v;
-                g.dst2[(size_t)m * g.dst_stride + row] = v;
-            } else {
-                atomicAdd(d, y);
+// one output value of a GEMV item
+__device__ __forceinline__ void gemv_out(Ctx& c, const Gemv& g, int slot, int expert, int m, int row, float y) {
+    if (g.out_kind == OUT_STORE) {
+        float* d = g.dst + (size_t)slot * g.dst_sstride + (size_t)m * g.dst_stride + row;
+        if (g.n_kc == 1)
+            *d = y;
+        else
+            atomicAdd(d, y);
+    } else if (g.out_kind == OUT_RESID) {
+        float* d = g.dst + (size_t)m * g.dst_stride + row;
+        if (g.n_kc == 1) {
+            const float v = __ldcg(d) + y;
+            *d = v;
+            g.dst2[(size_t)m * g.dst_stride + row] = v;
+        } else {
+            atomicAdd(d, y);
+        }
+    } else {  // OUT_SCALED: expert down projection added into the next residual
+        const float w = expert < 0 ? 1.0f : route_weight(c.ms, m, expert, c.p.topk);
+        if (w != 0.f) atomicAdd(g.dst + (size_t)m * g.dst_stride + row, w * y);
+    }
+}
+
+__device__ __forceinline__ void fma8(float& a, const uint4& w, const float (&x)[8]) {
+    a = fmaf(bf_lo(w.x), x[0], a);
+    a = fmaf(bf_hi(w.x), x[1], a);
+    a = fmaf(bf_lo(w.y), x[2], a);
+    a = fmaf(bf_hi(w.y), x[3], a);
+    a = fmaf(bf_lo(w.z), x[4], a);
+    a = fmaf(bf_hi(w.z), x[5], a);
+    a = fmaf(bf_lo(w.w), x[6], a);
+    a = fmaf(bf_hi(w.w), x[7], a);
+}
+
+// One warp's share of a weight tile: the warp owns rows [warp*RW, warp*RW+RW)
+// of the tile (RW = rows/8) and its lanes split the K panel into 16-byte
+// chunks; products against MTc staged tokens, a warp-shuffle reduction, and
+// the warp writes its own outputs. No CTA-wide barrier per tile.
+template <int MTc>
+__device__ void gemv_warp_tile(Ctx& c, const Gemv& g, const uint8_t* tile, int nr, const float* xs, int mt0,
+                               int mcount, int mbase, int slot, int expert, int r0) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int Kc = g.Kc, NC = Kc >> 3, RW = nr >> 3, rw0 = warp * RW;
+    const uint4* T4 = reinterpret_cast<const uint4*>(tile);
+    if (NC >= 32) {
+        const int JC = NC >> 5;
+        for (int r = 0; r < RW; r += 4) {
+            const int nrr = min(4, RW - r);
+            float acc[4][MTc];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int m = 0; m < MTc; ++m) acc[i][m] = 0.f;
+            for (int j = 0; j < JC; ++j) {
+                const int ch = lane + 32 * j;
+                float xv[MTc][8];
+#pragma unroll
+                for (int m = 0; m < MTc; ++m) {
+                    const float4 a = *reinterpret_cast<const float4*>(xs + (size_t)(mt0 + m) * Kc + ch * 8);
+                    const float4 b = *reinterpret_cast<const float4*>(xs + (size_t)(mt0 + m) * Kc + ch * 8 + 4);
+                    xv[m][0] = a.x; xv[m][1] = a.y; xv[m][2] = a.z; xv[m][3] = a.w;
+                    xv[m][4] = b.x; xv[m][5] = b.y; xv[m][6] = b.z; xv[m][7] = b.w;
+                }
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    if (i < nrr) {
+                        const uint4 w = T4[(size_t)(rw0 + r + i) * NC + ch];
+#pragma unroll
+                        for (int m = 0; m < MTc; ++m) fma8(acc[i][m], w, xv[m]);
+                    }
+                }
             }
-        } else {  // OUT_SCALED: routed expert down projection into the next residual
-            const float w = expert < 0 ? 1.0f : route_weight(c.ms, m, expert, c.p.topk);
-            if (w != 0.f) atomicAdd(g.dst + (size_t)m * g.dst_stride + row, w * y);
+#pragma unroll
+            for (int o = 16; o; o >>= 1)
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+#pragma unroll
+                    for (int m = 0; m < MTc; ++m) acc[i][m] += __shfl_xor_sync(0xffffffffu, acc[i][m], o);
+            // lane i*MTc + m writes value (row i, token m)
+            float myv = 0.f;
+            int mi = 4, mm = 0;
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int m = 0; m < MTc; ++m)
+                    if (lane == i * MTc + m) {
+                        myv = acc[i][m];
+                        mi = i;
+                        mm = m;
+                    }
+            if (mi < nrr && mm < mcount) gemv_out(c, g, slot, expert, mbase + mm, r0 + rw0 + r + mi, myv);
+        }
+    } else {
+        // short rows (K = 128): 32/NC rows per pass, NC lanes per row
+        const int G = 32 / NC, gi = lane / NC, ch = lane - gi * NC;
+        for (int pass = 0; pass < RW / G; ++pass) {
+            const int row = rw0 + pass * G + gi;
+            float acc[MTc];
+            const uint4 w = T4[(size_t)row * NC + ch];
+#pragma unroll
+            for (int m = 0; m < MTc; ++m) {
+                float xv[8];
+                const float4 a = *reinterpret_cast<const float4*>(xs + (size_t)(mt0 + m) * Kc + ch * 8);
+                const float4 b = *reinterpret_cast<const float4*>(xs + (size_t)(mt0 + m) * Kc + ch * 8 + 4);
+                xv[0] = a.x; xv[1] = a.y; xv[2] = a.z; xv[3] = a.w;
+                xv[4] = b.x; xv[5] = b.y; xv[6] = b.z; xv[7] = b.w;
+                acc[m] = 0.f;
+                fma8(acc[m], w, xv);
+            }
+            for (int o = NC >> 1; o; o >>= 1)
+#pragma unroll
+                for (int m = 0; m < MTc; ++m) acc[m] += __shfl_xor_sync(0xffffffffu, acc[m], o);
+            float myv = 0.f;
+#pragma unroll
+            for (int m = 0; m < MTc; ++m)
+                if (ch == m) myv = acc[m];
+            if (ch < mcount) gemv_out(c, g, slot, expert, mbase + ch, r0 + row, myv);
         }
     }
 }
 
-// consumer: one GEMV work item
-__device__ void cons_gemv(Ctx& c, const Gemv& g, int slot, int expert, int j) {
+// (re)stage the input of item j when it differs from what the buffer holds;
+// the staged input is identified by buffer, head group, K panel, token range
+// and gain: every GEMV input buffer is written once per step
+__device__ __forceinline__ bool restage(Ctx& c, const Gemv& g, const float* src, int grp_off, int kc, int m0,
+                                        int ms) {
+    if (c.sk_src == src && c.sk_off == grp_off && c.sk_kc == kc && c.sk_m0 == m0 && c.sk_kind == g.in_kind &&
+        c.sk_gain == g.gain)
+        return false;
+    cbar();  // everyone is done with the previous contents
+    stage_input(c, g, src, grp_off, kc, m0, ms);
+    cbar();
+    c.sk_src = src;
+    c.sk_off = grp_off;
+    c.sk_kc = kc;
+    c.sk_m0 = m0;
+    c.sk_kind = g.in_kind;
+    c.sk_gain = g.gain;
+    return true;
+}
+
+// M <= 2 tokens, K panel >= 256: each lane keeps its slice of the staged
+// input in registers for the whole range (loaded once per staging), so a
+// warp reads only its own weight rows from shared memory per tile.
+// inline bounded spin on a ring barrier (no calls: hot loops stay free of
+// register spills); false on timeout or abort
+__device__ __forceinline__ bool spin_wait(const Params& p, unsigned long long* bar, unsigned parity) {
+    if (mbar_test(bar, parity)) return true;
+    const long long t0 = gtimer();
+    for (unsigned it = 1;; ++it) {
+        if (mbar_test(bar, parity)) return true;
+        if ((it & 63) == 0 && (gtimer() - t0 > p.timeout_ns || ld_relaxed(&p.status[1]))) return false;
+    }
+}
+
+// M <= 2 tokens, K panel >= 256: a warp owns whole rows of each tile; lanes
+// split K into 16-byte chunks, reading the staged input from shared memory.
+// The tile loop holds no calls and stays well under the register budget (a
+// 9-warp CTA gets 168 registers per thread): spills would go to local memory,
+// which misses the small L1 left beside this kernel's shared memory.
+template <int MR>
+__device__ __noinline__ void gemv_range_reg(Ctx& c, const Gemv& g, int slot, int expert, int j_lo, int j_hi) {
     const Params& p = c.p;
-    const int kc = j / g.n_rb, rb = j - kc * g.n_rb;
-    const int r0 = rb * g.R, nr = min(g.R, g.N - r0);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int Kc = g.Kc, NC = Kc >> 3, JC = NC >> 5;
+    const int n_rb = g.n_rb, R = g.R, N = g.N, grp_rows = g.grp_rows, grp_stride = g.grp_stride;
+    const int out_kind = g.out_kind, n_kc = g.n_kc, dst_stride = g.dst_stride;
+    float* const dst = g.dst + (size_t)slot * g.dst_sstride;
+    float* const dst2 = g.dst2;
     const float* src = g.src + (size_t)slot * g.src_sstride;
-    const int grp_off = g.grp_rows ? (r0 / g.grp_rows) * g.grp_stride : 0;
-    const int cap = STAGE_FLOATS / g.Kc;
-    const int M = p.M;
-    const uint8_t* tile = nullptr;
-    for (int m0 = 0; m0 < M; m0 += cap) {
-        const int ms = min(cap, M - m0);
-        if (c.sk_src != src || c.sk_off != grp_off || c.sk_kc != kc || c.sk_m0 != m0 || c.sk_kind != g.in_kind) {
-            cbar();  // everyone is done with the previous contents
-            stage_input(c, g, src, grp_off, kc, m0, ms);
-            cbar();
-            c.sk_src = src;
-            c.sk_off = grp_off;
-            c.sk_kc = kc;
-            c.sk_m0 = m0;
-            c.sk_kind = g.in_kind;
+    Misc& ms = c.ms;
+    uint8_t* const ring = c.smem + SMEM_RING;
+    const float* const xs = c.stage();
+    CRing cr = c.cr;
+    bool dead = c.dead, timed_out = false;
+    float wtok0 = 1.f, wtok1 = 1.f;
+    if (expert >= 0) {
+        wtok0 = route_weight(ms, 0, expert, p.topk);
+        if (MR > 1) wtok1 = route_weight(ms, 1, expert, p.topk);
+    }
+    int j = j_lo;
+    while (j < j_hi) {
+        // a run of items sharing the staged input (same K panel and head group)
+        const int kc0 = j / n_rb;
+        const int g0 = grp_rows ? ((j - kc0 * n_rb) * R) / grp_rows : 0;
+        int jend = j + 1;
+        while (jend < j_hi) {
+            const int kc1 = jend / n_rb;
+            const int g1 = grp_rows ? ((jend - kc1 * n_rb) * R) / grp_rows : 0;
+            if (kc1 != kc0 || g1 != g0) break;
+            ++jend;
         }
-        if (!tile && !c.dead) tile = cons_wait(p, c.smem, c.ms, c.cr);
-        for (int mt0 = 0; mt0 < ms; mt0 += MT) {
-            const int cnt = min(MT, ms - mt0);
-            const int MTc = cnt == 1 ? 1 : (cnt == 2 ? 2 : 4);
-            if (tile) {
-                if (MTc == 1)
-                    gemv_compute<1>(tile, nr, g.Kc, c.stage(), mt0, c.red());
-                else if (MTc == 2)
-                    gemv_compute<2>(tile, nr, g.Kc, c.stage(), mt0, c.red());
+        restage(c, g, src, g0 * grp_stride, kc0, 0, MR);
+        for (; j < jend; ++j) {
+            const int kc = j / n_rb, rb = j - kc * n_rb;
+            const int r0 = rb * R, nr = min(R, N - r0);
+            const uint8_t* tile = nullptr;
+            if (!dead) {
+                if (spin_wait(p, &ms.full[cr.slot], cr.phase))
+                    tile = ring + cr.slot * SLOT_BYTES;
                 else
-                    gemv_compute<4>(tile, nr, g.Kc, c.stage(), mt0, c.red());
+                    dead = timed_out = true;
             }
-            if (m0 + mt0 + cnt >= M) cons_release(c.ms, c.cr);  // last use of the tile
-            cbar();
-            if (tile) gemv_epilogue(c, g, slot, expert, r0, nr, m0 + mt0, cnt, MTc);
-            cbar();
+            if (tile) {
+                const int RW = nr >> 3, rw0 = warp * RW;
+                for (int r = 0; r < RW; ++r) {
+                    const uint4* wr = reinterpret_cast<const uint4*>(tile) + (size_t)(rw0 + r) * NC + lane;
+                    const float* xl = xs + lane * 8;
+                    float a0[4] = {0.f, 0.f, 0.f, 0.f}, a1[4] = {0.f, 0.f, 0.f, 0.f};
+                    for (int q0 = 0; q0 < JC; q0 += 4) {
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            if (q0 + u < JC) {
+                                const uint4 w = wr[32 * (q0 + u)];
+                                const float* x = xl + 256 * (q0 + u);
+                                float xv[8];
+                                *reinterpret_cast<float4*>(xv) = *reinterpret_cast<const float4*>(x);
+                                *reinterpret_cast<float4*>(xv + 4) = *reinterpret_cast<const float4*>(x + 4);
+                                fma8(a0[u], w, xv);
+                                if (MR > 1) {
+                                    *reinterpret_cast<float4*>(xv) = *reinterpret_cast<const float4*>(x + Kc);
+                                    *reinterpret_cast<float4*>(xv + 4) = *reinterpret_cast<const float4*>(x + Kc + 4);
+                                    fma8(a1[u], w, xv);
+                                }
+                            }
+                        }
+                    }
+                    float y0 = (a0[0] + a0[1]) + (a0[2] + a0[3]);
+                    float y1 = (a1[0] + a1[1]) + (a1[2] + a1[3]);
+#pragma unroll
+                    for (int o = 16; o; o >>= 1) {
+                        y0 += __shfl_xor_sync(0xffffffffu, y0, o);
+                        if (MR > 1) y1 += __shfl_xor_sync(0xffffffffu, y1, o);
+                    }
+                    if (lane < MR) {
+                        const int m = lane;
+                        const float v = m ? y1 : y0;
+                        const int row = r0 + rw0 + r;
+                        float* d = dst + (size_t)m * dst_stride + row;
+                        if (out_kind == OUT_STORE) {
+                            if (n_kc == 1) *d = v; else atomicAdd(d, v);
+                        } else if (out_kind == OUT_RESID) {
+                            if (n_kc == 1) {
+                                const float nv = __ldcg(d) + v;
+                                *d = nv;
+                                dst2[(size_t)m * dst_stride + row] = nv;
+                            } else {
+                                atomicAdd(d, v);
+                            }
+                        } else {
+                            const float w = m ? wtok1 : wtok0;
+                            if (w != 0.f) atomicAdd(d, w * v);
+                        }
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ms.empty[cr.slot]);
+            if (++cr.slot == NSLOT) {
+                cr.slot = 0;
+                cr.phase ^= 1u;
+            }
         }
     }
+    if (timed_out) {
+        ms.abort = 1;
+        raise_status(p, ST_TIMEOUT, 0x210u);
+    }
+    c.set_ring(cr);
+    if (dead) c.dead = true;
+}
+
+// general path (any M, short K panels): input staged in shared memory
+__device__ __noinline__ void gemv_range_smem(Ctx& c, const Gemv& g, int slot, int expert, int j_lo, int j_hi) {
+    const Params& p = c.p;
+    const float* src = g.src + (size_t)slot * g.src_sstride;
+    const int cap = STAGE_FLOATS / g.Kc;
+    const int M = p.M;
+    for (int j = j_lo; j < j_hi; ++j) {
+        const int kc = j / g.n_rb, rb = j - kc * g.n_rb;
+        const int r0 = rb * g.R, nr = min(g.R, g.N - r0);
+        const int grp_off = g.grp_rows ? (r0 / g.grp_rows) * g.grp_stride : 0;
+        const uint8_t* tile = nullptr;
+        const long long ta = p.trace_items ? gtimer() : 0;
+        long long tb = ta, tc = ta;
+        for (int m0 = 0; m0 < M; m0 += cap) {
+            const int ms = min(cap, M - m0);
+            restage(c, g, src, grp_off, kc, m0, ms);
+            if (p.trace_items) tb = gtimer();
+            if (!tile && !c.dead) tile = cons_wait(p, c.smem, c.ms, c.cr);
+            if (p.trace_items) tc = gtimer();
+            if (tile) {
+                for (int mt0 = 0; mt0 < ms; mt0 += MT) {
+                    const int cnt = min(MT, ms - mt0);
+                    if (cnt == 1)
+                        gemv_warp_tile<1>(c, g, tile, nr, c.stage(), mt0, cnt, m0 + mt0, slot, expert, r0);
+                    else if (cnt == 2)
+                        gemv_warp_tile<2>(c, g, tile, nr, c.stage(), mt0, cnt, m0 + mt0, slot, expert, r0);
+                    else
+                        gemv_warp_tile<4>(c, g, tile, nr, c.stage(), mt0, cnt, m0 + mt0, slot, expert, r0);
+                }
+            }
+        }
+        cons_release(c.ms, c.cr);
+        if (p.trace_items && threadIdx.x == 0) trace_rec(c, 0x80000000u | c.cur_code, (unsigned)(tb - ta), ta, tc);
+    }
+}
+
+// consumer: GEMV work items [j_lo, j_hi) of one slot
+__device__ __noinline__ void cons_gemv(Ctx& c, const Gemv& g, int slot, int expert, int j_lo, int j_hi) {
+    if (g.Kc >= 256 && c.p.M == 1)
+        gemv_range_reg<1>(c, g, slot, expert, j_lo, j_hi);
+    else if (g.Kc >= 256 && c.p.M == 2)
+        gemv_range_reg<2>(c, g, slot, expert, j_lo, j_hi);
+    else
+        gemv_range_smem(c, g, slot, expert, j_lo, j_hi);
     if (*(volatile int*)&c.ms.abort) c.dead = true;
 }
 
-// producer: bulk-load the weight tile of one GEMV item
-__device__ void prod_gemv(Ctx& c, const Gemv& g, int expert, int j) {
-    const int kc = j / g.n_rb, rb = j - kc * g.n_rb;
-    const int r0 = rb * g.R, nr = min(g.R, g.N - r0);
-    const unsigned bytes = (unsigned)nr * g.Kc * 2u;
-    const uint16_t* src =
-        g.W + (expert >= 0 ? (size_t)expert * g.w_estride : 0) + (size_t)kc * g.N * g.Kc + (size_t)r0 * g.Kc;
-    int ok = 1;
-    if ((threadIdx.x & 31) == 0) {
-        uint8_t* dst = prod_begin(c.p, c.smem, c.ms, c.pr, bytes);
-        if (dst)
-            bulk_g2s(dst, src, bytes, &c.ms.full[c.pr.slot]);
-        else
-            ok = 0;
+// producer: bulk-load the weight tiles of items [lo, hi) (one slot). All
+// descriptor fields and the ring state live in registers for the loop.
+__device__ __noinline__ void prod_gemv(Ctx& c, const Gemv& g, int expert, int lo, int hi) {
+    const uint16_t* W = g.W + (expert >= 0 ? (size_t)expert * g.w_estride : 0);
+    const int n_rb = g.n_rb, R = g.R, N = g.N, Kc = g.Kc;
+    const Params& p = c.p;
+    Misc& ms = c.ms;
+    uint8_t* ring = c.smem + SMEM_RING;
+    PRing pr = c.pr;
+    int issued = c.issued;
+    const bool leader = (threadIdx.x & 31) == 0;
+    const unsigned long long pol = l2_evict_first();
+    for (int j = lo; j < hi; ++j) {
+        const int kc = j / n_rb, rb = j - kc * n_rb;
+        const int r0 = rb * R, nr = min(R, N - r0);
+        const unsigned bytes = (unsigned)nr * Kc * 2u;
+        const uint16_t* src = W + (size_t)kc * N * Kc + (size_t)r0 * Kc;
+        int ok = 1;
+        if (leader) {
+            if (spin_wait(p, &ms.empty[pr.slot], pr.phase ^ 1u)) {
+                mbar_expect_tx(&ms.full[pr.slot], bytes);
+                bulk_g2s_pol(ring + pr.slot * SLOT_BYTES, src, bytes, &ms.full[pr.slot], pol);
+            } else {
+                ok = 0;
+            }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) {
+            if (leader) raise_status(p, ST_TIMEOUT, 0x110u);
+            c.dead = true;
+            break;
+        }
+        ++issued;
+        prod_next(pr);
     }
-    ok = __shfl_sync(0xffffffffu, ok, 0);
-    if (!ok) {
-        c.dead = true;
-        return;
-    }
-    ++c.issued;
-    prod_next(c.pr);
+    c.set_pring(pr, issued);
 }
 
 template <bool PROD>
-__device__ void stage_gemv(Ctx& c, int l, const Gemv& g, const Deps& deps, int sig) {
+__device__ __noinline__ void stage_gemv(Ctx& c, int l, const Gemv& g, const Deps& deps, int sig) {
     const int n = gemv_items(g);
     int lo, hi;
     my_range(c.p, n, c.off, lo, hi);
     c.advance(n);
     if (lo >= hi) return;
-    c.sk_src = nullptr;  // a new stage: the input contents may have changed
     if constexpr (PROD) {
-        for (int j = lo; j < hi && !c.dead; ++j) prod_gemv(c, g, -1, j);
+        if (!c.dead) prod_gemv(c, g, -1, lo, hi);
     } else {
+        c.cur_code = ((unsigned)sig << 16) | (unsigned)l;
+        const long long t0 = gtimer();
         cwait(c, deps, 0x1000u | (unsigned)(l << 16) | (unsigned)sig);
-        for (int j = lo; j < hi; ++j) cons_gemv(c, g, 0, -1, j);
+        const long long t1 = gtimer();
+        cons_gemv(c, g, 0, -1, lo, hi);
         csignal(c, l, sig, (unsigned)(hi - lo));
+        trace_rec(c, ((unsigned)sig << 16) | (unsigned)l, (unsigned)(hi - lo), t0, t1);
     }
 }
 
@@ -325,7 +626,7 @@ __device__ void stage_gemv(Ctx& c, int l, const Gemv& g, const Deps& deps, int s
 // union of the selected experts (sorted by id) -> routed slots.
 // consumers: full routing into Misc; producer warp: slot list only.
 template <bool PROD>
-__device__ bool route(Ctx& c, int l) {
+__device__ __noinline__ bool route(Ctx& c, int l) {
     const Params& p = c.p;
     const Layer& Ld = p.layers[l];
     const int E = p.E, k = p.topk;
@@ -347,7 +648,9 @@ __device__ bool route(Ctx& c, int l) {
         for (int e = lane; e < E; e += 32) used[e] = 0;
         __syncwarp();
     } else {
+        const long long t0 = gtimer();
         cwait(c, deps1(l, C_ROUTER, (unsigned)gemv_items(Ld.g[G_ROUTER])), 0x400u);
+        trace_rec(c, (0x40u << 16) | (unsigned)l, 0u, t0, gtimer());
         for (int e = tid; e < E; e += NCT) used[e] = 0;
         cbar();
     }
@@ -445,7 +748,7 @@ __device__ bool route(Ctx& c, int l) {
 
 // routed-expert stage: items = slots x (row blocks x k panels), slot-major
 template <bool PROD>
-__device__ void stage_experts(Ctx& c, int l, const Gemv& g, bool down) {
+__device__ __noinline__ void stage_experts(Ctx& c, int l, const Gemv& g, bool down) {
     const Params& p = c.p;
     const int nslots = PROD ? c.ms.p_nslots : c.ms.n_slots;
     const uint8_t* slot_e = PROD ? c.ms.p_slot_e : c.ms.slot_e;
@@ -455,30 +758,32 @@ __device__ void stage_experts(Ctx& c, int l, const Gemv& g, bool down) {
     my_range(p, n, c.off, lo, hi);
     c.advance(n);
     if (lo >= hi) return;
-    c.sk_src = nullptr;
     if constexpr (PROD) {
-        for (int i = lo; i < hi && !c.dead; ++i) prod_gemv(c, g, slot_e[i / per], i % per);
+        for (int i = lo; i < hi && !c.dead;) {
+            const int s2 = i / per, iend = min(hi, (s2 + 1) * per);
+            prod_gemv(c, g, slot_e[s2], i - s2 * per, iend - s2 * per);
+            i = iend;
+        }
     } else {
         const Layer& Ld = p.layers[l];
-        int cur = -1;
-        unsigned cnt = 0;
-        for (int i = lo; i < hi; ++i) {
-            const int s = i / per;
-            if (s != cur) {
-                if (!down && cur >= 0) csignal(c, l, C_GU0 + cur, cnt);
-                cur = s;
-                cnt = 0;
-                // gate/up inputs were ready before routing (the router waited for
-                // the output projection); each down slot waits for its gate/up
-                if (down) cwait(c, deps1(l, C_GU0 + s, (unsigned)gemv_items(Ld.g[G_GU])), 0x500u);
+        c.cur_code = ((unsigned)(down ? C_DOWN : C_GU0) << 16) | (unsigned)l;
+        const long long t0 = gtimer();
+        long long tw = 0;
+        // a slot's items are contiguous: run them together; gate/up signals
+        // per slot, each down slot first waits for its gate/up
+        for (int i = lo; i < hi;) {
+            const int s2 = i / per, iend = min(hi, (s2 + 1) * per);
+            if (down) {
+                const long long a = gtimer();
+                cwait(c, deps1(l, C_GU0 + s2, (unsigned)gemv_items(Ld.g[G_GU])), 0x500u);
+                tw += gtimer() - a;
             }
-            cons_gemv(c, g, s, slot_e[s], i % per);
-            ++cnt;
+            cons_gemv(c, g, s2, slot_e[s2], i - s2 * per, iend - s2 * per);
+            if (!down) csignal(c, l, C_GU0 + s2, (unsigned)(iend - i));
+            i = iend;
         }
-        if (down)
-            csignal(c, l, C_DOWN, (unsigned)(hi - lo));
-        else if (cur >= 0)
-            csignal(c, l, C_GU0 + cur, cnt);
+        if (down) csignal(c, l, C_DOWN, (unsigned)(hi - lo));
+        trace_rec(c, ((unsigned)(down ? C_DOWN : C_GU0) << 16) | (unsigned)l, (unsigned)(hi - lo), t0, t0 + tw);
     }
 }
 
@@ -560,6 +865,7 @@ __device__ void gqa_rows(const Params& p, GqaState<DPL>& st, const float (&q)[8]
     }
     __syncwarp();
     // online softmax per query row over this warp's rows
+#pragma unroll 1
     for (int qr = 0; qr < Q; ++qr) {
         const int t = qr / Gq;
         float sv[8];
@@ -604,7 +910,7 @@ __device__ void gqa_rows(const Params& p, GqaState<DPL>& st, const float (&q)[8]
 }
 
 template <int DPL>
-__device__ void cons_attn_gqa(Ctx& c, int l, const AttnItem& it) {
+__device__ __noinline__ void cons_attn_gqa(Ctx& c, int l, const AttnItem& it) {
     const Params& p = c.p;
     const Layer& Ld = p.layers[l];
     const int hd = p.hd, Gq = p.Hq / p.Hkv, T = p.T, Q = T * Gq, half = hd / 2;
@@ -691,7 +997,7 @@ __device__ void cons_attn_gqa(Ctx& c, int l, const AttnItem& it) {
         for (int e = 0; e < DPL; ++e) w[2 + lane * DPL + e] = st.o[qr][e];
     }
     cbar();
-    float* out = p.part + ((((size_t)b * p.Hkv + g) * p.s_max + it.s) * Q) * W;
+    const size_t rbase = (((size_t)b * p.Hkv + g) * p.s_max + it.s) * Q;
     for (int i = tid; i < Q * W; i += NCT) {
         const int qr = i / W, e = i - qr * W;
         float mx = -INFINITY;
@@ -705,7 +1011,10 @@ __device__ void cons_attn_gqa(Ctx& c, int l, const AttnItem& it) {
                 if (mw != -INFINITY) v += ws[((size_t)w * Q + qr) * W + e] * expf(mw - mx);
             }
         }
-        out[(size_t)qr * W + e] = v;
+        if (e < 2)
+            p.part_ml[(rbase + qr) * 2 + e] = v;
+        else
+            p.part[(rbase + qr) * hd + (e - 2)] = v;
     }
     cbar();
 }
@@ -746,7 +1055,7 @@ __device__ __forceinline__ MlaSmem mla_smem(float* stage) {
 
 __device__ __forceinline__ uint32_t lds32(const uint16_t* p) { return *reinterpret_cast<const uint32_t*>(p); }
 
-__device__ void mla_chunk(const MlaSmem& S, const uint16_t* ck, const uint16_t* kr, int NR, int nvalid,
+__device__ __forceinline__ void mla_chunk(const MlaSmem& S, const uint16_t* ck, const uint16_t* kr, int NR, int nvalid,
                           float (&acc)[8][4]) {
     const int tid = ctid(), lane = tid & 31, warp = tid >> 5, g = lane >> 2, t4 = lane & 3;
     // ---- scores S[16][NR] = Q . KV^T ----
@@ -853,7 +1162,7 @@ __device__ void mla_chunk(const MlaSmem& S, const uint16_t* ck, const uint16_t* 
     }
 }
 
-__device__ void cons_attn_mla(Ctx& c, int l, const AttnItem& it) {
+__device__ __noinline__ void cons_attn_mla(Ctx& c, int l, const AttnItem& it) {
     const Params& p = c.p;
     const Layer& Ld = p.layers[l];
     const int tid = ctid(), lane = tid & 31, warp = tid >> 5, g = lane >> 2, t4 = lane & 3;
@@ -864,22 +1173,30 @@ __device__ void cons_attn_mla(Ctx& c, int l, const AttnItem& it) {
     c.sk_src = nullptr;
     // queries: [absorbed latent query (512) | roped rope query (64)] * scale, split hi/lo
     const int qh = p.nope + p.rd;
-    for (int i = tid; i < MLA_H * MLA_D; i += NCT) {
-        const int h = i / MLA_D, e = i - h * MLA_D;
-        float v;
-        if (e < MLA_KL) {
-            v = __ldcg(Ld.qlat + (size_t)m * MLA_H * MLA_KL + h * MLA_KL + e);
-        } else {
-            const int r = e - MLA_KL, hr = MLA_RD / 2, ri = r < hr ? r : r - hr;
-            const float* qr = Ld.q + (size_t)m * MLA_H * qh + h * qh + p.nope;
-            const float2 cs = p.rope[(size_t)pos * p.rope_half + ri];
-            const float x0 = __ldcg(qr + ri), x1 = __ldcg(qr + ri + hr);
-            v = r < hr ? (x0 * cs.x - x1 * cs.y) : (x1 * cs.x + x0 * cs.y);
+    const float sc = p.attn_scale;
+#pragma unroll 4
+    for (int i = tid; i < MLA_H * (MLA_KL / 4); i += NCT) {
+        const int h = i / (MLA_KL / 4), e = (i - h * (MLA_KL / 4)) * 4;
+        const float4 v = __ldcg(reinterpret_cast<const float4*>(Ld.qlat + (size_t)m * MLA_H * MLA_KL + h * MLA_KL + e));
+        const float f[4] = {v.x * sc, v.y * sc, v.z * sc, v.w * sc};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint16_t hi = f2bf(f[j]);
+            S.qhi[h * MLA_QS + e + j] = hi;
+            S.qlo[h * MLA_QS + e + j] = f2bf(f[j] - bf2f(hi));
         }
-        v *= p.attn_scale;
-        const uint16_t hi = f2bf(v);
-        S.qhi[h * MLA_QS + e] = hi;
-        S.qlo[h * MLA_QS + e] = f2bf(v - bf2f(hi));
+    }
+    for (int i = tid; i < MLA_H * (MLA_RD / 2); i += NCT) {
+        const int h = i / (MLA_RD / 2), ri = i - h * (MLA_RD / 2), hr = MLA_RD / 2;
+        const float* qr = Ld.q + (size_t)m * MLA_H * qh + h * qh + p.nope;
+        const float2 cs = p.rope[(size_t)pos * p.rope_half + ri];
+        const float x0 = __ldcg(qr + ri), x1 = __ldcg(qr + ri + hr);
+        const float f0 = (x0 * cs.x - x1 * cs.y) * sc, f1 = (x1 * cs.x + x0 * cs.y) * sc;
+        const uint16_t h0 = f2bf(f0), h1 = f2bf(f1);
+        S.qhi[h * MLA_QS + MLA_KL + ri] = h0;
+        S.qlo[h * MLA_QS + MLA_KL + ri] = f2bf(f0 - bf2f(h0));
+        S.qhi[h * MLA_QS + MLA_KL + ri + hr] = h1;
+        S.qlo[h * MLA_QS + MLA_KL + ri + hr] = f2bf(f1 - bf2f(h1));
     }
     if (tid < 16) {
         S.mst[tid] = -INFINITY;
@@ -901,45 +1218,38 @@ __device__ void cons_attn_mla(Ctx& c, int l, const AttnItem& it) {
 #pragma unroll
     for (int j = 0; j < 8; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
     for (int u = it.u_lo; u < it.u_hi; ++u) {
-        if (u < it.nch) {
-            const uint8_t* tile = c.dead ? nullptr : cons_wait(p, c.smem, c.ms, c.cr);
-            const int nvalid = min(MLA_CH, p.pos[b] - u * MLA_CH);
-            if (tile) {
-                mla_chunk(S, reinterpret_cast<const uint16_t*>(tile),
-                          reinterpret_cast<const uint16_t*>(tile + MLA_CH * MLA_CS * 2), MLA_CH, nvalid, acc);
-            } else {
-                cbar();
-                cbar();
-            }
-            cons_release(c.ms, c.cr);
+        // one code path for cached chunks (from the ring) and the new positions (tail rows in smem)
+        const bool ring_chunk = u < it.nch;
+        const uint8_t* tile = nullptr;
+        if (ring_chunk && !c.dead) tile = cons_wait(p, c.smem, c.ms, c.cr);
+        const uint16_t* ck = ring_chunk ? reinterpret_cast<const uint16_t*>(tile) : S.tc;
+        const uint16_t* kr = ring_chunk ? reinterpret_cast<const uint16_t*>(tile + MLA_CH * MLA_CS * 2) : S.tr;
+        const int NR = ring_chunk ? MLA_CH : 16;
+        const int nvalid = ring_chunk ? min(MLA_CH, p.pos[b] - u * MLA_CH) : t + 1;
+        if (ring_chunk && !tile) {
+            cbar();
+            cbar();
         } else {
-            mla_chunk(S, S.tc, S.tr, 16, t + 1, acc);
+            mla_chunk(S, ck, kr, NR, nvalid, acc);
         }
+        if (ring_chunk) cons_release(c.ms, c.cr);
     }
-    // partial: (max, sum) per head and the unnormalised O rows
+    // partial: unnormalised O rows and (max, sum) per head
     const size_t base = ((size_t)m * p.s_max + it.s) * MLA_H;
-    float* po = p.part + base * (MLA_KL + 2);
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
         const int dim = warp * 64 + j * 8 + 2 * t4;
-        float* r0 = po + (size_t)g * (MLA_KL + 2) + 2 + dim;
-        float* r1 = po + (size_t)(g + 8) * (MLA_KL + 2) + 2 + dim;
-        r0[0] = acc[j][0];
-        r0[1] = acc[j][1];
-        r1[0] = acc[j][2];
-        r1[1] = acc[j][3];
+        *reinterpret_cast<float2*>(p.part + (base + g) * MLA_KL + dim) = make_float2(acc[j][0], acc[j][1]);
+        *reinterpret_cast<float2*>(p.part + (base + g + 8) * MLA_KL + dim) = make_float2(acc[j][2], acc[j][3]);
     }
     cbar();
-    if (tid < 16) {
-        po[(size_t)tid * (MLA_KL + 2)] = S.mst[tid];
-        po[(size_t)tid * (MLA_KL + 2) + 1] = S.lst[tid];
-    }
+    if (tid < 16) *reinterpret_cast<float2*>(p.part_ml + (base + tid) * 2) = make_float2(S.mst[tid], S.lst[tid]);
     cbar();
 }
 
 // producer: bulk-load one MLA chunk (32 positions) into padded smem rows;
 // rows past the valid positions are filled from a zero buffer
-__device__ void prod_mla_chunk(Ctx& c, int l, int b, int u) {
+__device__ __noinline__ void prod_mla_chunk(Ctx& c, int l, int b, int u) {
     const Params& p = c.p;
     const int lane = threadIdx.x & 31;
     const int nvalid = min(MLA_CH, p.pos[b] - u * MLA_CH);
@@ -965,11 +1275,11 @@ __device__ void prod_mla_chunk(Ctx& c, int l, int b, int u) {
     bulk_g2s(dst + (size_t)r * MLA_CS * 2, srcc, MLA_KL * 2, &c.ms.full[c.pr.slot]);
     bulk_g2s(dst + (size_t)MLA_CH * MLA_CS * 2 + (size_t)r * MLA_RS * 2, srcr, MLA_RD * 2, &c.ms.full[c.pr.slot]);
     __syncwarp();
-    ++c.issued;
+    c.bump_issued();
     prod_next(c.pr);
 }
 
-__device__ void prod_gqa_chunk(Ctx& c, int l, int b, int g, int u) {
+__device__ __noinline__ void prod_gqa_chunk(Ctx& c, int l, int b, int g, int u) {
     const Params& p = c.p;
     const int hd = p.hd;
     const int nvalid = min(GQA_CH, p.pos[b] - u * GQA_CH);
@@ -990,12 +1300,12 @@ __device__ void prod_gqa_chunk(Ctx& c, int l, int b, int g, int u) {
         c.dead = true;
         return;
     }
-    ++c.issued;
+    c.bump_issued();
     prod_next(c.pr);
 }
 
 template <bool PROD>
-__device__ void stage_attn(Ctx& c, int l, const Deps& deps) {
+__device__ __noinline__ void stage_attn(Ctx& c, int l, const Deps& deps) {
     const Params& p = c.p;
     const int n = attn_items(p);
     int lo, hi;
@@ -1013,7 +1323,9 @@ __device__ void stage_attn(Ctx& c, int l, const Deps& deps) {
             }
         }
     } else {
+        const long long t0 = gtimer();
         cwait(c, deps, 0x600u | (unsigned)(l << 16));
+        const long long t1 = gtimer();
         for (int i = lo; i < hi; ++i) {
             const AttnItem it = attn_item(p, i);
             if (p.attn == 0) {
@@ -1026,6 +1338,7 @@ __device__ void stage_attn(Ctx& c, int l, const Deps& deps) {
             }
         }
         csignal(c, l, C_ATTN, (unsigned)(hi - lo));
+        trace_rec(c, ((unsigned)C_ATTN << 16) | (unsigned)l, (unsigned)(hi - lo), t0, t1);
     }
 }
 
@@ -1034,75 +1347,87 @@ __device__ void stage_attn(Ctx& c, int l, const Deps& deps) {
 // MLA: item (token, head, 128-dim chunk) -> olat[m][h*512 ...]
 __device__ int comb_items(const Params& p) { return p.attn == 0 ? p.M * p.Hq : p.M * MLA_H * 4; }
 
-__device__ void cons_comb(Ctx& c, int l, int i) {
+__device__ __noinline__ void cons_comb(Ctx& c, int l, int i) {
     const Params& p = c.p;
     const Layer& Ld = p.layers[l];
-    const int tid = ctid();
-    cbar();
+    const int tid = ctid(), lane = tid & 31, warp = tid >> 5;
+    size_t r0, rstride;
+    int S, D, d0, OL;
+    float* out;
     if (p.attn == 0) {
-        const int Gq = p.Hq / p.Hkv, Q = p.T * Gq, hd = p.hd, W = 2 + hd;
+        const int Gq = p.Hq / p.Hkv, Q = p.T * Gq;
         const int m = i / p.Hq, h = i - m * p.Hq, b = m / p.T, t = m - b * p.T;
         const int g = h / Gq, qr = t * Gq + (h - g * Gq);
-        const int units = nch_of(p, b, GQA_CH) + 1, tg = gqa_target(p), S = units < tg ? units : tg;
-        const float* base = p.part + (((size_t)b * p.Hkv + g) * p.s_max) * Q * W + (size_t)qr * W;
-        if (tid == 0) {
-            float mx = -INFINITY;
-            for (int s = 0; s < S; ++s) mx = fmaxf(mx, __ldcg(base + (size_t)s * Q * W));
-            float L = 0.f;
-            for (int s = 0; s < S; ++s) {
-                const float ms = __ldcg(base + (size_t)s * Q * W);
-                const float w = ms == -INFINITY ? 0.f : expf(ms - mx);
-                c.ms.cw[s] = w;
-                L += w * __ldcg(base + (size_t)s * Q * W + 1);
-            }
-            c.ms.cw[255] = 1.0f / L;
-        }
-        cbar();
-        for (int e = tid; e < hd; e += NCT) {
-            float v = 0.f;
-            for (int s = 0; s < S; ++s) v = fmaf(c.ms.cw[s], __ldcg(base + (size_t)s * Q * W + 2 + e), v);
-            Ld.o[(size_t)m * p.Hq * hd + h * hd + e] = v * c.ms.cw[255];
-        }
+        const int units = nch_of(p, b, GQA_CH) + 1, tg = gqa_target(p);
+        S = units < tg ? units : tg;
+        r0 = (((size_t)b * p.Hkv + g) * p.s_max) * Q + qr;
+        rstride = Q;
+        D = p.hd;
+        d0 = 0;
+        OL = p.hd;
+        out = Ld.o + (size_t)m * p.Hq * p.hd + h * p.hd;
     } else {
-        const int W = MLA_KL + 2;
         const int m = i / (MLA_H * 4), r = i - m * MLA_H * 4, h = r >> 2, dc = r & 3;
         const int b = m / p.T;
-        const int units = nch_of(p, b, MLA_CH) + 1, tg = mla_target(p), S = units < tg ? units : tg;
-        const float* base = p.part + ((size_t)m * p.s_max * MLA_H + h) * W;
-        const size_t sstride = (size_t)MLA_H * W;
-        if (tid == 0) {
-            float mx = -INFINITY;
-            for (int s = 0; s < S; ++s) mx = fmaxf(mx, __ldcg(base + s * sstride));
-            float L = 0.f;
-            for (int s = 0; s < S; ++s) {
-                const float ms = __ldcg(base + s * sstride);
-                const float w = ms == -INFINITY ? 0.f : expf(ms - mx);
-                c.ms.cw[s] = w;
-                L += w * __ldcg(base + s * sstride + 1);
-            }
-            c.ms.cw[255] = 1.0f / L;
-        }
-        cbar();
-        for (int e = tid; e < 128; e += NCT) {
-            const int dim = dc * 128 + e;
-            float v = 0.f;
-            for (int s = 0; s < S; ++s) v = fmaf(c.ms.cw[s], __ldcg(base + s * sstride + 2 + dim), v);
-            Ld.olat[(size_t)m * MLA_H * MLA_KL + h * MLA_KL + dim] = v * c.ms.cw[255];
-        }
+        const int units = nch_of(p, b, MLA_CH) + 1, tg = mla_target(p);
+        S = units < tg ? units : tg;
+        r0 = (size_t)m * p.s_max * MLA_H + h;
+        rstride = MLA_H;
+        D = 128;
+        d0 = dc * 128;
+        OL = MLA_KL;
+        out = Ld.olat + (size_t)m * MLA_H * MLA_KL + h * MLA_KL + d0;
     }
+    // split weights: w_s = exp(m_s - max) / sum_s exp(m_s - max) * l_s
+    float mv = -INFINITY, lv = 0.f;
+    if (tid < S) {
+        const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.part_ml + (r0 + tid * rstride) * 2));
+        mv = ml.x;
+        lv = ml.y;
+    }
+    const float mx = cblock_max(c, mv);
+    const float w = (tid < S && mv != -INFINITY) ? expf(mv - mx) : 0.f;
+    const float L = cblock_sum(c, w * lv);
+    if (tid < S) c.ms.cw[tid] = w / L;
+    cbar();
+    // weighted sum of the O partials: warps take splits, lanes take 4 dims
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (lane * 4 < D) {
+#pragma unroll 4
+        for (int s2 = warp; s2 < S; s2 += NCW) {
+            const float4 v = __ldcg(reinterpret_cast<const float4*>(p.part + (r0 + s2 * rstride) * OL + d0 + lane * 4));
+            const float cw = c.ms.cw[s2];
+            acc.x = fmaf(cw, v.x, acc.x);
+            acc.y = fmaf(cw, v.y, acc.y);
+            acc.z = fmaf(cw, v.z, acc.z);
+            acc.w = fmaf(cw, v.w, acc.w);
+        }
+        *reinterpret_cast<float4*>(c.red() + warp * 128 + lane * 4) = acc;
+    }
+    cbar();
+    for (int e = tid; e < D; e += NCT) {
+        float v = 0.f;
+#pragma unroll
+        for (int w2 = 0; w2 < NCW; ++w2) v += c.red()[w2 * 128 + e];
+        out[e] = v;
+    }
+    cbar();
 }
 
 template <bool PROD>
-__device__ void stage_comb(Ctx& c, int l, const Deps& deps) {
+__device__ __noinline__ void stage_comb(Ctx& c, int l, const Deps& deps) {
     const int n = comb_items(c.p);
     int lo, hi;
     my_range(c.p, n, c.off, lo, hi);
     c.advance(n);
     if constexpr (!PROD) {
         if (lo >= hi) return;
+        const long long t0 = gtimer();
         cwait(c, deps, 0x700u | (unsigned)(l << 16));
+        const long long t1 = gtimer();
         for (int i = lo; i < hi; ++i) cons_comb(c, l, i);
         csignal(c, l, C_COMB, (unsigned)(hi - lo));
+        trace_rec(c, ((unsigned)C_COMB << 16) | (unsigned)l, (unsigned)(hi - lo), t0, t1);
     }
 }
 
@@ -1110,7 +1435,7 @@ __device__ void stage_comb(Ctx& c, int l, const Deps& deps) {
 // item = token: latent = RMSNorm(kv_a latent part) * gain, k_rope = RoPE(kv_a
 // rope part); both rounded to bf16, written to the page and to newlat.
 template <bool PROD>
-__device__ void stage_append(Ctx& c, int l, const Deps& deps) {
+__device__ __noinline__ void stage_append(Ctx& c, int l, const Deps& deps) {
     const Params& p = c.p;
     const int n = p.M;
     int lo, hi;
@@ -1118,23 +1443,21 @@ __device__ void stage_append(Ctx& c, int l, const Deps& deps) {
     c.advance(n);
     if constexpr (!PROD) {
         if (lo >= hi) return;
+        const long long t0 = gtimer();
         cwait(c, deps, 0x800u | (unsigned)(l << 16));
+        const long long t1 = gtimer();
         const Layer& Ld = p.layers[l];
         const int tid = ctid(), lane = tid & 31, warp = tid >> 5;
         for (int m = lo; m < hi; ++m) {
             const int b = m / p.T, t = m - b * p.T, pos = p.pos[b] + t;
             const float* a = Ld.a + (size_t)m * Ld.a_stride + p.ql;
-            cbar();
-            if (warp == 0) {
-                float ss = 0.f;
-                for (int e = lane; e < MLA_KL; e += 32) {
-                    const float v = __ldcg(a + e);
-                    ss = fmaf(v, v, ss);
-                }
-#pragma unroll
-                for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-                if (lane == 0) c.ms.rms[0] = 1.0f / sqrtf(ss / (float)MLA_KL + p.eps);
+            float ss = 0.f;
+            for (int e = tid; e < MLA_KL; e += NCT) {
+                const float v = __ldcg(a + e);
+                ss = fmaf(v, v, ss);
             }
+            ss = cblock_sum(c, ss);
+            if (tid == 0) c.ms.rms[0] = 1.0f / sqrtf(ss / (float)MLA_KL + p.eps);
             cbar();
             uint16_t* pg = const_cast<uint16_t*>(page_ptr(p, p.kv_pool + (size_t)l * p.kv_layer_elems, b, pos / PAGE));
             const int pr = pos % PAGE;
@@ -1155,13 +1478,14 @@ __device__ void stage_append(Ctx& c, int l, const Deps& deps) {
             }
         }
         csignal(c, l, C_APP, (unsigned)(hi - lo));
+        trace_rec(c, ((unsigned)C_APP << 16) | (unsigned)l, (unsigned)(hi - lo), t0, t1);
     }
 }
 
 // ===================================================== residual carry ====
 // (only when the output projection is split over K: x_{l+1} += x_l)
 template <bool PROD>
-__device__ void stage_carry(Ctx& c, int l, const Deps& deps) {
+__device__ __noinline__ void stage_carry(Ctx& c, int l, const Deps& deps) {
     const Params& p = c.p;
     const int chunk = 2048;
     const int n = (p.M * p.d + chunk - 1) / chunk;
@@ -1183,7 +1507,7 @@ __device__ void stage_carry(Ctx& c, int l, const Deps& deps) {
 
 // ===================================================== head / verify ====
 template <bool PROD>
-__device__ void stage_argmax(Ctx& c, const Deps& deps) {
+__device__ __noinline__ void stage_argmax(Ctx& c, const Deps& deps) {
     const Params& p = c.p;
     const int n = p.M;
     int lo, hi;
@@ -1235,7 +1559,7 @@ __device__ void stage_argmax(Ctx& c, const Deps& deps) {
 }
 
 // ====================================================== init (consumers) ====
-__device__ bool init_phase(Ctx& c) {
+__device__ __noinline__ bool init_phase(Ctx& c) {
     const Params& p = c.p;
     const int tid = ctid();
     // every CTA checks the step's inputs itself (all reach the same verdict)
@@ -1265,6 +1589,7 @@ __device__ bool init_phase(Ctx& c) {
         x0[i] = bf2f(p.embed[(size_t)p.tokens[m] * p.d + e]);
     }
     csignal(c, p.L, C_INIT, 1u);
+    trace_rec(c, ((unsigned)C_INIT << 16) | (unsigned)p.L, 1u, c.t_start, c.t_start);
     return !c.dead;
 }
 
@@ -1278,7 +1603,7 @@ __device__ bool prod_check(const Params& p) {
 
 // ============================================================ program ====
 template <bool PROD>
-__device__ void program(Ctx& c) {
+__device__ __forceinline__ void program(Ctx& c) {
     const Params& p = c.p;
     if constexpr (PROD) {
         if (!prod_check(p)) return;
@@ -1404,7 +1729,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) megakernel(const __grid_constant_
     }
     __syncthreads();
     if (ms.abort) return;
-    Ctx c(p, smem);
+    // each warp's schedule state lives in shared memory (its lanes hold the
+    // same values): local memory would miss the small L1 left beside the
+    // 220 KB of shared memory this kernel uses
+    Ctx* cx = reinterpret_cast<Ctx*>(smem + SMEM_CTX) + (threadIdx.x >> 5);
+    if ((threadIdx.x & 31) == 0) new (cx) Ctx(p, smem);
+    __syncwarp();
+    Ctx& c = *cx;
     if (threadIdx.x >= NCT) {
         program<true>(c);
         if (c.dead) prod_drain(c);
