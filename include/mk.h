@@ -155,6 +155,28 @@ int mk_kv_read(const mk_kv* kv, int32_t layer, int32_t seq, int32_t pos0, int32_
 int mk_decode_step(mk_model* m, mk_kv* kv, const int32_t* tokens, const int32_t* positions, int32_t batch,
                    int32_t T, float* logits, int32_t* accept, void* stream);
 
+/* mk_decode_step without any allocation on the call path. The pages have no
+ * counterpart of this entry point: it is for callers that may not allocate
+ * device memory while they run -- code inside a host framework that owns a
+ * fixed memory pool or budget, or a latency-critical serving thread that
+ * must stay out of the driver's allocator.
+ * Same arguments and results as mk_decode_step. The step's scratch
+ * (activations, attention partials, dependency counters, status word, stage
+ * descriptors) lives in one static device array of 64 MiB that every device
+ * which loads this library holds until the process exits; a model whose
+ * step scratch (mk_info.scratch_bytes plus about 1.3 KB per layer) does not
+ * fit, or that has more than 128 layers, is rejected with
+ * MK_ERR_UNSUPPORTED. The first call on each device looks up the array's
+ * device address (set-up): make that first call before any stream capture.
+ * All calls share the array, which keeps the last call's contents; each call
+ * clears what must start at zero. Calls that overlap on the GPU (work of
+ * other streams or host threads still in flight) race on the array. The
+ * call synchronises `stream` and returns the step's device status itself
+ * (MK_OK, MK_ERR_TIMEOUT, MK_ERR_INVALID_ARG); mk_debug_routing does not see
+ * its routing. */
+int mk_decode_step_noalloc(mk_model* m, mk_kv* kv, const int32_t* tokens, const int32_t* positions, int32_t batch,
+                           int32_t T, float* logits, int32_t* accept, void* stream);
+
 /* Synchronise `stream` and return the device status of the last step
  * (MK_OK, MK_ERR_TIMEOUT, MK_ERR_INVALID_ARG). A failed status resets the
  * model's device state so the next step can run. */

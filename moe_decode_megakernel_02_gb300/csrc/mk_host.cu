@@ -784,3 +784,159 @@ void mk_free(void* h) {
 }
 
 }  // extern "C"
+
+// ===========================================================================
+// Decode step that allocates nothing (mk_decode_step_noalloc).
+//
+// Some callers may not allocate device memory on their call path: code that
+// runs while another component owns the allocator (a host framework with its
+// own fixed memory pool or a strict memory budget), code on a latency-critical
+// thread that must not enter the driver's allocator, or hosts that plan all
+// memory before serving starts. For them this entry point runs the same
+// megakernel as mk_decode_step, but takes its per-step scratch (activations,
+// attention partials, dependency counters, status word and the per-layer
+// stage descriptors) from one file-scope device array of fixed size instead
+// of the model's own scratch allocation. Weights, the KV cache, tokens,
+// positions and logits are the loaded model's / the caller's as usual.
+// ===========================================================================
+#include <mutex>
+
+#ifndef MK_NOALLOC_SCRATCH_BYTES
+#define MK_NOALLOC_SCRATCH_BYTES (64u << 20)  // 64 MiB, held by every device that loads the library
+#endif
+#define MK_NOALLOC_MAX_LAYERS 128
+#define MK_NOALLOC_MAX_DEVICES 64
+
+namespace {
+
+static __device__ __align__(256) uint8_t g_noalloc_scratch[MK_NOALLOC_SCRATCH_BYTES];
+
+// device address of g_noalloc_scratch per device (looked up once per device)
+void* g_noalloc_base[MK_NOALLOC_MAX_DEVICES];
+// host staging of the relocated stage descriptors (fixed size, no allocation)
+mk::Layer g_noalloc_layers[MK_NOALLOC_MAX_LAYERS];
+std::mutex g_noalloc_mu;
+
+// maps a pointer into the model's scratch allocation onto the same offset of
+// the static array; other pointers (weights, caller buffers) are unchanged
+struct Reloc {
+    const uint8_t* from;
+    size_t n;
+    uint8_t* to;
+    template <class T> T* operator()(T* p) const {
+        const uint8_t* b = reinterpret_cast<const uint8_t*>(p);
+        if (b >= from && b < from + n) return reinterpret_cast<T*>(to + (b - from));
+        return p;
+    }
+};
+
+void reloc_gemv(mk::Gemv& g, const Reloc& r) {
+    g.src = r(g.src);
+    g.dst = r(g.dst);
+    g.dst2 = r(g.dst2);
+}
+
+}  // namespace
+
+extern "C" int mk_decode_step_noalloc(mk_model* m, mk_kv* kv, const int32_t* tokens, const int32_t* positions,
+                                      int32_t batch, int32_t T, float* logits, int32_t* accept, void* stream) {
+    if (!m || m->magic != MODEL_MAGIC) return fail(MK_ERR_INVALID_ARG, "bad model handle");
+    if (!kv || kv->magic != KV_MAGIC) return fail(MK_ERR_INVALID_ARG, "bad kv handle");
+    if (kv->m != m) return fail(MK_ERR_STATE, "kv cache belongs to another model");
+    if (!tokens || !positions || !logits) return fail(MK_ERR_INVALID_ARG, "NULL tokens/positions/logits");
+    if (batch < 1 || batch > kv->batch) return fail(MK_ERR_INVALID_ARG, "batch %d out of range", batch);
+    if (T < 1 || T > m->cfg.max_tokens_per_seq) return fail(MK_ERR_INVALID_ARG, "T %d out of range", T);
+    if (accept && T < 2) return fail(MK_ERR_INVALID_ARG, "accept needs T > 1");
+    const int L = m->cfg.n_layers;
+    const size_t desc_off = align256(m->sbytes);
+    const size_t need = desc_off + sizeof(mk::Layer) * (size_t)L;
+    if (L > MK_NOALLOC_MAX_LAYERS || need > (size_t)MK_NOALLOC_SCRATCH_BYTES)
+        return fail(MK_ERR_UNSUPPORTED,
+                    "mk_decode_step_noalloc: this model needs %zu bytes of step scratch (%d layers); the static "
+                    "scratch holds at most %u bytes and %d layers -- use mk_decode_step",
+                    need, L, (unsigned)MK_NOALLOC_SCRATCH_BYTES, MK_NOALLOC_MAX_LAYERS);
+    int dev = 0;
+    CK(cudaGetDevice(&dev));
+    if (dev < 0 || dev >= MK_NOALLOC_MAX_DEVICES) return fail(MK_ERR_UNSUPPORTED, "device id %d too large", dev);
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_base[dev]) {
+        // set-up, once per device, with that device current: in host code the
+        // array's name is only a stand-in, the kernel needs its device address
+        void* ptr = nullptr;
+        CK(cudaGetSymbolAddress(&ptr, g_noalloc_scratch));
+        g_noalloc_base[dev] = ptr;
+    }
+    uint8_t* base = static_cast<uint8_t*>(g_noalloc_base[dev]);
+    cudaStream_t s = (cudaStream_t)stream;
+    const Reloc r{m->sblob, m->sbytes, base};
+    // the array keeps the previous call's contents: start from the model's
+    // scratch image (RoPE table, zero page) and clear the counters and status
+    CK(cudaMemcpyAsync(base, m->sblob, m->sbytes, cudaMemcpyDeviceToDevice, s));
+    CK(cudaMemsetAsync(r(m->ctr), 0, m->ctr_n * sizeof(unsigned), s));
+    CK(cudaMemsetAsync(r(m->status), 0, 64, s));
+    for (int l = 0; l < L; ++l) {
+        mk::Layer& Ld = g_noalloc_layers[l];
+        Ld = m->layers[l];
+        for (int gi = 0; gi < mk::NG; ++gi) reloc_gemv(Ld.g[gi], r);
+        Ld.a = r(Ld.a);
+        Ld.q = r(Ld.q);
+        Ld.qlat = r(Ld.qlat);
+        Ld.olat = r(Ld.olat);
+        Ld.o = r(Ld.o);
+        Ld.rlog = r(Ld.rlog);
+        Ld.x = r(Ld.x);
+        Ld.xn = r(Ld.xn);
+    }
+    mk::Layer* d_layers = reinterpret_cast<mk::Layer*>(base + desc_off);
+    CK(cudaMemcpyAsync(d_layers, g_noalloc_layers, sizeof(mk::Layer) * (size_t)L, cudaMemcpyHostToDevice, s));
+
+    mk::Params P = m->base;
+    P.layers = d_layers;
+    reloc_gemv(P.lm, r);
+    P.rope = r(P.rope);
+    P.zeros = r(P.zeros);
+    P.newlat = r(P.newlat);
+    P.part = r(P.part);
+    P.part_ml = r(P.part_ml);
+    P.amax = r(P.amax);
+    for (int z = 0; z < P.nz; ++z) P.zptr[z] = r(P.zptr[z]);
+    P.ctr = r(P.ctr);
+    P.status = r(P.status);
+    P.dbg_idx = r(m->dbg_idx);
+    P.dbg_w = r(m->dbg_w);
+    P.trace = nullptr;
+    P.trace_n = nullptr;
+    P.trace_items = 0;
+    P.page_elems = (long long)kv->page_elems;
+    P.pps = kv->pps;
+    P.btab = kv->btab;
+    P.kv_cap = kv->max_ctx;
+    P.kv_batch = kv->batch;
+    P.kv_pool = kv->pool;
+    P.kv_layer_elems = (long long)kv->layer_elems;
+    P.tokens = tokens;
+    P.pos = positions;
+    P.B = batch;
+    P.T = T;
+    P.M = batch * T;
+    P.logits = logits;
+    P.accept = accept;
+    P.lm.dst = logits;
+    if (P.lm.n_kc > 1) {
+        P.zptr[P.nz] = logits;
+        P.zn[P.nz++] = (long long)P.M * P.V;
+    }
+    P.parity = 0;
+    void* args[] = {&P};
+    CK(cudaLaunchCooperativeKernel((const void*)mk::megakernel, dim3(m->G), dim3(mk::NTHREADS), args,
+                                   mk::SMEM_TOTAL, s));
+    // report this step's device-side status before returning
+    CK(cudaStreamSynchronize(s));
+    unsigned st[4];
+    CK(cudaMemcpy(st, P.status, sizeof st, cudaMemcpyDeviceToHost));
+    if (st[0] == 0 && st[1] == 0) return MK_OK;
+    if (st[0] == mk::ST_TIMEOUT)
+        return fail(MK_ERR_TIMEOUT, "device wait timed out (where=0x%x, cta=%u)", st[2], st[3]);
+    if (st[0] == mk::ST_INVALID) return fail(MK_ERR_INVALID_ARG, "token id or position out of range for this step");
+    return fail(MK_ERR_CUDA, "device status %u", st[0]);
+}
