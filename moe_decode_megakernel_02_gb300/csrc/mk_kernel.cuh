@@ -267,6 +267,19 @@ __device__ __forceinline__ void gemv_out(Ctx& c, const Gemv& g, int slot, int ex
     }
 }
 
+// 8 products of bf16 weights and fp32 inputs held in registers (no
+// addressable local array: that would live in local memory)
+__device__ __forceinline__ void fma8v(float& a, const uint4 w, const float4 x0, const float4 x1) {
+    a = fmaf(bf_lo(w.x), x0.x, a);
+    a = fmaf(bf_hi(w.x), x0.y, a);
+    a = fmaf(bf_lo(w.y), x0.z, a);
+    a = fmaf(bf_hi(w.y), x0.w, a);
+    a = fmaf(bf_lo(w.z), x1.x, a);
+    a = fmaf(bf_hi(w.z), x1.y, a);
+    a = fmaf(bf_lo(w.w), x1.z, a);
+    a = fmaf(bf_hi(w.w), x1.w, a);
+}
+
 __device__ __forceinline__ void fma8(float& a, const uint4& w, const float (&x)[8]) {
     a = fmaf(bf_lo(w.x), x[0], a);
     a = fmaf(bf_hi(w.x), x[1], a);
@@ -459,15 +472,11 @@ __device__ __noinline__ void gemv_range_reg(Ctx& c, const Gemv& g, int slot, int
                             if (q0 + u < JC) {
                                 const uint4 w = wr[32 * (q0 + u)];
                                 const float* x = xl + 256 * (q0 + u);
-                                float xv[8];
-                                *reinterpret_cast<float4*>(xv) = *reinterpret_cast<const float4*>(x);
-                                *reinterpret_cast<float4*>(xv + 4) = *reinterpret_cast<const float4*>(x + 4);
-                                fma8(a0[u], w, xv);
-                                if (MR > 1) {
-                                    *reinterpret_cast<float4*>(xv) = *reinterpret_cast<const float4*>(x + Kc);
-                                    *reinterpret_cast<float4*>(xv + 4) = *reinterpret_cast<const float4*>(x + Kc + 4);
-                                    fma8(a1[u], w, xv);
-                                }
+                                fma8v(a0[u], w, *reinterpret_cast<const float4*>(x),
+                                      *reinterpret_cast<const float4*>(x + 4));
+                                if (MR > 1)
+                                    fma8v(a1[u], w, *reinterpret_cast<const float4*>(x + Kc),
+                                          *reinterpret_cast<const float4*>(x + Kc + 4));
                             }
                         }
                     }
@@ -1169,21 +1178,31 @@ __device__ __noinline__ void cons_attn_mla(Ctx& c, int l, const AttnItem& it) {
     const int b = it.b, t = it.g, m = b * p.T + t, pos = p.pos[b] + t;
     const bool tail = it.u_hi == it.nch + 1;
     MlaSmem S = mla_smem(c.stage());
+    const long long ta = p.trace_items ? gtimer() : 0;
     cbar();
     c.sk_src = nullptr;
     // queries: [absorbed latent query (512) | roped rope query (64)] * scale, split hi/lo
     const int qh = p.nope + p.rd;
     const float sc = p.attn_scale;
-#pragma unroll 4
-    for (int i = tid; i < MLA_H * (MLA_KL / 4); i += NCT) {
-        const int h = i / (MLA_KL / 4), e = (i - h * (MLA_KL / 4)) * 4;
-        const float4 v = __ldcg(reinterpret_cast<const float4*>(Ld.qlat + (size_t)m * MLA_H * MLA_KL + h * MLA_KL + e));
-        const float f[4] = {v.x * sc, v.y * sc, v.z * sc, v.w * sc};
+    {
+        // 2048 float4 of absorbed queries: all loads in flight, then split
+        // into bf16 hi/lo and store 4 values per 8-byte store
+        const float* qsrc = Ld.qlat + (size_t)m * MLA_H * MLA_KL;
+        float4 v[8];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const uint16_t hi = f2bf(f[j]);
-            S.qhi[h * MLA_QS + e + j] = hi;
-            S.qlo[h * MLA_QS + e + j] = f2bf(f[j] - bf2f(hi));
+        for (int k = 0; k < 8; ++k) v[k] = __ldcg(reinterpret_cast<const float4*>(qsrc) + tid + k * NCT);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int i = tid + k * NCT;  // float4 index: head i/128, element (i%128)*4
+            const int h = i >> 7, e = (i & 127) * 4;
+            const float f0 = v[k].x * sc, f1 = v[k].y * sc, f2 = v[k].z * sc, f3 = v[k].w * sc;
+            const uint16_t h0 = f2bf(f0), h1 = f2bf(f1), h2 = f2bf(f2), h3 = f2bf(f3);
+            const uint16_t l0 = f2bf(f0 - bf2f(h0)), l1 = f2bf(f1 - bf2f(h1)), l2 = f2bf(f2 - bf2f(h2)),
+                           l3 = f2bf(f3 - bf2f(h3));
+            *reinterpret_cast<uint2*>(S.qhi + h * MLA_QS + e) =
+                make_uint2((uint32_t)h0 | ((uint32_t)h1 << 16), (uint32_t)h2 | ((uint32_t)h3 << 16));
+            *reinterpret_cast<uint2*>(S.qlo + h * MLA_QS + e) =
+                make_uint2((uint32_t)l0 | ((uint32_t)l1 << 16), (uint32_t)l2 | ((uint32_t)l3 << 16));
         }
     }
     for (int i = tid; i < MLA_H * (MLA_RD / 2); i += NCT) {
@@ -1214,6 +1233,7 @@ __device__ __noinline__ void cons_attn_mla(Ctx& c, int l, const AttnItem& it) {
         }
     }
     cbar();
+    const long long tb = p.trace_items ? gtimer() : 0;
     float acc[8][4];
 #pragma unroll
     for (int j = 0; j < 8; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
@@ -1234,6 +1254,7 @@ __device__ __noinline__ void cons_attn_mla(Ctx& c, int l, const AttnItem& it) {
         }
         if (ring_chunk) cons_release(c.ms, c.cr);
     }
+    const long long tc = p.trace_items ? gtimer() : 0;
     // partial: unnormalised O rows and (max, sum) per head
     const size_t base = ((size_t)m * p.s_max + it.s) * MLA_H;
 #pragma unroll
@@ -1245,6 +1266,8 @@ __device__ __noinline__ void cons_attn_mla(Ctx& c, int l, const AttnItem& it) {
     cbar();
     if (tid < 16) *reinterpret_cast<float2*>(p.part_ml + (base + tid) * 2) = make_float2(S.mst[tid], S.lst[tid]);
     cbar();
+    // trace: staging ns in `n`, then chunk loop [t_wait = after staging, t_ready = chunks done]
+    if (p.trace_items) trace_rec(c, 0x80000000u | ((unsigned)C_ATTN << 16) | (unsigned)l, (unsigned)(tb - ta), tb, tc);
 }
 
 // producer: bulk-load one MLA chunk (32 positions) into padded smem rows;
