@@ -149,9 +149,17 @@ struct TraceRec {
 };
 
 // ----------------------------------------------------------- smem layout ----
+// one dependency of a stage: wait until counter (layer, which) >= target
+struct Dep {
+    int layer, which;
+    unsigned target;
+};
+
 struct Misc {
     unsigned long long full[NSLOT];
     unsigned long long empty[NSLOT];
+    Dep dep[3];                     // the next consumer wait (written and read by thread 0)
+    int ndep;
     int abort;
     int n_slots, p_nslots;
     float rms[MAX_M];
@@ -170,7 +178,18 @@ constexpr int SMEM_RED = SMEM_STAGE + STAGE_BYTES;
 constexpr int SMEM_MISC = SMEM_RED + RED_FLOATS * 4;
 constexpr int SMEM_CTX = (SMEM_MISC + (int)sizeof(Misc) + 15) & ~15;
 constexpr int CTX_BYTES = 128;  // per warp (checked against sizeof(Ctx))
-constexpr int SMEM_TOTAL = SMEM_CTX + (NCW + 1) * CTX_BYTES;
+// the current layer's descriptors, one copy for the consumers and one for
+// the producer warp (they can be in different layers): gpu-scope acquires
+// invalidate the L1, so descriptors read from global memory would cost an
+// L2 round trip at every use
+constexpr int LAYER_BYTES = ((int)sizeof(Layer) + 15) & ~15;
+constexpr int SMEM_LAYER = SMEM_CTX + (NCW + 1) * CTX_BYTES;
+constexpr int SMEM_PLAYER = SMEM_LAYER + LAYER_BYTES;
+// a copy of the kernel parameters: read through a reference, the parameter
+// block would be fetched like global data, again after every acquire
+constexpr int SMEM_PARAMS = SMEM_PLAYER + LAYER_BYTES;
+constexpr int SMEM_TOTAL = SMEM_PARAMS + (((int)sizeof(Params) + 15) & ~15);
+static_assert(SMEM_TOTAL <= 232448, "shared memory per CTA exceeds 227 KB");
 
 // ------------------------------------------------------------------ PTX ----
 __device__ __forceinline__ uint32_t su32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -189,6 +208,7 @@ __device__ __forceinline__ unsigned ld_relaxed(const unsigned* p) {
     asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
 }
+__device__ __forceinline__ void fence_acq_rel() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 __device__ __forceinline__ void red_release(unsigned* p, unsigned v) {
     asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
@@ -224,6 +244,21 @@ __device__ __forceinline__ void bulk_g2s_pol(void* dst, const void* src, unsigne
             su32(dst)),
         "l"(src), "r"(bytes), "r"(su32(bar)), "l"(pol)
         : "memory");
+}
+// start moving [src, src+bytes) from HBM into L2 (no completion to wait for):
+// the smem ring holds only a few tiles per SM, too few bytes in flight to
+// cover HBM latency under load; tiles prefetched into L2 further ahead fill
+// the ring at L2 latency instead
+__device__ __forceinline__ void l2_prefetch(const void* src, unsigned bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+// the same with an evict-last policy: small vectors every step re-reads
+// (norm gains, layer descriptors) stay in L2 while the weights stream past
+__device__ __forceinline__ void l2_prefetch_keep(const void* src, unsigned bytes) {
+    unsigned long long pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    asm volatile("cp.async.bulk.prefetch.L2.global.L2::cache_hint [%0], %1, %2;" ::"l"(src), "r"(bytes), "l"(pol)
+                 : "memory");
 }
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, unsigned bytes, unsigned long long* bar) {
     asm volatile(
@@ -264,11 +299,19 @@ __device__ __noinline__ void raise_status(const Params& p, unsigned code, unsign
 }
 
 // one thread: wait until *c >= target (acquire); false on abort / timeout
+// (polls with relaxed loads: every gpu-scope acquire invalidates the SM's L1;
+// the fence after the last poll completes the acquire pattern)
 __device__ __noinline__ bool wait_ge(const Params& p, const unsigned* c, unsigned target, unsigned where) {
-    if (ld_acquire(c) >= target) return true;
+    if (ld_relaxed(c) >= target) {
+        fence_acq_rel();
+        return true;
+    }
     const long long t0 = gtimer();
     for (unsigned it = 0;; ++it) {
-        if (ld_acquire(c) >= target) return true;
+        if (ld_relaxed(c) >= target) {
+            fence_acq_rel();
+            return true;
+        }
         if ((it & 31) == 31) {
             if (ld_relaxed(&p.status[1])) return false;
             if (gtimer() - t0 > p.timeout_ns) {

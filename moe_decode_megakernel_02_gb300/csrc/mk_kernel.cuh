@@ -6,10 +6,6 @@
 
 namespace mk {
 
-struct Dep {
-    int layer, which;
-    unsigned target;
-};
 struct Deps {
     Dep d[3];
     int n;
@@ -58,6 +54,10 @@ struct alignas(16) Ctx {
     }
     __device__ float* stage() { return reinterpret_cast<float*>(smem + SMEM_STAGE); }
     __device__ float* red() { return reinterpret_cast<float*>(smem + SMEM_RED); }
+    // this thread's side's copy of the current layer's descriptors
+    __device__ const Layer& layer() const {
+        return *reinterpret_cast<const Layer*>(smem + (threadIdx.x >= NCT ? SMEM_PLAYER : SMEM_LAYER));
+    }
     __device__ void advance(int n) {
         const int o = (int)((off + (long long)n) % p.G);
         __syncwarp();
@@ -87,28 +87,41 @@ static_assert(sizeof(Ctx) <= CTX_BYTES, "Ctx must fit its shared-memory slot");
 
 __device__ __forceinline__ int ctid() { return threadIdx.x; }
 
-// consumer: thread 0 waits for all deps, then every consumer thread passes a
-// barrier (so their later reads of other CTAs' data are ordered after it)
-__device__ bool cwait(Ctx& c, const Deps& ds, unsigned where) {
+// consumer: the stage's dependencies travel through shared memory (thread 0
+// writes them, thread 0 waits on them): stage functions are not inlined and
+// a struct passed by reference would live in each thread's stack
+__device__ __forceinline__ void set_deps(Ctx& c, const Deps& ds) {
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < 3; ++i)
+            if (i < ds.n) c.ms.dep[i] = ds.d[i];
+        c.ms.ndep = ds.n;
+    }
+}
+
+// consumer: thread 0 waits for the deps set by set_deps(), then every
+// consumer thread passes a barrier (so their later reads of other CTAs' data
+// are ordered after it)
+__device__ bool cwait(Ctx& c, unsigned where) {
     if (threadIdx.x == 0 && !c.dead) {
         bool ok = true;
-        for (int i = 0; i < ds.n && ok; ++i)
-            if (ds.d[i].target > 0) ok = wait_ge(c.p, ctr_of(c.p, ds.d[i].layer, ds.d[i].which), ds.d[i].target, where);
+        const int n = c.ms.ndep;
+        for (int i = 0; i < n && ok; ++i) {
+            const Dep d = c.ms.dep[i];
+            if (d.target > 0) ok = wait_ge(c.p, ctr_of(c.p, d.layer, d.which), d.target, where);
+        }
         if (!ok) c.ms.abort = 1;
-        __threadfence();
     }
     cbar();
     if (*(volatile int*)&c.ms.abort) c.dead = true;
     return !c.dead;
 }
 
-// consumer: all consumer threads' global writes done -> release `n` to a counter
+// consumer: all consumer threads' global writes done -> release `n` to a
+// counter (the barrier orders the other threads' writes before thread 0's
+// release, which is cumulative over them)
 __device__ void csignal(Ctx& c, int layer, int which, unsigned n) {
     cbar();
-    if (threadIdx.x == 0 && n) {
-        __threadfence();
-        red_release(ctr_of(c.p, layer, which), n);
-    }
+    if (threadIdx.x == 0 && n) red_release(ctr_of(c.p, layer, which), n);
     if (*(volatile int*)&c.ms.abort) c.dead = true;
 }
 
@@ -156,26 +169,114 @@ __device__ __forceinline__ void trace_rec(Ctx& c, unsigned code, unsigned n, lon
 // =============================================================== GEMV ====
 
 // fill stage[t][0..Kc) with f(input) for tokens m0 .. m0+ms-1
-__device__ __noinline__ void stage_input(Ctx& c, const Gemv& g, const float* src, int grp_off, int kc, int m0, int ms) {
+// small inputs (at most two 8-float chunks per thread, K panel a multiple
+// of 256 so a warp's chunks belong to one token): every global load is
+// issued up front into registers, the values never leave registers between
+// the sum of squares and the scaling, one barrier in between
+__device__ __forceinline__ void stage_input_small(Ctx& c, const Gemv& g, const float* src, int grp_off, int k0, int m0,
+                                                  int ms) {
+    const Params& p = c.p;
+    float* xs = c.stage();
+    const int Kc = g.Kc, tid = ctid(), lane = tid & 31;
+    const int total = ms * Kc, kind = g.in_kind, stride = g.src_stride;
+    float4 va[2], vb[2];
+    uint4 gw[2];
+    int t_[2];
+    bool ok[2];
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+        const int i = (tid + q * NCT) * 8;
+        ok[q] = i < total;
+        const int t = ok[q] ? i / Kc : 0, k = i - t * Kc;
+        t_[q] = t;
+        va[q] = vb[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+        gw[q] = make_uint4(0u, 0u, 0u, 0u);
+        if (ok[q]) {
+            const float* r = src + (size_t)(m0 + t) * stride + grp_off + k0 + k;
+            va[q] = __ldcg(reinterpret_cast<const float4*>(r));
+            vb[q] = __ldcg(reinterpret_cast<const float4*>(r + 4));
+            if (kind == IN_RMS) {
+                gw[q] = __ldg(reinterpret_cast<const uint4*>(g.gain + k0 + k));
+            } else if (kind == IN_SWIGLU) {
+                const float4 ua = __ldcg(reinterpret_cast<const float4*>(r + g.sw_off));
+                const float4 ub = __ldcg(reinterpret_cast<const float4*>(r + g.sw_off + 4));
+                va[q] = make_float4(silu(va[q].x) * ua.x, silu(va[q].y) * ua.y, silu(va[q].z) * ua.z, silu(va[q].w) * ua.w);
+                vb[q] = make_float4(silu(vb[q].x) * ub.x, silu(vb[q].y) * ub.y, silu(vb[q].z) * ub.z, silu(vb[q].w) * ub.w);
+            }
+        }
+    }
+    if (kind == IN_RMS) {
+        float* acc = c.ms.rms;  // zeroed by restage() before its leading barrier
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            float s2 = va[q].x * va[q].x;
+            s2 = fmaf(va[q].y, va[q].y, s2);
+            s2 = fmaf(va[q].z, va[q].z, s2);
+            s2 = fmaf(va[q].w, va[q].w, s2);
+            s2 = fmaf(vb[q].x, vb[q].x, s2);
+            s2 = fmaf(vb[q].y, vb[q].y, s2);
+            s2 = fmaf(vb[q].z, vb[q].z, s2);
+            s2 = fmaf(vb[q].w, vb[q].w, s2);
+#pragma unroll
+            for (int o = 16; o; o >>= 1) s2 += __shfl_xor_sync(0xffffffffu, s2, o);
+            if (lane == 0 && ok[q]) atomicAdd(&acc[t_[q]], s2);
+        }
+        cbar();
+        const float invK = 1.0f / (float)g.K;
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            if (!ok[q]) continue;
+            const float r = 1.0f / sqrtf(acc[t_[q]] * invK + p.eps);
+            const uint4 w = gw[q];
+            va[q] = make_float4(va[q].x * bf_lo(w.x) * r, va[q].y * bf_hi(w.x) * r, va[q].z * bf_lo(w.y) * r,
+                                va[q].w * bf_hi(w.y) * r);
+            vb[q] = make_float4(vb[q].x * bf_lo(w.z) * r, vb[q].y * bf_hi(w.z) * r, vb[q].z * bf_lo(w.w) * r,
+                                vb[q].w * bf_hi(w.w) * r);
+        }
+    }
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+        if (!ok[q]) continue;
+        const int i = (tid + q * NCT) * 8;
+        *reinterpret_cast<float4*>(xs + i) = va[q];
+        *reinterpret_cast<float4*>(xs + i + 4) = vb[q];
+    }
+}
+
+__device__ __forceinline__ void stage_input(Ctx& c, const Gemv& g, const float* src, int grp_off, int kc, int m0, int ms) {
     const Params& p = c.p;
     float* xs = c.stage();
     const int Kc = g.Kc, k0 = kc * Kc, tid = ctid(), lane = tid & 31, warp = tid >> 5;
     const int total = ms * Kc;
+    if (total <= 2 * NCT * 8 && (Kc & 255) == 0 && (g.in_kind != IN_RMS || g.n_kc == 1)) {
+        stage_input_small(c, g, src, g.in_kind == IN_RMS ? 0 : grp_off, k0, m0, ms);
+        return;
+    }
     if (g.in_kind == IN_RMS) {
-        // pass 1: per-token sum of squares over the whole row (all threads);
-        // when the staged chunk is the whole row its raw values land in xs
+        // c.ms.rms[] was zeroed by restage() before its leading barrier.
+        // Whole row staged (one K panel): one pass loads activations and
+        // gains together, stores x*gain and accumulates the sum of squares;
+        // the second pass only scales by 1/rms. Split panels: the sum of
+        // squares runs over the whole row first.
         float* acc = c.ms.rms;
-        for (int t = tid; t < ms; t += NCT) acc[t] = 0.f;
-        cbar();
         const bool whole = g.n_kc == 1;
         const int rowlen = g.K, tot = ms * rowlen;
+        const uint16_t* gain = g.gain;
         float part = 0.f;
         int cur = -1;
 #pragma unroll 4
         for (int i = tid * 4; i < tot; i += NCT * 4) {
             const int t = i / rowlen, k = i - t * rowlen;
             const float4 v = __ldcg(reinterpret_cast<const float4*>(src + (size_t)(m0 + t) * g.src_stride + k));
-            if (whole) *reinterpret_cast<float4*>(xs + i) = v;
+            if (whole) {
+                const uint2 gw = __ldg(reinterpret_cast<const uint2*>(gain + k));
+                float4 o;
+                o.x = v.x * bf_lo(gw.x);
+                o.y = v.y * bf_hi(gw.x);
+                o.z = v.z * bf_lo(gw.y);
+                o.w = v.w * bf_hi(gw.y);
+                *reinterpret_cast<float4*>(xs + i) = o;
+            }
             // a warp's 128 consecutive floats never straddle a row (rows are
             // multiples of 128 floats), so `t` changes uniformly in the warp
             if (t != cur) {
@@ -198,20 +299,26 @@ __device__ __noinline__ void stage_input(Ctx& c, const Gemv& g, const float* src
             if (lane == 0) atomicAdd(&acc[cur], part);
         }
         cbar();
-        if (tid < ms) acc[tid] = 1.0f / sqrtf(acc[tid] / (float)g.K + p.eps);
-        cbar();
+        const float invK = 1.0f / (float)g.K;
 #pragma unroll 4
         for (int i = tid * 4; i < total; i += NCT * 4) {
             const int t = i / Kc, k = i - t * Kc;
-            const float4 v = whole ? *reinterpret_cast<const float4*>(xs + i)
-                                   : __ldcg(reinterpret_cast<const float4*>(src + (size_t)(m0 + t) * g.src_stride + k0 + k));
-            uint2 gw = *reinterpret_cast<const uint2*>(g.gain + k0 + k);
-            const float r = acc[t];
+            const float r = 1.0f / sqrtf(acc[t] * invK + p.eps);
             float4 o;
-            o.x = v.x * r * bf_lo(gw.x);
-            o.y = v.y * r * bf_hi(gw.x);
-            o.z = v.z * r * bf_lo(gw.y);
-            o.w = v.w * r * bf_hi(gw.y);
+            if (whole) {
+                o = *reinterpret_cast<const float4*>(xs + i);
+                o.x *= r;
+                o.y *= r;
+                o.z *= r;
+                o.w *= r;
+            } else {
+                const float4 v = __ldcg(reinterpret_cast<const float4*>(src + (size_t)(m0 + t) * g.src_stride + k0 + k));
+                const uint2 gw = __ldg(reinterpret_cast<const uint2*>(gain + k0 + k));
+                o.x = v.x * bf_lo(gw.x) * r;
+                o.y = v.y * bf_hi(gw.x) * r;
+                o.z = v.z * bf_lo(gw.y) * r;
+                o.w = v.w * bf_hi(gw.y) * r;
+            }
             *reinterpret_cast<float4*>(xs + i) = o;
         }
     } else if (g.in_kind == IN_COPY) {
@@ -278,6 +385,18 @@ __device__ __forceinline__ void fma8v(float& a, const uint4 w, const float4 x0, 
     a = fmaf(bf_hi(w.z), x1.y, a);
     a = fmaf(bf_lo(w.w), x1.z, a);
     a = fmaf(bf_hi(w.w), x1.w, a);
+}
+
+// the same 8 products into two accumulators (halves the dependent chain)
+__device__ __forceinline__ void fma8v2(float& a, float& b, const uint4 w, const float4 x0, const float4 x1) {
+    a = fmaf(bf_lo(w.x), x0.x, a);
+    b = fmaf(bf_hi(w.x), x0.y, b);
+    a = fmaf(bf_lo(w.y), x0.z, a);
+    b = fmaf(bf_hi(w.y), x0.w, b);
+    a = fmaf(bf_lo(w.z), x1.x, a);
+    b = fmaf(bf_hi(w.z), x1.y, b);
+    a = fmaf(bf_lo(w.w), x1.z, a);
+    b = fmaf(bf_hi(w.w), x1.w, b);
 }
 
 __device__ __forceinline__ void fma8(float& a, const uint4& w, const float (&x)[8]) {
@@ -386,7 +505,10 @@ __device__ __forceinline__ bool restage(Ctx& c, const Gemv& g, const float* src,
     if (c.sk_src == src && c.sk_off == grp_off && c.sk_kc == kc && c.sk_m0 == m0 && c.sk_kind == g.in_kind &&
         c.sk_gain == g.gain)
         return false;
-    cbar();  // everyone is done with the previous contents
+    // nobody reads the RMS accumulators between stagings: zero them before
+    // the barrier that ends every use of the previous contents
+    if (g.in_kind == IN_RMS && ctid() < ms) c.ms.rms[ctid()] = 0.f;
+    cbar();
     stage_input(c, g, src, grp_off, kc, m0, ms);
     cbar();
     c.sk_src = src;
@@ -412,16 +534,62 @@ __device__ __forceinline__ bool spin_wait(const Params& p, unsigned long long* b
     }
 }
 
-// M <= 2 tokens, K panel >= 256: a warp owns whole rows of each tile; lanes
-// split K into 16-byte chunks, reading the staged input from shared memory.
-// The tile loop holds no calls and stays well under the register budget (a
-// 9-warp CTA gets 168 registers per thread): spills would go to local memory,
-// which misses the small L1 left beside this kernel's shared memory.
-template <int MR>
-__device__ __noinline__ void gemv_range_reg(Ctx& c, const Gemv& g, int slot, int expert, int j_lo, int j_hi) {
+// ---- split-K GEMV (M <= 8 tokens) ----
+// Every lane handles 8 rows of a tile against ONE 16-byte chunk of the K
+// panel, whose input values it keeps in registers for the whole run; per
+// tile it does 8 shared-memory loads and 64*MR FMAs. A warp's lanes form
+// 32/CPWP row groups of CPWP lanes (CPWP = 32, or 16 for K panels whose row
+// slices are 12 or 16 chunks); the row slice of a warp is CPW <= CPWP
+// chunks wide, and NKS warps (8, 4, 2 or 1) share the same rows with
+// different K slices. The warp reduces its 8*MR partials across the CPWP
+// lanes of a group (each halving step exchanges half of the values, so a
+// lane ends with one sum instead of 8), writes them to its own slot in
+// shared memory, and after one CTA barrier every output sums the NKS warps'
+// partials. The tile's shared-memory traffic is the weights once.
+//   Kc 2048: NKS 8, CPW 32 -> 8 rows    Kc 1024: NKS 4, CPW 32 -> 16 rows
+//   Kc  768: NKS 8, CPW 12 -> 16 rows   Kc  512: NKS 2, CPW 32 -> 32 rows
+//   Kc  256: NKS 1, CPW 32 -> 64 rows   Kc  128: NKS 1, CPW 16 -> 128 rows
+__device__ __forceinline__ int ks_nks(int Kc) {
+    return Kc == 2048 ? 8 : Kc == 1024 ? 4 : Kc == 768 ? 8 : Kc == 512 ? 2 : (Kc == 256 || Kc == 128) ? 1 : 0;
+}
+
+// reduce v[8][MR] across the CPWP lanes of a row group; afterwards a lane
+// holds in v[0] the sum for local row 4*b1 + 2*b2 + b3 (bits CPWP/2,
+// CPWP/4, CPWP/8 of its lane index)
+template <int CPWP, int MR>
+__device__ __forceinline__ void ks_reduce(float (&v)[8][MR]) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int lvl = 0; lvl < 3; ++lvl) {
+        const int o = CPWP >> (lvl + 1), half = 4 >> lvl;
+        const bool up = (lane & o) != 0;
+#pragma unroll
+        for (int k = 0; k < half; ++k)
+#pragma unroll
+            for (int m = 0; m < MR; ++m) {
+                const float send = up ? v[k][m] : v[k + half][m];
+                const float keep = up ? v[k + half][m] : v[k][m];
+                v[k][m] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+            }
+    }
+#pragma unroll
+    for (int o = CPWP / 16; o >= 1; o >>= 1)
+#pragma unroll
+        for (int m = 0; m < MR; ++m) v[0][m] += __shfl_xor_sync(0xffffffffu, v[0][m], o);
+}
+
+template <int CPWP, int MR>
+__device__ __forceinline__ void gemv_range_ks(Ctx& c, const Gemv& g, int slot, int expert, int j_lo, int j_hi) {
     const Params& p = c.p;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int Kc = g.Kc, NC = Kc >> 3, JC = NC >> 5;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, tid = threadIdx.x;
+    constexpr int RG = 32 / CPWP, RWT = 8 * RG;  // row groups per warp, rows per warp tile
+    const int M = p.M, Kc = g.Kc, NC = Kc >> 3, NKS = ks_nks(Kc), CPW = NC / NKS;
+    const int ks = warp % NKS, rb = warp / NKS;
+    const int rg = lane / CPWP, ch = lane % CPWP;
+    const bool act = ch < CPW;
+    const int chunk = ks * CPW + ch;
+    const int lrow = rg + RG * ((lane & (CPWP / 2) ? 4 : 0) + (lane & (CPWP / 4) ? 2 : 0) + (lane & (CPWP / 8) ? 1 : 0));
+    const bool writer = (lane & (CPWP / 8 - 1)) == 0;
     const int n_rb = g.n_rb, R = g.R, N = g.N, grp_rows = g.grp_rows, grp_stride = g.grp_stride;
     const int out_kind = g.out_kind, n_kc = g.n_kc, dst_stride = g.dst_stride;
     float* const dst = g.dst + (size_t)slot * g.dst_sstride;
@@ -430,13 +598,12 @@ __device__ __noinline__ void gemv_range_reg(Ctx& c, const Gemv& g, int slot, int
     Misc& ms = c.ms;
     uint8_t* const ring = c.smem + SMEM_RING;
     const float* const xs = c.stage();
+    float* const part = c.red();  // [2][NCW][RWT*MR]
+    const int ngrp = (M + MR - 1) / MR;
     CRing cr = c.cr;
     bool dead = c.dead, timed_out = false;
-    float wtok0 = 1.f, wtok1 = 1.f;
-    if (expert >= 0) {
-        wtok0 = route_weight(ms, 0, expert, p.topk);
-        if (MR > 1) wtok1 = route_weight(ms, 1, expert, p.topk);
-    }
+    int buf = 0;
+    float4 xa[MR], xb[MR];
     int j = j_lo;
     while (j < j_hi) {
         // a run of items sharing the staged input (same K panel and head group)
@@ -449,7 +616,182 @@ __device__ __noinline__ void gemv_range_reg(Ctx& c, const Gemv& g, int slot, int
             if (kc1 != kc0 || g1 != g0) break;
             ++jend;
         }
-        restage(c, g, src, g0 * grp_stride, kc0, 0, MR);
+        const long long ta = p.trace_items ? gtimer() : 0;
+        restage(c, g, src, g0 * grp_stride, kc0, 0, M);
+        const long long tb = p.trace_items ? gtimer() : 0;
+        long long tc = tb;
+        const int jrun = j;
+        for (; j < jend; ++j) {
+            const int kc = j / n_rb, rbk = j - kc * n_rb;
+            const int r0 = rbk * R, nr = min(R, N - r0);
+            const uint8_t* tile = nullptr;
+            if (!dead) {
+                if (spin_wait(p, &ms.full[cr.slot], cr.phase))
+                    tile = ring + cr.slot * SLOT_BYTES;
+                else
+                    dead = timed_out = true;
+            }
+            if (p.trace_items && j == jrun) tc = gtimer();
+            for (int gi = 0; gi < ngrp; ++gi) {
+                const int mb = gi * MR;
+                if (j == jrun || ngrp > 1) {
+#pragma unroll
+                    for (int m = 0; m < MR; ++m) {
+                        const bool ok = act && mb + m < M;
+                        const float* xp = xs + (size_t)(mb + m) * Kc + chunk * 8;
+                        xa[m] = ok ? *reinterpret_cast<const float4*>(xp) : make_float4(0.f, 0.f, 0.f, 0.f);
+                        xb[m] = ok ? *reinterpret_cast<const float4*>(xp + 4) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
+                }
+                float v[8][MR];
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+#pragma unroll
+                    for (int m = 0; m < MR; ++m) v[i][m] = 0.f;
+                if (tile) {
+                    const uint4* T4 = reinterpret_cast<const uint4*>(tile) + chunk;
+                    const int rw = rb * RWT + rg;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int r = rw + RG * i;
+                        if (act && r < nr) {
+                            const uint4 w = T4[(size_t)r * NC];
+#pragma unroll
+                            for (int m = 0; m < MR; ++m) fma8v(v[i][m], w, xa[m], xb[m]);
+                        }
+                    }
+                }
+                if (gi == ngrp - 1) {
+                    // the tile has been read: hand the slot back to the producer
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&ms.empty[cr.slot]);
+                }
+                ks_reduce<CPWP, MR>(v);
+                if (writer) {
+                    float* pw = part + (buf * NCW + warp) * RWT * MR + lrow * MR;
+#pragma unroll
+                    for (int m = 0; m < MR; ++m) pw[m] = v[0][m];
+                }
+                cbar();
+                if (tile) {
+                    for (int t = tid; t < nr * MR; t += NCT) {
+                        const int r = t / MR, mi = t - r * MR, m = mb + mi;
+                        if (m >= M) continue;
+                        const int b = r / RWT, rl = r - b * RWT;
+                        const float* q = part + ((buf * NCW + b * NKS) * RWT + rl) * MR + mi;
+                        float y = q[0];
+                        for (int k = 1; k < NKS; ++k) y += q[k * RWT * MR];
+                        const int row = r0 + r;
+                        float* d = dst + (size_t)m * dst_stride + row;
+                        if (out_kind == OUT_STORE) {
+                            if (n_kc == 1)
+                                *d = y;
+                            else
+                                atomicAdd(d, y);
+                        } else if (out_kind == OUT_RESID) {
+                            if (n_kc == 1) {
+                                const float nv = __ldcg(d) + y;
+                                *d = nv;
+                                dst2[(size_t)m * dst_stride + row] = nv;
+                            } else {
+                                atomicAdd(d, y);
+                            }
+                        } else {
+                            const float w = expert < 0 ? 1.0f : route_weight(ms, m, expert, p.topk);
+                            if (w != 0.f) atomicAdd(d, w * y);
+                        }
+                    }
+                }
+                buf ^= 1;
+            }
+            if (++cr.slot == NSLOT) {
+                cr.slot = 0;
+                cr.phase ^= 1u;
+            }
+        }
+        // item trace: one record per run (staging time, first tile ready, run done)
+        if (p.trace_items && threadIdx.x == 0) trace_rec(c, 0x80000000u | c.cur_code, (unsigned)(tb - ta), ta, tc);
+    }
+    if (timed_out) {
+        ms.abort = 1;
+        raise_status(p, ST_TIMEOUT, 0x210u);
+    }
+    c.set_ring(cr);
+    if (dead) c.dead = true;
+}
+
+// ---- one-token GEMV with the input in registers ----
+// A warp owns whole rows (rows warp, warp+8, ... of a tile) and its lanes
+// split the K panel into 16-byte chunks; the lane's chunks of the input
+// (lane + 32q, q < JC = Kc/256, at most 8 -> 64 floats) stay in registers for
+// the run. Per tile the shared-memory traffic is the weights once, there is
+// no CTA barrier, and the warps move on to the next tile independently.
+// K panels of 128 elements (16 chunks): two rows per warp pass, 16 lanes each.
+__device__ __forceinline__ void rx_out(const Params& p, Misc& ms, int out_kind, int n_kc, float* d, float* d2, int expert,
+                                       float y) {
+    if (out_kind == OUT_STORE) {
+        if (n_kc == 1)
+            *d = y;
+        else
+            atomicAdd(d, y);
+    } else if (out_kind == OUT_RESID) {
+        if (n_kc == 1) {
+            const float nv = __ldcg(d) + y;
+            *d = nv;
+            *d2 = nv;
+        } else {
+            atomicAdd(d, y);
+        }
+    } else {
+        const float w = expert < 0 ? 1.0f : route_weight(ms, 0, expert, p.topk);
+        if (w != 0.f) atomicAdd(d, w * y);
+    }
+}
+
+template <int JC>
+__device__ __forceinline__ void gemv_range_rx(Ctx& c, const Gemv& g, int slot, int expert, int j_lo, int j_hi) {
+    const Params& p = c.p;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    // JC chunks of 8 elements per lane (K panel = 256*JC); JC == 0: K panel 128
+    constexpr bool wide = JC > 0;
+    constexpr int NC = wide ? 32 * JC : 16;
+    const int n_rb = g.n_rb, R = g.R, N = g.N, grp_rows = g.grp_rows, grp_stride = g.grp_stride;
+    const int out_kind = g.out_kind, n_kc = g.n_kc;
+    float* const dst = g.dst + (size_t)slot * g.dst_sstride;
+    float* const dst2 = g.dst2;
+    const float* src = g.src + (size_t)slot * g.src_sstride;
+    Misc& ms = c.ms;
+    uint8_t* const ring = c.smem + SMEM_RING;
+    const float* const xs = c.stage();
+    CRing cr = c.cr;
+    bool dead = c.dead, timed_out = false;
+    constexpr int NX = wide ? JC : 1;
+    float4 xa[NX], xb[NX];
+    int j = j_lo;
+    while (j < j_hi) {
+        const int kc0 = j / n_rb;
+        const int g0 = grp_rows ? ((j - kc0 * n_rb) * R) / grp_rows : 0;
+        int jend = j + 1;
+        while (jend < j_hi) {
+            const int kc1 = jend / n_rb;
+            const int g1 = grp_rows ? ((jend - kc1 * n_rb) * R) / grp_rows : 0;
+            if (kc1 != kc0 || g1 != g0) break;
+            ++jend;
+        }
+        const long long ta = p.trace_items ? gtimer() : 0;
+        restage(c, g, src, g0 * grp_stride, kc0, 0, 1);
+        const long long tb = p.trace_items ? gtimer() : 0;
+        long long tc = tb;
+        {
+            const int ch0 = wide ? lane : (lane & 15);
+#pragma unroll
+            for (int q = 0; q < NX; ++q) {
+                const float* xp = xs + (ch0 + 32 * q) * 8;
+                xa[q] = *reinterpret_cast<const float4*>(xp);
+                xb[q] = *reinterpret_cast<const float4*>(xp + 4);
+            }
+        }
+        const int jrun = j;
         for (; j < jend; ++j) {
             const int kc = j / n_rb, rb = j - kc * n_rb;
             const int r0 = rb * R, nr = min(R, N - r0);
@@ -460,52 +802,43 @@ __device__ __noinline__ void gemv_range_reg(Ctx& c, const Gemv& g, int slot, int
                 else
                     dead = timed_out = true;
             }
+            if (p.trace_items && j == jrun) tc = gtimer();
             if (tile) {
-                const int RW = nr >> 3, rw0 = warp * RW;
-                for (int r = 0; r < RW; ++r) {
-                    const uint4* wr = reinterpret_cast<const uint4*>(tile) + (size_t)(rw0 + r) * NC + lane;
-                    const float* xl = xs + lane * 8;
-                    float a0[4] = {0.f, 0.f, 0.f, 0.f}, a1[4] = {0.f, 0.f, 0.f, 0.f};
-                    for (int q0 = 0; q0 < JC; q0 += 4) {
+                const uint4* T4 = reinterpret_cast<const uint4*>(tile);
+                if constexpr (wide) {
+                    for (int r = warp; r < nr; r += 8) {
+                        const uint4* w0 = T4 + (size_t)r * NC + lane;
+                        // loads in batches of four ahead of their FMAs, four accumulator chains
+                        float a[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                        for (int u = 0; u < 4; ++u) {
-                            if (q0 + u < JC) {
-                                const uint4 w = wr[32 * (q0 + u)];
-                                const float* x = xl + 256 * (q0 + u);
-                                fma8v(a0[u], w, *reinterpret_cast<const float4*>(x),
-                                      *reinterpret_cast<const float4*>(x + 4));
-                                if (MR > 1)
-                                    fma8v(a1[u], w, *reinterpret_cast<const float4*>(x + Kc),
-                                          *reinterpret_cast<const float4*>(x + Kc + 4));
-                            }
-                        }
-                    }
-                    float y0 = (a0[0] + a0[1]) + (a0[2] + a0[3]);
-                    float y1 = (a1[0] + a1[1]) + (a1[2] + a1[3]);
+                        for (int q0 = 0; q0 < JC; q0 += 4) {
+                            uint4 w[4];
 #pragma unroll
-                    for (int o = 16; o; o >>= 1) {
-                        y0 += __shfl_xor_sync(0xffffffffu, y0, o);
-                        if (MR > 1) y1 += __shfl_xor_sync(0xffffffffu, y1, o);
-                    }
-                    if (lane < MR) {
-                        const int m = lane;
-                        const float v = m ? y1 : y0;
-                        const int row = r0 + rw0 + r;
-                        float* d = dst + (size_t)m * dst_stride + row;
-                        if (out_kind == OUT_STORE) {
-                            if (n_kc == 1) *d = v; else atomicAdd(d, v);
-                        } else if (out_kind == OUT_RESID) {
-                            if (n_kc == 1) {
-                                const float nv = __ldcg(d) + v;
-                                *d = nv;
-                                dst2[(size_t)m * dst_stride + row] = nv;
-                            } else {
-                                atomicAdd(d, v);
-                            }
-                        } else {
-                            const float w = m ? wtok1 : wtok0;
-                            if (w != 0.f) atomicAdd(d, w * v);
+                            for (int u = 0; u < 4; ++u)
+                                if (q0 + u < JC) w[u] = w0[32 * (q0 + u)];
+#pragma unroll
+                            for (int u = 0; u < 4; ++u)
+                                if (q0 + u < JC) fma8v2(a[(2 * u) & 3], a[(2 * u + 1) & 3], w[u], xa[q0 + u], xb[q0 + u]);
                         }
+                        float ya = (a[0] + a[1]) + (a[2] + a[3]);
+#pragma unroll
+                        for (int o = 16; o; o >>= 1) ya += __shfl_xor_sync(0xffffffffu, ya, o);
+                        if (lane == 0) rx_out(p, ms, out_kind, n_kc, dst + r0 + r, dst2 + r0 + r, expert, ya);
+                    }
+                } else {
+                    // 16 chunks per row: lanes 0-15 row r, lanes 16-31 row r + 1
+                    const int half = lane >> 4, ch = lane & 15;
+                    for (int r = warp * 2; r < nr; r += 16) {
+                        const int rr = r + half;
+                        float a = 0.f;
+                        if (rr < nr) {
+                            float a1 = 0.f;
+                            fma8v2(a, a1, T4[(size_t)rr * NC + ch], xa[0], xb[0]);
+                            a += a1;
+                        }
+#pragma unroll
+                        for (int o = 8; o; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+                        if (ch == 0 && rr < nr) rx_out(p, ms, out_kind, n_kc, dst + r0 + rr, dst2 + r0 + rr, expert, a);
                     }
                 }
             }
@@ -516,6 +849,7 @@ __device__ __noinline__ void gemv_range_reg(Ctx& c, const Gemv& g, int slot, int
                 cr.phase ^= 1u;
             }
         }
+        if (p.trace_items && threadIdx.x == 0) trace_rec(c, 0x80000000u | c.cur_code, (unsigned)(tb - ta), ta, tc);
     }
     if (timed_out) {
         ms.abort = 1;
@@ -526,7 +860,7 @@ __device__ __noinline__ void gemv_range_reg(Ctx& c, const Gemv& g, int slot, int
 }
 
 // general path (any M, short K panels): input staged in shared memory
-__device__ __noinline__ void gemv_range_smem(Ctx& c, const Gemv& g, int slot, int expert, int j_lo, int j_hi) {
+__device__ __forceinline__ void gemv_range_smem(Ctx& c, const Gemv& g, int slot, int expert, int j_lo, int j_hi) {
     const Params& p = c.p;
     const float* src = g.src + (size_t)slot * g.src_sstride;
     const int cap = STAGE_FLOATS / g.Kc;
@@ -561,19 +895,56 @@ __device__ __noinline__ void gemv_range_smem(Ctx& c, const Gemv& g, int slot, in
     }
 }
 
-// consumer: GEMV work items [j_lo, j_hi) of one slot
-__device__ __noinline__ void cons_gemv(Ctx& c, const Gemv& g, int slot, int expert, int j_lo, int j_hi) {
-    if (g.Kc >= 256 && c.p.M == 1)
-        gemv_range_reg<1>(c, g, slot, expert, j_lo, j_hi);
-    else if (g.Kc >= 256 && c.p.M == 2)
-        gemv_range_reg<2>(c, g, slot, expert, j_lo, j_hi);
-    else
+// consumer: GEMV work items [j_lo, j_hi) of one slot, two or more tokens:
+// split-K path for two tokens, shared-memory path otherwise. A function of
+// its own: inlined next to the one-token path, the two would together need
+// more registers than a thread has, and spills go to local memory.
+__device__ __noinline__ void gemv_multi(Ctx& c, const Gemv& g, int slot, int expert, int j_lo, int j_hi) {
+    const int M = c.p.M, nks = ks_nks(g.Kc);
+    const bool narrow = g.Kc == 128 || g.Kc == 768;  // row slices of 16 / 12 chunks
+    const bool ks = M == 2 && nks > 0 && g.R <= (8 / nks) * (narrow ? 16 : 8);
+    if (!ks)
         gemv_range_smem(c, g, slot, expert, j_lo, j_hi);
+    else if (narrow)
+        gemv_range_ks<16, 2>(c, g, slot, expert, j_lo, j_hi);
+    else
+        gemv_range_ks<32, 2>(c, g, slot, expert, j_lo, j_hi);
+}
+
+// consumer: GEMV work items [j_lo, j_hi) of one slot
+__device__ __forceinline__ void cons_gemv(Ctx& c, const Gemv& g, int slot, int expert, int j_lo, int j_hi) {
+    const int M = c.p.M, Kc = g.Kc;
+    if (M == 1 && Kc == 2048)
+        gemv_range_rx<8>(c, g, slot, expert, j_lo, j_hi);
+    else if (M == 1 && Kc == 1024)
+        gemv_range_rx<4>(c, g, slot, expert, j_lo, j_hi);
+    else if (M == 1 && Kc == 768)
+        gemv_range_rx<3>(c, g, slot, expert, j_lo, j_hi);
+    else if (M == 1 && Kc == 512)
+        gemv_range_rx<2>(c, g, slot, expert, j_lo, j_hi);
+    else if (M == 1 && Kc == 256)
+        gemv_range_rx<1>(c, g, slot, expert, j_lo, j_hi);
+    else if (M == 1 && Kc == 128)
+        gemv_range_rx<0>(c, g, slot, expert, j_lo, j_hi);
+    else
+        gemv_multi(c, g, slot, expert, j_lo, j_hi);
     if (*(volatile int*)&c.ms.abort) c.dead = true;
 }
 
 // producer: bulk-load the weight tiles of items [lo, hi) (one slot). All
 // descriptor fields and the ring state live in registers for the loop.
+// L2 prefetch of weight tiles [lo, hi) of one slot (one lane per tile)
+__device__ __forceinline__ void prefetch_tiles(const Gemv& g, int expert, int lo, int hi) {
+    const uint16_t* W = g.W + (expert >= 0 ? (size_t)expert * g.w_estride : 0);
+    for (int j = lo + (int)(threadIdx.x & 31); j < hi; j += 32) {
+        const int kc = j / g.n_rb, rb = j - kc * g.n_rb;
+        const int r0 = rb * g.R, nr = min(g.R, g.N - r0);
+        l2_prefetch(W + (size_t)kc * g.N * g.Kc + (size_t)r0 * g.Kc, (unsigned)nr * g.Kc * 2u);
+    }
+}
+
+constexpr int PF_TILES = 8;  // L2 prefetch distance beyond the ring, in tiles
+
 __device__ __noinline__ void prod_gemv(Ctx& c, const Gemv& g, int expert, int lo, int hi) {
     const uint16_t* W = g.W + (expert >= 0 ? (size_t)expert * g.w_estride : 0);
     const int n_rb = g.n_rb, R = g.R, N = g.N, Kc = g.Kc;
@@ -584,11 +955,16 @@ __device__ __noinline__ void prod_gemv(Ctx& c, const Gemv& g, int expert, int lo
     int issued = c.issued;
     const bool leader = (threadIdx.x & 31) == 0;
     const unsigned long long pol = l2_evict_first();
+    prefetch_tiles(g, expert, lo, min(hi, lo + PF_TILES));
     for (int j = lo; j < hi; ++j) {
         const int kc = j / n_rb, rb = j - kc * n_rb;
         const int r0 = rb * R, nr = min(R, N - r0);
         const unsigned bytes = (unsigned)nr * Kc * 2u;
         const uint16_t* src = W + (size_t)kc * N * Kc + (size_t)r0 * Kc;
+        if (leader && j + PF_TILES < hi) {
+            const int jp = j + PF_TILES, kp = jp / n_rb, rp = (jp - kp * n_rb) * R;
+            l2_prefetch(W + (size_t)kp * N * Kc + (size_t)rp * Kc, (unsigned)min(R, N - rp) * Kc * 2u);
+        }
         int ok = 1;
         if (leader) {
             if (spin_wait(p, &ms.empty[pr.slot], pr.phase ^ 1u)) {
@@ -610,8 +986,43 @@ __device__ __noinline__ void prod_gemv(Ctx& c, const Gemv& g, int expert, int lo
     c.set_pring(pr, issued);
 }
 
+// consumer side of a GEMV stage (mode MM_PLAIN: items [lo, hi) of g after the
+// deps set by set_deps, then signal `sig`) or of a routed-expert stage
+// (MM_GU / MM_DOWN: items are slots x per-slot items; gate/up signals per
+// slot, each down slot first waits for its gate/up). The only call site of
+// the GEMV code, so it is compiled once.
+enum { MM_PLAIN = 0, MM_GU = 1, MM_DOWN = 2 };
+__device__ __noinline__ void cons_mm(Ctx& c, int l, const Gemv& g, int sig, int mode, int lo, int hi) {
+    const Params& p = c.p;
+    const int per = gemv_items(g);
+    const int code = mode == MM_PLAIN ? sig : (mode == MM_GU ? C_GU0 : C_DOWN);
+    c.cur_code = ((unsigned)code << 16) | (unsigned)l;
+    const long long t0 = gtimer();
+    long long tw = 0;
+    if (mode == MM_PLAIN) {
+        cwait(c, 0x1000u | (unsigned)(l << 16) | (unsigned)sig);
+        tw = gtimer() - t0;
+    }
+    for (int i = lo; i < hi;) {
+        const int s2 = mode == MM_PLAIN ? 0 : i / per;
+        const int iend = mode == MM_PLAIN ? hi : min(hi, (s2 + 1) * per);
+        if (mode == MM_DOWN) {
+            const long long a = gtimer();
+            set_deps(c, deps1(l, C_GU0 + s2, (unsigned)gemv_items(c.layer().g[G_GU])));
+            cwait(c, 0x500u);
+            tw += gtimer() - a;
+        }
+        const int expert = mode == MM_PLAIN ? -1 : (int)c.ms.slot_e[s2];
+        cons_gemv(c, g, s2, expert, i - s2 * per, iend - s2 * per);
+        if (mode == MM_GU) csignal(c, l, C_GU0 + s2, (unsigned)(iend - i));
+        i = iend;
+    }
+    if (mode != MM_GU) csignal(c, l, mode == MM_PLAIN ? sig : C_DOWN, (unsigned)(hi - lo));
+    trace_rec(c, ((unsigned)code << 16) | (unsigned)l, (unsigned)(hi - lo), t0, t0 + tw);
+}
+
 template <bool PROD>
-__device__ __noinline__ void stage_gemv(Ctx& c, int l, const Gemv& g, const Deps& deps, int sig) {
+__device__ __forceinline__ void stage_gemv(Ctx& c, int l, const Gemv& g, const Deps& deps, int sig) {
     const int n = gemv_items(g);
     int lo, hi;
     my_range(c.p, n, c.off, lo, hi);
@@ -620,13 +1031,8 @@ __device__ __noinline__ void stage_gemv(Ctx& c, int l, const Gemv& g, const Deps
     if constexpr (PROD) {
         if (!c.dead) prod_gemv(c, g, -1, lo, hi);
     } else {
-        c.cur_code = ((unsigned)sig << 16) | (unsigned)l;
-        const long long t0 = gtimer();
-        cwait(c, deps, 0x1000u | (unsigned)(l << 16) | (unsigned)sig);
-        const long long t1 = gtimer();
-        cons_gemv(c, g, 0, -1, lo, hi);
-        csignal(c, l, sig, (unsigned)(hi - lo));
-        trace_rec(c, ((unsigned)sig << 16) | (unsigned)l, (unsigned)(hi - lo), t0, t1);
+        set_deps(c, deps);
+        cons_mm(c, l, g, sig, MM_PLAIN, lo, hi);
     }
 }
 
@@ -637,7 +1043,7 @@ __device__ __noinline__ void stage_gemv(Ctx& c, int l, const Gemv& g, const Deps
 template <bool PROD>
 __device__ __noinline__ bool route(Ctx& c, int l) {
     const Params& p = c.p;
-    const Layer& Ld = p.layers[l];
+    const Layer& Ld = c.layer();
     const int E = p.E, k = p.topk;
     const int tid = threadIdx.x, lane = tid & 31;
     uint8_t* used = PROD ? c.ms.p_used : c.ms.used;
@@ -658,7 +1064,8 @@ __device__ __noinline__ bool route(Ctx& c, int l) {
         __syncwarp();
     } else {
         const long long t0 = gtimer();
-        cwait(c, deps1(l, C_ROUTER, (unsigned)gemv_items(Ld.g[G_ROUTER])), 0x400u);
+        set_deps(c, deps1(l, C_ROUTER, (unsigned)gemv_items(Ld.g[G_ROUTER])));
+        cwait(c, 0x400u);
         trace_rec(c, (0x40u << 16) | (unsigned)l, 0u, t0, gtimer());
         for (int e = tid; e < E; e += NCT) used[e] = 0;
         cbar();
@@ -757,10 +1164,9 @@ __device__ __noinline__ bool route(Ctx& c, int l) {
 
 // routed-expert stage: items = slots x (row blocks x k panels), slot-major
 template <bool PROD>
-__device__ __noinline__ void stage_experts(Ctx& c, int l, const Gemv& g, bool down) {
+__device__ __forceinline__ void stage_experts(Ctx& c, int l, const Gemv& g, bool down) {
     const Params& p = c.p;
     const int nslots = PROD ? c.ms.p_nslots : c.ms.n_slots;
-    const uint8_t* slot_e = PROD ? c.ms.p_slot_e : c.ms.slot_e;
     const int per = gemv_items(g);
     const int n = nslots * per;
     int lo, hi;
@@ -768,31 +1174,34 @@ __device__ __noinline__ void stage_experts(Ctx& c, int l, const Gemv& g, bool do
     c.advance(n);
     if (lo >= hi) return;
     if constexpr (PROD) {
+        const uint8_t* slot_e = c.ms.p_slot_e;
+        if (!down) {
+            // the routing is known: start every gate/up and down tile of this
+            // CTA towards L2 now (the down stage's items follow the shared
+            // expert's down projection in the item rotation)
+            for (int i = lo; i < hi;) {
+                const int s2 = i / per, iend = min(hi, (s2 + 1) * per);
+                prefetch_tiles(g, slot_e[s2], i - s2 * per, iend - s2 * per);
+                i = iend;
+            }
+            const Gemv& gd = c.layer().g[G_DOWN];
+            const int perd = gemv_items(gd), nd = nslots * perd;
+            const int n_sh = p.has_sh ? gemv_items(c.layer().g[G_SHDOWN]) : 0;
+            int dlo, dhi;
+            my_range(p, nd, (int)((c.off + (long long)n_sh) % p.G), dlo, dhi);
+            for (int i = dlo; i < dhi;) {
+                const int s2 = i / perd, iend = min(dhi, (s2 + 1) * perd);
+                prefetch_tiles(gd, slot_e[s2], i - s2 * perd, iend - s2 * perd);
+                i = iend;
+            }
+        }
         for (int i = lo; i < hi && !c.dead;) {
             const int s2 = i / per, iend = min(hi, (s2 + 1) * per);
             prod_gemv(c, g, slot_e[s2], i - s2 * per, iend - s2 * per);
             i = iend;
         }
     } else {
-        const Layer& Ld = p.layers[l];
-        c.cur_code = ((unsigned)(down ? C_DOWN : C_GU0) << 16) | (unsigned)l;
-        const long long t0 = gtimer();
-        long long tw = 0;
-        // a slot's items are contiguous: run them together; gate/up signals
-        // per slot, each down slot first waits for its gate/up
-        for (int i = lo; i < hi;) {
-            const int s2 = i / per, iend = min(hi, (s2 + 1) * per);
-            if (down) {
-                const long long a = gtimer();
-                cwait(c, deps1(l, C_GU0 + s2, (unsigned)gemv_items(Ld.g[G_GU])), 0x500u);
-                tw += gtimer() - a;
-            }
-            cons_gemv(c, g, s2, slot_e[s2], i - s2 * per, iend - s2 * per);
-            if (!down) csignal(c, l, C_GU0 + s2, (unsigned)(iend - i));
-            i = iend;
-        }
-        if (down) csignal(c, l, C_DOWN, (unsigned)(hi - lo));
-        trace_rec(c, ((unsigned)(down ? C_DOWN : C_GU0) << 16) | (unsigned)l, (unsigned)(hi - lo), t0, t0 + tw);
+        cons_mm(c, l, g, 0, down ? MM_DOWN : MM_GU, lo, hi);
     }
 }
 
@@ -919,9 +1328,9 @@ __device__ void gqa_rows(const Params& p, GqaState<DPL>& st, const float (&q)[8]
 }
 
 template <int DPL>
-__device__ __noinline__ void cons_attn_gqa(Ctx& c, int l, const AttnItem& it) {
+__device__ __forceinline__ void cons_attn_gqa(Ctx& c, int l, const AttnItem& it) {
     const Params& p = c.p;
-    const Layer& Ld = p.layers[l];
+    const Layer& Ld = c.layer();
     const int hd = p.hd, Gq = p.Hq / p.Hkv, T = p.T, Q = T * Gq, half = hd / 2;
     const int tid = ctid(), lane = tid & 31, warp = tid >> 5;
     const int b = it.b, g = it.g, pos0 = p.pos[b];
@@ -1171,9 +1580,9 @@ __device__ __forceinline__ void mla_chunk(const MlaSmem& S, const uint16_t* ck, 
     }
 }
 
-__device__ __noinline__ void cons_attn_mla(Ctx& c, int l, const AttnItem& it) {
+__device__ __forceinline__ void cons_attn_mla(Ctx& c, int l, const AttnItem& it) {
     const Params& p = c.p;
-    const Layer& Ld = p.layers[l];
+    const Layer& Ld = c.layer();
     const int tid = ctid(), lane = tid & 31, warp = tid >> 5, g = lane >> 2, t4 = lane & 3;
     const int b = it.b, t = it.g, m = b * p.T + t, pos = p.pos[b] + t;
     const bool tail = it.u_hi == it.nch + 1;
@@ -1327,8 +1736,28 @@ __device__ __noinline__ void prod_gqa_chunk(Ctx& c, int l, int b, int g, int u) 
     prod_next(c.pr);
 }
 
+__device__ __noinline__ void attn_cons(Ctx& c, int l, int lo, int hi) {
+    const Params& p = c.p;
+    const long long t0 = gtimer();
+    cwait(c, 0x600u | (unsigned)(l << 16));
+    const long long t1 = gtimer();
+    for (int i = lo; i < hi; ++i) {
+        const AttnItem it = attn_item(p, i);
+        if (p.attn == 0) {
+            if (p.hd == 128)
+                cons_attn_gqa<4>(c, l, it);
+            else
+                cons_attn_gqa<2>(c, l, it);
+        } else {
+            cons_attn_mla(c, l, it);
+        }
+    }
+    csignal(c, l, C_ATTN, (unsigned)(hi - lo));
+    trace_rec(c, ((unsigned)C_ATTN << 16) | (unsigned)l, (unsigned)(hi - lo), t0, t1);
+}
+
 template <bool PROD>
-__device__ __noinline__ void stage_attn(Ctx& c, int l, const Deps& deps) {
+__device__ __forceinline__ void stage_attn(Ctx& c, int l, const Deps& deps) {
     const Params& p = c.p;
     const int n = attn_items(p);
     int lo, hi;
@@ -1346,22 +1775,8 @@ __device__ __noinline__ void stage_attn(Ctx& c, int l, const Deps& deps) {
             }
         }
     } else {
-        const long long t0 = gtimer();
-        cwait(c, deps, 0x600u | (unsigned)(l << 16));
-        const long long t1 = gtimer();
-        for (int i = lo; i < hi; ++i) {
-            const AttnItem it = attn_item(p, i);
-            if (p.attn == 0) {
-                if (p.hd == 128)
-                    cons_attn_gqa<4>(c, l, it);
-                else
-                    cons_attn_gqa<2>(c, l, it);
-            } else {
-                cons_attn_mla(c, l, it);
-            }
-        }
-        csignal(c, l, C_ATTN, (unsigned)(hi - lo));
-        trace_rec(c, ((unsigned)C_ATTN << 16) | (unsigned)l, (unsigned)(hi - lo), t0, t1);
+        set_deps(c, deps);
+        attn_cons(c, l, lo, hi);
     }
 }
 
@@ -1370,9 +1785,9 @@ __device__ __noinline__ void stage_attn(Ctx& c, int l, const Deps& deps) {
 // MLA: item (token, head, 128-dim chunk) -> olat[m][h*512 ...]
 __device__ int comb_items(const Params& p) { return p.attn == 0 ? p.M * p.Hq : p.M * MLA_H * 4; }
 
-__device__ __noinline__ void cons_comb(Ctx& c, int l, int i) {
+__device__ __forceinline__ void cons_comb(Ctx& c, int l, int i) {
     const Params& p = c.p;
-    const Layer& Ld = p.layers[l];
+    const Layer& Ld = c.layer();
     const int tid = ctid(), lane = tid & 31, warp = tid >> 5;
     size_t r0, rstride;
     int S, D, d0, OL;
@@ -1437,78 +1852,101 @@ __device__ __noinline__ void cons_comb(Ctx& c, int l, int i) {
     cbar();
 }
 
+__device__ __noinline__ void comb_cons(Ctx& c, int l, int lo, int hi) {
+    const long long t0 = gtimer();
+    cwait(c, 0x700u | (unsigned)(l << 16));
+    const long long t1 = gtimer();
+    for (int i = lo; i < hi; ++i) cons_comb(c, l, i);
+    csignal(c, l, C_COMB, (unsigned)(hi - lo));
+    trace_rec(c, ((unsigned)C_COMB << 16) | (unsigned)l, (unsigned)(hi - lo), t0, t1);
+}
+
 template <bool PROD>
-__device__ __noinline__ void stage_comb(Ctx& c, int l, const Deps& deps) {
+__device__ __forceinline__ void stage_comb(Ctx& c, int l, const Deps& deps) {
     const int n = comb_items(c.p);
     int lo, hi;
     my_range(c.p, n, c.off, lo, hi);
     c.advance(n);
     if constexpr (!PROD) {
         if (lo >= hi) return;
-        const long long t0 = gtimer();
-        cwait(c, deps, 0x700u | (unsigned)(l << 16));
-        const long long t1 = gtimer();
-        for (int i = lo; i < hi; ++i) cons_comb(c, l, i);
-        csignal(c, l, C_COMB, (unsigned)(hi - lo));
-        trace_rec(c, ((unsigned)C_COMB << 16) | (unsigned)l, (unsigned)(hi - lo), t0, t1);
+        set_deps(c, deps);
+        comb_cons(c, l, lo, hi);
     }
 }
 
 // ========================================================= MLA append ====
 // item = token: latent = RMSNorm(kv_a latent part) * gain, k_rope = RoPE(kv_a
 // rope part); both rounded to bf16, written to the page and to newlat.
-template <bool PROD>
-__device__ __noinline__ void stage_append(Ctx& c, int l, const Deps& deps) {
+__device__ __noinline__ void append_cons(Ctx& c, int l, int lo, int hi) {
     const Params& p = c.p;
-    const int n = p.M;
+    const long long t0 = gtimer();
+    cwait(c, 0x800u | (unsigned)(l << 16));
+    const long long t1 = gtimer();
+    const Layer& Ld = c.layer();
+    const int tid = ctid(), lane = tid & 31, warp = tid >> 5;
+    for (int m = lo; m < hi; ++m) {
+        const int b = m / p.T, t = m - b * p.T, pos = p.pos[b] + t;
+        const float* a = Ld.a + (size_t)m * Ld.a_stride + p.ql;
+        float ss = 0.f;
+        for (int e = tid; e < MLA_KL; e += NCT) {
+            const float v = __ldcg(a + e);
+            ss = fmaf(v, v, ss);
+        }
+        ss = cblock_sum(c, ss);
+        if (tid == 0) c.ms.rms[0] = 1.0f / sqrtf(ss / (float)MLA_KL + p.eps);
+        cbar();
+        uint16_t* pg = const_cast<uint16_t*>(page_ptr(p, p.kv_pool + (size_t)l * p.kv_layer_elems, b, pos / PAGE));
+        const int pr = pos % PAGE;
+        uint16_t* nl = p.newlat + (size_t)m * MLA_D;
+        for (int e = tid; e < MLA_D; e += NCT) {
+            uint16_t v;
+            if (e < MLA_KL) {
+                v = f2bf(__ldcg(a + e) * c.ms.rms[0] * bf2f(Ld.kv_norm[e]));
+                pg[(size_t)pr * MLA_KL + e] = v;
+            } else {
+                const int r = e - MLA_KL, hr = MLA_RD / 2, ri = r < hr ? r : r - hr;
+                const float2 cs = p.rope[(size_t)pos * p.rope_half + ri];
+                const float x0 = __ldcg(a + MLA_KL + ri), x1 = __ldcg(a + MLA_KL + ri + hr);
+                v = f2bf(r < hr ? (x0 * cs.x - x1 * cs.y) : (x1 * cs.x + x0 * cs.y));
+                pg[(size_t)PAGE * MLA_KL + (size_t)pr * MLA_RD + r] = v;
+            }
+            nl[e] = v;
+        }
+    }
+    csignal(c, l, C_APP, (unsigned)(hi - lo));
+    trace_rec(c, ((unsigned)C_APP << 16) | (unsigned)l, (unsigned)(hi - lo), t0, t1);
+}
+
+template <bool PROD>
+__device__ __forceinline__ void stage_append(Ctx& c, int l, const Deps& deps) {
+    const int n = c.p.M;
     int lo, hi;
-    my_range(p, n, c.off, lo, hi);
+    my_range(c.p, n, c.off, lo, hi);
     c.advance(n);
     if constexpr (!PROD) {
         if (lo >= hi) return;
-        const long long t0 = gtimer();
-        cwait(c, deps, 0x800u | (unsigned)(l << 16));
-        const long long t1 = gtimer();
-        const Layer& Ld = p.layers[l];
-        const int tid = ctid(), lane = tid & 31, warp = tid >> 5;
-        for (int m = lo; m < hi; ++m) {
-            const int b = m / p.T, t = m - b * p.T, pos = p.pos[b] + t;
-            const float* a = Ld.a + (size_t)m * Ld.a_stride + p.ql;
-            float ss = 0.f;
-            for (int e = tid; e < MLA_KL; e += NCT) {
-                const float v = __ldcg(a + e);
-                ss = fmaf(v, v, ss);
-            }
-            ss = cblock_sum(c, ss);
-            if (tid == 0) c.ms.rms[0] = 1.0f / sqrtf(ss / (float)MLA_KL + p.eps);
-            cbar();
-            uint16_t* pg = const_cast<uint16_t*>(page_ptr(p, p.kv_pool + (size_t)l * p.kv_layer_elems, b, pos / PAGE));
-            const int pr = pos % PAGE;
-            uint16_t* nl = p.newlat + (size_t)m * MLA_D;
-            for (int e = tid; e < MLA_D; e += NCT) {
-                uint16_t v;
-                if (e < MLA_KL) {
-                    v = f2bf(__ldcg(a + e) * c.ms.rms[0] * bf2f(Ld.kv_norm[e]));
-                    pg[(size_t)pr * MLA_KL + e] = v;
-                } else {
-                    const int r = e - MLA_KL, hr = MLA_RD / 2, ri = r < hr ? r : r - hr;
-                    const float2 cs = p.rope[(size_t)pos * p.rope_half + ri];
-                    const float x0 = __ldcg(a + MLA_KL + ri), x1 = __ldcg(a + MLA_KL + ri + hr);
-                    v = f2bf(r < hr ? (x0 * cs.x - x1 * cs.y) : (x1 * cs.x + x0 * cs.y));
-                    pg[(size_t)PAGE * MLA_KL + (size_t)pr * MLA_RD + r] = v;
-                }
-                nl[e] = v;
-            }
-        }
-        csignal(c, l, C_APP, (unsigned)(hi - lo));
-        trace_rec(c, ((unsigned)C_APP << 16) | (unsigned)l, (unsigned)(hi - lo), t0, t1);
+        set_deps(c, deps);
+        append_cons(c, l, lo, hi);
     }
 }
 
 // ===================================================== residual carry ====
 // (only when the output projection is split over K: x_{l+1} += x_l)
+__device__ __noinline__ void carry_cons(Ctx& c, int l, int lo, int hi) {
+    const Params& p = c.p;
+    const int chunk = 2048;
+    cwait(c, 0x900u | (unsigned)(l << 16));
+    const Layer& Ld = c.layer();
+    const int total = p.M * p.d;
+    for (int i = lo * chunk + ctid(); i < min(hi * chunk, total); i += NCT) {
+        const int m = i / p.d, e = i - m * p.d;
+        atomicAdd(Ld.xn + (size_t)m * p.d + e, __ldcg(Ld.x + (size_t)m * p.d + e));
+    }
+    csignal(c, l, C_CARRY, (unsigned)(hi - lo));
+}
+
 template <bool PROD>
-__device__ __noinline__ void stage_carry(Ctx& c, int l, const Deps& deps) {
+__device__ __forceinline__ void stage_carry(Ctx& c, int l, const Deps& deps) {
     const Params& p = c.p;
     const int chunk = 2048;
     const int n = (p.M * p.d + chunk - 1) / chunk;
@@ -1517,67 +1955,66 @@ __device__ __noinline__ void stage_carry(Ctx& c, int l, const Deps& deps) {
     c.advance(n);
     if constexpr (!PROD) {
         if (lo >= hi) return;
-        cwait(c, deps, 0x900u | (unsigned)(l << 16));
-        const Layer& Ld = p.layers[l];
-        const int total = p.M * p.d;
-        for (int i = lo * chunk + ctid(); i < min(hi * chunk, total); i += NCT) {
-            const int m = i / p.d, e = i - m * p.d;
-            atomicAdd(Ld.xn + (size_t)m * p.d + e, __ldcg(Ld.x + (size_t)m * p.d + e));
-        }
-        csignal(c, l, C_CARRY, (unsigned)(hi - lo));
+        set_deps(c, deps);
+        carry_cons(c, l, lo, hi);
     }
 }
 
 // ===================================================== head / verify ====
-template <bool PROD>
-__device__ __noinline__ void stage_argmax(Ctx& c, const Deps& deps) {
+__device__ __noinline__ void argmax_cons(Ctx& c, int lo, int hi) {
     const Params& p = c.p;
-    const int n = p.M;
+    cwait(c, 0xa00u);
+    const int tid = ctid(), lane = tid & 31, warp = tid >> 5;
+    float* bv = c.red();
+    int* bi = reinterpret_cast<int*>(c.red() + NCW);
+    for (int m = lo; m < hi; ++m) {
+        const float* lg = p.logits + (size_t)m * p.V;
+        float v = -INFINITY;
+        int id = 0x7fffffff;
+        for (int e = tid; e < p.V; e += NCT) {
+            const float x = __ldcg(lg + e);
+            if (x > v || (x == v && e < id)) {
+                v = x;
+                id = e;
+            }
+        }
+#pragma unroll
+        for (int o = 16; o; o >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, v, o);
+            const int oi = __shfl_xor_sync(0xffffffffu, id, o);
+            if (ov > v || (ov == v && oi < id)) {
+                v = ov;
+                id = oi;
+            }
+        }
+        cbar();
+        if (lane == 0) {
+            bv[warp] = v;
+            bi[warp] = id;
+        }
+        cbar();
+        if (tid == 0) {
+            for (int w = 1; w < NCW; ++w)
+                if (bv[w] > v || (bv[w] == v && bi[w] < id)) {
+                    v = bv[w];
+                    id = bi[w];
+                }
+            p.amax[m] = id;
+        }
+    }
+    csignal(c, p.L, C_AMAX, (unsigned)(hi - lo));
+}
+
+template <bool PROD>
+__device__ __forceinline__ void stage_argmax(Ctx& c, const Deps& deps) {
+    const int n = c.p.M;
     int lo, hi;
-    my_range(p, n, c.off, lo, hi);
+    my_range(c.p, n, c.off, lo, hi);
     c.advance(n);
     if constexpr (!PROD) {
         if (lo >= hi) return;
-        cwait(c, deps, 0xa00u);
-        const int tid = ctid(), lane = tid & 31, warp = tid >> 5;
-        float* bv = c.red();
-        int* bi = reinterpret_cast<int*>(c.red() + NCW);
-        for (int m = lo; m < hi; ++m) {
-            const float* lg = p.logits + (size_t)m * p.V;
-            float v = -INFINITY;
-            int id = 0x7fffffff;
-            for (int e = tid; e < p.V; e += NCT) {
-                const float x = __ldcg(lg + e);
-                if (x > v || (x == v && e < id)) {
-                    v = x;
-                    id = e;
-                }
-            }
-#pragma unroll
-            for (int o = 16; o; o >>= 1) {
-                const float ov = __shfl_xor_sync(0xffffffffu, v, o);
-                const int oi = __shfl_xor_sync(0xffffffffu, id, o);
-                if (ov > v || (ov == v && oi < id)) {
-                    v = ov;
-                    id = oi;
-                }
-            }
-            cbar();
-            if (lane == 0) {
-                bv[warp] = v;
-                bi[warp] = id;
-            }
-            cbar();
-            if (tid == 0) {
-                for (int w = 1; w < NCW; ++w)
-                    if (bv[w] > v || (bv[w] == v && bi[w] < id)) {
-                        v = bv[w];
-                        id = bi[w];
-                    }
-                p.amax[m] = id;
-            }
-        }
-        csignal(c, p.L, C_AMAX, (unsigned)(hi - lo));
+        set_deps(c, deps);
+        argmax_cons(c, lo, hi);
     }
 }
 
@@ -1624,6 +2061,80 @@ __device__ bool prod_check(const Params& p) {
     return true;
 }
 
+// producer, at the start of an MLA layer: start this CTA's attention chunks
+// (latent rows and rope rows of the cached prefix) towards L2, so that the
+// ring fills them at L2 latency when the attention stage comes. The item
+// rotation offset of the attention stage follows from the stages before it.
+__device__ __noinline__ void prefetch_attn_mla(Ctx& c, int l) {
+    const Params& p = c.p;
+    const Layer& Ld = c.layer();
+    const long long ahead = (long long)gemv_items(Ld.g[G_A]) + gemv_items(Ld.g[G_QB]) + p.M + gemv_items(Ld.g[G_QLAT]);
+    int lo, hi;
+    my_range(p, attn_items(p), (int)((c.off + ahead) % p.G), lo, hi);
+    const int lane = threadIdx.x & 31;
+    const uint16_t* pool = p.kv_pool + (size_t)l * p.kv_layer_elems;
+    for (int i = lo; i < hi; ++i) {
+        const AttnItem it = attn_item(p, i);
+        const int u1 = min(it.u_hi, it.nch);
+        for (int u = it.u_lo + lane; u < u1; u += 32) {
+            const int nvalid = min(MLA_CH, p.pos[it.b] - u * MLA_CH);
+            const uint16_t* pg = page_ptr(p, pool, it.b, (u * MLA_CH) / PAGE);
+            const int r0 = (u * MLA_CH) % PAGE;
+            l2_prefetch(pg + (size_t)r0 * MLA_KL, (unsigned)nvalid * MLA_KL * 2u);
+            l2_prefetch(pg + (size_t)PAGE * MLA_KL + (size_t)r0 * MLA_RD, (unsigned)nvalid * MLA_RD * 2u);
+        }
+    }
+}
+
+// producer, at the start of layer l: the next layer's descriptors and norm
+// gains (or the head's final norm gain) towards L2, kept there
+__device__ __noinline__ void prefetch_next_small(Ctx& c, int l) {
+    const Params& p = c.p;
+    const int lane = threadIdx.x & 31;
+    if (l + 1 < p.L) {
+        const Layer* nx = p.layers + l + 1;
+        if (lane == 0) l2_prefetch_keep(nx, (unsigned)sizeof(Layer));
+        const uint16_t* gp = nullptr;
+        int n = 0;
+        if (lane == 1) {
+            gp = nx->g[G_A].gain;
+            n = nx->g[G_A].K;
+        } else if (lane == 2 && nx->g[G_QB].in_kind == IN_RMS) {
+            gp = nx->g[G_QB].gain;
+            n = nx->g[G_QB].K;
+        } else if (lane == 3 && p.attn == 1) {
+            gp = nx->kv_norm;
+            n = MLA_KL;
+        } else if (lane == 4) {
+            const Gemv& f = p.E > 0 ? nx->g[G_ROUTER] : nx->g[G_SHGU];
+            gp = f.gain;
+            n = f.K;
+        }
+        if (gp && n > 0) l2_prefetch_keep(gp, (unsigned)n * 2u);
+    } else if (lane == 0 && p.lm.gain) {
+        l2_prefetch_keep(p.lm.gain, (unsigned)p.lm.K * 2u);
+    }
+}
+
+// copy layer l's descriptors into this side's shared-memory slot (the
+// leading barrier ends every use of the previous layer's copy)
+template <bool PROD>
+__device__ __forceinline__ void load_layer(Ctx& c, int l) {
+    constexpr int N16 = (int)sizeof(Layer) / 16;
+    static_assert(sizeof(Layer) % 16 == 0, "Layer is copied in 16-byte pieces");
+    const uint4* src = reinterpret_cast<const uint4*>(c.p.layers + l);
+    uint4* dst = reinterpret_cast<uint4*>(c.smem + (PROD ? SMEM_PLAYER : SMEM_LAYER));
+    if constexpr (PROD) {
+        __syncwarp();
+        for (int i = threadIdx.x & 31; i < N16; i += 32) dst[i] = __ldg(src + i);
+        __syncwarp();
+    } else {
+        cbar();
+        for (int i = ctid(); i < N16; i += NCT) dst[i] = __ldg(src + i);
+        cbar();
+    }
+}
+
 // ============================================================ program ====
 template <bool PROD>
 __device__ __forceinline__ void program(Ctx& c) {
@@ -1638,7 +2149,12 @@ __device__ __forceinline__ void program(Ctx& c) {
         if constexpr (PROD) {
             if (c.dead) return;
         }
-        const Layer& Ld = p.layers[l];
+        load_layer<PROD>(c, l);
+        if constexpr (PROD) {
+            if (p.attn == 1) prefetch_attn_mla(c, l);
+            prefetch_next_small(c, l);
+        }
+        const Layer& Ld = c.layer();
         Deps prev;
         if (l == 0) {
             prev = deps1(p.L, C_INIT, (unsigned)p.G);
@@ -1676,15 +2192,20 @@ __device__ __forceinline__ void program(Ctx& c) {
             stage_carry<PROD>(c, l, deps1(l, C_O, nO));
             n_carry = (p.M * p.d + 2047) / 2048;
         }
+        // routed gate/up first: the shared expert's down projection (whose
+        // input is ready well before the routing) fills the gap before the
+        // routed down projections, instead of delaying the routed experts
+        n_down = 0;
+        if (p.E > 0) {
+            if (!route<PROD>(c, l) && PROD) return;
+            stage_experts<PROD>(c, l, Ld.g[G_GU], false);
+        }
         n_shdown = 0;
         if (p.has_sh) {
             stage_gemv<PROD>(c, l, Ld.g[G_SHDOWN], deps1(l, C_SHGU, (unsigned)gemv_items(Ld.g[G_SHGU])), C_SHDOWN);
             n_shdown = gemv_items(Ld.g[G_SHDOWN]);
         }
-        n_down = 0;
         if (p.E > 0) {
-            if (!route<PROD>(c, l) && PROD) return;
-            stage_experts<PROD>(c, l, Ld.g[G_GU], false);
             stage_experts<PROD>(c, l, Ld.g[G_DOWN], true);
             n_down = (PROD ? c.ms.p_nslots : c.ms.n_slots) * gemv_items(Ld.g[G_DOWN]);
         }
@@ -1702,7 +2223,8 @@ __device__ __forceinline__ void program(Ctx& c) {
         stage_argmax<PROD>(c, deps1(p.L, C_LM, (unsigned)gemv_items(p.lm)));
         if constexpr (!PROD) {
             if (blockIdx.x == 0) {
-                cwait(c, deps1(p.L, C_AMAX, (unsigned)p.M), 0xb00u);
+                set_deps(c, deps1(p.L, C_AMAX, (unsigned)p.M));
+                cwait(c, 0xb00u);
                 const int b = ctid();
                 if (b < p.B && !c.dead) {
                     int a = 0;
@@ -1750,13 +2272,19 @@ __global__ void __launch_bounds__(NTHREADS, 1) megakernel(const __grid_constant_
         ms.n_slots = ms.p_nslots = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
+    {
+        static_assert(sizeof(Params) % 4 == 0, "Params is copied in 4-byte words");
+        const uint32_t* ps = reinterpret_cast<const uint32_t*>(&p);
+        uint32_t* pd = reinterpret_cast<uint32_t*>(smem + SMEM_PARAMS);
+        for (int i = threadIdx.x; i < (int)(sizeof(Params) / 4); i += blockDim.x) pd[i] = ps[i];
+    }
     __syncthreads();
     if (ms.abort) return;
     // each warp's schedule state lives in shared memory (its lanes hold the
     // same values): local memory would miss the small L1 left beside the
     // 220 KB of shared memory this kernel uses
     Ctx* cx = reinterpret_cast<Ctx*>(smem + SMEM_CTX) + (threadIdx.x >> 5);
-    if ((threadIdx.x & 31) == 0) new (cx) Ctx(p, smem);
+    if ((threadIdx.x & 31) == 0) new (cx) Ctx(*reinterpret_cast<const Params*>(smem + SMEM_PARAMS), smem);
     __syncwarp();
     Ctx& c = *cx;
     if (threadIdx.x >= NCT) {
