@@ -56,7 +56,7 @@ constexpr int MLA_CHUNK_BYTES = MLA_CH * MLA_CS * 2 + MLA_CH * MLA_RS * 2;
 static_assert(MLA_CHUNK_BYTES <= SLOT_BYTES, "MLA chunk must fit a slot");
 
 enum InKind { IN_COPY = 0, IN_RMS = 1, IN_SWIGLU = 2 };
-enum OutKind { OUT_STORE = 0, OUT_RESID = 1, OUT_SCALED = 2 };
+enum OutKind { OUT_STORE = 0, OUT_RESID = 1, OUT_SCALED = 2, OUT_ACC = 3 };  // OUT_ACC: += into a CTA-private buffer
 enum StatusCode { ST_OK = 0, ST_INVALID = 1, ST_TIMEOUT = 5 };
 
 // A matrix-vector stage: out[m][row] (+)= W[row, :] . f(in)[m, :]
@@ -79,10 +79,30 @@ struct Gemv {
     float* dst2;                  // OUT_RESID: next layer's residual
 };
 
-enum { G_A = 0, G_QB, G_QLAT, G_UV, G_O, G_ROUTER, G_SHGU, G_SHDOWN, G_GU, G_DOWN, NG };
+enum { G_A = 0, G_QB, G_QLAT, G_UV, G_O, G_ROUTER, NG };
+
+// SwiGLU experts as units: unit u of an expert owns F of its Fi intermediate
+// dimensions. Its gate and up rows (2F rows of the gate/up matrix, whose rows
+// are stored unit-major: gate rows then up rows of unit 0, of unit 1, ...)
+// and its F columns of the down matrix (stored per unit as [d][F]) are all a
+// CTA needs to add the unit's share of the expert output to the residual:
+// no exchange between CTAs inside the FFN.
+struct FfnKind {
+    const uint16_t* gu;       // [n_kc][2*Fi][Kc], rows unit-major
+    const uint16_t* dn;       // [nu][d][F]
+    long long gu_es, dn_es;   // elements between routed experts
+    int Fi, F, nu;            // intermediate width, unit width, units per expert
+    int R, Rd;                // gate/up rows per tile, down rows per tile
+};
+struct Ffn {
+    FfnKind k[2];             // [0] routed experts, [1] shared expert
+    int Kc, n_kc;             // gate/up K panel
+    const uint16_t* gain;     // FFN RMSNorm gain
+};
 
 struct Layer {
     Gemv g[NG];
+    Ffn ffn;
     const uint16_t* kv_norm;  // MLA latent RMSNorm gain
     const float* a;           // GQA: q|k|v   MLA: c_q | latent | k_rope   [M][a_stride]
     const float* q;           // MLA: q_b output [M][H*(nope+rope)]
@@ -128,6 +148,9 @@ struct Params {
     float* zptr[6];
     long long zn[6];                // floats to zero at the start of the step
     int nz, carry;                  // carry: residual copied by items (split-K output projection)
+    int gs;                         // CTAs [0, gs) run the shared expert, [gs, G) router + routed experts
+    float* ubuf;                    // per CTA: expert-unit gate/up and hidden values when shared memory is short
+    long long ubuf_stride;          // floats per CTA
     unsigned* ctr;                  // [2][L+1][NCTR]
     int parity;
     unsigned* status;               // [0] code [1] abort [2] where [3] cta
@@ -160,6 +183,8 @@ struct Misc {
     unsigned long long empty[NSLOT];
     Dep dep[3];                     // the next consumer wait (written and read by thread 0)
     int ndep;
+    Gemv ug, pug;                   // expert-unit gate/up GEMV (consumers, producer)
+    float uw[MAX_M];                // expert-unit routing weight per token
     int abort;
     int n_slots, p_nslots;
     float rms[MAX_M];
@@ -177,7 +202,7 @@ constexpr int SMEM_STAGE = NSLOT * SLOT_BYTES;
 constexpr int SMEM_RED = SMEM_STAGE + STAGE_BYTES;
 constexpr int SMEM_MISC = SMEM_RED + RED_FLOATS * 4;
 constexpr int SMEM_CTX = (SMEM_MISC + (int)sizeof(Misc) + 15) & ~15;
-constexpr int CTX_BYTES = 128;  // per warp (checked against sizeof(Ctx))
+constexpr int CTX_BYTES = 160;  // per warp (checked against sizeof(Ctx))
 // the current layer's descriptors, one copy for the consumers and one for
 // the producer warp (they can be in different layers): gpu-scope acquires
 // invalidate the L1, so descriptors read from global memory would cost an
@@ -350,6 +375,17 @@ __device__ __forceinline__ void my_range(const Params& p, int n, int off, int& l
     if (v >= p.G) v -= p.G;
     lo = (int)((long long)v * n / p.G);
     hi = (int)((long long)(v + 1) * n / p.G);
+}
+
+// n items over the CTAs [c0, c0 + gc) only (empty range for the others)
+__device__ __forceinline__ void my_range_sub(int n, int c0, int gc, int& lo, int& hi) {
+    const int v = (int)blockIdx.x - c0;
+    if (v < 0 || v >= gc) {
+        lo = hi = 0;
+        return;
+    }
+    lo = (int)((long long)v * n / gc);
+    hi = (int)((long long)(v + 1) * n / gc);
 }
 
 __device__ __forceinline__ int gemv_items(const Gemv& g) { return g.n_rb * g.n_kc; }

@@ -97,6 +97,26 @@ Dims dims_of(const mk_config& c) {
 
 bool k_ok(int K) { return K == 128 || (K > 0 && K % 256 == 0 && (K <= 2048 || K % 1024 == 0 || K % 512 == 0)); }
 
+// unit width for an expert of Fi intermediate dimensions on a d-wide model:
+// about 384 KB of gate/up weights per unit; 0 if no width divides Fi
+int unit_width(int Fi, int d) {
+    const int target = 98304 / d;
+    for (int F : {64, 48, 32, 16})
+        if ((F <= target || F == 16) && Fi % F == 0) return F;
+    return 0;
+}
+
+// gate/up K panel (as for every GEMV) and rows per tile dividing 2F
+void unit_geometry(int d, int F, int& Kc, int& R, int& Rd) {
+    Kc = d > 2048 ? (d % 1024 == 0 ? 1024 : (d % 512 == 0 ? 512 : 256)) : d;
+    R = (mk::TILE_MAX / (2 * Kc)) / 8 * 8;
+    if (R > 2 * F) R = 2 * F;
+    while (R > 8 && (2 * F) % R) R -= 8;
+    Rd = mk::TILE_MAX / (2 * F) / 256 * 256;
+    if (Rd < 256) Rd = 256;
+    if (Rd > d) Rd = d;
+}
+
 int validate(const mk_config* c) {
     if (!c) return fail(MK_ERR_INVALID_ARG, "cfg is NULL");
     if (c->n_layers < 1 || c->d_model < 1 || c->vocab < 1 || c->max_batch < 1 || c->max_tokens_per_seq < 1 ||
@@ -129,6 +149,8 @@ int validate(const mk_config* c) {
     if (d.sh < 0 || d.sh > 1) return fail(MK_ERR_UNSUPPORTED, "n_shared_experts must be 0 or 1");
     if (d.sh && (d.sffn % 8 || !k_ok(d.sffn))) return fail(MK_ERR_UNSUPPORTED, "shared_ffn_dim");
     if (d.E == 0 && !d.sh) return fail(MK_ERR_UNSUPPORTED, "model needs routed or shared experts");
+    if (d.E && !unit_width(d.ffn, d.d)) return fail(MK_ERR_UNSUPPORTED, "ffn_dim must be a multiple of 16");
+    if (d.sh && !unit_width(d.sffn, d.d)) return fail(MK_ERR_UNSUPPORTED, "shared_ffn_dim must be a multiple of 16");
     if (d.V % 8) return fail(MK_ERR_UNSUPPORTED, "vocab must be a multiple of 8");
     return MK_OK;
 }
@@ -167,6 +189,35 @@ int pack_rows(uint16_t* dst, int N, int K, int Kc, int row0, const void* src, in
                              rows, cudaMemcpyDefault, s));
     }
     return MK_OK;
+}
+
+// SwiGLU expert as units of F intermediate dimensions (see mk::FfnKind):
+// gate/up rows unit-major, [n_kc][2 Fi][Kc]; row 2F u + j is gate row uF + j
+// (j < F) or up row uF + j - F
+__global__ void pack_gu_units(uint16_t* __restrict__ dst, const uint16_t* __restrict__ gate,
+                              const uint16_t* __restrict__ up, int Fi, int d, int F, int Kc) {
+    const size_t per_kc = (size_t)2 * Fi * Kc, n8 = (size_t)(d / Kc) * per_kc / 8;
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += (size_t)gridDim.x * blockDim.x) {
+        const size_t e = i * 8;
+        const int kc = (int)(e / per_kc);
+        const size_t rem = e - (size_t)kc * per_kc;
+        const int row = (int)(rem / Kc), k = (int)(rem - (size_t)row * Kc);
+        const int u = row / (2 * F), j = row - u * 2 * F;
+        const uint16_t* src = j < F ? gate + (size_t)(u * F + j) * d : up + (size_t)(u * F + j - F) * d;
+        *reinterpret_cast<uint4*>(dst + e) = *reinterpret_cast<const uint4*>(src + (size_t)kc * Kc + k);
+    }
+}
+
+// down matrix [d][Fi] -> per unit [nu][d][F]
+__global__ void pack_dn_units(uint16_t* __restrict__ dst, const uint16_t* __restrict__ src, int Fi, int d, int F) {
+    const size_t n8 = (size_t)d * Fi / 8, per_u = (size_t)d * F;
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += (size_t)gridDim.x * blockDim.x) {
+        const size_t e = i * 8;
+        const int u = (int)(e / per_u);
+        const size_t rem = e - (size_t)u * per_u;
+        const int r = (int)(rem / F), f = (int)(rem - (size_t)r * F);
+        *reinterpret_cast<uint4*>(dst + e) = *reinterpret_cast<const uint4*>(src + (size_t)r * Fi + (size_t)u * F + f);
+    }
 }
 
 __global__ void transpose_heads(const uint16_t* __restrict__ in, uint16_t* __restrict__ out, int H, int rows_in,
@@ -321,10 +372,11 @@ int mk_load_weights(const mk_config* cfg, const mk_weight* table, int32_t n, voi
     const size_t s_qlat = D.gqa ? 0 : stake((size_t)L * Mx * D.Hq * D.kl * 4);
     const size_t s_olat = D.gqa ? 0 : stake((size_t)L * Mx * D.Hq * D.kl * 4);
     const size_t s_o = stake((size_t)L * Mx * D.o_in * 4);
-    const int nsl = D.E ? (int)std::min<size_t>((size_t)D.E, Mx * D.k) : 0;
     const size_t s_rlog = D.E ? stake((size_t)L * Mx * D.E * 4) : 0;
-    const size_t s_gu = D.E ? stake((size_t)L * nsl * Mx * 2 * D.ffn * 4) : 0;
-    const size_t s_shgu = D.sh ? stake((size_t)L * Mx * 2 * D.sffn * 4) : 0;
+    // expert units: per CTA, gate/up outputs and hidden values of at most one
+    // expert's units for every token
+    const size_t ubuf_stride = (size_t)3 * std::max(D.E ? D.ffn : 0, D.sh ? D.sffn : 0) * Mx;
+    const size_t s_ubuf = stake((size_t)m->G * ubuf_stride * 4);
     const size_t part_rows = D.gqa ? (size_t)cfg->max_batch * D.Hkv * m->G * Q8 : (size_t)Mx * m->G * mk::MLA_H;
     const size_t s_part = stake(part_rows * (D.gqa ? D.hd : mk::MLA_KL) * 4);
     const size_t s_part_ml = stake(part_rows * 2 * 4);
@@ -375,6 +427,8 @@ int mk_load_weights(const mk_config* cfg, const mk_weight* table, int32_t n, voi
     CK(cudaMemcpyAsync(W + off_fn, p, (size_t)d * 2, cudaMemcpyDefault, s));
     uint16_t* tmp = nullptr;  // device staging for the MLA W_uk transpose
     if (!D.gqa) CK(cudaMalloc(&tmp, (size_t)D.Hq * (D.nope + D.vd) * D.kl * 2));
+    uint16_t* etmp = nullptr;  // device staging of one expert (gate, up, down)
+    CK(cudaMalloc(&etmp, (size_t)3 * std::max(D.E ? D.ffn : 0, D.sh ? D.sffn : 0) * d * 2));
     for (int l = 0; l < L; ++l) {
         const Off& o = lo[l];
         NEED(MK_W_ATTN_NORM, l, 0);
@@ -409,27 +463,35 @@ int mk_load_weights(const mk_config* cfg, const mk_weight* table, int32_t n, voi
         }
         NEED(MK_W_WO, l, 0);
         PACK(W + o.o, d, D.o_in, 0, p, d);
+        // experts: gate, up and down go through a device copy, then into the
+        // unit layout
+        auto pack_expert = [&](int kgate, int kup, int kdown, int e, int Fi, uint16_t* gu, uint16_t* dn) -> int {
+            const size_t n = (size_t)Fi * d;
+            const int F = unit_width(Fi, d);
+            int Kc, R, Rd;
+            unit_geometry(d, F, Kc, R, Rd);
+            if ((r = need(kgate, l, e, &p))) return r;
+            CK(cudaMemcpyAsync(etmp, p, n * 2, cudaMemcpyDefault, s));
+            if ((r = need(kup, l, e, &p))) return r;
+            CK(cudaMemcpyAsync(etmp + n, p, n * 2, cudaMemcpyDefault, s));
+            if ((r = need(kdown, l, e, &p))) return r;
+            CK(cudaMemcpyAsync(etmp + 2 * n, p, n * 2, cudaMemcpyDefault, s));
+            pack_gu_units<<<1024, 256, 0, s>>>(gu, etmp, etmp + n, Fi, d, F, Kc);
+            CK(cudaGetLastError());
+            pack_dn_units<<<1024, 256, 0, s>>>(dn, etmp + 2 * n, Fi, d, F);
+            CK(cudaGetLastError());
+            return MK_OK;
+        };
         if (D.E) {
             NEED(MK_W_ROUTER, l, 0);
             PACK(W + o.router, D.E, d, 0, p, D.E);
-            for (int e = 0; e < D.E; ++e) {
-                uint16_t* gu = W + o.gu + (size_t)e * 2 * D.ffn * d;
-                NEED(MK_W_GATE, l, e);
-                PACK(gu, 2 * D.ffn, d, 0, p, D.ffn);
-                NEED(MK_W_UP, l, e);
-                PACK(gu, 2 * D.ffn, d, D.ffn, p, D.ffn);
-                NEED(MK_W_DOWN, l, e);
-                PACK(W + o.down + (size_t)e * d * D.ffn, d, D.ffn, 0, p, d);
-            }
+            for (int e = 0; e < D.E; ++e)
+                if ((r = pack_expert(MK_W_GATE, MK_W_UP, MK_W_DOWN, e, D.ffn, W + o.gu + (size_t)e * 2 * D.ffn * d,
+                                     W + o.down + (size_t)e * d * D.ffn)))
+                    return bail(r);
         }
-        if (D.sh) {
-            NEED(MK_W_SH_GATE, l, 0);
-            PACK(W + o.shgu, 2 * D.sffn, d, 0, p, D.sffn);
-            NEED(MK_W_SH_UP, l, 0);
-            PACK(W + o.shgu, 2 * D.sffn, d, D.sffn, p, D.sffn);
-            NEED(MK_W_SH_DOWN, l, 0);
-            PACK(W + o.shdown, d, D.sffn, 0, p, d);
-        }
+        if (D.sh && (r = pack_expert(MK_W_SH_GATE, MK_W_SH_UP, MK_W_SH_DOWN, 0, D.sffn, W + o.shgu, W + o.shdown)))
+            return bail(r);
     }
 #undef NEED
 #undef PACK
@@ -448,6 +510,7 @@ int mk_load_weights(const mk_config* cfg, const mk_weight* table, int32_t n, voi
         CK(cudaStreamSynchronize(s));  // rt and tmp go out of scope
     }
     if (tmp) CK(cudaFree(tmp));
+    CK(cudaFree(etmp));
 
     // ---- stage descriptors ----
     m->layers.resize(L);
@@ -486,29 +549,29 @@ int mk_load_weights(const mk_config* cfg, const mk_weight* table, int32_t n, voi
             Ld.g[mk::G_UV].grp_stride = D.kl;
         }
         make_gemv(Ld.g[mk::G_O], W + o.o, d, D.o_in, mk::IN_COPY, ob, D.o_in, nullptr, mk::OUT_RESID, x, d, xn);
+        Ld.ffn.gain = W + o.fn;
+        auto set_kind = [&](mk::FfnKind& K, int Fi, const uint16_t* gu, const uint16_t* dn) {
+            K.gu = gu;
+            K.dn = dn;
+            K.gu_es = (long long)2 * Fi * d;
+            K.dn_es = (long long)d * Fi;
+            K.Fi = Fi;
+            K.F = unit_width(Fi, d);
+            K.nu = Fi / K.F;
+            int Kc, R, Rd;
+            unit_geometry(d, K.F, Kc, R, Rd);
+            K.R = R;
+            K.Rd = Rd;
+            Ld.ffn.Kc = Kc;
+            Ld.ffn.n_kc = d / Kc;
+        };
         if (D.E) {
             float* rlog = F(s_rlog) + (size_t)l * Mx * D.E;
-            float* gu = F(s_gu) + (size_t)l * nsl * Mx * 2 * D.ffn;
             Ld.rlog = rlog;
             make_gemv(Ld.g[mk::G_ROUTER], W + o.router, D.E, d, mk::IN_RMS, x, d, W + o.fn, mk::OUT_STORE, rlog, D.E);
-            make_gemv(Ld.g[mk::G_GU], W + o.gu, 2 * D.ffn, d, mk::IN_RMS, x, d, W + o.fn, mk::OUT_STORE, gu,
-                      2 * D.ffn);
-            Ld.g[mk::G_GU].w_estride = (long long)2 * D.ffn * d;
-            Ld.g[mk::G_GU].dst_sstride = (long long)Mx * 2 * D.ffn;
-            make_gemv(Ld.g[mk::G_DOWN], W + o.down, d, D.ffn, mk::IN_SWIGLU, gu, 2 * D.ffn, nullptr, mk::OUT_SCALED,
-                      xn, d);
-            Ld.g[mk::G_DOWN].w_estride = (long long)d * D.ffn;
-            Ld.g[mk::G_DOWN].src_sstride = (long long)Mx * 2 * D.ffn;
-            Ld.g[mk::G_DOWN].sw_off = D.ffn;
+            set_kind(Ld.ffn.k[0], D.ffn, W + o.gu, W + o.down);
         }
-        if (D.sh) {
-            float* shgu = F(s_shgu) + (size_t)l * Mx * 2 * D.sffn;
-            make_gemv(Ld.g[mk::G_SHGU], W + o.shgu, 2 * D.sffn, d, mk::IN_RMS, x, d, W + o.fn, mk::OUT_STORE, shgu,
-                      2 * D.sffn);
-            make_gemv(Ld.g[mk::G_SHDOWN], W + o.shdown, d, D.sffn, mk::IN_SWIGLU, shgu, 2 * D.sffn, nullptr,
-                      mk::OUT_SCALED, xn, d);
-            Ld.g[mk::G_SHDOWN].sw_off = D.sffn;
-        }
+        if (D.sh) set_kind(Ld.ffn.k[1], D.sffn, W + o.shgu, W + o.shdown);
     }
     (void)Mxi;
     CK(cudaMalloc(&m->d_layers, sizeof(mk::Layer) * L));
@@ -541,20 +604,14 @@ int mk_load_weights(const mk_config* cfg, const mk_weight* table, int32_t n, voi
         P.trace_items = atoi(getenv("MK_TRACE")) > 1;
     }
     P.amax = reinterpret_cast<int*>(S + s_amax);
+    P.ubuf = F(s_ubuf);
+    P.ubuf_stride = (long long)ubuf_stride;
     // buffers accumulated with atomics (K split into panels) are cleared at the start of each step
     P.carry = m->layers[0].g[mk::G_O].n_kc > 1;
     int nz = 0;
     if (m->layers[0].g[mk::G_A].n_kc > 1) {
         P.zptr[nz] = F(s_a);
         P.zn[nz++] = (long long)L * Mx * D.a_rows;
-    }
-    if (D.sh && m->layers[0].g[mk::G_SHGU].n_kc > 1) {
-        P.zptr[nz] = F(s_shgu);
-        P.zn[nz++] = (long long)L * Mx * 2 * D.sffn;
-    }
-    if (D.E && m->layers[0].g[mk::G_GU].n_kc > 1) {
-        P.zptr[nz] = F(s_gu);
-        P.zn[nz++] = (long long)L * nsl * Mx * 2 * D.ffn;
     }
     if (P.carry) {
         P.zptr[nz] = F(s_x) + (size_t)Mx * d;
@@ -681,6 +738,23 @@ int mk_kv_read(const mk_kv* kv, int32_t layer, int32_t seq, int32_t pos0, int32_
     return kv_copy(kv, layer, seq, pos0, n, rows, stream, 0);
 }
 
+// CTAs given to the shared expert (the rest run the router and the routed
+// experts), in proportion to the weight bytes each group streams; the routed
+// bytes use the expected number of distinct experts of M tokens picking
+// top_k of E experts each uniformly at random
+static int ffn_split(const mk_model* m, int M) {
+    const Dims D = dims_of(m->cfg);
+    if (!D.E) return m->G;
+    if (!D.sh) return 0;
+    const double sh = 3.0 * D.d * D.sffn;
+    const double uniq = D.E * (1.0 - std::pow(1.0 - (double)D.k / D.E, (double)M));
+    const double rt = uniq * 3.0 * D.d * D.ffn + (double)D.E * D.d;
+    int gs = (int)std::lround(m->G * sh / (sh + rt));
+    if (gs < 1) gs = 1;
+    if (gs > m->G - 1) gs = m->G - 1;
+    return gs;
+}
+
 int mk_decode_step(mk_model* m, mk_kv* kv, const int32_t* tokens, const int32_t* positions, int32_t batch,
                    int32_t T, float* logits, int32_t* accept, void* stream) {
     if (!m || m->magic != MODEL_MAGIC) return fail(MK_ERR_INVALID_ARG, "bad model handle");
@@ -703,6 +777,7 @@ int mk_decode_step(mk_model* m, mk_kv* kv, const int32_t* tokens, const int32_t*
     P.B = batch;
     P.T = T;
     P.M = batch * T;
+    P.gs = ffn_split(m, P.M);
     P.logits = logits;
     P.accept = accept;
     P.lm.dst = logits;
@@ -899,6 +974,7 @@ extern "C" int mk_decode_step_noalloc(mk_model* m, mk_kv* kv, const int32_t* tok
     P.part = r(P.part);
     P.part_ml = r(P.part_ml);
     P.amax = r(P.amax);
+    P.ubuf = r(P.ubuf);
     for (int z = 0; z < P.nz; ++z) P.zptr[z] = r(P.zptr[z]);
     P.ctr = r(P.ctr);
     P.status = r(P.status);
@@ -919,6 +995,7 @@ extern "C" int mk_decode_step_noalloc(mk_model* m, mk_kv* kv, const int32_t* tok
     P.B = batch;
     P.T = T;
     P.M = batch * T;
+    P.gs = ffn_split(m, P.M);
     P.logits = logits;
     P.accept = accept;
     P.lm.dst = logits;

@@ -39,6 +39,8 @@ struct alignas(16) Ctx {
     int issued;  // producer: ring fills issued
     long long t_start;
     unsigned cur_code;  // trace: stage being run
+    int pl, pst;                     // program position: layer, stage
+    int n_down, n_shdown, n_carry;   // items the current layer's last stages signal
     __device__ Ctx(const Params& pp, uint8_t* s)
         : p(pp), smem(s), ms(*reinterpret_cast<Misc*>(s + SMEM_MISC)), off(0), dead(false) {
         cr.slot = 0;
@@ -49,6 +51,8 @@ struct alignas(16) Ctx {
         sk_gain = nullptr;
         sk_off = sk_kc = sk_m0 = sk_kind = -1;
         issued = 0;
+        pl = pst = 0;
+        n_down = n_shdown = n_carry = 0;
         t_start = gtimer();
         if (pp.trace && threadIdx.x == 0) pp.trace_n[blockIdx.x] = 0;
     }
@@ -73,6 +77,17 @@ struct alignas(16) Ctx {
     __device__ void set_ring(const CRing& v) {
         __syncwarp();
         cr = v;
+        __syncwarp();
+    }
+    __device__ void set_pos(int l, int st) {
+        __syncwarp();
+        pl = l;
+        pst = st;
+        __syncwarp();
+    }
+    __device__ void set_count(int& field, int v) {
+        __syncwarp();
+        field = v;
         __syncwarp();
     }
     __device__ void set_pring(const PRing& v, int iss) {
@@ -368,9 +383,11 @@ __device__ __forceinline__ void gemv_out(Ctx& c, const Gemv& g, int slot, int ex
         } else {
             atomicAdd(d, y);
         }
-    } else {  // OUT_SCALED: expert down projection added into the next residual
+    } else if (g.out_kind == OUT_SCALED) {  // expert down projection added into the next residual
         const float w = expert < 0 ? 1.0f : route_weight(c.ms, m, expert, c.p.topk);
         if (w != 0.f) atomicAdd(g.dst + (size_t)m * g.dst_stride + row, w * y);
+    } else {  // OUT_ACC: this thread owns the value
+        g.dst[(size_t)m * g.dst_stride + row] += y;
     }
 }
 
@@ -696,9 +713,11 @@ __device__ __forceinline__ void gemv_range_ks(Ctx& c, const Gemv& g, int slot, i
                             } else {
                                 atomicAdd(d, y);
                             }
-                        } else {
+                        } else if (out_kind == OUT_SCALED) {
                             const float w = expert < 0 ? 1.0f : route_weight(ms, m, expert, p.topk);
                             if (w != 0.f) atomicAdd(d, w * y);
+                        } else {
+                            *d += y;
                         }
                     }
                 }
@@ -742,9 +761,11 @@ __device__ __forceinline__ void rx_out(const Params& p, Misc& ms, int out_kind, 
         } else {
             atomicAdd(d, y);
         }
-    } else {
+    } else if (out_kind == OUT_SCALED) {
         const float w = expert < 0 ? 1.0f : route_weight(ms, 0, expert, p.topk);
         if (w != 0.f) atomicAdd(d, w * y);
+    } else {
+        *d += y;
     }
 }
 
@@ -986,54 +1007,17 @@ __device__ __noinline__ void prod_gemv(Ctx& c, const Gemv& g, int expert, int lo
     c.set_pring(pr, issued);
 }
 
-// consumer side of a GEMV stage (mode MM_PLAIN: items [lo, hi) of g after the
-// deps set by set_deps, then signal `sig`) or of a routed-expert stage
-// (MM_GU / MM_DOWN: items are slots x per-slot items; gate/up signals per
-// slot, each down slot first waits for its gate/up). The only call site of
-// the GEMV code, so it is compiled once.
-enum { MM_PLAIN = 0, MM_GU = 1, MM_DOWN = 2 };
-__device__ __noinline__ void cons_mm(Ctx& c, int l, const Gemv& g, int sig, int mode, int lo, int hi) {
-    const Params& p = c.p;
-    const int per = gemv_items(g);
-    const int code = mode == MM_PLAIN ? sig : (mode == MM_GU ? C_GU0 : C_DOWN);
-    c.cur_code = ((unsigned)code << 16) | (unsigned)l;
+// consumer side of a GEMV stage: items [lo, hi) of g after the deps set by
+// set_deps, then signal `sig`. The only call site of the GEMV code besides
+// the expert units, so it is compiled twice in all.
+__device__ __noinline__ void cons_mm(Ctx& c, int l, const Gemv& g, int sig, int lo, int hi) {
+    c.cur_code = ((unsigned)sig << 16) | (unsigned)l;
     const long long t0 = gtimer();
-    long long tw = 0;
-    if (mode == MM_PLAIN) {
-        cwait(c, 0x1000u | (unsigned)(l << 16) | (unsigned)sig);
-        tw = gtimer() - t0;
-    }
-    for (int i = lo; i < hi;) {
-        const int s2 = mode == MM_PLAIN ? 0 : i / per;
-        const int iend = mode == MM_PLAIN ? hi : min(hi, (s2 + 1) * per);
-        if (mode == MM_DOWN) {
-            const long long a = gtimer();
-            set_deps(c, deps1(l, C_GU0 + s2, (unsigned)gemv_items(c.layer().g[G_GU])));
-            cwait(c, 0x500u);
-            tw += gtimer() - a;
-        }
-        const int expert = mode == MM_PLAIN ? -1 : (int)c.ms.slot_e[s2];
-        cons_gemv(c, g, s2, expert, i - s2 * per, iend - s2 * per);
-        if (mode == MM_GU) csignal(c, l, C_GU0 + s2, (unsigned)(iend - i));
-        i = iend;
-    }
-    if (mode != MM_GU) csignal(c, l, mode == MM_PLAIN ? sig : C_DOWN, (unsigned)(hi - lo));
-    trace_rec(c, ((unsigned)code << 16) | (unsigned)l, (unsigned)(hi - lo), t0, t0 + tw);
-}
-
-template <bool PROD>
-__device__ __forceinline__ void stage_gemv(Ctx& c, int l, const Gemv& g, const Deps& deps, int sig) {
-    const int n = gemv_items(g);
-    int lo, hi;
-    my_range(c.p, n, c.off, lo, hi);
-    c.advance(n);
-    if (lo >= hi) return;
-    if constexpr (PROD) {
-        if (!c.dead) prod_gemv(c, g, -1, lo, hi);
-    } else {
-        set_deps(c, deps);
-        cons_mm(c, l, g, sig, MM_PLAIN, lo, hi);
-    }
+    cwait(c, 0x1000u | (unsigned)(l << 16) | (unsigned)sig);
+    const long long t1 = gtimer();
+    cons_gemv(c, g, 0, -1, lo, hi);
+    csignal(c, l, sig, (unsigned)(hi - lo));
+    trace_rec(c, ((unsigned)sig << 16) | (unsigned)l, (unsigned)(hi - lo), t0, t1);
 }
 
 // ============================================================ routing ====
@@ -1160,49 +1144,6 @@ __device__ __noinline__ bool route(Ctx& c, int l) {
         cbar();
     }
     return true;
-}
-
-// routed-expert stage: items = slots x (row blocks x k panels), slot-major
-template <bool PROD>
-__device__ __forceinline__ void stage_experts(Ctx& c, int l, const Gemv& g, bool down) {
-    const Params& p = c.p;
-    const int nslots = PROD ? c.ms.p_nslots : c.ms.n_slots;
-    const int per = gemv_items(g);
-    const int n = nslots * per;
-    int lo, hi;
-    my_range(p, n, c.off, lo, hi);
-    c.advance(n);
-    if (lo >= hi) return;
-    if constexpr (PROD) {
-        const uint8_t* slot_e = c.ms.p_slot_e;
-        if (!down) {
-            // the routing is known: start every gate/up and down tile of this
-            // CTA towards L2 now (the down stage's items follow the shared
-            // expert's down projection in the item rotation)
-            for (int i = lo; i < hi;) {
-                const int s2 = i / per, iend = min(hi, (s2 + 1) * per);
-                prefetch_tiles(g, slot_e[s2], i - s2 * per, iend - s2 * per);
-                i = iend;
-            }
-            const Gemv& gd = c.layer().g[G_DOWN];
-            const int perd = gemv_items(gd), nd = nslots * perd;
-            const int n_sh = p.has_sh ? gemv_items(c.layer().g[G_SHDOWN]) : 0;
-            int dlo, dhi;
-            my_range(p, nd, (int)((c.off + (long long)n_sh) % p.G), dlo, dhi);
-            for (int i = dlo; i < dhi;) {
-                const int s2 = i / perd, iend = min(dhi, (s2 + 1) * perd);
-                prefetch_tiles(gd, slot_e[s2], i - s2 * perd, iend - s2 * perd);
-                i = iend;
-            }
-        }
-        for (int i = lo; i < hi && !c.dead;) {
-            const int s2 = i / per, iend = min(hi, (s2 + 1) * per);
-            prod_gemv(c, g, slot_e[s2], i - s2 * per, iend - s2 * per);
-            i = iend;
-        }
-    } else {
-        cons_mm(c, l, g, 0, down ? MM_DOWN : MM_GU, lo, hi);
-    }
 }
 
 // ====================================================== GQA attention ====
@@ -1756,30 +1697,6 @@ __device__ __noinline__ void attn_cons(Ctx& c, int l, int lo, int hi) {
     trace_rec(c, ((unsigned)C_ATTN << 16) | (unsigned)l, (unsigned)(hi - lo), t0, t1);
 }
 
-template <bool PROD>
-__device__ __forceinline__ void stage_attn(Ctx& c, int l, const Deps& deps) {
-    const Params& p = c.p;
-    const int n = attn_items(p);
-    int lo, hi;
-    my_range(p, n, c.off, lo, hi);
-    c.advance(n);
-    if (lo >= hi) return;
-    if constexpr (PROD) {
-        for (int i = lo; i < hi && !c.dead; ++i) {
-            const AttnItem it = attn_item(p, i);
-            for (int u = it.u_lo; u < min(it.u_hi, it.nch) && !c.dead; ++u) {
-                if (p.attn == 0)
-                    prod_gqa_chunk(c, l, it.b, it.g, u);
-                else
-                    prod_mla_chunk(c, l, it.b, u);
-            }
-        }
-    } else {
-        set_deps(c, deps);
-        attn_cons(c, l, lo, hi);
-    }
-}
-
 // ======================================================== combine ====
 // GQA: item (token, q head) -> o[m][h*hd ...]
 // MLA: item (token, head, 128-dim chunk) -> olat[m][h*512 ...]
@@ -1861,19 +1778,6 @@ __device__ __noinline__ void comb_cons(Ctx& c, int l, int lo, int hi) {
     trace_rec(c, ((unsigned)C_COMB << 16) | (unsigned)l, (unsigned)(hi - lo), t0, t1);
 }
 
-template <bool PROD>
-__device__ __forceinline__ void stage_comb(Ctx& c, int l, const Deps& deps) {
-    const int n = comb_items(c.p);
-    int lo, hi;
-    my_range(c.p, n, c.off, lo, hi);
-    c.advance(n);
-    if constexpr (!PROD) {
-        if (lo >= hi) return;
-        set_deps(c, deps);
-        comb_cons(c, l, lo, hi);
-    }
-}
-
 // ========================================================= MLA append ====
 // item = token: latent = RMSNorm(kv_a latent part) * gain, k_rope = RoPE(kv_a
 // rope part); both rounded to bf16, written to the page and to newlat.
@@ -1917,19 +1821,6 @@ __device__ __noinline__ void append_cons(Ctx& c, int l, int lo, int hi) {
     trace_rec(c, ((unsigned)C_APP << 16) | (unsigned)l, (unsigned)(hi - lo), t0, t1);
 }
 
-template <bool PROD>
-__device__ __forceinline__ void stage_append(Ctx& c, int l, const Deps& deps) {
-    const int n = c.p.M;
-    int lo, hi;
-    my_range(c.p, n, c.off, lo, hi);
-    c.advance(n);
-    if constexpr (!PROD) {
-        if (lo >= hi) return;
-        set_deps(c, deps);
-        append_cons(c, l, lo, hi);
-    }
-}
-
 // ===================================================== residual carry ====
 // (only when the output projection is split over K: x_{l+1} += x_l)
 __device__ __noinline__ void carry_cons(Ctx& c, int l, int lo, int hi) {
@@ -1943,21 +1834,6 @@ __device__ __noinline__ void carry_cons(Ctx& c, int l, int lo, int hi) {
         atomicAdd(Ld.xn + (size_t)m * p.d + e, __ldcg(Ld.x + (size_t)m * p.d + e));
     }
     csignal(c, l, C_CARRY, (unsigned)(hi - lo));
-}
-
-template <bool PROD>
-__device__ __forceinline__ void stage_carry(Ctx& c, int l, const Deps& deps) {
-    const Params& p = c.p;
-    const int chunk = 2048;
-    const int n = (p.M * p.d + chunk - 1) / chunk;
-    int lo, hi;
-    my_range(p, n, c.off, lo, hi);
-    c.advance(n);
-    if constexpr (!PROD) {
-        if (lo >= hi) return;
-        set_deps(c, deps);
-        carry_cons(c, l, lo, hi);
-    }
 }
 
 // ===================================================== head / verify ====
@@ -2003,19 +1879,6 @@ __device__ __noinline__ void argmax_cons(Ctx& c, int lo, int hi) {
         }
     }
     csignal(c, p.L, C_AMAX, (unsigned)(hi - lo));
-}
-
-template <bool PROD>
-__device__ __forceinline__ void stage_argmax(Ctx& c, const Deps& deps) {
-    const int n = c.p.M;
-    int lo, hi;
-    my_range(c.p, n, c.off, lo, hi);
-    c.advance(n);
-    if constexpr (!PROD) {
-        if (lo >= hi) return;
-        set_deps(c, deps);
-        argmax_cons(c, lo, hi);
-    }
 }
 
 // ====================================================== init (consumers) ====
@@ -2106,9 +1969,8 @@ __device__ __noinline__ void prefetch_next_small(Ctx& c, int l) {
             gp = nx->kv_norm;
             n = MLA_KL;
         } else if (lane == 4) {
-            const Gemv& f = p.E > 0 ? nx->g[G_ROUTER] : nx->g[G_SHGU];
-            gp = f.gain;
-            n = f.K;
+            gp = nx->ffn.gain;
+            n = p.d;
         }
         if (gp && n > 0) l2_prefetch_keep(gp, (unsigned)n * 2u);
     } else if (lane == 0 && p.lm.gain) {
@@ -2135,105 +1997,495 @@ __device__ __forceinline__ void load_layer(Ctx& c, int l) {
     }
 }
 
-// ============================================================ program ====
-template <bool PROD>
-__device__ __forceinline__ void program(Ctx& c) {
+// ======================================================= producer leaves ====
+__device__ __noinline__ void prod_plain(Ctx& c, const Gemv& g, int lo, int hi) { prod_gemv(c, g, -1, lo, hi); }
+
+// attention chunks of items [lo, hi) into the ring
+__device__ __noinline__ void prod_attn(Ctx& c, int l, int lo, int hi) {
     const Params& p = c.p;
-    if constexpr (PROD) {
-        if (!prod_check(p)) return;
-    } else {
-        if (!init_phase(c)) return;
-    }
-    int n_down = 0, n_shdown = 0, n_carry = 0;
-    for (int l = 0; l < p.L; ++l) {
-        if constexpr (PROD) {
-            if (c.dead) return;
-        }
-        load_layer<PROD>(c, l);
-        if constexpr (PROD) {
-            if (p.attn == 1) prefetch_attn_mla(c, l);
-            prefetch_next_small(c, l);
-        }
-        const Layer& Ld = c.layer();
-        Deps prev;
-        if (l == 0) {
-            prev = deps1(p.L, C_INIT, (unsigned)p.G);
-        } else {
-            prev.n = 3;
-            prev.d[0] = {l - 1, C_DOWN, (unsigned)n_down};
-            prev.d[1] = {l - 1, C_SHDOWN, (unsigned)n_shdown};
-            prev.d[2] = {l - 1, C_CARRY, (unsigned)n_carry};
-        }
-        const unsigned nA = (unsigned)gemv_items(Ld.g[G_A]);
-        if (p.attn == 1) {
-            stage_gemv<PROD>(c, l, Ld.g[G_A], prev, C_A);
-            stage_gemv<PROD>(c, l, Ld.g[G_QB], deps1(l, C_A, nA), C_QB);
-            stage_append<PROD>(c, l, deps1(l, C_A, nA));
-            stage_gemv<PROD>(c, l, Ld.g[G_QLAT], deps1(l, C_QB, (unsigned)gemv_items(Ld.g[G_QB])), C_QLAT);
-            Deps da;
-            da.n = 2;
-            da.d[0] = {l, C_QLAT, (unsigned)gemv_items(Ld.g[G_QLAT])};
-            da.d[1] = {l, C_APP, (unsigned)p.M};
-            stage_attn<PROD>(c, l, da);
-            stage_comb<PROD>(c, l, deps1(l, C_ATTN, (unsigned)attn_items(p)));
-            stage_gemv<PROD>(c, l, Ld.g[G_UV], deps1(l, C_COMB, (unsigned)comb_items(p)), C_UV);
-            stage_gemv<PROD>(c, l, Ld.g[G_O], deps1(l, C_UV, (unsigned)gemv_items(Ld.g[G_UV])), C_O);
-        } else {
-            stage_gemv<PROD>(c, l, Ld.g[G_A], prev, C_A);
-            stage_attn<PROD>(c, l, deps1(l, C_A, nA));
-            stage_comb<PROD>(c, l, deps1(l, C_ATTN, (unsigned)attn_items(p)));
-            stage_gemv<PROD>(c, l, Ld.g[G_O], deps1(l, C_COMB, (unsigned)comb_items(p)), C_O);
-        }
-        const unsigned nO = (unsigned)gemv_items(Ld.g[G_O]);
-        if (p.E > 0) stage_gemv<PROD>(c, l, Ld.g[G_ROUTER], deps1(l, C_O, nO), C_ROUTER);
-        if (p.has_sh) stage_gemv<PROD>(c, l, Ld.g[G_SHGU], deps1(l, C_O, nO), C_SHGU);
-        n_carry = 0;
-        if (p.carry) {
-            stage_carry<PROD>(c, l, deps1(l, C_O, nO));
-            n_carry = (p.M * p.d + 2047) / 2048;
-        }
-        // routed gate/up first: the shared expert's down projection (whose
-        // input is ready well before the routing) fills the gap before the
-        // routed down projections, instead of delaying the routed experts
-        n_down = 0;
-        if (p.E > 0) {
-            if (!route<PROD>(c, l) && PROD) return;
-            stage_experts<PROD>(c, l, Ld.g[G_GU], false);
-        }
-        n_shdown = 0;
-        if (p.has_sh) {
-            stage_gemv<PROD>(c, l, Ld.g[G_SHDOWN], deps1(l, C_SHGU, (unsigned)gemv_items(Ld.g[G_SHGU])), C_SHDOWN);
-            n_shdown = gemv_items(Ld.g[G_SHDOWN]);
-        }
-        if (p.E > 0) {
-            stage_experts<PROD>(c, l, Ld.g[G_DOWN], true);
-            n_down = (PROD ? c.ms.p_nslots : c.ms.n_slots) * gemv_items(Ld.g[G_DOWN]);
+    for (int i = lo; i < hi && !c.dead; ++i) {
+        const AttnItem it = attn_item(p, i);
+        for (int u = it.u_lo; u < min(it.u_hi, it.nch) && !c.dead; ++u) {
+            if (p.attn == 0)
+                prod_gqa_chunk(c, l, it.b, it.g, u);
+            else
+                prod_mla_chunk(c, l, it.b, u);
         }
     }
-    if constexpr (PROD) {
-        if (c.dead) return;
+}
+
+// ========================================================= FFN units ====
+// A segment is units [u0, u1) of one expert (kind 0: a routed expert, kind 1:
+// the shared expert). Consumers: gate/up rows of the segment (one GEMV over
+// rows [2F u0, 2F u1) of the expert's unit-major gate/up matrix, into a
+// CTA-private buffer), hidden = silu(gate) * up, then the segment's down
+// columns against the hidden values, added into the residual with the
+// expert's routing weight. The producer streams the same tiles.
+
+// gate/up outputs hs [M][2F n] then hidden h [M][n][F] (n units): the upper
+// half of the reduction area (the split-K GEMV uses the lower half) when
+// they fit, else this CTA's slice of a global buffer
+__device__ __forceinline__ float* unit_buf(Ctx& c, int floats) {
+    if (floats <= RED_FLOATS / 2) return c.red() + RED_FLOATS / 2;
+    return c.p.ubuf + (size_t)blockIdx.x * c.p.ubuf_stride;
+}
+
+__device__ __forceinline__ void unit_gemv(const Params& p, const Layer& Ld, Gemv& ug, int kind, int expert, int u0,
+                                          int u1, float* hs) {
+    const FfnKind& K = Ld.ffn.k[kind];
+    ug.W = K.gu + (expert >= 0 ? (size_t)expert * K.gu_es : 0);
+    ug.w_estride = 0;
+    ug.N = 2 * K.Fi;
+    ug.K = p.d;
+    ug.Kc = Ld.ffn.Kc;
+    ug.R = K.R;
+    ug.n_kc = Ld.ffn.n_kc;
+    ug.n_rb = 2 * K.Fi / K.R;
+    ug.in_kind = IN_RMS;
+    ug.src = Ld.x;
+    ug.src_stride = p.d;
+    ug.src_sstride = 0;
+    ug.gain = Ld.ffn.gain;
+    ug.grp_rows = 0;
+    ug.grp_stride = 0;
+    ug.sw_off = 0;
+    ug.out_kind = OUT_ACC;
+    ug.dst = hs - (size_t)2 * K.F * u0;  // rows [2F u0, 2F u1) land at hs[0 ..)
+    ug.dst_stride = 2 * K.F * (u1 - u0);
+    ug.dst_sstride = 0;
+    ug.dst2 = nullptr;
+}
+
+// one thread's rows of a down tile (nr rows x F), one token, hidden values
+// of the unit in registers
+template <int F8>
+__device__ __forceinline__ void down_rows1(const uint8_t* tile, int nr, const float* hu, float w, float* xo) {
+    float4 ha[F8], hb[F8];
+#pragma unroll
+    for (int q = 0; q < F8; ++q) {
+        ha[q] = *reinterpret_cast<const float4*>(hu + 8 * q);
+        hb[q] = *reinterpret_cast<const float4*>(hu + 8 * q + 4);
     }
-    Deps last;
-    last.n = 3;
-    last.d[0] = {p.L - 1, C_DOWN, (unsigned)n_down};
-    last.d[1] = {p.L - 1, C_SHDOWN, (unsigned)n_shdown};
-    last.d[2] = {p.L - 1, C_CARRY, (unsigned)n_carry};
-    stage_gemv<PROD>(c, p.L, p.lm, last, C_LM);
-    if (p.accept) {
-        stage_argmax<PROD>(c, deps1(p.L, C_LM, (unsigned)gemv_items(p.lm)));
-        if constexpr (!PROD) {
-            if (blockIdx.x == 0) {
-                set_deps(c, deps1(p.L, C_AMAX, (unsigned)p.M));
-                cwait(c, 0xb00u);
-                const int b = ctid();
-                if (b < p.B && !c.dead) {
-                    int a = 0;
-                    while (a < p.T - 1 && __ldcg(p.amax + b * p.T + a) == p.tokens[b * p.T + a + 1]) ++a;
-                    p.accept[b] = a + 1;
+    const uint4* T4 = reinterpret_cast<const uint4*>(tile);
+    for (int r = ctid(); r < nr; r += NCT) {
+        float a = 0.f, b = 0.f;
+#pragma unroll
+        for (int q = 0; q < F8; ++q) fma8v2(a, b, T4[(size_t)r * F8 + q], ha[q], hb[q]);
+        atomicAdd(xo + r, w * (a + b));
+    }
+}
+
+__device__ __noinline__ void unit_seg_cons(Ctx& c, int l, int kind, int expert, int u0, int u1) {
+    const Params& p = c.p;
+    const Layer& Ld = c.layer();
+    const FfnKind& K = Ld.ffn.k[kind];
+    const int F = K.F, n = u1 - u0, rows = 2 * F * n, M = p.M, d = p.d, tid = ctid();
+    float* hs = unit_buf(c, 3 * F * n * M);
+    float* h = hs + (size_t)rows * M;
+    cbar();  // the previous segment's down rows may still read its hidden values here
+    for (int i = tid; i < rows * M; i += NCT) hs[i] = 0.f;
+    if (tid < M) c.ms.uw[tid] = expert < 0 ? 1.0f : route_weight(c.ms, tid, expert, p.topk);
+    if (tid == 0) unit_gemv(p, Ld, c.ms.ug, kind, expert, u0, u1, hs);
+    cbar();
+    const int n_rb = 2 * K.Fi / K.R, rpu = 2 * F / K.R;
+    for (int kc = 0; kc < Ld.ffn.n_kc; ++kc) cons_gemv(c, c.ms.ug, 0, -1, kc * n_rb + u0 * rpu, kc * n_rb + u1 * rpu);
+    cbar();
+    for (int i = tid; i < F * n * M; i += NCT) {
+        const int m = i / (F * n), rem = i - m * F * n, uu = rem / F, f = rem - uu * F;
+        const float* g = hs + (size_t)m * rows + uu * 2 * F;
+        h[i] = silu(g[f]) * g[F + f];
+    }
+    cbar();
+    // down columns of each unit: tiles of Rd rows x F from the ring
+    Misc& ms = c.ms;
+    uint8_t* const ring = c.smem + SMEM_RING;
+    CRing cr = c.cr;
+    bool dead = c.dead, timed_out = false;
+    const int nt = (d + K.Rd - 1) / K.Rd;
+    for (int uu = 0; uu < n; ++uu) {
+        for (int t = 0; t < nt; ++t) {
+            const int r0 = t * K.Rd, nr = min(K.Rd, d - r0);
+            const uint8_t* tile = nullptr;
+            if (!dead) {
+                if (spin_wait(p, &ms.full[cr.slot], cr.phase))
+                    tile = ring + cr.slot * SLOT_BYTES;
+                else
+                    dead = timed_out = true;
+            }
+            if (tile) {
+                if (M == 1) {
+                    const float* hu = h + uu * F;
+                    float* xo = Ld.xn + r0;
+                    const float w = ms.uw[0];
+                    if (w != 0.f) {
+                        if (F == 64) down_rows1<8>(tile, nr, hu, w, xo);
+                        else if (F == 48) down_rows1<6>(tile, nr, hu, w, xo);
+                        else if (F == 32) down_rows1<4>(tile, nr, hu, w, xo);
+                        else down_rows1<2>(tile, nr, hu, w, xo);
+                    }
+                } else {
+                    const uint16_t* T = reinterpret_cast<const uint16_t*>(tile);
+                    for (int r = tid; r < nr; r += NCT) {
+                        for (int m = 0; m < M; ++m) {
+                            const float w = ms.uw[m];
+                            if (w == 0.f) continue;
+                            const float* hu = h + ((size_t)m * n + uu) * F;
+                            float a = 0.f;
+                            for (int f = 0; f < F; ++f) a = fmaf(bf2f(T[(size_t)r * F + f]), hu[f], a);
+                            atomicAdd(Ld.xn + (size_t)m * d + r0 + r, w * a);
+                        }
+                    }
                 }
+            }
+            __syncwarp();
+            if ((tid & 31) == 0) mbar_arrive(&ms.empty[cr.slot]);
+            if (++cr.slot == NSLOT) {
+                cr.slot = 0;
+                cr.phase ^= 1u;
             }
         }
     }
+    if (timed_out) {
+        ms.abort = 1;
+        raise_status(p, ST_TIMEOUT, 0x220u);
+    }
+    c.set_ring(cr);
+    if (dead) c.dead = true;
+}
+
+// producer: the segment's tiles into the ring (and, first, towards L2)
+__device__ __noinline__ void unit_seg_prod(Ctx& c, int kind, int expert, int u0, int u1) {
+    const Params& p = c.p;
+    const Layer& Ld = c.layer();
+    const FfnKind& K = Ld.ffn.k[kind];
+    const int F = K.F, d = p.d, lane = threadIdx.x & 31, Kc = Ld.ffn.Kc;
+    const uint16_t* gu = K.gu + (expert >= 0 ? (size_t)expert * K.gu_es : 0);
+    const uint16_t* dn = K.dn + (expert >= 0 ? (size_t)expert * K.dn_es : 0);
+    // L2 prefetch: per K panel the segment's gate/up rows are contiguous, and
+    // so are its down blocks; pieces of at most 64 KB, one lane each
+    {
+        const size_t piece = 32768;  // elements
+        for (int kc = 0; kc < Ld.ffn.n_kc; ++kc) {
+            const uint16_t* b = gu + (size_t)kc * 2 * K.Fi * Kc + (size_t)u0 * 2 * F * Kc;
+            const size_t n = (size_t)(u1 - u0) * 2 * F * Kc;
+            for (size_t o = (size_t)lane * piece; o < n; o += 32 * piece)
+                l2_prefetch(b + o, (unsigned)(min(piece, n - o) * 2));
+        }
+        const uint16_t* b = dn + (size_t)u0 * d * F;
+        const size_t n = (size_t)(u1 - u0) * d * F;
+        for (size_t o = (size_t)lane * piece; o < n; o += 32 * piece) l2_prefetch(b + o, (unsigned)(min(piece, n - o) * 2));
+    }
+    if (lane == 0) unit_gemv(p, Ld, c.ms.pug, kind, expert, u0, u1, nullptr);
+    __syncwarp();
+    const int n_rb = 2 * K.Fi / K.R, rpu = 2 * F / K.R;
+    for (int kc = 0; kc < Ld.ffn.n_kc && !c.dead; ++kc)
+        prod_gemv(c, c.ms.pug, -1, kc * n_rb + u0 * rpu, kc * n_rb + u1 * rpu);
+    Misc& ms = c.ms;
+    uint8_t* ring = c.smem + SMEM_RING;
+    PRing pr = c.pr;
+    int issued = c.issued;
+    const unsigned long long pol = l2_evict_first();
+    const int nt = (d + K.Rd - 1) / K.Rd;
+    for (int u = u0; u < u1 && !c.dead; ++u) {
+        for (int t = 0; t < nt; ++t) {
+            const int r0 = t * K.Rd, nr = min(K.Rd, d - r0);
+            const unsigned bytes = (unsigned)nr * F * 2u;
+            int ok = 1;
+            if (lane == 0) {
+                if (spin_wait(p, &ms.empty[pr.slot], pr.phase ^ 1u)) {
+                    mbar_expect_tx(&ms.full[pr.slot], bytes);
+                    bulk_g2s_pol(ring + pr.slot * SLOT_BYTES, dn + ((size_t)u * d + r0) * F, bytes, &ms.full[pr.slot], pol);
+                } else {
+                    ok = 0;
+                }
+            }
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) {
+                if (lane == 0) raise_status(p, ST_TIMEOUT, 0x120u);
+                c.dead = true;
+                break;
+            }
+            ++issued;
+            prod_next(pr);
+        }
+    }
+    c.set_pring(pr, issued);
+}
+
+// the FFN of layer l: the shared expert's units on CTAs [0, gs), the router
+// result and the routed experts' units (slot-major) on the others
+template <bool PROD>
+__device__ __noinline__ void ffn_stage(Ctx& c, int l) {
+    const Params& p = c.p;
+    const Layer& Ld = c.layer();
+    const long long t0 = gtimer();
+    c.cur_code = ((unsigned)C_DOWN << 16) | (unsigned)l;
+    int done = 0;
+    if ((int)blockIdx.x < p.gs) {
+        if (p.has_sh) {
+            int lo, hi;
+            my_range_sub(Ld.ffn.k[1].nu, 0, p.gs, lo, hi);
+            if (lo < hi) {
+                if constexpr (PROD) {
+                    unit_seg_prod(c, 1, -1, lo, hi);
+                } else {
+                    set_deps(c, deps1(l, C_O, (unsigned)gemv_items(Ld.g[G_O])));
+                    cwait(c, 0x1100u | (unsigned)(l << 16));
+                    unit_seg_cons(c, l, 1, -1, lo, hi);
+                    done += hi - lo;
+                }
+            }
+        }
+        if (p.E > 0 && !route<PROD>(c, l) && PROD) {
+            c.dead = true;
+            return;
+        }
+    } else {
+        if (!route<PROD>(c, l) && PROD) {
+            c.dead = true;
+            return;
+        }
+        const FfnKind& K = Ld.ffn.k[0];
+        const int nslots = PROD ? c.ms.p_nslots : c.ms.n_slots;
+        const uint8_t* slot_e = PROD ? c.ms.p_slot_e : c.ms.slot_e;
+        int lo, hi;
+        my_range_sub(nslots * K.nu, p.gs, p.G - p.gs, lo, hi);
+        for (int i = lo; i < hi && !(PROD && c.dead);) {
+            const int s2 = i / K.nu, iend = min(hi, (s2 + 1) * K.nu);
+            if constexpr (PROD)
+                unit_seg_prod(c, 0, slot_e[s2], i - s2 * K.nu, iend - s2 * K.nu);
+            else
+                unit_seg_cons(c, l, 0, slot_e[s2], i - s2 * K.nu, iend - s2 * K.nu);
+            i = iend;
+        }
+        done = hi - lo;
+    }
+    const int nslots = PROD ? c.ms.p_nslots : c.ms.n_slots;
+    c.set_count(c.n_down, (p.has_sh ? Ld.ffn.k[1].nu : 0) + (p.E > 0 ? nslots * Ld.ffn.k[0].nu : 0));
+    if constexpr (!PROD) {
+        csignal(c, l, C_DOWN, (unsigned)done);
+        trace_rec(c, ((unsigned)C_DOWN << 16) | (unsigned)l, (unsigned)done, t0, t0);
+    }
+}
+
+// verify acceptance (consumers of CTA 0): 1 + the number of leading draft
+// tokens that equal the argmax of the logits at the position before them
+__device__ __noinline__ void accept_cons(Ctx& c) {
+    const Params& p = c.p;
+    set_deps(c, deps1(p.L, C_AMAX, (unsigned)p.M));
+    cwait(c, 0xb00u);
+    const int b = ctid();
+    if (b < p.B && !c.dead) {
+        int a = 0;
+        while (a < p.T - 1 && __ldcg(p.amax + b * p.T + a) == p.tokens[b * p.T + a + 1]) ++a;
+        p.accept[b] = a + 1;
+    }
+}
+
+// ============================================================ program ====
+// The decode step is a fixed sequence of stages: per layer
+//   MLA: A QB APP QLAT ATTN COMB UV O, GQA: A ATTN COMB O,
+//   then ROUTER CARRY FFN (expert units: shared on CTAs [0, gs), routed on the rest)
+// (stages the model does not have are skipped), then LM ARGMAX ACCEPT.
+// exec_stage() runs one stage and advances the position, which lives in
+// shared memory like the rest of the program state: the stage bodies are
+// large functions, and anything a caller kept in registers across a call
+// into them would be spilled to local memory.
+enum StageId {
+    S_A = 0, S_QB, S_APP, S_QLAT, S_ATTN, S_COMB, S_UV, S_O, S_ROUTER, S_CARRY, S_FFN,
+    S_NLAYER, S_LM = S_NLAYER, S_AMAX, S_ACCEPT, S_END
+};
+
+template <bool PROD>
+__device__ __noinline__ bool exec_stage(Ctx& c) {
+    const Params& p = c.p;
+    if constexpr (PROD) {
+        if (c.dead) return false;
+    }
+    const int l = c.pl, st = c.pst;
+    if (st == S_END) return false;
+    {
+        int nl = l, nst = st + 1;
+        if (l < p.L && nst == S_NLAYER) {
+            nl = l + 1;
+            nst = nl == p.L ? S_LM : 0;
+        }
+        c.set_pos(nl, nst);
+    }
+    const bool mla = p.attn == 1;
+    // GEMV-type stages set these and fall through to the common tail
+    const Gemv* g = nullptr;
+    Deps deps;
+    deps.n = 0;
+    int sig = 0, ls = l;
+    int c0 = 0, gc = 0;  // gc > 0: the stage's items go to CTAs [c0, c0 + gc) only
+    if (l < p.L) {
+        const Layer& Ld = c.layer();
+        switch (st) {
+            case S_A: {
+                load_layer<PROD>(c, l);
+                if constexpr (PROD) {
+                    if (mla) prefetch_attn_mla(c, l);
+                    prefetch_next_small(c, l);
+                }
+                if (l == 0) {
+                    deps = deps1(p.L, C_INIT, (unsigned)p.G);
+                } else {
+                    deps.n = 3;
+                    deps.d[0] = {l - 1, C_DOWN, (unsigned)c.n_down};
+                    deps.d[1] = {l - 1, C_SHDOWN, (unsigned)c.n_shdown};
+                    deps.d[2] = {l - 1, C_CARRY, (unsigned)c.n_carry};
+                }
+                c.set_count(c.n_down, 0);
+                c.set_count(c.n_shdown, 0);
+                c.set_count(c.n_carry, 0);
+                g = &c.layer().g[G_A];
+                sig = C_A;
+                break;
+            }
+            case S_QB:
+                if (!mla) return true;
+                g = &Ld.g[G_QB];
+                deps = deps1(l, C_A, (unsigned)gemv_items(Ld.g[G_A]));
+                sig = C_QB;
+                break;
+            case S_APP: {
+                if (!mla) return true;
+                int lo, hi;
+                my_range(p, p.M, c.off, lo, hi);
+                c.advance(p.M);
+                if (!PROD && lo < hi) {
+                    set_deps(c, deps1(l, C_A, (unsigned)gemv_items(Ld.g[G_A])));
+                    append_cons(c, l, lo, hi);
+                }
+                return true;
+            }
+            case S_QLAT:
+                if (!mla) return true;
+                g = &Ld.g[G_QLAT];
+                deps = deps1(l, C_QB, (unsigned)gemv_items(Ld.g[G_QB]));
+                sig = C_QLAT;
+                break;
+            case S_ATTN: {
+                const int n = attn_items(p);
+                int lo, hi;
+                my_range(p, n, c.off, lo, hi);
+                c.advance(n);
+                if (lo >= hi) return true;
+                if constexpr (PROD) {
+                    prod_attn(c, l, lo, hi);
+                } else {
+                    Deps da;
+                    if (mla) {
+                        da.n = 2;
+                        da.d[0] = {l, C_QLAT, (unsigned)gemv_items(Ld.g[G_QLAT])};
+                        da.d[1] = {l, C_APP, (unsigned)p.M};
+                    } else {
+                        da = deps1(l, C_A, (unsigned)gemv_items(Ld.g[G_A]));
+                    }
+                    set_deps(c, da);
+                    attn_cons(c, l, lo, hi);
+                }
+                return true;
+            }
+            case S_COMB: {
+                const int n = comb_items(p);
+                int lo, hi;
+                my_range(p, n, c.off, lo, hi);
+                c.advance(n);
+                if (!PROD && lo < hi) {
+                    set_deps(c, deps1(l, C_ATTN, (unsigned)attn_items(p)));
+                    comb_cons(c, l, lo, hi);
+                }
+                return true;
+            }
+            case S_UV:
+                if (!mla) return true;
+                g = &Ld.g[G_UV];
+                deps = deps1(l, C_COMB, (unsigned)comb_items(p));
+                sig = C_UV;
+                break;
+            case S_O:
+                g = &Ld.g[G_O];
+                deps = mla ? deps1(l, C_UV, (unsigned)gemv_items(Ld.g[G_UV])) : deps1(l, C_COMB, (unsigned)comb_items(p));
+                sig = C_O;
+                break;
+            // the router runs on the routed-expert CTAs (the shared expert's
+            // CTAs start their units meanwhile)
+            case S_ROUTER:
+                if (p.E == 0) return true;
+                g = &Ld.g[G_ROUTER];
+                deps = deps1(l, C_O, (unsigned)gemv_items(Ld.g[G_O]));
+                sig = C_ROUTER;
+                c0 = p.gs;
+                gc = p.G - p.gs;
+                break;
+            case S_CARRY: {
+                if (!p.carry) return true;
+                const int chunk = 2048;
+                const int n = (p.M * p.d + chunk - 1) / chunk;
+                c.set_count(c.n_carry, n);
+                int lo, hi;
+                my_range(p, n, c.off, lo, hi);
+                c.advance(n);
+                if (!PROD && lo < hi) {
+                    set_deps(c, deps1(l, C_O, (unsigned)gemv_items(Ld.g[G_O])));
+                    carry_cons(c, l, lo, hi);
+                }
+                return true;
+            }
+            case S_FFN:
+                ffn_stage<PROD>(c, l);
+                return true;
+            default:
+                return true;
+        }
+    } else {
+        switch (st) {
+            case S_LM:
+                g = &p.lm;
+                deps.n = 3;
+                deps.d[0] = {p.L - 1, C_DOWN, (unsigned)c.n_down};
+                deps.d[1] = {p.L - 1, C_SHDOWN, (unsigned)c.n_shdown};
+                deps.d[2] = {p.L - 1, C_CARRY, (unsigned)c.n_carry};
+                sig = C_LM;
+                ls = p.L;
+                break;
+            case S_AMAX: {
+                if (!p.accept) return true;
+                int lo, hi;
+                my_range(p, p.M, c.off, lo, hi);
+                c.advance(p.M);
+                if (!PROD && lo < hi) {
+                    set_deps(c, deps1(p.L, C_LM, (unsigned)gemv_items(p.lm)));
+                    argmax_cons(c, lo, hi);
+                }
+                return true;
+            }
+            case S_ACCEPT:
+                if (!PROD && p.accept && blockIdx.x == 0) accept_cons(c);
+                return true;
+            default:
+                return true;
+        }
+    }
+    // plain GEMV stage
+    const int n = gemv_items(*g);
+    int lo, hi;
+    if (gc > 0) {
+        my_range_sub(n, c0, gc, lo, hi);
+    } else {
+        my_range(p, n, c.off, lo, hi);
+        c.advance(n);
+    }
+    if (lo >= hi) return true;
+    if constexpr (PROD) {
+        if (!c.dead) prod_plain(c, *g, lo, hi);
+    } else {
+        set_deps(c, deps);
+        cons_mm(c, ls, *g, sig, lo, hi);
+    }
+    return true;
 }
 
 // producer epilogue after an abort: wait (bounded) for the bulk copies it
@@ -2288,10 +2540,16 @@ __global__ void __launch_bounds__(NTHREADS, 1) megakernel(const __grid_constant_
     __syncwarp();
     Ctx& c = *cx;
     if (threadIdx.x >= NCT) {
-        program<true>(c);
+        if (prod_check(c.p))
+            while (exec_stage<true>(c)) {
+            }
+        else
+            c.dead = true;
         if (c.dead) prod_drain(c);
     } else {
-        program<false>(c);
+        if (init_phase(c))
+            while (exec_stage<false>(c)) {
+            }
     }
 }
 

@@ -52,8 +52,9 @@ def test_noalloc_rejects_models_beyond_the_static_scratch():
     import torch
     import moe_decode_megakernel_02_gb300 as mk
     from moe_decode_megakernel_02_gb300 import workload
-    cfg = configs.scaled(configs.DEEP, n_layers=8)  # batch 8: ~72 MB of step scratch
-    model = workload.load_synthetic(cfg, max_batch=8, max_tokens_per_seq=1, max_ctx=80)
+    # positions up to 300k: the RoPE table alone is ~77 MB of step scratch
+    cfg = configs.scaled(configs.DEEP, n_layers=2)
+    model = workload.load_synthetic(cfg, max_batch=8, max_tokens_per_seq=1, max_ctx=300_000)
     assert model.info().scratch_bytes > 64 << 20
     kv = mk.KVCache(model, 8, 80)
     tok = torch.zeros((8, 1), dtype=torch.int32, device="cuda")
