@@ -179,7 +179,13 @@ int mk_decode_step_noalloc(mk_model* m, mk_kv* kv, const int32_t* tokens, const 
 
 /* Synchronise `stream` and return the device status of the last step
  * (MK_OK, MK_ERR_TIMEOUT, MK_ERR_INVALID_ARG). A failed status resets the
- * model's device state so the next step can run. */
+ * model's device state so the next step can run.
+ * Every wait inside the step (on another CTA's progress or on a copy into
+ * shared memory) gives up after the limit set by the environment variable
+ * MK_WAIT_NS (nanoseconds, read at mk_load_weights; default 2 s): the step
+ * records MK_ERR_TIMEOUT and all CTAs leave, the context stays usable.
+ * Testing that path: while the environment variable MK_TEST_STALL is set,
+ * mk_decode_step makes CTA 0 first wait on a counter nothing signals. */
 int mk_step_status(mk_model* m, void* stream);
 
 /* Routing of the last step: host arrays idx [L][batch*T][k] (int32) and

@@ -149,6 +149,7 @@ struct Params {
     long long zn[6];                // floats to zero at the start of the step
     int nz, carry;                  // carry: residual copied by items (split-K output projection)
     int gs;                         // CTAs [0, gs) run the shared expert, [gs, G) router + routed experts
+    int stall;                      // testing: CTA 0 first waits on a counter nothing signals (ends in a timeout)
     float* ubuf;                    // per CTA: expert-unit gate/up and hidden values when shared memory is short
     long long ubuf_stride;          // floats per CTA
     unsigned* ctr;                  // [2][L+1][NCTR]

@@ -778,6 +778,7 @@ int mk_decode_step(mk_model* m, mk_kv* kv, const int32_t* tokens, const int32_t*
     P.T = T;
     P.M = batch * T;
     P.gs = ffn_split(m, P.M);
+    P.stall = getenv("MK_TEST_STALL") != nullptr;
     P.logits = logits;
     P.accept = accept;
     P.lm.dst = logits;

@@ -1900,6 +1900,16 @@ __device__ __noinline__ bool init_phase(Ctx& c) {
         c.dead = true;
         return false;
     }
+    if (p.stall && blockIdx.x == 0) {
+        // failure-detection test: a wait whose counter nothing signals runs
+        // into the time limit, records MK_ERR_TIMEOUT and makes every CTA leave
+        if (tid == 0 && !wait_ge(p, ctr_of(p, p.L, C_GU0), 1u, 0xe00u)) c.ms.abort = 1;
+        cbar();
+        if (c.ms.abort) {
+            c.dead = true;
+            return false;
+        }
+    }
     const size_t gtid = (size_t)blockIdx.x * NCT + tid, gstride = (size_t)p.G * NCT;
     // counters of the other parity are used by the next step: clear them now
     unsigned* other = p.ctr + (size_t)(p.parity ^ 1) * (p.L + 1) * NCTR;
@@ -2083,6 +2093,7 @@ __device__ __noinline__ void unit_seg_cons(Ctx& c, int l, int kind, int expert, 
     float* hs = unit_buf(c, 3 * F * n * M);
     float* h = hs + (size_t)rows * M;
     cbar();  // the previous segment's down rows may still read its hidden values here
+    const long long tu0 = p.trace_items ? gtimer() : 0;
     for (int i = tid; i < rows * M; i += NCT) hs[i] = 0.f;
     if (tid < M) c.ms.uw[tid] = expert < 0 ? 1.0f : route_weight(c.ms, tid, expert, p.topk);
     if (tid == 0) unit_gemv(p, Ld, c.ms.ug, kind, expert, u0, u1, hs);
@@ -2090,6 +2101,7 @@ __device__ __noinline__ void unit_seg_cons(Ctx& c, int l, int kind, int expert, 
     const int n_rb = 2 * K.Fi / K.R, rpu = 2 * F / K.R;
     for (int kc = 0; kc < Ld.ffn.n_kc; ++kc) cons_gemv(c, c.ms.ug, 0, -1, kc * n_rb + u0 * rpu, kc * n_rb + u1 * rpu);
     cbar();
+    const long long tu1 = p.trace_items ? gtimer() : 0;
     for (int i = tid; i < F * n * M; i += NCT) {
         const int m = i / (F * n), rem = i - m * F * n, uu = rem / F, f = rem - uu * F;
         const float* g = hs + (size_t)m * rows + uu * 2 * F;
@@ -2145,6 +2157,9 @@ __device__ __noinline__ void unit_seg_cons(Ctx& c, int l, int kind, int expert, 
             }
         }
     }
+    // unit trace: gate/up time, then gate/up + hidden, then down (first record field: gate/up)
+    if (p.trace_items && tid == 0) trace_rec(c, 0x80000000u | (((unsigned)C_DOWN + 1) << 16) | (unsigned)l,
+                                             (unsigned)(tu1 - tu0), tu0, tu1);
     if (timed_out) {
         ms.abort = 1;
         raise_status(p, ST_TIMEOUT, 0x220u);
