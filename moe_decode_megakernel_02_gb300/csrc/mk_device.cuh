@@ -148,7 +148,7 @@ struct Params {
     float* zptr[6];
     long long zn[6];                // floats to zero at the start of the step
     int nz, carry;                  // carry: residual copied by items (split-K output projection)
-    int gs;                         // CTAs [0, gs) run the shared expert, [gs, G) router + routed experts
+    int gs, gr;                     // CTAs [0, gs): shared expert, [G-gr, G): router, between: routed experts
     int stall;                      // testing: CTA 0 first waits on a counter nothing signals (ends in a timeout)
     float* ubuf;                    // per CTA: expert-unit gate/up and hidden values when shared memory is short
     long long ubuf_stride;          // floats per CTA
@@ -186,6 +186,7 @@ struct Misc {
     int ndep;
     Gemv ug, pug;                   // expert-unit gate/up GEMV (consumers, producer)
     float uw[MAX_M];                // expert-unit routing weight per token
+    long long tdbg[4];              // trace: clock64 marks of the expert-unit gate/up GEMV
     int abort;
     int n_slots, p_nslots;
     float rms[MAX_M];
@@ -374,8 +375,9 @@ __device__ __forceinline__ unsigned* ctr_of(const Params& p, int layer, int whic
 __device__ __forceinline__ void my_range(const Params& p, int n, int off, int& lo, int& hi) {
     int v = (int)blockIdx.x + off;
     if (v >= p.G) v -= p.G;
-    lo = (int)((long long)v * n / p.G);
-    hi = (int)((long long)(v + 1) * n / p.G);
+    // 32-bit products (G <= 255 CTAs, n < 2^23 items): 64-bit division is a long software sequence
+    lo = v * n / p.G;
+    hi = (v + 1) * n / p.G;
 }
 
 // n items over the CTAs [c0, c0 + gc) only (empty range for the others)
@@ -385,8 +387,8 @@ __device__ __forceinline__ void my_range_sub(int n, int c0, int gc, int& lo, int
         lo = hi = 0;
         return;
     }
-    lo = (int)((long long)v * n / gc);
-    hi = (int)((long long)(v + 1) * n / gc);
+    lo = v * n / gc;
+    hi = (v + 1) * n / gc;
 }
 
 __device__ __forceinline__ int gemv_items(const Gemv& g) { return g.n_rb * g.n_kc; }

@@ -112,8 +112,7 @@ void unit_geometry(int d, int F, int& Kc, int& R, int& Rd) {
     R = (mk::TILE_MAX / (2 * Kc)) / 8 * 8;
     if (R > 2 * F) R = 2 * F;
     while (R > 8 && (2 * F) % R) R -= 8;
-    Rd = mk::TILE_MAX / (2 * F) / 256 * 256;
-    if (Rd < 256) Rd = 256;
+    Rd = mk::SLOT_BYTES / (2 * F) / 128 * 128;  // down tiles fill a ring slot
     if (Rd > d) Rd = d;
 }
 
@@ -601,7 +600,7 @@ int mk_load_weights(const mk_config* cfg, const mk_weight* table, int32_t n, voi
         P.trace = reinterpret_cast<mk::TraceRec*>(S + s_trace);
         P.trace_n = reinterpret_cast<unsigned*>(S + s_trace_n);
         P.trace_cap = trace_cap;
-        P.trace_items = atoi(getenv("MK_TRACE")) > 1;
+        P.trace_items = atoi(getenv("MK_TRACE")) > 2 ? 2 : atoi(getenv("MK_TRACE")) > 1 ? 1 : 0;
     }
     P.amax = reinterpret_cast<int*>(S + s_amax);
     P.ubuf = F(s_ubuf);
@@ -738,21 +737,31 @@ int mk_kv_read(const mk_kv* kv, int32_t layer, int32_t seq, int32_t pos0, int32_
     return kv_copy(kv, layer, seq, pos0, n, rows, stream, 0);
 }
 
-// CTAs given to the shared expert (the rest run the router and the routed
-// experts), in proportion to the weight bytes each group streams; the routed
-// bytes use the expected number of distinct experts of M tokens picking
-// top_k of E experts each uniformly at random
-static int ffn_split(const mk_model* m, int M) {
+int gemv_items_host(const mk::Gemv& g) { return g.n_rb * g.n_kc; }
+
+// FFN CTA groups: gr CTAs run the router (one per router tile), gs CTAs the
+// shared expert's units, the rest the routed experts' units; gs follows the
+// two kinds' unit counts, the routed count taken as the expected number of
+// distinct experts of M tokens picking top_k of E uniformly at random
+static void ffn_split(const mk_model* m, int M, int& gs, int& gr) {
     const Dims D = dims_of(m->cfg);
-    if (!D.E) return m->G;
-    if (!D.sh) return 0;
-    const double sh = 3.0 * D.d * D.sffn;
+    const mk::Layer& L0 = m->layers[0];
+    gr = D.E ? std::min(gemv_items_host(L0.g[mk::G_ROUTER]), m->G / 4) : 0;
+    if (!D.E) {
+        gs = m->G;
+        return;
+    }
+    if (!D.sh) {
+        gs = 0;
+        return;
+    }
+    const double us = L0.ffn.k[1].nu;
     const double uniq = D.E * (1.0 - std::pow(1.0 - (double)D.k / D.E, (double)M));
-    const double rt = uniq * 3.0 * D.d * D.ffn + (double)D.E * D.d;
-    int gs = (int)std::lround(m->G * sh / (sh + rt));
+    const double ur = uniq * L0.ffn.k[0].nu;
+    const int avail = m->G - gr;
+    gs = (int)std::lround(avail * us / (us + ur));
     if (gs < 1) gs = 1;
-    if (gs > m->G - 1) gs = m->G - 1;
-    return gs;
+    if (gs > avail - 1) gs = avail - 1;
 }
 
 int mk_decode_step(mk_model* m, mk_kv* kv, const int32_t* tokens, const int32_t* positions, int32_t batch,
@@ -777,7 +786,7 @@ int mk_decode_step(mk_model* m, mk_kv* kv, const int32_t* tokens, const int32_t*
     P.B = batch;
     P.T = T;
     P.M = batch * T;
-    P.gs = ffn_split(m, P.M);
+    ffn_split(m, P.M, P.gs, P.gr);
     P.stall = getenv("MK_TEST_STALL") != nullptr;
     P.logits = logits;
     P.accept = accept;
@@ -996,7 +1005,7 @@ extern "C" int mk_decode_step_noalloc(mk_model* m, mk_kv* kv, const int32_t* tok
     P.B = batch;
     P.T = T;
     P.M = batch * T;
-    P.gs = ffn_split(m, P.M);
+    ffn_split(m, P.M, P.gs, P.gr);
     P.logits = logits;
     P.accept = accept;
     P.lm.dst = logits;

@@ -170,7 +170,7 @@ __device__ float cblock_max(Ctx& c, float v) {
 __device__ __forceinline__ void trace_rec(Ctx& c, unsigned code, unsigned n, long long t0, long long t1) {
     if (!c.p.trace || threadIdx.x != 0) return;
     unsigned* cnt = c.p.trace_n + blockIdx.x;
-    const unsigned i = *cnt;
+    const unsigned i = atomicAdd(cnt, 1u);
     if (i >= (unsigned)c.p.trace_cap) return;
     TraceRec* r = c.p.trace + (size_t)blockIdx.x * c.p.trace_cap + i;
     r->code = code;
@@ -178,7 +178,19 @@ __device__ __forceinline__ void trace_rec(Ctx& c, unsigned code, unsigned n, lon
     r->t_wait = t0;
     r->t_ready = t1;
     r->t_end = gtimer();
-    *cnt = i + 1;
+}
+
+// a trace record from any thread (per-warp records, MK_TRACE=3)
+__device__ __forceinline__ void trace_rec_any(Ctx& c, unsigned code, unsigned n, long long t0, long long t1) {
+    unsigned* cnt = c.p.trace_n + blockIdx.x;
+    const unsigned i = atomicAdd(cnt, 1u);
+    if (i >= (unsigned)c.p.trace_cap) return;
+    TraceRec* r = c.p.trace + (size_t)blockIdx.x * c.p.trace_cap + i;
+    r->code = code;
+    r->n = n;
+    r->t_wait = t0;
+    r->t_ready = t1;
+    r->t_end = gtimer();
 }
 
 // =============================================================== GEMV ====
@@ -258,7 +270,7 @@ __device__ __forceinline__ void stage_input_small(Ctx& c, const Gemv& g, const f
     }
 }
 
-__device__ __forceinline__ void stage_input(Ctx& c, const Gemv& g, const float* src, int grp_off, int kc, int m0, int ms) {
+__device__ __noinline__ void stage_input(Ctx& c, const Gemv& g, const float* src, int grp_off, int kc, int m0, int ms) {
     const Params& p = c.p;
     float* xs = c.stage();
     const int Kc = g.Kc, k0 = kc * Kc, tid = ctid(), lane = tid & 31, warp = tid >> 5;
@@ -435,12 +447,15 @@ template <int MTc>
 __device__ void gemv_warp_tile(Ctx& c, const Gemv& g, const uint8_t* tile, int nr, const float* xs, int mt0,
                                int mcount, int mbase, int slot, int expert, int r0) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int Kc = g.Kc, NC = Kc >> 3, RW = nr >> 3, rw0 = warp * RW;
+    // warp w owns rows [w RW, w RW + RW) of the tile, clipped to nr (tiles of
+    // fewer than 8 rows leave some warps without rows)
+    const int Kc = g.Kc, NC = Kc >> 3, RW = (nr + 7) >> 3, rw0 = warp * RW;
+    const int RWv = max(0, min(RW, nr - rw0));  // this warp's rows
     const uint4* T4 = reinterpret_cast<const uint4*>(tile);
     if (NC >= 32) {
         const int JC = NC >> 5;
-        for (int r = 0; r < RW; r += 4) {
-            const int nrr = min(4, RW - r);
+        for (int r = 0; r < RWv; r += 4) {
+            const int nrr = min(4, RWv - r);
             float acc[4][MTc];
 #pragma unroll
             for (int i = 0; i < 4; ++i)
@@ -488,10 +503,11 @@ __device__ void gemv_warp_tile(Ctx& c, const Gemv& g, const uint8_t* tile, int n
     } else {
         // short rows (K = 128): 32/NC rows per pass, NC lanes per row
         const int G = 32 / NC, gi = lane / NC, ch = lane - gi * NC;
-        for (int pass = 0; pass < RW / G; ++pass) {
-            const int row = rw0 + pass * G + gi;
+        for (int pass = 0; pass < (RWv + G - 1) / G; ++pass) {
+            const int rl = pass * G + gi, row = rw0 + rl;
+            const bool rv = rl < RWv;
             float acc[MTc];
-            const uint4 w = T4[(size_t)row * NC + ch];
+            const uint4 w = rv ? T4[(size_t)row * NC + ch] : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
             for (int m = 0; m < MTc; ++m) {
                 float xv[8];
@@ -509,7 +525,7 @@ __device__ void gemv_warp_tile(Ctx& c, const Gemv& g, const uint8_t* tile, int n
 #pragma unroll
             for (int m = 0; m < MTc; ++m)
                 if (ch == m) myv = acc[m];
-            if (ch < mcount) gemv_out(c, g, slot, expert, mbase + ch, r0 + row, myv);
+            if (rv && ch < mcount) gemv_out(c, g, slot, expert, mbase + ch, r0 + row, myv);
         }
     }
 }
@@ -549,6 +565,18 @@ __device__ __forceinline__ bool spin_wait(const Params& p, unsigned long long* b
         if (mbar_test(bar, parity)) return true;
         if ((it & 63) == 0 && (gtimer() - t0 > p.timeout_ns || ld_relaxed(&p.status[1]))) return false;
     }
+}
+
+// end of the run of items that share the staged input (same K panel and,
+// for grouped inputs, the same head group) starting at item j of panel kc0,
+// row block rb0: items [j, jend) -- arithmetic only, no per-item divisions
+__device__ __forceinline__ int run_end(int j, int j_hi, int n_rb, int rb0, int R, int grp_rows, int g0) {
+    int rb_end = n_rb;  // the panel ends the run
+    if (grp_rows) {
+        const int gb = (g0 + 1) * grp_rows;  // first row of the next group
+        rb_end = min(n_rb, (gb + R - 1) / R);
+    }
+    return min(j_hi, j + (rb_end - rb0));
 }
 
 // ---- split-K GEMV (M <= 8 tokens) ----
@@ -624,22 +652,16 @@ __device__ __forceinline__ void gemv_range_ks(Ctx& c, const Gemv& g, int slot, i
     int j = j_lo;
     while (j < j_hi) {
         // a run of items sharing the staged input (same K panel and head group)
-        const int kc0 = j / n_rb;
-        const int g0 = grp_rows ? ((j - kc0 * n_rb) * R) / grp_rows : 0;
-        int jend = j + 1;
-        while (jend < j_hi) {
-            const int kc1 = jend / n_rb;
-            const int g1 = grp_rows ? ((jend - kc1 * n_rb) * R) / grp_rows : 0;
-            if (kc1 != kc0 || g1 != g0) break;
-            ++jend;
-        }
+        const int kc0 = j / n_rb, rb0 = j - kc0 * n_rb;
+        const int g0 = grp_rows ? (rb0 * R) / grp_rows : 0;
+        const int jend = run_end(j, j_hi, n_rb, rb0, R, grp_rows, g0);
         const long long ta = p.trace_items ? gtimer() : 0;
         restage(c, g, src, g0 * grp_stride, kc0, 0, M);
         const long long tb = p.trace_items ? gtimer() : 0;
         long long tc = tb;
         const int jrun = j;
         for (; j < jend; ++j) {
-            const int kc = j / n_rb, rbk = j - kc * n_rb;
+            const int rbk = rb0 + (j - jrun);  // same K panel for the whole run
             const int r0 = rbk * R, nr = min(R, N - r0);
             const uint8_t* tile = nullptr;
             if (!dead) {
@@ -769,6 +791,59 @@ __device__ __forceinline__ void rx_out(const Params& p, Misc& ms, int out_kind, 
     }
 }
 
+// sums of RB per-lane values over the warp: after log2(RB) halving steps
+// (each lane keeps half of its values and adds its partner's other half)
+// and plain steps for the remaining lane bits, v[0] of every lane holds the
+// full sum of value b = its lane bits 16, 8, 4 (high to low, as many as
+// log2 RB) -- returned; lanes whose low 5 - log2(RB) bits are 0 are one
+// writer per value
+template <int RB>
+__device__ __forceinline__ int rx_reduce(float (&v)[RB]) {
+    const int lane = threadIdx.x & 31;
+    int b = 0;
+#pragma unroll
+    for (int lvl = 0, n = RB; n > 1; ++lvl, n >>= 1) {
+        const int o = 16 >> lvl, half = n / 2;
+        const bool up = (lane & o) != 0;
+#pragma unroll
+        for (int k = 0; k < RB / 2; ++k) {
+            if (k < half) {
+                const float send = up ? v[k] : v[k + half];
+                const float keep = up ? v[k + half] : v[k];
+                v[k] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+            }
+        }
+        if (up) b += half;
+    }
+    constexpr int LV = RB == 1 ? 0 : (RB == 2 ? 1 : (RB == 4 ? 2 : (RB == 8 ? 3 : 4)));
+#pragma unroll
+    for (int o = 16 >> LV; o >= 1; o >>= 1) v[0] += __shfl_xor_sync(0xffffffffu, v[0], o);
+    return b;
+}
+
+// 8 values per lane summed over each 16-lane half: halving over lane bits
+// 8, 4, 2, then bit 1; returns the value index v[0] now holds
+__device__ __forceinline__ int rx_reduce16(float (&v)[8]) {
+    const int lane = threadIdx.x & 31;
+    int k = 0;
+#pragma unroll
+    for (int lvl = 0, n = 8; n > 1; ++lvl, n >>= 1) {
+        const int o = 8 >> lvl, half = n / 2;
+        const bool up = (lane & o) != 0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if (j < half) {
+                const float send = up ? v[j] : v[j + half];
+                const float keep = up ? v[j + half] : v[j];
+                v[j] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+            }
+        }
+        if (up) k += half;
+    }
+    v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
+    return k;
+}
+
 template <int JC>
 __device__ __forceinline__ void gemv_range_rx(Ctx& c, const Gemv& g, int slot, int expert, int j_lo, int j_hi) {
     const Params& p = c.p;
@@ -788,17 +863,13 @@ __device__ __forceinline__ void gemv_range_rx(Ctx& c, const Gemv& g, int slot, i
     bool dead = c.dead, timed_out = false;
     constexpr int NX = wide ? JC : 1;
     float4 xa[NX], xb[NX];
+    if (p.trace_items == 1 && threadIdx.x == 0) ms.tdbg[0] = clock64();
     int j = j_lo;
     while (j < j_hi) {
-        const int kc0 = j / n_rb;
-        const int g0 = grp_rows ? ((j - kc0 * n_rb) * R) / grp_rows : 0;
-        int jend = j + 1;
-        while (jend < j_hi) {
-            const int kc1 = jend / n_rb;
-            const int g1 = grp_rows ? ((jend - kc1 * n_rb) * R) / grp_rows : 0;
-            if (kc1 != kc0 || g1 != g0) break;
-            ++jend;
-        }
+        const int kc0 = j / n_rb, rb0 = j - kc0 * n_rb;
+        const int g0 = grp_rows ? (rb0 * R) / grp_rows : 0;
+        const int jend = run_end(j, j_hi, n_rb, rb0, R, grp_rows, g0);
+        if (p.trace_items == 1 && threadIdx.x == 0) ms.tdbg[1] = clock64();
         const long long ta = p.trace_items ? gtimer() : 0;
         restage(c, g, src, g0 * grp_stride, kc0, 0, 1);
         const long long tb = p.trace_items ? gtimer() : 0;
@@ -814,7 +885,59 @@ __device__ __forceinline__ void gemv_range_rx(Ctx& c, const Gemv& g, int slot, i
         }
         const int jrun = j;
         for (; j < jend; ++j) {
-            const int kc = j / n_rb, rb = j - kc * n_rb;
+            if constexpr (JC == 8) {
+                // K panel 2048 (8 rows per tile, one per warp): two tiles per
+                // iteration, both rows' loads and FMAs in flight together and
+                // one reduction for the two sums
+                if (j + 1 < jend && !dead) {
+                    const int r0A = (rb0 + (j - jrun)) * R, nrA = min(R, N - r0A);
+                    const int r0B = r0A + R, nrB = min(R, N - r0B);
+                    CRing crB = cr;
+                    if (++crB.slot == NSLOT) {
+                        crB.slot = 0;
+                        crB.phase ^= 1u;
+                    }
+                    if (!spin_wait(p, &ms.full[cr.slot], cr.phase) || !spin_wait(p, &ms.full[crB.slot], crB.phase)) {
+                        dead = timed_out = true;
+                    } else {
+                        if (p.trace_items && j == jrun) tc = gtimer();
+                        const uint4* wA = reinterpret_cast<const uint4*>(ring + cr.slot * SLOT_BYTES) + (size_t)warp * NC + lane;
+                        const uint4* wB = reinterpret_cast<const uint4*>(ring + crB.slot * SLOT_BYTES) + (size_t)warp * NC + lane;
+                        float a[4] = {0.f, 0.f, 0.f, 0.f}, b[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                        for (int q0 = 0; q0 < 8; q0 += 2) {
+                            uint4 u[4];
+                            u[0] = wA[32 * q0];
+                            u[1] = wA[32 * (q0 + 1)];
+                            u[2] = wB[32 * q0];
+                            u[3] = wB[32 * (q0 + 1)];
+                            fma8v2(a[0], a[1], u[0], xa[q0], xb[q0]);
+                            fma8v2(a[2], a[3], u[1], xa[q0 + 1], xb[q0 + 1]);
+                            fma8v2(b[0], b[1], u[2], xa[q0], xb[q0]);
+                            fma8v2(b[2], b[3], u[3], xa[q0 + 1], xb[q0 + 1]);
+                        }
+                        float v[2] = {(a[0] + a[1]) + (a[2] + a[3]), (b[0] + b[1]) + (b[2] + b[3])};
+                        const int which = rx_reduce<2>(v);  // lane 0: tile A, lane 16: tile B
+                        if ((lane & 15) == 0) {
+                            const int row = (which ? r0B : r0A) + warp;
+                            if (warp < (which ? nrB : nrA)) rx_out(p, ms, out_kind, n_kc, dst + row, dst2 + row, expert, v[0]);
+                        }
+                    }
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive(&ms.empty[cr.slot]);
+                        mbar_arrive(&ms.empty[crB.slot]);
+                    }
+                    cr = crB;
+                    if (++cr.slot == NSLOT) {
+                        cr.slot = 0;
+                        cr.phase ^= 1u;
+                    }
+                    ++j;
+                    continue;
+                }
+            }
+            const int rb = rb0 + (j - jrun);
             const int r0 = rb * R, nr = min(R, N - r0);
             const uint8_t* tile = nullptr;
             if (!dead) {
@@ -827,39 +950,61 @@ __device__ __forceinline__ void gemv_range_rx(Ctx& c, const Gemv& g, int slot, i
             if (tile) {
                 const uint4* T4 = reinterpret_cast<const uint4*>(tile);
                 if constexpr (wide) {
-                    for (int r = warp; r < nr; r += 8) {
-                        const uint4* w0 = T4 + (size_t)r * NC + lane;
-                        // loads in batches of four ahead of their FMAs, four accumulator chains
-                        float a[4] = {0.f, 0.f, 0.f, 0.f};
+                    // RB rows of the warp at a time (rows warp*RB + b + 8*RB*k):
+                    // all their loads and FMAs first, then one transposed
+                    // reduction for the RB sums
+                    constexpr int RB = JC >= 8 ? 1 : (JC >= 3 ? 2 : (JC == 2 ? 4 : 8));
+                    for (int rbase = warp * RB; rbase < nr; rbase += 8 * RB) {
+                        float v[RB];
 #pragma unroll
-                        for (int q0 = 0; q0 < JC; q0 += 4) {
-                            uint4 w[4];
+                        for (int b = 0; b < RB; ++b) {
+                            const int r = rbase + b;
+                            float a[4] = {0.f, 0.f, 0.f, 0.f};
+                            if (r < nr) {
+                                const uint4* w0 = T4 + (size_t)r * NC + lane;
 #pragma unroll
-                            for (int u = 0; u < 4; ++u)
-                                if (q0 + u < JC) w[u] = w0[32 * (q0 + u)];
+                                for (int q0 = 0; q0 < JC; q0 += 4) {
+                                    uint4 w[4];
 #pragma unroll
-                            for (int u = 0; u < 4; ++u)
-                                if (q0 + u < JC) fma8v2(a[(2 * u) & 3], a[(2 * u + 1) & 3], w[u], xa[q0 + u], xb[q0 + u]);
+                                    for (int u = 0; u < 4; ++u)
+                                        if (q0 + u < JC) w[u] = w0[32 * (q0 + u)];
+#pragma unroll
+                                    for (int u = 0; u < 4; ++u)
+                                        if (q0 + u < JC)
+                                            fma8v2(a[(2 * u) & 3], a[(2 * u + 1) & 3], w[u], xa[q0 + u], xb[q0 + u]);
+                                }
+                            }
+                            v[b] = (a[0] + a[1]) + (a[2] + a[3]);
                         }
-                        float ya = (a[0] + a[1]) + (a[2] + a[3]);
-#pragma unroll
-                        for (int o = 16; o; o >>= 1) ya += __shfl_xor_sync(0xffffffffu, ya, o);
-                        if (lane == 0) rx_out(p, ms, out_kind, n_kc, dst + r0 + r, dst2 + r0 + r, expert, ya);
+                        const int b = rx_reduce<RB>(v);
+                        const int r = rbase + b;
+                        if ((lane & (32 / RB - 1)) == 0 && r < nr)
+                            rx_out(p, ms, out_kind, n_kc, dst + r0 + r, dst2 + r0 + r, expert, v[0]);
                     }
                 } else {
-                    // 16 chunks per row: lanes 0-15 row r, lanes 16-31 row r + 1
+                    // 16 chunks per row: lanes 0-15 row r, lanes 16-31 row r + 1,
+                    // r = 2 warp + 16 k; all 8 passes first, then one reduction
                     const int half = lane >> 4, ch = lane & 15;
-                    for (int r = warp * 2; r < nr; r += 16) {
-                        const int rr = r + half;
-                        float a = 0.f;
-                        if (rr < nr) {
-                            float a1 = 0.f;
-                            fma8v2(a, a1, T4[(size_t)rr * NC + ch], xa[0], xb[0]);
-                            a += a1;
-                        }
+                    float v[8];
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        const int rr = warp * 2 + half + 16 * k;
+                        float a = 0.f, a1 = 0.f;
+                        if (rr < nr) fma8v2(a, a1, T4[(size_t)rr * NC + ch], xa[0], xb[0]);
+                        v[k] = a + a1;
+                    }
+                    // halving over lane bits 8, 4, 2 of the 16-lane half, then bit 1
+                    const int k = rx_reduce16(v);
+                    const int rr = warp * 2 + half + 16 * k;
+                    if ((ch & 1) == 0 && rr < nr) rx_out(p, ms, out_kind, n_kc, dst + r0 + rr, dst2 + r0 + rr, expert, v[0]);
+                    for (int r = warp * 2 + 128; r < nr; r += 16) {  // tiles of more than 128 rows
+                        const int r2 = r + half;
+                        float a = 0.f, a1 = 0.f;
+                        if (r2 < nr) fma8v2(a, a1, T4[(size_t)r2 * NC + ch], xa[0], xb[0]);
+                        a += a1;
 #pragma unroll
                         for (int o = 8; o; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
-                        if (ch == 0 && rr < nr) rx_out(p, ms, out_kind, n_kc, dst + r0 + rr, dst2 + r0 + rr, expert, a);
+                        if (ch == 0 && r2 < nr) rx_out(p, ms, out_kind, n_kc, dst + r0 + r2, dst2 + r0 + r2, expert, a);
                     }
                 }
             }
@@ -870,7 +1015,10 @@ __device__ __forceinline__ void gemv_range_rx(Ctx& c, const Gemv& g, int slot, i
                 cr.phase ^= 1u;
             }
         }
-        if (p.trace_items && threadIdx.x == 0) trace_rec(c, 0x80000000u | c.cur_code, (unsigned)(tb - ta), ta, tc);
+        if (p.trace_items == 1 && threadIdx.x == 0) trace_rec(c, 0x80000000u | c.cur_code, (unsigned)(tb - ta), ta, tc);
+        if (p.trace_items == 1 && threadIdx.x == 0) ms.tdbg[2] = clock64();
+        if (p.trace_items == 2 && lane == 0)
+            trace_rec_any(c, 0xC0000000u | ((unsigned)warp << 24) | c.cur_code, (unsigned)(tb - ta), ta, tc);
     }
     if (timed_out) {
         ms.abort = 1;
@@ -932,8 +1080,10 @@ __device__ __noinline__ void gemv_multi(Ctx& c, const Gemv& g, int slot, int exp
         gemv_range_ks<32, 2>(c, g, slot, expert, j_lo, j_hi);
 }
 
-// consumer: GEMV work items [j_lo, j_hi) of one slot
-__device__ __forceinline__ void cons_gemv(Ctx& c, const Gemv& g, int slot, int expert, int j_lo, int j_hi) {
+// consumer: GEMV work items [j_lo, j_hi) of one slot (one copy of the GEMV
+// code for the plain stages and the expert units: every stage's code runs
+// once per layer, and a smaller footprint keeps it in the instruction cache)
+__device__ __noinline__ void cons_gemv(Ctx& c, const Gemv& g, int slot, int expert, int j_lo, int j_hi) {
     const int M = c.p.M, Kc = g.Kc;
     if (M == 1 && Kc == 2048)
         gemv_range_rx<8>(c, g, slot, expert, j_lo, j_hi);
@@ -976,15 +1126,25 @@ __device__ __noinline__ void prod_gemv(Ctx& c, const Gemv& g, int expert, int lo
     int issued = c.issued;
     const bool leader = (threadIdx.x & 31) == 0;
     const unsigned long long pol = l2_evict_first();
-    prefetch_tiles(g, expert, lo, min(hi, lo + PF_TILES));
+    // panel / row block of item j and of item j + PF_TILES, advanced per item;
+    // the window's first tiles go towards L2 after the first copy is issued
+    int kc = lo / n_rb, rb = lo - kc * n_rb;
+    int kp = (lo + PF_TILES) / n_rb, rbp = lo + PF_TILES - kp * n_rb;
     for (int j = lo; j < hi; ++j) {
-        const int kc = j / n_rb, rb = j - kc * n_rb;
         const int r0 = rb * R, nr = min(R, N - r0);
         const unsigned bytes = (unsigned)nr * Kc * 2u;
         const uint16_t* src = W + (size_t)kc * N * Kc + (size_t)r0 * Kc;
         if (leader && j + PF_TILES < hi) {
-            const int jp = j + PF_TILES, kp = jp / n_rb, rp = (jp - kp * n_rb) * R;
+            const int rp = rbp * R;
             l2_prefetch(W + (size_t)kp * N * Kc + (size_t)rp * Kc, (unsigned)min(R, N - rp) * Kc * 2u);
+        }
+        if (++rb == n_rb) {
+            rb = 0;
+            ++kc;
+        }
+        if (++rbp == n_rb) {
+            rbp = 0;
+            ++kp;
         }
         int ok = 1;
         if (leader) {
@@ -1003,13 +1163,14 @@ __device__ __noinline__ void prod_gemv(Ctx& c, const Gemv& g, int expert, int lo
         }
         ++issued;
         prod_next(pr);
+        if (j == lo) prefetch_tiles(g, expert, lo + 1, min(hi, lo + PF_TILES));
     }
     c.set_pring(pr, issued);
 }
 
 // consumer side of a GEMV stage: items [lo, hi) of g after the deps set by
-// set_deps, then signal `sig`. The only call site of the GEMV code besides
-// the expert units, so it is compiled twice in all.
+// set_deps, then signal `sig` (the GEMV code, cons_gemv, is shared with the
+// expert units).
 __device__ __noinline__ void cons_mm(Ctx& c, int l, const Gemv& g, int sig, int lo, int hi) {
     c.cur_code = ((unsigned)sig << 16) | (unsigned)l;
     const long long t0 = gtimer();
@@ -1025,7 +1186,7 @@ __device__ __noinline__ void cons_mm(Ctx& c, int l, const Gemv& g, int sig, int 
 // union of the selected experts (sorted by id) -> routed slots.
 // consumers: full routing into Misc; producer warp: slot list only.
 template <bool PROD>
-__device__ __noinline__ bool route(Ctx& c, int l) {
+__device__ __forceinline__ bool route(Ctx& c, int l) {
     const Params& p = c.p;
     const Layer& Ld = c.layer();
     const int E = p.E, k = p.topk;
@@ -1063,6 +1224,54 @@ __device__ __noinline__ bool route(Ctx& c, int l) {
         for (int i = 0; i < MAX_E / 32; ++i) {
             const int e = lane + 32 * i;
             v[i] = e < E ? __ldcg(lg + e) : -INFINITY;
+        }
+        if (E <= 64 && !__any_sync(0xffffffffu, v[0] != v[0] || v[1] != v[1])) {
+            // up to 64 experts: each lane ranks its two logits against all
+            // others (greater value, or equal value and lower id, ranks
+            // first) -- independent shuffles instead of k dependent argmax
+            // rounds; the selected experts are those of rank < k
+            int rk[2] = {0, 0};
+#pragma unroll 4
+            for (int sl = 0; sl < 32; ++sl) {
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    const float ov = __shfl_sync(0xffffffffu, v[i], sl);
+                    const int oe = sl + 32 * i;
+#pragma unroll
+                    for (int q = 0; q < 2; ++q) rk[q] += (ov > v[q] || (ov == v[q] && oe < lane + 32 * q)) ? 1 : 0;
+                }
+            }
+            // renormalised top-k probabilities = softmax over the selected
+            // logits; the largest logit (rank 0) is the largest of all
+            float mx = fmaxf(v[0], v[1]);
+#pragma unroll
+            for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+            float ex[2], den = 0.f;
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                const bool s = rk[q] < k && lane + 32 * q < E;
+                ex[q] = s ? expf(v[q] - mx) : 0.f;
+                den += ex[q];
+            }
+#pragma unroll
+            for (int o = 16; o; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                const int e = lane + 32 * q;
+                if (rk[q] < k && e < E) {
+                    used[e] = 1;
+                    if constexpr (!PROD) {
+                        c.ms.ridx[m][rk[q]] = (uint8_t)e;
+                        c.ms.rw[m][rk[q]] = ex[q] / den;
+                        if (blockIdx.x == 0 && p.dbg_idx) {
+                            const size_t o = ((size_t)l * p.M + m) * k + rk[q];
+                            p.dbg_idx[o] = e;
+                            p.dbg_w[o] = ex[q] / den;
+                        }
+                    }
+                }
+            }
+            continue;
         }
         float sel[MAX_K];
         int sid[MAX_K];
@@ -1745,17 +1954,30 @@ __device__ __forceinline__ void cons_comb(Ctx& c, int l, int i) {
     const float L = cblock_sum(c, w * lv);
     if (tid < S) c.ms.cw[tid] = w / L;
     cbar();
-    // weighted sum of the O partials: warps take splits, lanes take 4 dims
+    // weighted sum of the O partials: warps take splits, lanes take 4 dims;
+    // a thread's split loads (up to CSPW) are all issued before the first
+    // is used, so the sum costs one L2 round trip instead of one per few
+    // splits (the partials were just written by other CTAs)
+    constexpr int CSPW = 20;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     if (lane * 4 < D) {
-#pragma unroll 4
-        for (int s2 = warp; s2 < S; s2 += NCW) {
-            const float4 v = __ldcg(reinterpret_cast<const float4*>(p.part + (r0 + s2 * rstride) * OL + d0 + lane * 4));
-            const float cw = c.ms.cw[s2];
-            acc.x = fmaf(cw, v.x, acc.x);
-            acc.y = fmaf(cw, v.y, acc.y);
-            acc.z = fmaf(cw, v.z, acc.z);
-            acc.w = fmaf(cw, v.w, acc.w);
+        for (int sb = warp; sb < S; sb += NCW * CSPW) {
+            float4 v[CSPW];
+#pragma unroll
+            for (int k = 0; k < CSPW; ++k) {
+                const int s2 = sb + NCW * k;
+                v[k] = s2 < S ? __ldcg(reinterpret_cast<const float4*>(p.part + (r0 + s2 * rstride) * OL + d0 + lane * 4))
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int k = 0; k < CSPW; ++k) {
+                const int s2 = sb + NCW * k;
+                const float cw = s2 < S ? c.ms.cw[s2] : 0.f;
+                acc.x = fmaf(cw, v[k].x, acc.x);
+                acc.y = fmaf(cw, v[k].y, acc.y);
+                acc.z = fmaf(cw, v[k].z, acc.z);
+                acc.w = fmaf(cw, v[k].w, acc.w);
+            }
         }
         *reinterpret_cast<float4*>(c.red() + warp * 128 + lane * 4) = acc;
     }
@@ -2092,16 +2314,28 @@ __device__ __noinline__ void unit_seg_cons(Ctx& c, int l, int kind, int expert, 
     const int F = K.F, n = u1 - u0, rows = 2 * F * n, M = p.M, d = p.d, tid = ctid();
     float* hs = unit_buf(c, 3 * F * n * M);
     float* h = hs + (size_t)rows * M;
+    const long long tue = p.trace_items ? gtimer() : 0;
     cbar();  // the previous segment's down rows may still read its hidden values here
     const long long tu0 = p.trace_items ? gtimer() : 0;
+    if (p.trace_items && tid == 0) trace_rec(c, 0x80000000u | (((unsigned)C_DOWN + 5) << 16) | (unsigned)l, 0u, tue, tu0);
     for (int i = tid; i < rows * M; i += NCT) hs[i] = 0.f;
     if (tid < M) c.ms.uw[tid] = expert < 0 ? 1.0f : route_weight(c.ms, tid, expert, p.topk);
     if (tid == 0) unit_gemv(p, Ld, c.ms.ug, kind, expert, u0, u1, hs);
     cbar();
+    const long long tz = p.trace_items ? gtimer() : 0;
+    const long long cz = clock64();
     const int n_rb = 2 * K.Fi / K.R, rpu = 2 * F / K.R;
     for (int kc = 0; kc < Ld.ffn.n_kc; ++kc) cons_gemv(c, c.ms.ug, 0, -1, kc * n_rb + u0 * rpu, kc * n_rb + u1 * rpu);
+    const long long tg = p.trace_items ? gtimer() : 0;
+    const long long cg = clock64();
+    // clock cycles: entry of the GEMV, its run start, its run end, return
+    if (p.trace_items == 1 && tid == 0)
+        trace_rec(c, 0x80000000u | (((unsigned)C_DOWN + 3) << 16) | (unsigned)l, (unsigned)(c.ms.tdbg[0] - cz),
+                  c.ms.tdbg[1] - cz, cg - c.ms.tdbg[2]);
     cbar();
     const long long tu1 = p.trace_items ? gtimer() : 0;
+    if (p.trace_items && tid == 0) trace_rec(c, 0x80000000u | (((unsigned)C_DOWN + 2) << 16) | (unsigned)l,
+                                             (unsigned)(tz - tu0), tg, tu1);
     for (int i = tid; i < F * n * M; i += NCT) {
         const int m = i / (F * n), rem = i - m * F * n, uu = rem / F, f = rem - uu * F;
         const float* g = hs + (size_t)m * rows + uu * 2 * F;
@@ -2113,9 +2347,13 @@ __device__ __noinline__ void unit_seg_cons(Ctx& c, int l, int kind, int expert, 
     uint8_t* const ring = c.smem + SMEM_RING;
     CRing cr = c.cr;
     bool dead = c.dead, timed_out = false;
-    const int nt = (d + K.Rd - 1) / K.Rd;
+    // tiles in a rotated order per CTA: the CTAs' atomic additions into the
+    // residual then go to different rows at any moment instead of all to the
+    // same few L2 slices (the producer streams the same order)
+    const int nt = (d + K.Rd - 1) / K.Rd, rot = (int)(blockIdx.x % (unsigned)nt);
     for (int uu = 0; uu < n; ++uu) {
-        for (int t = 0; t < nt; ++t) {
+        for (int t0 = 0; t0 < nt; ++t0) {
+            const int t = t0 + rot < nt ? t0 + rot : t0 + rot - nt;
             const int r0 = t * K.Rd, nr = min(K.Rd, d - r0);
             const uint8_t* tile = nullptr;
             if (!dead) {
@@ -2176,7 +2414,14 @@ __device__ __noinline__ void unit_seg_prod(Ctx& c, int kind, int expert, int u0,
     const int F = K.F, d = p.d, lane = threadIdx.x & 31, Kc = Ld.ffn.Kc;
     const uint16_t* gu = K.gu + (expert >= 0 ? (size_t)expert * K.gu_es : 0);
     const uint16_t* dn = K.dn + (expert >= 0 ? (size_t)expert * K.dn_es : 0);
-    // L2 prefetch: per K panel the segment's gate/up rows are contiguous, and
+    if (lane == 0) unit_gemv(p, Ld, c.ms.pug, kind, expert, u0, u1, nullptr);
+    __syncwarp();
+    const int n_rb = 2 * K.Fi / K.R, rpu = 2 * F / K.R;
+    // the first ring-full of gate/up tiles is requested before the L2
+    // prefetch of the rest of the segment, which would queue ahead of it
+    const int first = min(NSLOT, (u1 - u0) * rpu);
+    prod_gemv(c, c.ms.pug, -1, u0 * rpu, u0 * rpu + first);
+    // then the L2 prefetch: per K panel the segment's gate/up rows are contiguous, and
     // so are its down blocks; pieces of at most 64 KB, one lane each
     {
         const size_t piece = 32768;  // elements
@@ -2190,19 +2435,17 @@ __device__ __noinline__ void unit_seg_prod(Ctx& c, int kind, int expert, int u0,
         const size_t n = (size_t)(u1 - u0) * d * F;
         for (size_t o = (size_t)lane * piece; o < n; o += 32 * piece) l2_prefetch(b + o, (unsigned)(min(piece, n - o) * 2));
     }
-    if (lane == 0) unit_gemv(p, Ld, c.ms.pug, kind, expert, u0, u1, nullptr);
-    __syncwarp();
-    const int n_rb = 2 * K.Fi / K.R, rpu = 2 * F / K.R;
     for (int kc = 0; kc < Ld.ffn.n_kc && !c.dead; ++kc)
-        prod_gemv(c, c.ms.pug, -1, kc * n_rb + u0 * rpu, kc * n_rb + u1 * rpu);
+        prod_gemv(c, c.ms.pug, -1, kc * n_rb + u0 * rpu + (kc == 0 ? first : 0), kc * n_rb + u1 * rpu);
     Misc& ms = c.ms;
     uint8_t* ring = c.smem + SMEM_RING;
     PRing pr = c.pr;
     int issued = c.issued;
     const unsigned long long pol = l2_evict_first();
-    const int nt = (d + K.Rd - 1) / K.Rd;
+    const int nt = (d + K.Rd - 1) / K.Rd, rot = (int)(blockIdx.x % (unsigned)nt);  // the consumers' tile order
     for (int u = u0; u < u1 && !c.dead; ++u) {
-        for (int t = 0; t < nt; ++t) {
+        for (int t0 = 0; t0 < nt; ++t0) {
+            const int t = t0 + rot < nt ? t0 + rot : t0 + rot - nt;
             const int r0 = t * K.Rd, nr = min(K.Rd, d - r0);
             const unsigned bytes = (unsigned)nr * F * 2u;
             int ok = 1;
@@ -2256,15 +2499,27 @@ __device__ __noinline__ void ffn_stage(Ctx& c, int l) {
             return;
         }
     } else {
+        if constexpr (!PROD) {
+            // stage the normalised input of the expert GEMVs while the router
+            // is still running (it depends only on the residual and the FFN
+            // norm gain, not on the routing)
+            if (threadIdx.x == 0) unit_gemv(p, Ld, c.ms.ug, 0, 0, 0, 1, c.red() + RED_FLOATS / 2);
+            set_deps(c, deps1(l, C_O, (unsigned)gemv_items(Ld.g[G_O])));
+            cwait(c, 0x1200u | (unsigned)(l << 16));
+            if (p.M * Ld.ffn.Kc <= STAGE_FLOATS) restage(c, c.ms.ug, Ld.x, 0, 0, 0, p.M);
+        }
+        const long long tr0 = p.trace_items ? gtimer() : 0;
         if (!route<PROD>(c, l) && PROD) {
             c.dead = true;
             return;
         }
+        if (!PROD && p.trace_items && threadIdx.x == 0)
+            trace_rec(c, 0x80000000u | (((unsigned)C_DOWN + 4) << 16) | (unsigned)l, 0u, tr0, gtimer());
         const FfnKind& K = Ld.ffn.k[0];
         const int nslots = PROD ? c.ms.p_nslots : c.ms.n_slots;
         const uint8_t* slot_e = PROD ? c.ms.p_slot_e : c.ms.slot_e;
         int lo, hi;
-        my_range_sub(nslots * K.nu, p.gs, p.G - p.gs, lo, hi);
+        my_range_sub(nslots * K.nu, p.gs, p.G - p.gs - p.gr, lo, hi);
         for (int i = lo; i < hi && !(PROD && c.dead);) {
             const int s2 = i / K.nu, iend = min(hi, (s2 + 1) * K.nu);
             if constexpr (PROD)
@@ -2425,15 +2680,15 @@ __device__ __noinline__ bool exec_stage(Ctx& c) {
                 deps = mla ? deps1(l, C_UV, (unsigned)gemv_items(Ld.g[G_UV])) : deps1(l, C_COMB, (unsigned)comb_items(p));
                 sig = C_O;
                 break;
-            // the router runs on the routed-expert CTAs (the shared expert's
-            // CTAs start their units meanwhile)
+            // the router runs on its own CTAs [G - gr, G): the routed units
+            // wait for it, the shared units do not
             case S_ROUTER:
                 if (p.E == 0) return true;
                 g = &Ld.g[G_ROUTER];
                 deps = deps1(l, C_O, (unsigned)gemv_items(Ld.g[G_O]));
                 sig = C_ROUTER;
-                c0 = p.gs;
-                gc = p.G - p.gs;
+                c0 = p.G - p.gr;
+                gc = p.gr;
                 break;
             case S_CARRY: {
                 if (!p.carry) return true;
