@@ -116,7 +116,13 @@ typedef struct mk_info {
  * exactly once) into the library's packed layout. The caller keeps ownership
  * of its buffers. Errors: INVALID_ARG (bad/missing/duplicate tensor),
  * UNSUPPORTED (shape the kernel does not implement), OOM, CUDA.
- * Synchronises `stream` before returning. */
+ * Synchronises `stream` before returning.
+ * Schedule: for steps of two or more tokens, when the attention output
+ * projection has one K panel, the CTAs that compute it also accumulate the
+ * router logits of their rows, and the step has no separate router stage.
+ * With the environment variable MK_ROUTER_STAGE=1 set at this call, the
+ * model always keeps the separate router stage (the schedule used
+ * otherwise); results agree within rounding. */
 int mk_load_weights(const mk_config* cfg, const mk_weight* table, int32_t n, void* stream, mk_model** out);
 
 /* Paged KV cache for `batch` sequences of up to `max_ctx` positions each

@@ -43,6 +43,11 @@ constexpr int RED_FLOATS = 1024;
 constexpr int MT = 4;                     // tokens per register group in the GEMV
 constexpr int MAX_M = 64;                 // batch * tokens per step
 constexpr int MAX_E = 256;
+// router logits accumulated by the output projection's CTAs go to one of
+// ROUTER_COPIES copies (by CTA), so that few CTAs add into the same lines;
+// a token's row holds E logits and the sum of squares, padded to 4 floats
+constexpr int ROUTER_COPIES = 16;
+__host__ __device__ constexpr int router_row(int E) { return (E + 4) & ~3; }
 constexpr int MAX_K = 8;
 constexpr int GQA_CH = 64;                // positions per GQA chunk (= one page)
 constexpr int MLA_CH = 32;                // positions per MLA chunk (half a page)
@@ -109,7 +114,7 @@ struct Layer {
     const float* qlat;        // MLA: absorbed queries [M][H*kl]
     float* olat;              // MLA: combined latent attention output [M][H*kl]
     float* o;                 // attention output [M][Hq*hd | H*vd]
-    const float* rlog;        // router logits [M][E]
+    float* rlog;              // router stage output: logits [M][router_row(E)]
     float* x;                 // residual entering the layer [M][d]
     float* xn;                // residual leaving the layer [M][d]
     int a_stride;
@@ -150,6 +155,8 @@ struct Params {
     int nz, carry;                  // carry: residual copied by items (split-K output projection)
     int gs, gr;                     // CTAs [0, gs): shared expert, [G-gr, G): router, between: routed experts
     int stall;                      // testing: CTA 0 first waits on a counter nothing signals (ends in a timeout)
+    int rfuse;                      // router logits accumulated by the output projection's CTAs (no router stage)
+    float* racc;                    // their accumulators [L][ROUTER_COPIES][M][router_row(E)], zero at step start
     float* ubuf;                    // per CTA: expert-unit gate/up and hidden values when shared memory is short
     long long ubuf_stride;          // floats per CTA
     unsigned* ctr;                  // [2][L+1][NCTR]
@@ -186,6 +193,11 @@ struct Misc {
     int ndep;
     Gemv ug, pug;                   // expert-unit gate/up GEMV (consumers, producer)
     float uw[MAX_M];                // expert-unit routing weight per token
+    // tokens of the current GEMV: gm of them, token i staged at row gt[i] of
+    // the staging area (all tokens in order, except in a routed expert's
+    // units, which take only the tokens routed to the expert)
+    uint8_t gt[MAX_M];
+    int gm;
     long long tdbg[4];              // trace: clock64 marks of the expert-unit gate/up GEMV
     int abort;
     int n_slots, p_nslots;

@@ -55,6 +55,7 @@ struct mk_model {
     std::vector<mk::Layer> layers;
     mk::Layer* d_layers = nullptr;
     mk::Params base;  // everything except the per-step fields
+    bool rfuse_ok;    // the router can be folded into the output projection
     unsigned* ctr = nullptr;
     size_t ctr_n = 0;
     unsigned* status = nullptr;
@@ -153,6 +154,8 @@ int validate(const mk_config* c) {
     if (d.V % 8) return fail(MK_ERR_UNSUPPORTED, "vocab must be a multiple of 8");
     return MK_OK;
 }
+
+int gemv_items_host(const mk::Gemv& g) { return g.n_rb * g.n_kc; }
 
 void make_gemv(mk::Gemv& g, const uint16_t* W, int N, int K, int in_kind, const float* src, int src_stride,
                const uint16_t* gain, int out_kind, float* dst, int dst_stride, float* dst2 = nullptr) {
@@ -371,7 +374,8 @@ int mk_load_weights(const mk_config* cfg, const mk_weight* table, int32_t n, voi
     const size_t s_qlat = D.gqa ? 0 : stake((size_t)L * Mx * D.Hq * D.kl * 4);
     const size_t s_olat = D.gqa ? 0 : stake((size_t)L * Mx * D.Hq * D.kl * 4);
     const size_t s_o = stake((size_t)L * Mx * D.o_in * 4);
-    const size_t s_rlog = D.E ? stake((size_t)L * Mx * D.E * 4) : 0;
+    const size_t s_rlog = D.E ? stake((size_t)L * Mx * mk::router_row(D.E) * 4) : 0;
+    const size_t s_racc = D.E ? stake((size_t)L * mk::ROUTER_COPIES * Mx * mk::router_row(D.E) * 4) : 0;
     // expert units: per CTA, gate/up outputs and hidden values of at most one
     // expert's units for every token
     const size_t ubuf_stride = (size_t)3 * std::max(D.E ? D.ffn : 0, D.sh ? D.sffn : 0) * Mx;
@@ -565,9 +569,10 @@ int mk_load_weights(const mk_config* cfg, const mk_weight* table, int32_t n, voi
             Ld.ffn.n_kc = d / Kc;
         };
         if (D.E) {
-            float* rlog = F(s_rlog) + (size_t)l * Mx * D.E;
+            float* rlog = F(s_rlog) + (size_t)l * Mx * mk::router_row(D.E);
             Ld.rlog = rlog;
-            make_gemv(Ld.g[mk::G_ROUTER], W + o.router, D.E, d, mk::IN_RMS, x, d, W + o.fn, mk::OUT_STORE, rlog, D.E);
+            make_gemv(Ld.g[mk::G_ROUTER], W + o.router, D.E, d, mk::IN_RMS, x, d, W + o.fn, mk::OUT_STORE, rlog,
+                      mk::router_row(D.E));
             set_kind(Ld.ffn.k[0], D.ffn, W + o.gu, W + o.down);
         }
         if (D.sh) set_kind(Ld.ffn.k[1], D.sffn, W + o.shgu, W + o.shdown);
@@ -615,6 +620,20 @@ int mk_load_weights(const mk_config* cfg, const mk_weight* table, int32_t n, voi
     if (P.carry) {
         P.zptr[nz] = F(s_x) + (size_t)Mx * d;
         P.zn[nz++] = (long long)L * Mx * d;
+    }
+    // the router folded into the output projection: possible when that
+    // projection has one K panel (its rows are final in the CTA that computes
+    // them) and a CTA's rows of every token (twice) and its logit sums fit
+    // the staging area
+    {
+        const mk::Gemv& go = m->layers[0].g[mk::G_O];
+        const int items = gemv_items_host(go), per_cta = (items + m->G - 1) / m->G;
+        const char* ev = getenv("MK_ROUTER_STAGE");
+        m->rfuse_ok = D.E > 0 && go.n_kc == 1 && go.out_kind == mk::OUT_RESID && go.R % 8 == 0 && go.N % 8 == 0 &&
+                      m->layers[0].g[mk::G_ROUTER].Kc % 8 == 0 &&
+                      (2 * per_cta * go.R + mk::router_row(D.E)) * Mx <= mk::STAGE_FLOATS && !(ev && atoi(ev) > 0);
+        P.rfuse = 0;  // per step
+        P.racc = D.E ? F(s_racc) : nullptr;
     }
     P.nz = nz;  // logits (split-K head) are added per step in mk_decode_step
     m->ctr = reinterpret_cast<unsigned*>(S + s_ctr);
@@ -737,16 +756,14 @@ int mk_kv_read(const mk_kv* kv, int32_t layer, int32_t seq, int32_t pos0, int32_
     return kv_copy(kv, layer, seq, pos0, n, rows, stream, 0);
 }
 
-int gemv_items_host(const mk::Gemv& g) { return g.n_rb * g.n_kc; }
-
 // FFN CTA groups: gr CTAs run the router (one per router tile), gs CTAs the
 // shared expert's units, the rest the routed experts' units; gs follows the
-// two kinds' unit counts, the routed count taken as the expected number of
-// distinct experts of M tokens picking top_k of E uniformly at random
-static void ffn_split(const mk_model* m, int M, int& gs, int& gr) {
+// two kinds' expected work, the routed unit count taken as the expected
+// number of distinct experts of M tokens picking top_k of E uniformly at random
+static void ffn_split(const mk_model* m, int M, bool rfuse, int& gs, int& gr) {
     const Dims D = dims_of(m->cfg);
     const mk::Layer& L0 = m->layers[0];
-    gr = D.E ? std::min(gemv_items_host(L0.g[mk::G_ROUTER]), m->G / 4) : 0;
+    gr = D.E && !rfuse ? std::min(gemv_items_host(L0.g[mk::G_ROUTER]), m->G / 4) : 0;
     if (!D.E) {
         gs = m->G;
         return;
@@ -755,13 +772,31 @@ static void ffn_split(const mk_model* m, int M, int& gs, int& gr) {
         gs = 0;
         return;
     }
-    const double us = L0.ffn.k[1].nu;
+    // a unit's time grows with its token count (the weights stream once, the
+    // arithmetic is per token): about 1 + 0.35 (t - 1) tile times for t tokens.
+    // A routed expert's units take only its own tokens (M k / distinct on
+    // average) when the routed CTAs stage all tokens' input in one K panel.
+    const auto cost = [](double t) { return 1.0 + 0.35 * (t - 1.0); };
     const double uniq = D.E * (1.0 - std::pow(1.0 - (double)D.k / D.E, (double)M));
-    const double ur = uniq * L0.ffn.k[0].nu;
+    const bool compact = M > 1 && L0.ffn.n_kc == 1 && M * L0.ffn.Kc <= mk::STAGE_FLOATS;
+    const double us = L0.ffn.k[1].nu * cost(M);
+    const double ur = uniq * L0.ffn.k[0].nu * cost(compact ? M * D.k / uniq : M);
     const int avail = m->G - gr;
     gs = (int)std::lround(avail * us / (us + ur));
     if (gs < 1) gs = 1;
     if (gs > avail - 1) gs = avail - 1;
+}
+
+// per step: the router folded into the output projection for two or more
+// tokens (one token routes sooner with its own router stage, which overlaps
+// the shared expert), and the FFN CTA groups
+static void step_router(const mk_model* m, mk::Params& P) {
+    P.rfuse = m->rfuse_ok && P.M >= 2;
+    if (P.rfuse) {
+        P.zptr[P.nz] = P.racc;
+        P.zn[P.nz++] = (long long)P.L * mk::ROUTER_COPIES * P.M * mk::router_row(P.E);
+    }
+    ffn_split(m, P.M, P.rfuse, P.gs, P.gr);
 }
 
 int mk_decode_step(mk_model* m, mk_kv* kv, const int32_t* tokens, const int32_t* positions, int32_t batch,
@@ -786,7 +821,7 @@ int mk_decode_step(mk_model* m, mk_kv* kv, const int32_t* tokens, const int32_t*
     P.B = batch;
     P.T = T;
     P.M = batch * T;
-    ffn_split(m, P.M, P.gs, P.gr);
+    step_router(m, P);
     P.stall = getenv("MK_TEST_STALL") != nullptr;
     P.logits = logits;
     P.accept = accept;
@@ -985,6 +1020,7 @@ extern "C" int mk_decode_step_noalloc(mk_model* m, mk_kv* kv, const int32_t* tok
     P.part_ml = r(P.part_ml);
     P.amax = r(P.amax);
     P.ubuf = r(P.ubuf);
+    P.racc = r(P.racc);
     for (int z = 0; z < P.nz; ++z) P.zptr[z] = r(P.zptr[z]);
     P.ctr = r(P.ctr);
     P.status = r(P.status);
@@ -1005,7 +1041,7 @@ extern "C" int mk_decode_step_noalloc(mk_model* m, mk_kv* kv, const int32_t* tok
     P.B = batch;
     P.T = T;
     P.M = batch * T;
-    ffn_split(m, P.M, P.gs, P.gr);
+    step_router(m, P);
     P.logits = logits;
     P.accept = accept;
     P.lm.dst = logits;

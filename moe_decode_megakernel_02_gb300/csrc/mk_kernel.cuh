@@ -452,6 +452,10 @@ __device__ void gemv_warp_tile(Ctx& c, const Gemv& g, const uint8_t* tile, int n
     const int Kc = g.Kc, NC = Kc >> 3, RW = (nr + 7) >> 3, rw0 = warp * RW;
     const int RWv = max(0, min(RW, nr - rw0));  // this warp's rows
     const uint4* T4 = reinterpret_cast<const uint4*>(tile);
+    // staged row of token mbase + m: the staging holds tokens from mbase - mt0 on
+    int xrow[MTc];
+#pragma unroll
+    for (int m = 0; m < MTc; ++m) xrow[m] = m < mcount ? (int)c.ms.gt[mbase + m] - (mbase - mt0) : mt0 + m;
     if (NC >= 32) {
         const int JC = NC >> 5;
         for (int r = 0; r < RWv; r += 4) {
@@ -466,8 +470,8 @@ __device__ void gemv_warp_tile(Ctx& c, const Gemv& g, const uint8_t* tile, int n
                 float xv[MTc][8];
 #pragma unroll
                 for (int m = 0; m < MTc; ++m) {
-                    const float4 a = *reinterpret_cast<const float4*>(xs + (size_t)(mt0 + m) * Kc + ch * 8);
-                    const float4 b = *reinterpret_cast<const float4*>(xs + (size_t)(mt0 + m) * Kc + ch * 8 + 4);
+                    const float4 a = *reinterpret_cast<const float4*>(xs + (size_t)xrow[m] * Kc + ch * 8);
+                    const float4 b = *reinterpret_cast<const float4*>(xs + (size_t)xrow[m] * Kc + ch * 8 + 4);
                     xv[m][0] = a.x; xv[m][1] = a.y; xv[m][2] = a.z; xv[m][3] = a.w;
                     xv[m][4] = b.x; xv[m][5] = b.y; xv[m][6] = b.z; xv[m][7] = b.w;
                 }
@@ -511,8 +515,8 @@ __device__ void gemv_warp_tile(Ctx& c, const Gemv& g, const uint8_t* tile, int n
 #pragma unroll
             for (int m = 0; m < MTc; ++m) {
                 float xv[8];
-                const float4 a = *reinterpret_cast<const float4*>(xs + (size_t)(mt0 + m) * Kc + ch * 8);
-                const float4 b = *reinterpret_cast<const float4*>(xs + (size_t)(mt0 + m) * Kc + ch * 8 + 4);
+                const float4 a = *reinterpret_cast<const float4*>(xs + (size_t)xrow[m] * Kc + ch * 8);
+                const float4 b = *reinterpret_cast<const float4*>(xs + (size_t)xrow[m] * Kc + ch * 8 + 4);
                 xv[0] = a.x; xv[1] = a.y; xv[2] = a.z; xv[3] = a.w;
                 xv[4] = b.x; xv[5] = b.y; xv[6] = b.z; xv[7] = b.w;
                 acc[m] = 0.f;
@@ -628,7 +632,7 @@ __device__ __forceinline__ void gemv_range_ks(Ctx& c, const Gemv& g, int slot, i
     const Params& p = c.p;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, tid = threadIdx.x;
     constexpr int RG = 32 / CPWP, RWT = 8 * RG;  // row groups per warp, rows per warp tile
-    const int M = p.M, Kc = g.Kc, NC = Kc >> 3, NKS = ks_nks(Kc), CPW = NC / NKS;
+    const int M = c.ms.gm, Kc = g.Kc, NC = Kc >> 3, NKS = ks_nks(Kc), CPW = NC / NKS;
     const int ks = warp % NKS, rb = warp / NKS;
     const int rg = lane / CPWP, ch = lane % CPWP;
     const bool act = ch < CPW;
@@ -677,7 +681,7 @@ __device__ __forceinline__ void gemv_range_ks(Ctx& c, const Gemv& g, int slot, i
 #pragma unroll
                     for (int m = 0; m < MR; ++m) {
                         const bool ok = act && mb + m < M;
-                        const float* xp = xs + (size_t)(mb + m) * Kc + chunk * 8;
+                        const float* xp = xs + (size_t)(ok ? ms.gt[mb + m] : 0) * Kc + chunk * 8;
                         xa[m] = ok ? *reinterpret_cast<const float4*>(xp) : make_float4(0.f, 0.f, 0.f, 0.f);
                         xb[m] = ok ? *reinterpret_cast<const float4*>(xp + 4) : make_float4(0.f, 0.f, 0.f, 0.f);
                     }
@@ -858,7 +862,7 @@ __device__ __forceinline__ void gemv_range_rx(Ctx& c, const Gemv& g, int slot, i
     const float* src = g.src + (size_t)slot * g.src_sstride;
     Misc& ms = c.ms;
     uint8_t* const ring = c.smem + SMEM_RING;
-    const float* const xs = c.stage();
+    const float* const xs = c.stage() + (size_t)ms.gt[0] * g.Kc;  // the token's staged row
     CRing cr = c.cr;
     bool dead = c.dead, timed_out = false;
     constexpr int NX = wide ? JC : 1;
@@ -1033,7 +1037,7 @@ __device__ __forceinline__ void gemv_range_smem(Ctx& c, const Gemv& g, int slot,
     const Params& p = c.p;
     const float* src = g.src + (size_t)slot * g.src_sstride;
     const int cap = STAGE_FLOATS / g.Kc;
-    const int M = p.M;
+    const int M = c.ms.gm;
     for (int j = j_lo; j < j_hi; ++j) {
         const int kc = j / g.n_rb, rb = j - kc * g.n_rb;
         const int r0 = rb * g.R, nr = min(g.R, g.N - r0);
@@ -1069,9 +1073,11 @@ __device__ __forceinline__ void gemv_range_smem(Ctx& c, const Gemv& g, int slot,
 // its own: inlined next to the one-token path, the two would together need
 // more registers than a thread has, and spills go to local memory.
 __device__ __noinline__ void gemv_multi(Ctx& c, const Gemv& g, int slot, int expert, int j_lo, int j_hi) {
-    const int M = c.p.M, nks = ks_nks(g.Kc);
+    const int M = c.ms.gm, nks = ks_nks(g.Kc);
     const bool narrow = g.Kc == 128 || g.Kc == 768;  // row slices of 16 / 12 chunks
-    const bool ks = M == 2 && nks > 0 && g.R <= (8 / nks) * (narrow ? 16 : 8);
+    // split K (input in registers for the whole run, two tokens at a time)
+    // when every token's K panel is staged at once
+    const bool ks = M >= 2 && nks > 0 && g.R <= (8 / nks) * (narrow ? 16 : 8) && M * g.Kc <= STAGE_FLOATS;
     if (!ks)
         gemv_range_smem(c, g, slot, expert, j_lo, j_hi);
     else if (narrow)
@@ -1084,7 +1090,7 @@ __device__ __noinline__ void gemv_multi(Ctx& c, const Gemv& g, int slot, int exp
 // code for the plain stages and the expert units: every stage's code runs
 // once per layer, and a smaller footprint keeps it in the instruction cache)
 __device__ __noinline__ void cons_gemv(Ctx& c, const Gemv& g, int slot, int expert, int j_lo, int j_hi) {
-    const int M = c.p.M, Kc = g.Kc;
+    const int M = c.ms.gm, Kc = g.Kc;
     if (M == 1 && Kc == 2048)
         gemv_range_rx<8>(c, g, slot, expert, j_lo, j_hi);
     else if (M == 1 && Kc == 1024)
@@ -1115,6 +1121,7 @@ __device__ __forceinline__ void prefetch_tiles(const Gemv& g, int expert, int lo
 }
 
 constexpr int PF_TILES = 8;  // L2 prefetch distance beyond the ring, in tiles
+constexpr int UNIT_PF_BYTES = 640 * 1024;  // expert units: L2 prefetch up front, per CTA
 
 __device__ __noinline__ void prod_gemv(Ctx& c, const Gemv& g, int expert, int lo, int hi) {
     const uint16_t* W = g.W + (expert >= 0 ? (size_t)expert * g.w_estride : 0);
@@ -1171,12 +1178,93 @@ __device__ __noinline__ void prod_gemv(Ctx& c, const Gemv& g, int expert, int lo
 // consumer side of a GEMV stage: items [lo, hi) of g after the deps set by
 // set_deps, then signal `sig` (the GEMV code, cons_gemv, is shared with the
 // expert units).
+// consumers, output projection with the router folded in (one K panel, so
+// this CTA's rows [R lo, R hi) of the new residual are final after its
+// GEMV): their share of every token's router logits, sum_i Wr[e][i] g[i] x[i]
+// (the 1/rms factor is applied by the reader), and of the sum of squares of
+// x, added into this CTA's copy of the layer's accumulators (vector
+// reductions, one per 4 floats). The accumulators start at zero (cleared at
+// the start of the step) and are complete when every item of the output
+// projection has been signalled.
+__device__ __noinline__ void router_part(Ctx& c, int l, const Gemv& go, int lo, int hi) {
+    const Params& p = c.p;
+    const Layer& Ld = c.layer();
+    const Gemv& gr = Ld.g[G_ROUTER];
+    const int r_lo = lo * go.R, nr = min(go.N, hi * go.R) - r_lo;  // a multiple of 8
+    const int E = p.E, M = p.M, tid = ctid(), Kc = gr.Kc, RS = router_row(E);
+    float* xg = c.stage();            // [M][nr] x g
+    float* xs = xg + M * nr;          // [M][nr] x
+    float* sums = xs + M * nr;        // [M][RS]
+    cbar();                           // this CTA's stores of the rows are visible to all its threads
+    for (int i = tid; i < M * nr; i += NCT) {
+        const int m = i / nr, r = i - m * nr;
+        const float x = __ldcg(go.dst + (size_t)m * go.dst_stride + r_lo + r);
+        xg[i] = x * bf2f(gr.gain[r_lo + r]);
+        xs[i] = x;
+    }
+    for (int i = tid; i < M * RS; i += NCT) sums[i] = 0.f;
+    cbar();
+    // thread: expert e, 8-row groups sub, sub + 4, ...; tokens 8 at a time
+    const int sub = tid & 3, ng = nr >> 3;
+    for (int e0 = 0; e0 < E; e0 += NCT / 4) {
+        const int e = e0 + (tid >> 2);
+        for (int m0 = 0; m0 < M; m0 += 8) {
+            float s[8], s2[8];
+#pragma unroll
+            for (int t = 0; t < 8; ++t) s[t] = s2[t] = 0.f;
+            if (e < E) {
+                for (int q = sub; q < ng; q += 4) {
+                    const int i = r_lo + 8 * q, kc = i / Kc;
+                    const uint4 w = *reinterpret_cast<const uint4*>(gr.W + ((size_t)kc * E + e) * Kc + (i - kc * Kc));
+#pragma unroll
+                    for (int t = 0; t < 8; ++t) {
+                        if (m0 + t < M) {
+                            const float4* xm = reinterpret_cast<const float4*>(xg + (m0 + t) * nr + 8 * q);
+                            fma8v2(s[t], s2[t], w, xm[0], xm[1]);
+                        }
+                    }
+                }
+            }
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+                if (m0 + t < M) {
+                    float v = s[t] + s2[t];
+                    v += __shfl_xor_sync(0xffffffffu, v, 1);
+                    v += __shfl_xor_sync(0xffffffffu, v, 2);
+                    if (sub == 0 && e < E) sums[(m0 + t) * RS + e] = v;
+                }
+            }
+        }
+    }
+    // sums of squares: warp w takes tokens w, w + NCW, ...
+    const int lane = tid & 31;
+    for (int m = tid >> 5; m < M; m += NCW) {
+        float q = 0.f;
+        for (int r = lane; r < nr; r += 32) {
+            const float x = xs[m * nr + r];
+            q = fmaf(x, x, q);
+        }
+#pragma unroll
+        for (int o = 16; o; o >>= 1) q += __shfl_xor_sync(0xffffffffu, q, o);
+        if (lane == 0) sums[m * RS + E] = q;
+    }
+    cbar();
+    float* acc = p.racc + ((size_t)l * ROUTER_COPIES + blockIdx.x % ROUTER_COPIES) * M * RS;
+    for (int i = 4 * tid; i < M * RS; i += 4 * NCT) {
+        const float4 v = *reinterpret_cast<const float4*>(sums + i);
+        asm volatile("red.relaxed.gpu.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(acc + i), "f"(v.x), "f"(v.y),
+                     "f"(v.z), "f"(v.w)
+                     : "memory");
+    }
+}
+
 __device__ __noinline__ void cons_mm(Ctx& c, int l, const Gemv& g, int sig, int lo, int hi) {
     c.cur_code = ((unsigned)sig << 16) | (unsigned)l;
     const long long t0 = gtimer();
     cwait(c, 0x1000u | (unsigned)(l << 16) | (unsigned)sig);
     const long long t1 = gtimer();
     cons_gemv(c, g, 0, -1, lo, hi);
+    if (sig == C_O && c.p.rfuse && !c.dead) router_part(c, l, g, lo, hi);
     csignal(c, l, sig, (unsigned)(hi - lo));
     trace_rec(c, ((unsigned)sig << 16) | (unsigned)l, (unsigned)(hi - lo), t0, t1);
 }
@@ -1196,7 +1284,8 @@ __device__ __forceinline__ bool route(Ctx& c, int l) {
     if constexpr (PROD) {
         int ok = 1;
         if (lane == 0) {
-            ok = wait_ge(p, ctr_of(p, l, C_ROUTER), (unsigned)gemv_items(Ld.g[G_ROUTER]), 0x300u);
+            ok = p.rfuse ? wait_ge(p, ctr_of(p, l, C_O), (unsigned)gemv_items(Ld.g[G_O]), 0x300u)
+                         : wait_ge(p, ctr_of(p, l, C_ROUTER), (unsigned)gemv_items(Ld.g[G_ROUTER]), 0x300u);
             __threadfence();
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -1209,7 +1298,8 @@ __device__ __forceinline__ bool route(Ctx& c, int l) {
         __syncwarp();
     } else {
         const long long t0 = gtimer();
-        set_deps(c, deps1(l, C_ROUTER, (unsigned)gemv_items(Ld.g[G_ROUTER])));
+        set_deps(c, p.rfuse ? deps1(l, C_O, (unsigned)gemv_items(Ld.g[G_O]))
+                            : deps1(l, C_ROUTER, (unsigned)gemv_items(Ld.g[G_ROUTER])));
         cwait(c, 0x400u);
         trace_rec(c, (0x40u << 16) | (unsigned)l, 0u, t0, gtimer());
         for (int e = tid; e < E; e += NCT) used[e] = 0;
@@ -1219,11 +1309,30 @@ __device__ __forceinline__ bool route(Ctx& c, int l) {
     const int nw = PROD ? 1 : NCW;
     for (int m = warp; m < p.M; m += nw) {
         float v[MAX_E / 32];
-        const float* lg = Ld.rlog + (size_t)m * E;
+        const int RS = router_row(E);
+        const float* lg = (p.rfuse ? p.racc + (size_t)l * ROUTER_COPIES * p.M * RS : Ld.rlog) + (size_t)m * RS;
 #pragma unroll
         for (int i = 0; i < MAX_E / 32; ++i) {
             const int e = lane + 32 * i;
             v[i] = e < E ? __ldcg(lg + e) : -INFINITY;
+        }
+        if (p.rfuse) {
+            // accumulated logits: the sum over the copies, times 1/rms of the
+            // residual (mean square over d)
+            float ss = lane == 0 ? __ldcg(lg + E) : 0.f;
+#pragma unroll
+            for (int cp = 1; cp < ROUTER_COPIES; ++cp) {
+                const float* lc = lg + (size_t)cp * p.M * RS;
+#pragma unroll
+                for (int i = 0; i < MAX_E / 32; ++i) {
+                    const int e = lane + 32 * i;
+                    if (e < E) v[i] += __ldcg(lc + e);
+                }
+                if (lane == 0) ss += __ldcg(lc + E);
+            }
+            const float sc = 1.0f / sqrtf(__shfl_sync(0xffffffffu, ss, 0) * (1.0f / (float)p.d) + p.eps);
+#pragma unroll
+            for (int i = 0; i < MAX_E / 32; ++i) v[i] *= sc;
         }
         if (E <= 64 && !__any_sync(0xffffffffu, v[0] != v[0] || v[1] != v[1])) {
             // up to 64 experts: each lane ranks its two logits against all
@@ -2208,6 +2317,13 @@ __device__ __noinline__ void prefetch_next_small(Ctx& c, int l) {
     } else if (lane == 0 && p.lm.gain) {
         l2_prefetch_keep(p.lm.gain, (unsigned)p.lm.K * 2u);
     }
+    // router folded into the output projection: layer l's router weights
+    // towards L2 (64 KB per CTA), read at the end of the output projection
+    if (p.rfuse && lane == 5) {
+        const Gemv& gr = c.layer().g[G_ROUTER];
+        const size_t bytes = (size_t)gr.N * gr.K * 2, o = (size_t)blockIdx.x * 65536;
+        if (o < bytes) l2_prefetch(reinterpret_cast<const uint8_t*>(gr.W) + o, (unsigned)min((size_t)65536, bytes - o));
+    }
 }
 
 // copy layer l's descriptors into this side's shared-memory slot (the
@@ -2281,7 +2397,8 @@ __device__ __forceinline__ void unit_gemv(const Params& p, const Layer& Ld, Gemv
     ug.grp_rows = 0;
     ug.grp_stride = 0;
     ug.sw_off = 0;
-    ug.out_kind = OUT_ACC;
+    // one K panel: every value is written once; otherwise the panels add up
+    ug.out_kind = Ld.ffn.n_kc == 1 ? OUT_STORE : OUT_ACC;
     ug.dst = hs - (size_t)2 * K.F * u0;  // rows [2F u0, 2F u1) land at hs[0 ..)
     ug.dst_stride = 2 * K.F * (u1 - u0);
     ug.dst_sstride = 0;
@@ -2307,19 +2424,72 @@ __device__ __forceinline__ void down_rows1(const uint8_t* tile, int nr, const fl
     }
 }
 
+// one thread's rows of a down tile (nr rows x F), several tokens: the row's
+// weights in registers, token i's hidden values at hu + i hstride, its
+// output row gt[i] of xo (stride d), scaled by its routing weight
+template <int F8>
+__device__ __forceinline__ void down_rowsM(const uint8_t* tile, int nr, const float* hu, int hstride, int M,
+                                           const Misc& ms, float* xo, int d) {
+    const uint4* T4 = reinterpret_cast<const uint4*>(tile);
+    for (int r = ctid(); r < nr; r += NCT) {
+        uint4 w[F8];
+#pragma unroll
+        for (int q = 0; q < F8; ++q) w[q] = T4[(size_t)r * F8 + q];
+        for (int i = 0; i < M; ++i) {
+            const float wt = ms.uw[i];
+            if (wt == 0.f) continue;
+            const float* hi = hu + (size_t)i * hstride;
+            float a = 0.f, b = 0.f;
+#pragma unroll
+            for (int q = 0; q < F8; ++q)
+                fma8v2(a, b, w[q], *reinterpret_cast<const float4*>(hi + 8 * q),
+                       *reinterpret_cast<const float4*>(hi + 8 * q + 4));
+            atomicAdd(xo + (size_t)ms.gt[i] * d + r, wt * (a + b));
+        }
+    }
+}
+
 __device__ __noinline__ void unit_seg_cons(Ctx& c, int l, int kind, int expert, int u0, int u1) {
     const Params& p = c.p;
     const Layer& Ld = c.layer();
     const FfnKind& K = Ld.ffn.k[kind];
-    const int F = K.F, n = u1 - u0, rows = 2 * F * n, M = p.M, d = p.d, tid = ctid();
-    float* hs = unit_buf(c, 3 * F * n * M);
-    float* h = hs + (size_t)rows * M;
+    const int F = K.F, n = u1 - u0, rows = 2 * F * n, d = p.d, tid = ctid();
     const long long tue = p.trace_items ? gtimer() : 0;
     cbar();  // the previous segment's down rows may still read its hidden values here
     const long long tu0 = p.trace_items ? gtimer() : 0;
     if (p.trace_items && tid == 0) trace_rec(c, 0x80000000u | (((unsigned)C_DOWN + 5) << 16) | (unsigned)l, 0u, tue, tu0);
-    for (int i = tid; i < rows * M; i += NCT) hs[i] = 0.f;
-    if (tid < M) c.ms.uw[tid] = expert < 0 ? 1.0f : route_weight(c.ms, tid, expert, p.topk);
+    // the tokens of this expert: a routed expert takes only the tokens routed
+    // to it when every token's input is staged in one K panel (the routed
+    // CTAs stage it before routing); otherwise all tokens, weight 0 or not
+    if (tid < 32) {
+        const bool compact = expert >= 0 && p.M > 1 && Ld.ffn.n_kc == 1 && p.M * Ld.ffn.Kc <= STAGE_FLOATS;
+        const int lane = tid;
+        float w[2];
+        bool sel[2];
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            const int m = lane + 32 * q;
+            w[q] = m < p.M ? (expert < 0 ? 1.0f : route_weight(c.ms, m, expert, p.topk)) : 0.f;
+            sel[q] = m < p.M && (!compact || w[q] != 0.f);
+        }
+        const unsigned b0 = __ballot_sync(0xffffffffu, sel[0]), b1 = __ballot_sync(0xffffffffu, sel[1]);
+        const unsigned lt = (1u << lane) - 1u;
+        const int pos[2] = {__popc(b0 & lt), __popc(b0) + __popc(b1 & lt)};
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            if (sel[q]) {
+                c.ms.gt[pos[q]] = (uint8_t)(lane + 32 * q);
+                c.ms.uw[pos[q]] = w[q];
+            }
+        }
+        if (lane == 0) c.ms.gm = __popc(b0) + __popc(b1);
+    }
+    cbar();
+    const int M = c.ms.gm;
+    float* hs = unit_buf(c, 3 * F * n * M);
+    float* h = hs + (size_t)rows * M;
+    if (Ld.ffn.n_kc > 1)
+        for (int i = tid; i < rows * M; i += NCT) hs[i] = 0.f;
     if (tid == 0) unit_gemv(p, Ld, c.ms.ug, kind, expert, u0, u1, hs);
     cbar();
     const long long tz = p.trace_items ? gtimer() : 0;
@@ -2365,7 +2535,7 @@ __device__ __noinline__ void unit_seg_cons(Ctx& c, int l, int kind, int expert, 
             if (tile) {
                 if (M == 1) {
                     const float* hu = h + uu * F;
-                    float* xo = Ld.xn + r0;
+                    float* xo = Ld.xn + (size_t)ms.gt[0] * d + r0;
                     const float w = ms.uw[0];
                     if (w != 0.f) {
                         if (F == 64) down_rows1<8>(tile, nr, hu, w, xo);
@@ -2374,17 +2544,12 @@ __device__ __noinline__ void unit_seg_cons(Ctx& c, int l, int kind, int expert, 
                         else down_rows1<2>(tile, nr, hu, w, xo);
                     }
                 } else {
-                    const uint16_t* T = reinterpret_cast<const uint16_t*>(tile);
-                    for (int r = tid; r < nr; r += NCT) {
-                        for (int m = 0; m < M; ++m) {
-                            const float w = ms.uw[m];
-                            if (w == 0.f) continue;
-                            const float* hu = h + ((size_t)m * n + uu) * F;
-                            float a = 0.f;
-                            for (int f = 0; f < F; ++f) a = fmaf(bf2f(T[(size_t)r * F + f]), hu[f], a);
-                            atomicAdd(Ld.xn + (size_t)m * d + r0 + r, w * a);
-                        }
-                    }
+                    float* xo = Ld.xn + r0;
+                    const float* hu = h + uu * F;
+                    if (F == 64) down_rowsM<8>(tile, nr, hu, n * F, M, ms, xo, d);
+                    else if (F == 48) down_rowsM<6>(tile, nr, hu, n * F, M, ms, xo, d);
+                    else if (F == 32) down_rowsM<4>(tile, nr, hu, n * F, M, ms, xo, d);
+                    else down_rowsM<2>(tile, nr, hu, n * F, M, ms, xo, d);
                 }
             }
             __syncwarp();
@@ -2421,18 +2586,24 @@ __device__ __noinline__ void unit_seg_prod(Ctx& c, int kind, int expert, int u0,
     // prefetch of the rest of the segment, which would queue ahead of it
     const int first = min(NSLOT, (u1 - u0) * rpu);
     prod_gemv(c, c.ms.pug, -1, u0 * rpu, u0 * rpu + first);
-    // then the L2 prefetch: per K panel the segment's gate/up rows are contiguous, and
-    // so are its down blocks; pieces of at most 64 KB, one lane each
+    // then the L2 prefetch of the segment's first units (per K panel their
+    // gate/up rows are contiguous, and so are their down blocks; pieces of at
+    // most 64 KB, one lane each). Only about UNIT_PF_BYTES per CTA up front:
+    // every CTA's whole segment at once would not fit in L2. The gate/up
+    // copies that follow keep their own prefetch window; the down loop
+    // prefetches one unit ahead.
+    const size_t piece = 32768;  // elements
+    const int unit_elems = 3 * F * d;
+    const int npf = min(u1 - u0, max(1, UNIT_PF_BYTES / (2 * unit_elems)));
     {
-        const size_t piece = 32768;  // elements
         for (int kc = 0; kc < Ld.ffn.n_kc; ++kc) {
             const uint16_t* b = gu + (size_t)kc * 2 * K.Fi * Kc + (size_t)u0 * 2 * F * Kc;
-            const size_t n = (size_t)(u1 - u0) * 2 * F * Kc;
+            const size_t n = (size_t)npf * 2 * F * Kc;
             for (size_t o = (size_t)lane * piece; o < n; o += 32 * piece)
                 l2_prefetch(b + o, (unsigned)(min(piece, n - o) * 2));
         }
         const uint16_t* b = dn + (size_t)u0 * d * F;
-        const size_t n = (size_t)(u1 - u0) * d * F;
+        const size_t n = (size_t)npf * d * F;
         for (size_t o = (size_t)lane * piece; o < n; o += 32 * piece) l2_prefetch(b + o, (unsigned)(min(piece, n - o) * 2));
     }
     for (int kc = 0; kc < Ld.ffn.n_kc && !c.dead; ++kc)
@@ -2444,6 +2615,12 @@ __device__ __noinline__ void unit_seg_prod(Ctx& c, int kind, int expert, int u0,
     const unsigned long long pol = l2_evict_first();
     const int nt = (d + K.Rd - 1) / K.Rd, rot = (int)(blockIdx.x % (unsigned)nt);  // the consumers' tile order
     for (int u = u0; u < u1 && !c.dead; ++u) {
+        if (u + 1 < u1 && u + 1 >= u0 + npf) {
+            const uint16_t* b = dn + (size_t)(u + 1) * d * F;
+            const size_t n = (size_t)d * F;
+            for (size_t o = (size_t)lane * piece; o < n; o += 32 * piece)
+                l2_prefetch(b + o, (unsigned)(min(piece, n - o) * 2));
+        }
         for (int t0 = 0; t0 < nt; ++t0) {
             const int t = t0 + rot < nt ? t0 + rot : t0 + rot - nt;
             const int r0 = t * K.Rd, nr = min(K.Rd, d - r0);
@@ -2534,6 +2711,10 @@ __device__ __noinline__ void ffn_stage(Ctx& c, int l) {
     c.set_count(c.n_down, (p.has_sh ? Ld.ffn.k[1].nu : 0) + (p.E > 0 ? nslots * Ld.ffn.k[0].nu : 0));
     if constexpr (!PROD) {
         csignal(c, l, C_DOWN, (unsigned)done);
+        // back to all tokens in order for the stages that follow (their
+        // readers pass a barrier first)
+        if (threadIdx.x < MAX_M) c.ms.gt[threadIdx.x] = (uint8_t)threadIdx.x;
+        if (threadIdx.x == 0) c.ms.gm = p.M;
         trace_rec(c, ((unsigned)C_DOWN << 16) | (unsigned)l, (unsigned)done, t0, t0);
     }
 }
@@ -2683,7 +2864,7 @@ __device__ __noinline__ bool exec_stage(Ctx& c) {
             // the router runs on its own CTAs [G - gr, G): the routed units
             // wait for it, the shared units do not
             case S_ROUTER:
-                if (p.E == 0) return true;
+                if (p.E == 0 || p.rfuse) return true;
                 g = &Ld.g[G_ROUTER];
                 deps = deps1(l, C_O, (unsigned)gemv_items(Ld.g[G_O]));
                 sig = C_ROUTER;
@@ -2792,6 +2973,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) megakernel(const __grid_constant_
         // resets it (mk_step_status): refuse to run on stale state
         ms.abort = ld_relaxed(&p.status[1]) ? 1 : 0;
         ms.n_slots = ms.p_nslots = 0;
+        for (int i = 0; i < MAX_M; ++i) ms.gt[i] = (uint8_t)i;
+        ms.gm = p.M;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     {

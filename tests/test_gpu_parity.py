@@ -90,3 +90,13 @@ def test_verify_step_reduced_layers():
     cfg = configs.scaled(configs.VERIFY, n_layers=2)
     g, o, rep = _run(cfg, 8, 7, 1, 2000, want_accept=True)
     assert np.all((g[0]["accept"] >= 1) & (g[0]["accept"] <= 7))
+
+
+@pytest.mark.parametrize("name,B", [("mid", 4), ("deep", 2)])
+def test_separate_router_stage(monkeypatch, name, B):
+    # the schedule with its own router stage (used for one token, or when the
+    # output projection splits K); by default steps of two or more tokens fold
+    # the router into the output projection
+    monkeypatch.setenv("MK_ROUTER_STAGE", "1")
+    cfg = configs.scaled(configs.ALL[name], n_layers=2)
+    _run(cfg, B, 1, 1, cfg["ctx"])
