@@ -46,7 +46,7 @@ constexpr int MAX_E = 256;
 // router logits accumulated by the output projection's CTAs go to one of
 // ROUTER_COPIES copies (by CTA), so that few CTAs add into the same lines;
 // a token's row holds E logits and the sum of squares, padded to 4 floats
-constexpr int ROUTER_COPIES = 16;
+constexpr int ROUTER_COPIES = 8;
 __host__ __device__ constexpr int router_row(int E) { return (E + 4) & ~3; }
 constexpr int MAX_K = 8;
 constexpr int GQA_CH = 64;                // positions per GQA chunk (= one page)
@@ -204,8 +204,8 @@ struct Misc {
     float rms[MAX_M];
     uint8_t slot_e[MAX_E];          // consumer: routed slot -> expert
     uint8_t p_slot_e[MAX_E];        // producer copy
-    uint8_t used[MAX_E];
-    uint8_t p_used[MAX_E];
+    alignas(4) uint8_t used[MAX_E];    // tokens routed to each expert (consumers)
+    alignas(4) uint8_t p_used[MAX_E];  // producer copy
     uint8_t ridx[MAX_M][MAX_K];
     float rw[MAX_M][MAX_K];
     float cw[256];                  // combine weights

@@ -773,14 +773,16 @@ static void ffn_split(const mk_model* m, int M, bool rfuse, int& gs, int& gr) {
         return;
     }
     // a unit's time grows with its token count (the weights stream once, the
-    // arithmetic is per token): about 1 + 0.35 (t - 1) tile times for t tokens.
+    // arithmetic is per token): about 1 + 0.8 (t - 1) tile times for t tokens.
     // A routed expert's units take only its own tokens (M k / distinct on
-    // average) when the routed CTAs stage all tokens' input in one K panel.
-    const auto cost = [](double t) { return 1.0 + 0.35 * (t - 1.0); };
+    // average) and the shared expert's run per group of 4 tokens when all
+    // tokens' input is staged in one K panel.
+    const auto cost = [](double t) { return 1.0 + 0.8 * (t - 1.0); };
     const double uniq = D.E * (1.0 - std::pow(1.0 - (double)D.k / D.E, (double)M));
-    const bool compact = M > 1 && L0.ffn.n_kc == 1 && M * L0.ffn.Kc <= mk::STAGE_FLOATS;
-    const double us = L0.ffn.k[1].nu * cost(M);
-    const double ur = uniq * L0.ffn.k[0].nu * cost(compact ? M * D.k / uniq : M);
+    const bool stage_all = M > 1 && L0.ffn.n_kc == 1 && M * L0.ffn.Kc <= mk::STAGE_FLOATS;
+    const int ntg = M > 4 && stage_all ? (M + 3) / 4 : 1;
+    const double us = L0.ffn.k[1].nu * ntg * cost(ntg > 1 ? M / (double)ntg : M);
+    const double ur = uniq * L0.ffn.k[0].nu * cost(stage_all ? M * D.k / uniq : M);
     const int avail = m->G - gr;
     gs = (int)std::lround(avail * us / (us + ur));
     if (gs < 1) gs = 1;

@@ -848,7 +848,7 @@ __device__ __forceinline__ int rx_reduce16(float (&v)[8]) {
     return k;
 }
 
-template <int JC>
+template <int JC, bool MT = false>
 __device__ __forceinline__ void gemv_range_rx(Ctx& c, const Gemv& g, int slot, int expert, int j_lo, int j_hi) {
     const Params& p = c.p;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -856,13 +856,16 @@ __device__ __forceinline__ void gemv_range_rx(Ctx& c, const Gemv& g, int slot, i
     constexpr bool wide = JC > 0;
     constexpr int NC = wide ? 32 * JC : 16;
     const int n_rb = g.n_rb, R = g.R, N = g.N, grp_rows = g.grp_rows, grp_stride = g.grp_stride;
-    const int out_kind = g.out_kind, n_kc = g.n_kc;
+    const int out_kind = g.out_kind, n_kc = g.n_kc, dst_stride = g.dst_stride;
     float* const dst = g.dst + (size_t)slot * g.dst_sstride;
     float* const dst2 = g.dst2;
     const float* src = g.src + (size_t)slot * g.src_sstride;
     Misc& ms = c.ms;
     uint8_t* const ring = c.smem + SMEM_RING;
-    const float* const xs = c.stage() + (size_t)ms.gt[0] * g.Kc;  // the token's staged row
+    const float* const xs = c.stage();
+    // tokens: MT (wide panels only) up to 4, each tile once per token and the
+    // input reloaded per token; otherwise one, its input in registers for the run
+    const int ntok = MT ? ms.gm : 1;
     CRing cr = c.cr;
     bool dead = c.dead, timed_out = false;
     constexpr int NX = wide ? JC : 1;
@@ -875,18 +878,20 @@ __device__ __forceinline__ void gemv_range_rx(Ctx& c, const Gemv& g, int slot, i
         const int jend = run_end(j, j_hi, n_rb, rb0, R, grp_rows, g0);
         if (p.trace_items == 1 && threadIdx.x == 0) ms.tdbg[1] = clock64();
         const long long ta = p.trace_items ? gtimer() : 0;
-        restage(c, g, src, g0 * grp_stride, kc0, 0, 1);
+        restage(c, g, src, g0 * grp_stride, kc0, 0, p.M);
         const long long tb = p.trace_items ? gtimer() : 0;
         long long tc = tb;
-        {
-            const int ch0 = wide ? lane : (lane & 15);
+        const int ch0 = wide ? lane : (lane & 15);
+        const auto load_x = [&](int tk) {
+            const float* xt = xs + (size_t)ms.gt[tk] * g.Kc;
 #pragma unroll
             for (int q = 0; q < NX; ++q) {
-                const float* xp = xs + (ch0 + 32 * q) * 8;
+                const float* xp = xt + (ch0 + 32 * q) * 8;
                 xa[q] = *reinterpret_cast<const float4*>(xp);
                 xb[q] = *reinterpret_cast<const float4*>(xp + 4);
             }
-        }
+        };
+        load_x(0);
         const int jrun = j;
         for (; j < jend; ++j) {
             if constexpr (JC == 8) {
@@ -907,24 +912,28 @@ __device__ __forceinline__ void gemv_range_rx(Ctx& c, const Gemv& g, int slot, i
                         if (p.trace_items && j == jrun) tc = gtimer();
                         const uint4* wA = reinterpret_cast<const uint4*>(ring + cr.slot * SLOT_BYTES) + (size_t)warp * NC + lane;
                         const uint4* wB = reinterpret_cast<const uint4*>(ring + crB.slot * SLOT_BYTES) + (size_t)warp * NC + lane;
-                        float a[4] = {0.f, 0.f, 0.f, 0.f}, b[4] = {0.f, 0.f, 0.f, 0.f};
+                        for (int tk = 0; tk < ntok; ++tk) {
+                            if (MT) load_x(tk);
+                            float a[4] = {0.f, 0.f, 0.f, 0.f}, b[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                        for (int q0 = 0; q0 < 8; q0 += 2) {
-                            uint4 u[4];
-                            u[0] = wA[32 * q0];
-                            u[1] = wA[32 * (q0 + 1)];
-                            u[2] = wB[32 * q0];
-                            u[3] = wB[32 * (q0 + 1)];
-                            fma8v2(a[0], a[1], u[0], xa[q0], xb[q0]);
-                            fma8v2(a[2], a[3], u[1], xa[q0 + 1], xb[q0 + 1]);
-                            fma8v2(b[0], b[1], u[2], xa[q0], xb[q0]);
-                            fma8v2(b[2], b[3], u[3], xa[q0 + 1], xb[q0 + 1]);
-                        }
-                        float v[2] = {(a[0] + a[1]) + (a[2] + a[3]), (b[0] + b[1]) + (b[2] + b[3])};
-                        const int which = rx_reduce<2>(v);  // lane 0: tile A, lane 16: tile B
-                        if ((lane & 15) == 0) {
-                            const int row = (which ? r0B : r0A) + warp;
-                            if (warp < (which ? nrB : nrA)) rx_out(p, ms, out_kind, n_kc, dst + row, dst2 + row, expert, v[0]);
+                            for (int q0 = 0; q0 < 8; q0 += 2) {
+                                uint4 u[4];
+                                u[0] = wA[32 * q0];
+                                u[1] = wA[32 * (q0 + 1)];
+                                u[2] = wB[32 * q0];
+                                u[3] = wB[32 * (q0 + 1)];
+                                fma8v2(a[0], a[1], u[0], xa[q0], xb[q0]);
+                                fma8v2(a[2], a[3], u[1], xa[q0 + 1], xb[q0 + 1]);
+                                fma8v2(b[0], b[1], u[2], xa[q0], xb[q0]);
+                                fma8v2(b[2], b[3], u[3], xa[q0 + 1], xb[q0 + 1]);
+                            }
+                            float v[2] = {(a[0] + a[1]) + (a[2] + a[3]), (b[0] + b[1]) + (b[2] + b[3])};
+                            const int which = rx_reduce<2>(v);  // lane 0: tile A, lane 16: tile B
+                            if ((lane & 15) == 0) {
+                                const int row = (which ? r0B : r0A) + warp + tk * dst_stride;
+                                if (warp < (which ? nrB : nrA))
+                                    rx_out(p, ms, out_kind, n_kc, dst + row, dst2 + row, expert, v[0]);
+                            }
                         }
                     }
                     __syncwarp();
@@ -958,6 +967,8 @@ __device__ __forceinline__ void gemv_range_rx(Ctx& c, const Gemv& g, int slot, i
                     // all their loads and FMAs first, then one transposed
                     // reduction for the RB sums
                     constexpr int RB = JC >= 8 ? 1 : (JC >= 3 ? 2 : (JC == 2 ? 4 : 8));
+                    for (int tk = 0; tk < ntok; ++tk) {
+                    if (MT) load_x(tk);
                     for (int rbase = warp * RB; rbase < nr; rbase += 8 * RB) {
                         float v[RB];
 #pragma unroll
@@ -982,8 +993,9 @@ __device__ __forceinline__ void gemv_range_rx(Ctx& c, const Gemv& g, int slot, i
                         }
                         const int b = rx_reduce<RB>(v);
                         const int r = rbase + b;
-                        if ((lane & (32 / RB - 1)) == 0 && r < nr)
-                            rx_out(p, ms, out_kind, n_kc, dst + r0 + r, dst2 + r0 + r, expert, v[0]);
+                        const size_t o = (size_t)tk * dst_stride + r0 + r;
+                        if ((lane & (32 / RB - 1)) == 0 && r < nr) rx_out(p, ms, out_kind, n_kc, dst + o, dst2 + o, expert, v[0]);
+                    }
                     }
                 } else {
                     // 16 chunks per row: lanes 0-15 row r, lanes 16-31 row r + 1,
@@ -1091,10 +1103,17 @@ __device__ __noinline__ void gemv_multi(Ctx& c, const Gemv& g, int slot, int exp
 // once per layer, and a smaller footprint keeps it in the instruction cache)
 __device__ __noinline__ void cons_gemv(Ctx& c, const Gemv& g, int slot, int expert, int j_lo, int j_hi) {
     const int M = c.ms.gm, Kc = g.Kc;
+    // K panels of 2048 and 1024: the register path also for 2 to 4 tokens
+    // (each tile once per token)
+    const bool mt = M >= 2 && M <= 4 && g.out_kind != OUT_SCALED;
     if (M == 1 && Kc == 2048)
         gemv_range_rx<8>(c, g, slot, expert, j_lo, j_hi);
+    else if (mt && Kc == 2048)
+        gemv_range_rx<8, true>(c, g, slot, expert, j_lo, j_hi);
     else if (M == 1 && Kc == 1024)
         gemv_range_rx<4>(c, g, slot, expert, j_lo, j_hi);
+    else if (mt && Kc == 1024)
+        gemv_range_rx<4, true>(c, g, slot, expert, j_lo, j_hi);
     else if (M == 1 && Kc == 768)
         gemv_range_rx<3>(c, g, slot, expert, j_lo, j_hi);
     else if (M == 1 && Kc == 512)
@@ -1270,6 +1289,59 @@ __device__ __noinline__ void cons_mm(Ctx& c, int l, const Gemv& g, int sig, int 
 }
 
 // ============================================================ routing ====
+// one more token routed to expert e (8-bit counts, added through their word)
+__device__ __forceinline__ void count_token(uint8_t* cnt, int e) {
+    atomicAdd(reinterpret_cast<unsigned*>(cnt + (e & ~3)), 1u << (8 * (e & 3)));
+}
+
+// routed expert units (slot-major, nu per slot) over gc CTAs by expected
+// time: a unit of an expert with t tokens weighs 5 + 4 (t - 1). CTA ci takes
+// the units whose start weight s satisfies ci W <= s gc < (ci + 1) W, a
+// contiguous range [lo, hi). Every warp computes it alike (no shared state).
+__device__ __forceinline__ int routed_first(const uint8_t* cnt, const uint8_t* slot_e, int nslots, int nu, long long T,
+                                            int gc) {
+    const int lane = threadIdx.x & 31;
+    long long base = 0;  // start weight of the chunk's first slot
+    for (int s0 = 0; s0 < nslots; s0 += 32) {
+        const int s = s0 + lane;
+        const int wu = s < nslots ? 5 + 4 * ((int)cnt[slot_e[s]] - 1) : 0;
+        long long inc = (long long)wu * nu;  // inclusive scan of the slot weights
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const long long t = __shfl_up_sync(0xffffffffu, inc, o);
+            if (lane >= o) inc += t;
+        }
+        const long long S = base + inc - (long long)wu * nu;  // this slot's start
+        // the slot holds the first unit at or past T when its last unit does
+        const bool hit = s < nslots && (S + (long long)(nu - 1) * wu) * gc >= T;
+        const unsigned b = __ballot_sync(0xffffffffu, hit);
+        if (b) {
+            const int src = __ffs(b) - 1;
+            const long long Ss = __shfl_sync(0xffffffffu, S, src);
+            const int w = __shfl_sync(0xffffffffu, wu, src);
+            const long long need = T - Ss * gc;  // first u with (Ss + u w) gc >= T
+            const int u = need <= 0 ? 0 : (int)((need + (long long)w * gc - 1) / ((long long)w * gc));
+            return (s0 + src) * nu + u;
+        }
+        base += __shfl_sync(0xffffffffu, inc, 31);
+    }
+    return nslots * nu;
+}
+
+__device__ __forceinline__ void routed_range(const uint8_t* cnt, const uint8_t* slot_e, int nslots, int nu, int ci,
+                                             int gc, int& lo, int& hi) {
+    const int lane = threadIdx.x & 31;
+    long long W = 0;
+    for (int s = lane; s < nslots; s += 32) W += (long long)(5 + 4 * ((int)cnt[slot_e[s]] - 1)) * nu;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) W += __shfl_xor_sync(0xffffffffu, W, o);
+    if (ci < 0 || ci >= gc) {
+        lo = hi = 0;
+        return;
+    }
+    lo = routed_first(cnt, slot_e, nslots, nu, (long long)ci * W, gc);
+    hi = routed_first(cnt, slot_e, nslots, nu, (long long)(ci + 1) * W, gc);
+}
 // softmax / top-k of the router logits of every token (ties -> lower id),
 // union of the selected experts (sorted by id) -> routed slots.
 // consumers: full routing into Misc; producer warp: slot list only.
@@ -1319,18 +1391,25 @@ __device__ __forceinline__ bool route(Ctx& c, int l) {
         if (p.rfuse) {
             // accumulated logits: the sum over the copies, times 1/rms of the
             // residual (mean square over d)
-            float ss = lane == 0 ? __ldcg(lg + E) : 0.f;
+            // (each batch of loads issued together: one L2 round trip per batch)
+            const size_t cs = (size_t)p.M * RS;
+            float q[ROUTER_COPIES];
 #pragma unroll
-            for (int cp = 1; cp < ROUTER_COPIES; ++cp) {
-                const float* lc = lg + (size_t)cp * p.M * RS;
+            for (int cp = 0; cp < ROUTER_COPIES; ++cp) q[cp] = __ldcg(lg + cp * cs + E);
+            float ss = 0.f;
 #pragma unroll
-                for (int i = 0; i < MAX_E / 32; ++i) {
+            for (int cp = 0; cp < ROUTER_COPIES; ++cp) ss += q[cp];
+#pragma unroll
+            for (int i = 0; i < MAX_E / 32; ++i) {
+                if (32 * i < E) {
                     const int e = lane + 32 * i;
-                    if (e < E) v[i] += __ldcg(lc + e);
+#pragma unroll
+                    for (int cp = 1; cp < ROUTER_COPIES; ++cp) q[cp] = e < E ? __ldcg(lg + cp * cs + e) : 0.f;
+#pragma unroll
+                    for (int cp = 1; cp < ROUTER_COPIES; ++cp) v[i] += q[cp];
                 }
-                if (lane == 0) ss += __ldcg(lc + E);
             }
-            const float sc = 1.0f / sqrtf(__shfl_sync(0xffffffffu, ss, 0) * (1.0f / (float)p.d) + p.eps);
+            const float sc = 1.0f / sqrtf(ss * (1.0f / (float)p.d) + p.eps);
 #pragma unroll
             for (int i = 0; i < MAX_E / 32; ++i) v[i] *= sc;
         }
@@ -1368,7 +1447,7 @@ __device__ __forceinline__ bool route(Ctx& c, int l) {
             for (int q = 0; q < 2; ++q) {
                 const int e = lane + 32 * q;
                 if (rk[q] < k && e < E) {
-                    used[e] = 1;
+                    count_token(used, e);
                     if constexpr (!PROD) {
                         c.ms.ridx[m][rk[q]] = (uint8_t)e;
                         c.ms.rw[m][rk[q]] = ex[q] / den;
@@ -1422,7 +1501,7 @@ __device__ __forceinline__ bool route(Ctx& c, int l) {
                 den += w[j];
             }
             for (int j = 0; j < k; ++j) {
-                used[sid[j]] = 1;
+                count_token(used, sid[j]);
                 if constexpr (!PROD) {
                     c.ms.ridx[m][j] = (uint8_t)sid[j];
                     c.ms.rw[m][j] = w[j] / den;
@@ -2449,7 +2528,7 @@ __device__ __forceinline__ void down_rowsM(const uint8_t* tile, int nr, const fl
     }
 }
 
-__device__ __noinline__ void unit_seg_cons(Ctx& c, int l, int kind, int expert, int u0, int u1) {
+__device__ __noinline__ void unit_seg_cons(Ctx& c, int l, int kind, int expert, int u0, int u1, int m_lo, int m_hi) {
     const Params& p = c.p;
     const Layer& Ld = c.layer();
     const FfnKind& K = Ld.ffn.k[kind];
@@ -2460,7 +2539,8 @@ __device__ __noinline__ void unit_seg_cons(Ctx& c, int l, int kind, int expert, 
     if (p.trace_items && tid == 0) trace_rec(c, 0x80000000u | (((unsigned)C_DOWN + 5) << 16) | (unsigned)l, 0u, tue, tu0);
     // the tokens of this expert: a routed expert takes only the tokens routed
     // to it when every token's input is staged in one K panel (the routed
-    // CTAs stage it before routing); otherwise all tokens, weight 0 or not
+    // CTAs stage it before routing), otherwise all tokens, weight 0 or not;
+    // the shared expert takes tokens [m_lo, m_hi)
     if (tid < 32) {
         const bool compact = expert >= 0 && p.M > 1 && Ld.ffn.n_kc == 1 && p.M * Ld.ffn.Kc <= STAGE_FLOATS;
         const int lane = tid;
@@ -2469,8 +2549,9 @@ __device__ __noinline__ void unit_seg_cons(Ctx& c, int l, int kind, int expert, 
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
             const int m = lane + 32 * q;
-            w[q] = m < p.M ? (expert < 0 ? 1.0f : route_weight(c.ms, m, expert, p.topk)) : 0.f;
-            sel[q] = m < p.M && (!compact || w[q] != 0.f);
+            const bool in = expert < 0 ? m >= m_lo && m < m_hi : m < p.M;
+            w[q] = in ? (expert < 0 ? 1.0f : route_weight(c.ms, m, expert, p.topk)) : 0.f;
+            sel[q] = in && (!compact || w[q] != 0.f);
         }
         const unsigned b0 = __ballot_sync(0xffffffffu, sel[0]), b1 = __ballot_sync(0xffffffffu, sel[1]);
         const unsigned lt = (1u << lane) - 1u;
@@ -2560,9 +2641,11 @@ __device__ __noinline__ void unit_seg_cons(Ctx& c, int l, int kind, int expert, 
             }
         }
     }
-    // unit trace: gate/up time, then gate/up + hidden, then down (first record field: gate/up)
-    if (p.trace_items && tid == 0) trace_rec(c, 0x80000000u | (((unsigned)C_DOWN + 1) << 16) | (unsigned)l,
-                                             (unsigned)(tu1 - tu0), tu0, tu1);
+    // unit trace: segment start, gate/up + hidden done, down done; the first
+    // field packs the token count, the unit count and the expert id
+    if (p.trace_items && tid == 0)
+        trace_rec(c, 0x80000000u | (((unsigned)C_DOWN + 1) << 16) | (unsigned)l,
+                  ((unsigned)M << 16) | ((unsigned)(u1 - u0) << 8) | ((unsigned)expert & 0xffu), tu0, tu1);
     if (timed_out) {
         ms.abort = 1;
         raise_status(p, ST_TIMEOUT, 0x220u);
@@ -2656,19 +2739,34 @@ __device__ __noinline__ void ffn_stage(Ctx& c, int l) {
     const long long t0 = gtimer();
     c.cur_code = ((unsigned)C_DOWN << 16) | (unsigned)l;
     int done = 0;
+    // more than 4 tokens, all staged in one K panel: the shared expert's
+    // units run once per group of 4 tokens (work items unit x group, for more
+    // CTAs and the register GEMV path)
+    const bool stage_all = p.M > 1 && Ld.ffn.n_kc == 1 && p.M * Ld.ffn.Kc <= STAGE_FLOATS;
+    const int ntg = p.M > 4 && stage_all ? (p.M + 3) / 4 : 1;
     if ((int)blockIdx.x < p.gs) {
         if (p.has_sh) {
+            const int nu = Ld.ffn.k[1].nu;
             int lo, hi;
-            my_range_sub(Ld.ffn.k[1].nu, 0, p.gs, lo, hi);
+            my_range_sub(nu * ntg, 0, p.gs, lo, hi);
             if (lo < hi) {
-                if constexpr (PROD) {
-                    unit_seg_prod(c, 1, -1, lo, hi);
-                } else {
+                if constexpr (!PROD) {
+                    if (ntg > 1 && threadIdx.x == 0) unit_gemv(p, Ld, c.ms.ug, 1, -1, 0, 1, c.red() + RED_FLOATS / 2);
                     set_deps(c, deps1(l, C_O, (unsigned)gemv_items(Ld.g[G_O])));
                     cwait(c, 0x1100u | (unsigned)(l << 16));
-                    unit_seg_cons(c, l, 1, -1, lo, hi);
-                    done += hi - lo;
+                    if (ntg > 1) restage(c, c.ms.ug, Ld.x, 0, 0, 0, p.M);
                 }
+                for (int i = lo; i < hi && !(PROD && c.dead);) {
+                    const int tg = i / nu, iend = min(hi, (tg + 1) * nu);
+                    if constexpr (PROD) {
+                        unit_seg_prod(c, 1, -1, i - tg * nu, iend - tg * nu);
+                    } else {
+                        const int m0 = ntg > 1 ? 4 * tg : 0, m1 = ntg > 1 ? min(p.M, m0 + 4) : p.M;
+                        unit_seg_cons(c, l, 1, -1, i - tg * nu, iend - tg * nu, m0, m1);
+                    }
+                    i = iend;
+                }
+                done += hi - lo;
             }
         }
         if (p.E > 0 && !route<PROD>(c, l) && PROD) {
@@ -2696,19 +2794,20 @@ __device__ __noinline__ void ffn_stage(Ctx& c, int l) {
         const int nslots = PROD ? c.ms.p_nslots : c.ms.n_slots;
         const uint8_t* slot_e = PROD ? c.ms.p_slot_e : c.ms.slot_e;
         int lo, hi;
-        my_range_sub(nslots * K.nu, p.gs, p.G - p.gs - p.gr, lo, hi);
+        routed_range(PROD ? c.ms.p_used : c.ms.used, slot_e, nslots, K.nu, (int)blockIdx.x - p.gs,
+                     p.G - p.gs - p.gr, lo, hi);
         for (int i = lo; i < hi && !(PROD && c.dead);) {
             const int s2 = i / K.nu, iend = min(hi, (s2 + 1) * K.nu);
             if constexpr (PROD)
                 unit_seg_prod(c, 0, slot_e[s2], i - s2 * K.nu, iend - s2 * K.nu);
             else
-                unit_seg_cons(c, l, 0, slot_e[s2], i - s2 * K.nu, iend - s2 * K.nu);
+                unit_seg_cons(c, l, 0, slot_e[s2], i - s2 * K.nu, iend - s2 * K.nu, 0, p.M);
             i = iend;
         }
         done = hi - lo;
     }
     const int nslots = PROD ? c.ms.p_nslots : c.ms.n_slots;
-    c.set_count(c.n_down, (p.has_sh ? Ld.ffn.k[1].nu : 0) + (p.E > 0 ? nslots * Ld.ffn.k[0].nu : 0));
+    c.set_count(c.n_down, (p.has_sh ? Ld.ffn.k[1].nu * ntg : 0) + (p.E > 0 ? nslots * Ld.ffn.k[0].nu : 0));
     if constexpr (!PROD) {
         csignal(c, l, C_DOWN, (unsigned)done);
         // back to all tokens in order for the stages that follow (their
