@@ -647,7 +647,11 @@ __device__ __forceinline__ void gemv_range_ks(Ctx& c, const Gemv& g, int slot, i
     Misc& ms = c.ms;
     uint8_t* const ring = c.smem + SMEM_RING;
     const float* const xs = c.stage();
-    float* const part = c.red();  // [2][NCW][RWT*MR]
+    // tokens in chunks of MC (one CTA barrier and one final sum per chunk),
+    // each chunk in groups of MR (partials written without a barrier);
+    // partials [2][NCW][RWT * MC] in the first half of the reduction area
+    constexpr int MC = (32 / RWT) > MR ? (32 / RWT) : MR;
+    float* const part = c.red();
     const int ngrp = (M + MR - 1) / MR;
     CRing cr = c.cr;
     bool dead = c.dead, timed_out = false;
@@ -675,55 +679,57 @@ __device__ __forceinline__ void gemv_range_ks(Ctx& c, const Gemv& g, int slot, i
                     dead = timed_out = true;
             }
             if (p.trace_items && j == jrun) tc = gtimer();
-            for (int gi = 0; gi < ngrp; ++gi) {
-                const int mb = gi * MR;
-                if (j == jrun || ngrp > 1) {
+            for (int mc0 = 0; mc0 < M; mc0 += MC) {
+                const int mcn = min(MC, M - mc0);
+                for (int mb = mc0; mb < mc0 + mcn; mb += MR) {
+                    if (j == jrun || ngrp > 1) {
 #pragma unroll
-                    for (int m = 0; m < MR; ++m) {
-                        const bool ok = act && mb + m < M;
-                        const float* xp = xs + (size_t)(ok ? ms.gt[mb + m] : 0) * Kc + chunk * 8;
-                        xa[m] = ok ? *reinterpret_cast<const float4*>(xp) : make_float4(0.f, 0.f, 0.f, 0.f);
-                        xb[m] = ok ? *reinterpret_cast<const float4*>(xp + 4) : make_float4(0.f, 0.f, 0.f, 0.f);
-                    }
-                }
-                float v[8][MR];
-#pragma unroll
-                for (int i = 0; i < 8; ++i)
-#pragma unroll
-                    for (int m = 0; m < MR; ++m) v[i][m] = 0.f;
-                if (tile) {
-                    const uint4* T4 = reinterpret_cast<const uint4*>(tile) + chunk;
-                    const int rw = rb * RWT + rg;
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const int r = rw + RG * i;
-                        if (act && r < nr) {
-                            const uint4 w = T4[(size_t)r * NC];
-#pragma unroll
-                            for (int m = 0; m < MR; ++m) fma8v(v[i][m], w, xa[m], xb[m]);
+                        for (int m = 0; m < MR; ++m) {
+                            const bool ok = act && mb + m < M;
+                            const float* xp = xs + (size_t)(ok ? ms.gt[mb + m] : 0) * Kc + chunk * 8;
+                            xa[m] = ok ? *reinterpret_cast<const float4*>(xp) : make_float4(0.f, 0.f, 0.f, 0.f);
+                            xb[m] = ok ? *reinterpret_cast<const float4*>(xp + 4) : make_float4(0.f, 0.f, 0.f, 0.f);
                         }
                     }
+                    float v[8][MR];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+#pragma unroll
+                        for (int m = 0; m < MR; ++m) v[i][m] = 0.f;
+                    if (tile) {
+                        const uint4* T4 = reinterpret_cast<const uint4*>(tile) + chunk;
+                        const int rw = rb * RWT + rg;
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const int r = rw + RG * i;
+                            if (act && r < nr) {
+                                const uint4 w = T4[(size_t)r * NC];
+#pragma unroll
+                                for (int m = 0; m < MR; ++m) fma8v(v[i][m], w, xa[m], xb[m]);
+                            }
+                        }
+                    }
+                    ks_reduce<CPWP, MR>(v);
+                    if (writer) {
+                        float* pw = part + (buf * NCW + warp) * RWT * MC + lrow * MC + (mb - mc0);
+#pragma unroll
+                        for (int m = 0; m < MR; ++m)
+                            if (mb + m < mc0 + mcn) pw[m] = v[0][m];
+                    }
                 }
-                if (gi == ngrp - 1) {
+                if (mc0 + MC >= M) {
                     // the tile has been read: hand the slot back to the producer
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&ms.empty[cr.slot]);
                 }
-                ks_reduce<CPWP, MR>(v);
-                if (writer) {
-                    float* pw = part + (buf * NCW + warp) * RWT * MR + lrow * MR;
-#pragma unroll
-                    for (int m = 0; m < MR; ++m) pw[m] = v[0][m];
-                }
                 cbar();
                 if (tile) {
-                    for (int t = tid; t < nr * MR; t += NCT) {
-                        const int r = t / MR, mi = t - r * MR, m = mb + mi;
-                        if (m >= M) continue;
+                    for (int t = tid; t < nr * mcn; t += NCT) {
+                        const int r = t / mcn, mi = t - r * mcn, m = mc0 + mi;
                         const int b = r / RWT, rl = r - b * RWT;
-                        const float* q = part + ((buf * NCW + b * NKS) * RWT + rl) * MR + mi;
+                        const float* q = part + ((buf * NCW + b * NKS) * RWT + rl) * MC + mi;
                         float y = q[0];
-                        for (int k = 1; k < NKS; ++k) y += q[k * RWT * MR];
+                        for (int k = 1; k < NKS; ++k) y += q[k * RWT * MC];
                         const int row = r0 + r;
                         float* d = dst + (size_t)m * dst_stride + row;
                         if (out_kind == OUT_STORE) {
