@@ -53,8 +53,11 @@ def test_mid_batch1():
     _run(cfg, 1, 1, 2, cfg["ctx"])
 
 
-@pytest.mark.parametrize("B", [4, 8])
+@pytest.mark.parametrize("B", [3, 4, 6, 8])
 def test_mid_batched(B):
+    # 3: the one-token register path run once per token; 6: the shared
+    # expert in token groups of 4 and 2; every batch: routed experts on
+    # their own tokens only
     cfg = configs.MID
     _run(cfg, B, 1, 1, cfg["ctx"])
 
