@@ -198,6 +198,14 @@ int mk_step_status(mk_model* m, void* stream);
  * w [L][batch*T][k] (float). Synchronises `stream`. MoE models only. */
 int mk_debug_routing(mk_model* m, int32_t* idx_out, float* w_out, void* stream);
 
+/* Greedy argmax of every logits row of the last step that was given an
+ * `accept` buffer (computed by the step itself; ties -> lower token id):
+ * `out` int32 [batch*T], host or device memory. A speculative loop takes the
+ * token after the accepted prefix of sequence b from row b*T + accept[b] - 1.
+ * Synchronises `stream`. Errors: INVALID_ARG (NULL), STATE (the last step had
+ * no accept buffer). */
+int mk_last_argmax(mk_model* m, int32_t* out, void* stream);
+
 int mk_model_info(const mk_model* m, mk_info* out);
 
 /* Stage trace of the last step, recorded when the environment variable

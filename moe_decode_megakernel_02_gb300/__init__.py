@@ -20,7 +20,7 @@ OK, ERR_INVALID_ARG, ERR_OOM, ERR_CUDA, ERR_UNSUPPORTED, ERR_TIMEOUT, ERR_STATE 
 ATTN_GQA, ATTN_MLA = 0, 1
 EXPORTS = ("mk_load_weights", "mk_alloc_kv", "mk_kv_set_block_table", "mk_kv_pages_per_seq", "mk_kv_write",
            "mk_kv_read", "mk_decode_step", "mk_decode_step_noalloc", "mk_step_status", "mk_debug_routing",
-           "mk_model_info", "mk_trace_read", "mk_free", "mk_last_error")
+           "mk_last_argmax", "mk_model_info", "mk_trace_read", "mk_free", "mk_last_error")
 TRACE_CAP = 8192
 
 
@@ -78,6 +78,7 @@ def lib():
         L.mk_decode_step_noalloc.argtypes = [P, P, P, P, I32, I32, P, P, P]
         L.mk_step_status.argtypes = [P, P]
         L.mk_debug_routing.argtypes = [P, P, P, P]
+        L.mk_last_argmax.argtypes = [P, P, P]
         L.mk_model_info.argtypes = [P, ctypes.POINTER(Info)]
         L.mk_trace_read.argtypes = [P, P, ctypes.c_int64, P, P]
         L.mk_free.argtypes = [P]
@@ -85,7 +86,7 @@ def lib():
         L.mk_last_error.restype = ctypes.c_char_p
         for f in ("mk_load_weights", "mk_alloc_kv", "mk_kv_set_block_table", "mk_kv_write", "mk_kv_read",
                   "mk_decode_step", "mk_decode_step_noalloc", "mk_step_status", "mk_debug_routing",
-                  "mk_model_info", "mk_trace_read"):
+                  "mk_last_argmax", "mk_model_info", "mk_trace_read"):
             getattr(L, f).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -155,6 +156,12 @@ class Model:
         w = np.zeros((L, M, k), dtype=np.float32)
         _check(lib().mk_debug_routing(self.h, idx.ctypes.data, w.ctypes.data, _stream(stream)))
         return idx, w
+
+    def last_argmax(self, out, stream=None):
+        """Argmax of every row of the last step that had an accept buffer, into
+        `out` (int32 tensor of batch*T entries, host or device)."""
+        _check(lib().mk_last_argmax(self.h, out.data_ptr(), _stream(stream)))
+        return out
 
     def trace(self, stream=None):
         """Stage trace of the last step (needs MK_TRACE=1 at load): structured numpy array per record."""

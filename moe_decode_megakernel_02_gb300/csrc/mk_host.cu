@@ -62,6 +62,7 @@ struct mk_model {
     int* dbg_idx = nullptr;
     float* dbg_w = nullptr;
     int last_M = 0;
+    const int* last_amax = nullptr;  // argmax of the last step's rows (steps given an accept buffer)
     uint64_t steps = 0;
     int live_kv = 0;
 };
@@ -841,6 +842,7 @@ int mk_decode_step(mk_model* m, mk_kv* kv, const int32_t* tokens, const int32_t*
                                    mk::SMEM_TOTAL, s));
     m->steps++;
     m->last_M = P.M;
+    m->last_amax = accept ? P.amax : nullptr;
     return MK_OK;
 }
 
@@ -882,6 +884,14 @@ int mk_debug_routing(mk_model* m, int32_t* idx_out, float* w_out, void* stream) 
     // the device buffers are laid out [L][M][k] for the last step's M
     CK(cudaMemcpy(idx_out, m->dbg_idx, n * 4, cudaMemcpyDeviceToHost));
     CK(cudaMemcpy(w_out, m->dbg_w, n * 4, cudaMemcpyDeviceToHost));
+    return MK_OK;
+}
+
+int mk_last_argmax(mk_model* m, int32_t* out, void* stream) {
+    if (!m || m->magic != MODEL_MAGIC || !out) return fail(MK_ERR_INVALID_ARG, "bad arguments");
+    if (!m->last_amax) return fail(MK_ERR_STATE, "the last step was not given an accept buffer");
+    CK(cudaStreamSynchronize((cudaStream_t)stream));
+    CK(cudaMemcpy(out, m->last_amax, (size_t)m->last_M * 4, cudaMemcpyDefault));
     return MK_OK;
 }
 
@@ -1055,6 +1065,8 @@ extern "C" int mk_decode_step_noalloc(mk_model* m, mk_kv* kv, const int32_t* tok
     void* args[] = {&P};
     CK(cudaLaunchCooperativeKernel((const void*)mk::megakernel, dim3(m->G), dim3(mk::NTHREADS), args,
                                    mk::SMEM_TOTAL, s));
+    m->last_M = P.M;
+    m->last_amax = accept ? P.amax : nullptr;
     // report this step's device-side status before returning
     CK(cudaStreamSynchronize(s));
     unsigned st[4];

@@ -46,6 +46,7 @@ def test_null_arguments_are_rejected():
     assert L.mk_alloc_kv(None, 1, 16, ctypes.byref(out)) == mk.ERR_INVALID_ARG
     assert L.mk_decode_step(None, None, None, None, 1, 1, None, None, None) == mk.ERR_INVALID_ARG
     assert L.mk_step_status(None, None) == mk.ERR_INVALID_ARG
+    assert L.mk_last_argmax(None, None, None) == mk.ERR_INVALID_ARG
     L.mk_free(None)
 
 
