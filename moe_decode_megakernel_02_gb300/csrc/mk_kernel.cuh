@@ -557,9 +557,6 @@ __device__ __forceinline__ bool restage(Ctx& c, const Gemv& g, const float* src,
     return true;
 }
 
-// M <= 2 tokens, K panel >= 256: each lane keeps its slice of the staged
-// input in registers for the whole range (loaded once per staging), so a
-// warp reads only its own weight rows from shared memory per tile.
 // inline bounded spin on a ring barrier (no calls: hot loops stay free of
 // register spills); false on timeout or abort
 __device__ __forceinline__ bool spin_wait(const Params& p, unsigned long long* bar, unsigned parity) {
@@ -593,8 +590,9 @@ __device__ __forceinline__ int run_end(int j, int j_hi, int n_rb, int rb0, int R
 // different K slices. The warp reduces its 8*MR partials across the CPWP
 // lanes of a group (each halving step exchanges half of the values, so a
 // lane ends with one sum instead of 8), writes them to its own slot in
-// shared memory, and after one CTA barrier every output sums the NKS warps'
-// partials. The tile's shared-memory traffic is the weights once.
+// shared memory, and after one CTA barrier per chunk of up to MC tokens
+// every output of the chunk sums the NKS warps' partials. Tokens come MR at
+// a time; the tile's weights are read once per MR tokens.
 //   Kc 2048: NKS 8, CPW 32 -> 8 rows    Kc 1024: NKS 4, CPW 32 -> 16 rows
 //   Kc  768: NKS 8, CPW 12 -> 16 rows   Kc  512: NKS 2, CPW 32 -> 32 rows
 //   Kc  256: NKS 1, CPW 32 -> 64 rows   Kc  128: NKS 1, CPW 16 -> 128 rows
@@ -778,6 +776,8 @@ __device__ __forceinline__ void gemv_range_ks(Ctx& c, const Gemv& g, int slot, i
 // the run. Per tile the shared-memory traffic is the weights once, there is
 // no CTA barrier, and the warps move on to the next tile independently.
 // K panels of 128 elements (16 chunks): two rows per warp pass, 16 lanes each.
+// The MT instances take 2 to 4 tokens (the token map's rows of the staging
+// area): each tile once per token, the token's input reloaded each time.
 __device__ __forceinline__ void rx_out(const Params& p, Misc& ms, int out_kind, int n_kc, float* d, float* d2, int expert,
                                        float y) {
     if (out_kind == OUT_STORE) {
@@ -1087,7 +1087,8 @@ __device__ __forceinline__ void gemv_range_smem(Ctx& c, const Gemv& g, int slot,
 }
 
 // consumer: GEMV work items [j_lo, j_hi) of one slot, two or more tokens:
-// split-K path for two tokens, shared-memory path otherwise. A function of
+// split-K path when every token's K panel is staged at once, shared-memory
+// path otherwise. A function of
 // its own: inlined next to the one-token path, the two would together need
 // more registers than a thread has, and spills go to local memory.
 __device__ __noinline__ void gemv_multi(Ctx& c, const Gemv& g, int slot, int expert, int j_lo, int j_hi) {
@@ -1200,9 +1201,6 @@ __device__ __noinline__ void prod_gemv(Ctx& c, const Gemv& g, int expert, int lo
     c.set_pring(pr, issued);
 }
 
-// consumer side of a GEMV stage: items [lo, hi) of g after the deps set by
-// set_deps, then signal `sig` (the GEMV code, cons_gemv, is shared with the
-// expert units).
 // consumers, output projection with the router folded in (one K panel, so
 // this CTA's rows [R lo, R hi) of the new residual are final after its
 // GEMV): their share of every token's router logits, sum_i Wr[e][i] g[i] x[i]
@@ -1283,6 +1281,9 @@ __device__ __noinline__ void router_part(Ctx& c, int l, const Gemv& go, int lo, 
     }
 }
 
+// consumer side of a GEMV stage: items [lo, hi) of g after the deps set by
+// set_deps, then signal `sig` (the GEMV code, cons_gemv, is shared with the
+// expert units).
 __device__ __noinline__ void cons_mm(Ctx& c, int l, const Gemv& g, int sig, int lo, int hi) {
     c.cur_code = ((unsigned)sig << 16) | (unsigned)l;
     const long long t0 = gtimer();
