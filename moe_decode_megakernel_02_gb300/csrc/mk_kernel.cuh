@@ -1215,6 +1215,8 @@ __device__ __noinline__ void router_part(Ctx& c, int l, const Gemv& go, int lo, 
     const Gemv& gr = Ld.g[G_ROUTER];
     const int r_lo = lo * go.R, nr = min(go.N, hi * go.R) - r_lo;  // a multiple of 8
     const int E = p.E, M = p.M, tid = ctid(), Kc = gr.Kc, RS = router_row(E);
+    // the staging area is reused as scratch; its recorded key stays that of
+    // the output projection's input, a per-layer buffer no later GEMV reads
     float* xg = c.stage();            // [M][nr] x g
     float* xs = xg + M * nr;          // [M][nr] x
     float* sums = xs + M * nr;        // [M][RS]
