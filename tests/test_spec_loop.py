@@ -110,6 +110,67 @@ def test_bad_arguments():
         loop.step()
 
 
+class OracleVerifyModel:
+    """The oracle's verify step behind the loop's model interface (CPU)."""
+
+    def __init__(self, om, okv):
+        self.om, self.okv, self.amax = om, okv, None
+
+    def decode_step(self, kv, tokens, positions, logits, accept, stream=None):
+        import oracle
+        r = oracle.decode(self.om, self.okv, tokens.numpy(), positions.numpy(), precision=64)
+        self.amax = r["logits"].argmax(-1).reshape(-1).astype(np.int32)  # first maximum: lower id on ties
+        accept.copy_(torch.from_numpy(r["accept"].astype(np.int32)))
+
+    def check(self, stream=None):
+        pass
+
+    def last_argmax(self, out, stream=None):
+        out.copy_(torch.from_numpy(self.amax))
+        return out
+
+
+def test_loop_over_the_oracle_verify_step_decodes_greedily():
+    # the oracle's cache keeps the rows of rejected drafts until the next step
+    # overwrites them: the loop must still reproduce one-token greedy decoding
+    import oracle
+    from synth import configs
+    cfg = configs.TINY
+    B, T, ctx, N = 2, 5, cfg["ctx"], 24
+    om = oracle.Model(cfg)
+    first = np.array([3, 700], dtype=np.int32)
+    pos0 = np.array([ctx, ctx - 10], dtype=np.int32)
+
+    kv = oracle.KV(om, B, ctx + 64)
+    kv.prefill(cfg["seed"], ctx)
+    tok, pos, ref, gap = first.copy(), pos0.copy(), [[] for _ in range(B)], [[] for _ in range(B)]
+    for _ in range(N):
+        lg = oracle.decode(om, kv, tok[:, None], pos, precision=64)["logits"][:, 0]
+        srt = np.sort(lg, axis=1)
+        nxt = lg.argmax(1).astype(np.int32)
+        for b in range(B):
+            ref[b].append(int(nxt[b]))
+            gap[b].append(float(srt[b, -1] - srt[b, -2]))
+        tok, pos = nxt, pos + 1
+    kv.close()
+
+    kv = oracle.KV(om, B, ctx + 64)
+    kv.prefill(cfg["seed"], ctx)
+    wrong = {1, 2, 9}
+    loop = GreedySpecLoop(OracleVerifyModel(om, kv), None, first, pos0, T, cfg["vocab"],
+                          PlantedDrafter(ref, cfg["vocab"], wrong=lambda b, i: i in wrong), device="cpu")
+    while min(len(e) for e in loop.emitted) < N - T:
+        loop.step()
+    # drafts 0..3 with 1 wrong -> 2; drafts 2..5 with 2 wrong -> 1; drafts 3..6 -> 5; drafts 8..11 with 9 wrong -> 2
+    assert [int(a[0]) for a in loop.accepts[:4]] == [2, 1, 5, 2]
+    for b in range(B):
+        n = min(len(loop.emitted[b]), N)
+        i = next((i for i in range(n) if loop.emitted[b][i] != ref[b][i]), n)
+        assert i == n or gap[b][i] < 1e-9, (b, i)
+    kv.close()
+    om.close()
+
+
 @pytest.mark.gpu
 def test_verify_loop_matches_plain_greedy_decoding():
     import time
