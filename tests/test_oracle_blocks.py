@@ -118,3 +118,26 @@ def test_attend_special_cases_and_library():
     Kf, Vf = synth.bf16_to_f32(Kn).astype(np.float64), synth.bf16_to_f32(Vn).astype(np.float64)
     ref = sp_softmax(Kf @ q * 0.25) @ Vf
     assert np.allclose(oracle.attend(q, Kn, Vn, 0.25), ref, rtol=1e-12, atol=1e-14)
+
+
+def test_router_folded_into_output_rows_equals_norm_then_matmul():
+    # the GPU path for two or more tokens: each CTA adds its rows' share of
+    # sum_i Wr[e,i] g_i x_i and of sum_i x_i^2 into one of 8 copies; the reader
+    # sums the copies and scales by 1/rms. Same logits as RMSNorm then Wr.
+    rng = np.random.default_rng(7)
+    d, E, eps = 2048, 64, 1e-6
+    x = rng.standard_normal(d) * 3
+    g = bf16(1 + 0.02 * rng.standard_normal(d))
+    Wr = synth.bf16_to_f32(bf16(0.02 * rng.standard_normal((E, d)))).astype(np.float64)
+    plain = Wr @ oracle.rmsnorm(x, g, eps)
+    gf = synth.bf16_to_f32(g).astype(np.float64)
+    acc = np.zeros((8, E + 1))
+    rows = np.array_split(np.arange(d), 152)  # one row range per CTA
+    for cta, r in enumerate(rows):
+        acc[cta % 8, :E] += Wr[:, r] @ (gf[r] * x[r])
+        acc[cta % 8, E] += x[r] @ x[r]
+    tot = acc.sum(0)
+    folded = tot[:E] / np.sqrt(tot[E] / d + eps)
+    assert np.allclose(folded, plain, rtol=1e-12, atol=1e-12)
+    # top-k unchanged by the common positive scale
+    assert np.array_equal(oracle.topk(folded, 8)[0], oracle.topk(tot[:E], 8)[0])
