@@ -46,7 +46,7 @@
 extern "C" {
 #endif
 
-#define MK_ABI_VERSION 1
+#define MK_ABI_VERSION 2
 
 typedef enum mk_status {
     MK_OK = 0,
@@ -125,6 +125,20 @@ typedef struct mk_info {
  * otherwise); results agree within rounding. */
 int mk_load_weights(const mk_config* cfg, const mk_weight* table, int32_t n, void* stream, mk_model** out);
 
+/* mk_load_weights over seeded synthetic weights generated in device memory:
+ * every tensor the model of `cfg` has, element i of tensor (kind, layer,
+ * expert) drawn by the input recipe's counter-based generator (SplitMix64
+ * hash of (seed, tensor id, i), Irwin-Hall(12) normal draw, bf16 round to
+ * nearest even; matrices and embeddings N(0, 0.02), RMSNorm gains
+ * 1 + N(0, 0.02)). The same numbers a caller gets from the generator module
+ * on the host, so a CPU reference can rebuild the model from (cfg, seed).
+ * Holds a temporary device copy of all weights during the call (about the
+ * size of mk_info.weight_bytes). Errors as mk_load_weights. Synchronises
+ * `stream`. The pages use trained weights; the synthetic model stands in for
+ * them with the stated shapes (workload descriptions of the deep MoE model:
+ * bf16 weights drawn from N(0, 0.02)). */
+int mk_load_synthetic(const mk_config* cfg, uint64_t seed, void* stream, mk_model** out);
+
 /* Paged KV cache for `batch` sequences of up to `max_ctx` positions each
  * (must be <= cfg.max_ctx, batch <= cfg.max_batch). Pages hold
  * cfg.kv_page_size positions. The default block table interleaves the
@@ -173,15 +187,27 @@ int mk_decode_step(mk_model* m, mk_kv* kv, const int32_t* tokens, const int32_t*
  * step scratch (mk_info.scratch_bytes plus about 1.3 KB per layer) does not
  * fit, or that has more than 128 layers, is rejected with
  * MK_ERR_UNSUPPORTED. The first call on each device looks up the array's
- * device address (set-up): make that first call before any stream capture.
- * All calls share the array, which keeps the last call's contents; each call
- * clears what must start at zero. Calls that overlap on the GPU (work of
- * other streams or host threads still in flight) race on the array. The
- * call synchronises `stream` and returns the step's device status itself
- * (MK_OK, MK_ERR_TIMEOUT, MK_ERR_INVALID_ARG); mk_debug_routing does not see
- * its routing. */
+ * device address (set-up): make that first call before any stream capture
+ * begins. All calls share the array, which keeps the last call's contents;
+ * each call clears what must start at zero (dependency counters, status
+ * word) and, when another model used the array last, copies in the model's
+ * constant tables (RoPE angles, a zero page). Calls that overlap on the GPU
+ * (work of other streams or host threads still in flight) race on the
+ * array. The model's own scratch is neither read nor written. The call
+ * synchronises `stream` and returns the step's device status itself
+ * (MK_OK, MK_ERR_TIMEOUT, MK_ERR_INVALID_ARG); afterwards mk_debug_routing
+ * returns MK_ERR_STATE (this path keeps no routing record) and
+ * mk_last_argmax reads the static array. */
 int mk_decode_step_noalloc(mk_model* m, mk_kv* kv, const int32_t* tokens, const int32_t* positions, int32_t batch,
                            int32_t T, float* logits, int32_t* accept, void* stream);
+
+/* Fault injection on the host (testing the caller's error handling; the GPU
+ * is never made to fault): while the environment variable MK_FAULT is
+ *   "oom"     mk_load_weights, mk_load_synthetic and mk_alloc_kv fail with
+ *             MK_ERR_OOM before they allocate anything;
+ *   "bad_arg" mk_load_weights, mk_decode_step and mk_decode_step_noalloc
+ *             reject their arguments with MK_ERR_INVALID_ARG.
+ * Each failure sets mk_last_error() to a message naming MK_FAULT. */
 
 /* Synchronise `stream` and return the device status of the last step
  * (MK_OK, MK_ERR_TIMEOUT, MK_ERR_INVALID_ARG). A failed status resets the
@@ -194,9 +220,23 @@ int mk_decode_step_noalloc(mk_model* m, mk_kv* kv, const int32_t* tokens, const 
  * mk_decode_step makes CTA 0 first wait on a counter nothing signals. */
 int mk_step_status(mk_model* m, void* stream);
 
-/* Routing of the last step: host arrays idx [L][batch*T][k] (int32) and
- * w [L][batch*T][k] (float). Synchronises `stream`. MoE models only. */
-int mk_debug_routing(mk_model* m, int32_t* idx_out, float* w_out, void* stream);
+/* Routing of the last step, as computed on the device: host arrays
+ * idx [L][batch*T][k] (int32, in rank order: largest router logit first),
+ * w [L][batch*T][k] (float, renormalised top-k weights) and, when margin_out
+ * is not NULL, margin [L][batch*T] (float: the k-th largest router logit
+ * minus the (k+1)-th, +inf when k equals the expert count; a parity check
+ * accepts a different expert set only where this margin is small).
+ * Synchronises `stream`. MoE models only. Errors: STATE when the model has
+ * no router, no step ran yet, or the last step ran through
+ * mk_decode_step_noalloc (which keeps no routing record). */
+int mk_debug_routing(mk_model* m, int32_t* idx_out, float* w_out, float* margin_out, void* stream);
+
+/* Copy `bytes` bytes at `offset` of the model's own per-step scratch
+ * allocation (mk_info.scratch_bytes) to host memory `host_out`. A debugging
+ * aid: tests use it to check that mk_decode_step_noalloc leaves the model's
+ * scratch untouched. Synchronises `stream`. Errors: INVALID_ARG when the
+ * range is outside the scratch. */
+int mk_debug_scratch_read(mk_model* m, int64_t offset, int64_t bytes, void* host_out, void* stream);
 
 /* Greedy argmax of every logits row of the last step that was given an
  * `accept` buffer (computed by the step itself; ties -> lower token id):

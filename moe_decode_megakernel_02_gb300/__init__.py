@@ -13,21 +13,33 @@ import os
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _ROOT = os.path.dirname(_HERE)
 _BUILD = os.path.join(_HERE, "_build")
-LIB = os.path.join(_BUILD, "libmk.so")
+# the library this process loads: libmk.so, or another build of the same
+# sources named by MK_LIB (the 2-slot ring build used by the shrunken-ring
+# parity check)
+LIB = os.environ.get("MK_LIB") or os.path.join(_BUILD, "libmk.so")
+LIB_NSLOT2 = os.path.join(_BUILD, "libmk_nslot2.so")
 HEADER = os.path.join(_ROOT, "include", "mk.h")
 
 OK, ERR_INVALID_ARG, ERR_OOM, ERR_CUDA, ERR_UNSUPPORTED, ERR_TIMEOUT, ERR_STATE = 0, -1, -2, -3, -4, -5, -6
 ATTN_GQA, ATTN_MLA = 0, 1
-EXPORTS = ("mk_load_weights", "mk_alloc_kv", "mk_kv_set_block_table", "mk_kv_pages_per_seq", "mk_kv_write",
-           "mk_kv_read", "mk_decode_step", "mk_decode_step_noalloc", "mk_step_status", "mk_debug_routing",
-           "mk_last_argmax", "mk_model_info", "mk_trace_read", "mk_free", "mk_last_error")
+EXPORTS = ("mk_load_weights", "mk_load_synthetic", "mk_alloc_kv", "mk_kv_set_block_table", "mk_kv_pages_per_seq",
+           "mk_kv_write", "mk_kv_read", "mk_decode_step", "mk_decode_step_noalloc", "mk_step_status",
+           "mk_debug_routing", "mk_debug_scratch_read", "mk_last_argmax", "mk_model_info", "mk_trace_read", "mk_free",
+           "mk_last_error")
 TRACE_CAP = 8192
 
 
 def build_cmds() -> list:
+    """nvcc commands for the library (the megakernel, its host side and the
+    synthetic loader, which links the input generator module) and for a
+    second build of the same sources with a 2-slot ring (MK_NSLOT=2)."""
     os.makedirs(_BUILD, exist_ok=True)
-    return [["nvcc", "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo", "-std=c++17",
-             "-Xcompiler", "-fPIC", "-shared", os.path.join(_HERE, "csrc", "mk_host.cu"), "-o", LIB]]
+    srcs = [os.path.join(_HERE, "csrc", "mk_host.cu"), os.path.join(_HERE, "csrc", "mk_synth.cu"),
+            os.path.join(_ROOT, "synth", "synth_cuda.cu"), os.path.join(_ROOT, "synth", "synth_host.c")]
+    base = ["nvcc", "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo", "-std=c++17",
+            "-Xcompiler", "-fPIC", "-shared", "-lpthread"]
+    return [base + srcs + ["-o", os.path.join(_BUILD, "libmk.so")],
+            base + ["-DMK_NSLOT=2"] + srcs + ["-o", LIB_NSLOT2]]
 
 
 class Config(ctypes.Structure):
@@ -68,6 +80,7 @@ def lib():
         L = ctypes.CDLL(LIB)
         P, I32 = ctypes.c_void_p, ctypes.c_int32
         L.mk_load_weights.argtypes = [ctypes.POINTER(Config), ctypes.POINTER(Weight), I32, P, ctypes.POINTER(P)]
+        L.mk_load_synthetic.argtypes = [ctypes.POINTER(Config), ctypes.c_uint64, P, ctypes.POINTER(P)]
         L.mk_alloc_kv.argtypes = [P, I32, I32, ctypes.POINTER(P)]
         L.mk_kv_set_block_table.argtypes = [P, P]
         L.mk_kv_pages_per_seq.argtypes = [P]
@@ -77,16 +90,17 @@ def lib():
         L.mk_decode_step.argtypes = [P, P, P, P, I32, I32, P, P, P]
         L.mk_decode_step_noalloc.argtypes = [P, P, P, P, I32, I32, P, P, P]
         L.mk_step_status.argtypes = [P, P]
-        L.mk_debug_routing.argtypes = [P, P, P, P]
+        L.mk_debug_routing.argtypes = [P, P, P, P, P]
+        L.mk_debug_scratch_read.argtypes = [P, ctypes.c_int64, ctypes.c_int64, P, P]
         L.mk_last_argmax.argtypes = [P, P, P]
         L.mk_model_info.argtypes = [P, ctypes.POINTER(Info)]
         L.mk_trace_read.argtypes = [P, P, ctypes.c_int64, P, P]
         L.mk_free.argtypes = [P]
         L.mk_free.restype = None
         L.mk_last_error.restype = ctypes.c_char_p
-        for f in ("mk_load_weights", "mk_alloc_kv", "mk_kv_set_block_table", "mk_kv_write", "mk_kv_read",
-                  "mk_decode_step", "mk_decode_step_noalloc", "mk_step_status", "mk_debug_routing",
-                  "mk_last_argmax", "mk_model_info", "mk_trace_read"):
+        for f in ("mk_load_weights", "mk_load_synthetic", "mk_alloc_kv", "mk_kv_set_block_table", "mk_kv_write",
+                  "mk_kv_read", "mk_decode_step", "mk_decode_step_noalloc", "mk_step_status", "mk_debug_routing",
+                  "mk_debug_scratch_read", "mk_last_argmax", "mk_model_info", "mk_trace_read"):
             getattr(L, f).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -115,12 +129,21 @@ def make_config(cfg, max_batch, max_tokens_per_seq, max_ctx) -> Config:
 class Model:
     """A loaded model: mk_load_weights over a list of (kind, layer, expert, data_ptr)."""
 
-    def __init__(self, config: Config, table, stream=None):
-        arr = (Weight * len(table))(*[Weight(k, l, e, 0, p) for (k, l, e, p) in table])
+    def __init__(self, config: Config, table=None, stream=None, seed=None):
         h = ctypes.c_void_p()
         self.config = config
-        _check(lib().mk_load_weights(ctypes.byref(config), arr, len(table), _stream(stream), ctypes.byref(h)))
+        if table is None:
+            # seeded synthetic weights generated on the device (mk_load_synthetic)
+            _check(lib().mk_load_synthetic(ctypes.byref(config), int(seed), _stream(stream), ctypes.byref(h)))
+        else:
+            arr = (Weight * len(table))(*[Weight(k, l, e, 0, p) for (k, l, e, p) in table])
+            _check(lib().mk_load_weights(ctypes.byref(config), arr, len(table), _stream(stream), ctypes.byref(h)))
         self.h = h
+
+    @classmethod
+    def synthetic(cls, config: Config, seed: int, stream=None) -> "Model":
+        """mk_load_synthetic: the model of `config` with the generator's seeded weights."""
+        return cls(config, None, stream, seed)
 
     def info(self) -> Info:
         out = Info()
@@ -150,12 +173,22 @@ class Model:
         _check(self.status(stream))
 
     def routing(self, M, stream=None):
+        """Routing of the last step: idx [L, M, k], w [L, M, k], margin [L, M] (k-th minus (k+1)-th logit)."""
         import numpy as np
         L, k = self.config.n_layers, self.config.top_k
         idx = np.zeros((L, M, k), dtype=np.int32)
         w = np.zeros((L, M, k), dtype=np.float32)
-        _check(lib().mk_debug_routing(self.h, idx.ctypes.data, w.ctypes.data, _stream(stream)))
-        return idx, w
+        mg = np.zeros((L, M), dtype=np.float32)
+        _check(lib().mk_debug_routing(self.h, idx.ctypes.data, w.ctypes.data, mg.ctypes.data, _stream(stream)))
+        return idx, w, mg
+
+    def scratch(self, offset=0, nbytes=None, stream=None):
+        """Bytes [offset, offset + nbytes) of the model's own step scratch (numpy uint8)."""
+        import numpy as np
+        n = self.info().scratch_bytes - offset if nbytes is None else nbytes
+        out = np.empty(n, dtype=np.uint8)
+        _check(lib().mk_debug_scratch_read(self.h, offset, n, out.ctypes.data, _stream(stream)))
+        return out
 
     def last_argmax(self, out, stream=None):
         """Argmax of every row of the last step that had an accept buffer, into

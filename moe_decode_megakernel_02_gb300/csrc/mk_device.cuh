@@ -5,7 +5,7 @@
 // is a fixed program of stages; the work items of every stage are spread
 // over the CTAs. Every CTA's producer warp walks the same program as its
 // consumers and streams each weight tile / KV chunk its consumers will need
-// into a 4-slot shared-memory ring with TMA bulk copies
+// into a shared-memory ring of NSLOT slots (3 by default) with TMA bulk copies
 // (cp.async.bulk + mbarrier complete_tx). Weight tiles depend on no
 // activation, so the producer runs ahead across stage and layer boundaries
 // while the consumers wait for their inputs: this is the GPU form of the
@@ -166,8 +166,9 @@ struct Params {
     int parity;
     unsigned* status;               // [0] code [1] abort [2] where [3] cta
     long long timeout_ns;
-    int* dbg_idx;
+    int* dbg_idx;                   // routing of the step (written by CTA 0): [L][M][k]
     float* dbg_w;
+    float* dbg_margin;              // [L][M]: k-th minus (k+1)-th router logit (+inf when k = E)
     struct TraceRec* trace;         // optional stage trace [G][trace_cap]
     unsigned* trace_n;              // records written per CTA
     int trace_cap;

@@ -7,6 +7,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <atomic>
 #include <map>
 #include <string>
 #include <tuple>
@@ -42,6 +43,17 @@ constexpr uint32_t KV_MAGIC = 0x4d4b4b56u;     // "MKKV"
 
 size_t align256(size_t n) { return (n + 255) & ~(size_t)255; }
 
+// host-side fault injection: MK_FAULT names the failure to report
+bool fault(const char* what) {
+    const char* e = getenv("MK_FAULT");
+    return e && strcmp(e, what) == 0;
+}
+
+uint64_t next_serial() {
+    static std::atomic<uint64_t> n{0};
+    return ++n;
+}
+
 }  // namespace
 
 struct mk_model {
@@ -61,9 +73,12 @@ struct mk_model {
     unsigned* status = nullptr;
     int* dbg_idx = nullptr;
     float* dbg_w = nullptr;
+    float* dbg_margin = nullptr;
     int last_M = 0;
+    bool last_noalloc = false;  // the last step ran in the static scratch (its routing is not in dbg_*)
     const int* last_amax = nullptr;  // argmax of the last step's rows (steps given an accept buffer)
     uint64_t steps = 0;
+    uint64_t serial = 0;  // distinct per loaded model in this process
     int live_kv = 0;
 };
 
@@ -281,12 +296,23 @@ extern "C" {
 
 const char* mk_last_error(void) { return g_err.c_str(); }
 
+// failures found in the library's other translation units (mk_synth.cu)
+__attribute__((visibility("hidden"))) int mk_set_error_(int code, const char* msg) {
+    g_err = msg;
+    return code;
+}
+__attribute__((visibility("hidden"))) int mk_fault_oom_(void) {
+    return fault("oom") ? fail(MK_ERR_OOM, "allocation refused (injected by MK_FAULT=oom)") : MK_OK;
+}
+
 int mk_load_weights(const mk_config* cfg, const mk_weight* table, int32_t n, void* stream, mk_model** out) {
     if (!out) return fail(MK_ERR_INVALID_ARG, "out is NULL");
     *out = nullptr;
     int rc = validate(cfg);
     if (rc) return rc;
     if (!table || n < 1) return fail(MK_ERR_INVALID_ARG, "empty weight table");
+    if (fault("bad_arg")) return fail(MK_ERR_INVALID_ARG, "arguments rejected (injected by MK_FAULT=bad_arg)");
+    if (fault("oom")) return fail(MK_ERR_OOM, "allocation refused (injected by MK_FAULT=oom)");
     cudaStream_t s = (cudaStream_t)stream;
     const Dims D = dims_of(*cfg);
 
@@ -308,6 +334,7 @@ int mk_load_weights(const mk_config* cfg, const mk_weight* table, int32_t n, voi
 
     mk_model* m = new mk_model();
     m->magic = MODEL_MAGIC;
+    m->serial = next_serial();
     m->cfg = *cfg;
     auto bail = [&](int code) {
         if (m->wblob) cudaFree(m->wblob);
@@ -396,6 +423,7 @@ int mk_load_weights(const mk_config* cfg, const mk_weight* table, int32_t n, voi
     const size_t s_status = stake(64);
     const size_t s_dbgi = D.E ? stake((size_t)L * Mx * D.k * 4) : 0;
     const size_t s_dbgw = D.E ? stake((size_t)L * Mx * D.k * 4) : 0;
+    const size_t s_dbgm = D.E ? stake((size_t)L * Mx * 4) : 0;
     const int rope_dim = D.gqa ? D.hd : D.rd;
     const int npos = cfg->max_ctx + cfg->max_tokens_per_seq;
     const size_t s_rope = stake((size_t)npos * (rope_dim / 2) * 8);
@@ -646,6 +674,7 @@ int mk_load_weights(const mk_config* cfg, const mk_weight* table, int32_t n, voi
     if (D.E) {
         m->dbg_idx = reinterpret_cast<int*>(S + s_dbgi);
         m->dbg_w = reinterpret_cast<float*>(S + s_dbgw);
+        m->dbg_margin = reinterpret_cast<float*>(S + s_dbgm);
     }
     CK(cudaStreamSynchronize(s));
     *out = m;
@@ -672,6 +701,7 @@ int mk_alloc_kv(const mk_model* m, int32_t batch, int32_t max_ctx, mk_kv** out) 
     if (batch < 1 || batch > m->cfg.max_batch) return fail(MK_ERR_INVALID_ARG, "batch out of range");
     if (max_ctx < 1 || max_ctx > m->cfg.max_ctx + m->cfg.max_tokens_per_seq)
         return fail(MK_ERR_INVALID_ARG, "max_ctx out of range");
+    if (fault("oom")) return fail(MK_ERR_OOM, "allocation refused (injected by MK_FAULT=oom)");
     const Dims D = dims_of(m->cfg);
     mk_kv* kv = new mk_kv();
     kv->magic = KV_MAGIC;
@@ -811,6 +841,7 @@ int mk_decode_step(mk_model* m, mk_kv* kv, const int32_t* tokens, const int32_t*
     if (batch < 1 || batch > kv->batch) return fail(MK_ERR_INVALID_ARG, "batch %d out of range", batch);
     if (T < 1 || T > m->cfg.max_tokens_per_seq) return fail(MK_ERR_INVALID_ARG, "T %d out of range", T);
     if (accept && T < 2) return fail(MK_ERR_INVALID_ARG, "accept needs T > 1");
+    if (fault("bad_arg")) return fail(MK_ERR_INVALID_ARG, "arguments rejected (injected by MK_FAULT=bad_arg)");
     mk::Params P = m->base;
     P.page_elems = (long long)kv->page_elems;
     P.pps = kv->pps;
@@ -836,12 +867,14 @@ int mk_decode_step(mk_model* m, mk_kv* kv, const int32_t* tokens, const int32_t*
     P.parity = (int)(m->steps & 1);
     P.dbg_idx = m->dbg_idx;
     P.dbg_w = m->dbg_w;
+    P.dbg_margin = m->dbg_margin;
     cudaStream_t s = (cudaStream_t)stream;
     void* args[] = {&P};
     CK(cudaLaunchCooperativeKernel((const void*)mk::megakernel, dim3(m->G), dim3(mk::NTHREADS), args,
                                    mk::SMEM_TOTAL, s));
     m->steps++;
     m->last_M = P.M;
+    m->last_noalloc = false;
     m->last_amax = accept ? P.amax : nullptr;
     return MK_OK;
 }
@@ -876,14 +909,28 @@ int mk_trace_read(mk_model* m, void* recs_out, int64_t bytes, int32_t* counts_ou
     return MK_OK;
 }
 
-int mk_debug_routing(mk_model* m, int32_t* idx_out, float* w_out, void* stream) {
+int mk_debug_routing(mk_model* m, int32_t* idx_out, float* w_out, float* margin_out, void* stream) {
     if (!m || m->magic != MODEL_MAGIC || !idx_out || !w_out) return fail(MK_ERR_INVALID_ARG, "bad arguments");
     if (!m->dbg_idx) return fail(MK_ERR_STATE, "model has no router");
+    if (m->last_M == 0) return fail(MK_ERR_STATE, "no step has run on this model");
+    if (m->last_noalloc)
+        return fail(MK_ERR_STATE, "the last step ran through mk_decode_step_noalloc, which keeps no routing record");
     CK(cudaStreamSynchronize((cudaStream_t)stream));
     const size_t n = (size_t)m->cfg.n_layers * m->last_M * m->cfg.top_k;
-    // the device buffers are laid out [L][M][k] for the last step's M
+    // the device buffers are laid out [L][M][k] and [L][M] for the last step's M
     CK(cudaMemcpy(idx_out, m->dbg_idx, n * 4, cudaMemcpyDeviceToHost));
     CK(cudaMemcpy(w_out, m->dbg_w, n * 4, cudaMemcpyDeviceToHost));
+    if (margin_out)
+        CK(cudaMemcpy(margin_out, m->dbg_margin, (size_t)m->cfg.n_layers * m->last_M * 4, cudaMemcpyDeviceToHost));
+    return MK_OK;
+}
+
+int mk_debug_scratch_read(mk_model* m, int64_t offset, int64_t bytes, void* host_out, void* stream) {
+    if (!m || m->magic != MODEL_MAGIC || !host_out) return fail(MK_ERR_INVALID_ARG, "bad model handle or NULL output");
+    if (offset < 0 || bytes < 0 || (uint64_t)offset + (uint64_t)bytes > m->sbytes)
+        return fail(MK_ERR_INVALID_ARG, "range outside the scratch (%zu bytes)", m->sbytes);
+    CK(cudaStreamSynchronize((cudaStream_t)stream));
+    if (bytes) CK(cudaMemcpy(host_out, m->sblob + offset, (size_t)bytes, cudaMemcpyDeviceToHost));
     return MK_OK;
 }
 
@@ -945,6 +992,9 @@ static __device__ __align__(256) uint8_t g_noalloc_scratch[MK_NOALLOC_SCRATCH_BY
 
 // device address of g_noalloc_scratch per device (looked up once per device)
 void* g_noalloc_base[MK_NOALLOC_MAX_DEVICES];
+// serial of the model whose read-only tables (RoPE, zero page) the array
+// holds, per device (0: none)
+uint64_t g_noalloc_seeded[MK_NOALLOC_MAX_DEVICES];
 // host staging of the relocated stage descriptors (fixed size, no allocation)
 mk::Layer g_noalloc_layers[MK_NOALLOC_MAX_LAYERS];
 std::mutex g_noalloc_mu;
@@ -979,6 +1029,7 @@ extern "C" int mk_decode_step_noalloc(mk_model* m, mk_kv* kv, const int32_t* tok
     if (batch < 1 || batch > kv->batch) return fail(MK_ERR_INVALID_ARG, "batch %d out of range", batch);
     if (T < 1 || T > m->cfg.max_tokens_per_seq) return fail(MK_ERR_INVALID_ARG, "T %d out of range", T);
     if (accept && T < 2) return fail(MK_ERR_INVALID_ARG, "accept needs T > 1");
+    if (fault("bad_arg")) return fail(MK_ERR_INVALID_ARG, "arguments rejected (injected by MK_FAULT=bad_arg)");
     const int L = m->cfg.n_layers;
     const size_t desc_off = align256(m->sbytes);
     const size_t need = desc_off + sizeof(mk::Layer) * (size_t)L;
@@ -1001,9 +1052,20 @@ extern "C" int mk_decode_step_noalloc(mk_model* m, mk_kv* kv, const int32_t* tok
     uint8_t* base = static_cast<uint8_t*>(g_noalloc_base[dev]);
     cudaStream_t s = (cudaStream_t)stream;
     const Reloc r{m->sblob, m->sbytes, base};
-    // the array keeps the previous call's contents: start from the model's
-    // scratch image (RoPE table, zero page) and clear the counters and status
-    CK(cudaMemcpyAsync(base, m->sblob, m->sbytes, cudaMemcpyDeviceToDevice, s));
+    // the array keeps the previous call's contents. The step reads two
+    // tables it does not write -- the RoPE table and a zero page -- which are
+    // seeded from the model's scratch when another model used the array
+    // last (both are constant after mk_load_weights, so this copy never
+    // races with steps of the model in flight); every other region the step
+    // reads is written earlier in the same step, except the counters and the
+    // status word, which are cleared here.
+    if (g_noalloc_seeded[dev] != m->serial) {
+        const size_t rope_bytes = (size_t)m->base.rope_npos * m->base.rope_half * sizeof(float2);
+        CK(cudaMemcpyAsync(const_cast<float2*>(r(m->base.rope)), m->base.rope, rope_bytes, cudaMemcpyDeviceToDevice,
+                           s));
+        CK(cudaMemsetAsync(const_cast<uint16_t*>(r(m->base.zeros)), 0, 4096, s));
+        g_noalloc_seeded[dev] = m->serial;
+    }
     CK(cudaMemsetAsync(r(m->ctr), 0, m->ctr_n * sizeof(unsigned), s));
     CK(cudaMemsetAsync(r(m->status), 0, 64, s));
     for (int l = 0; l < L; ++l) {
@@ -1038,6 +1100,7 @@ extern "C" int mk_decode_step_noalloc(mk_model* m, mk_kv* kv, const int32_t* tok
     P.status = r(P.status);
     P.dbg_idx = r(m->dbg_idx);
     P.dbg_w = r(m->dbg_w);
+    P.dbg_margin = r(m->dbg_margin);
     P.trace = nullptr;
     P.trace_n = nullptr;
     P.trace_items = 0;
@@ -1066,6 +1129,7 @@ extern "C" int mk_decode_step_noalloc(mk_model* m, mk_kv* kv, const int32_t* tok
     CK(cudaLaunchCooperativeKernel((const void*)mk::megakernel, dim3(m->G), dim3(mk::NTHREADS), args,
                                    mk::SMEM_TOTAL, s));
     m->last_M = P.M;
+    m->last_noalloc = true;
     m->last_amax = accept ? P.amax : nullptr;
     // report this step's device-side status before returning
     CK(cudaStreamSynchronize(s));

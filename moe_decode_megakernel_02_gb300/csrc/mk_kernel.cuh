@@ -1452,6 +1452,24 @@ __device__ __forceinline__ bool route(Ctx& c, int l) {
             }
 #pragma unroll
             for (int o = 16; o; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+            if (!PROD && blockIdx.x == 0 && p.dbg_margin) {
+                // router margin of this token: the k-th largest logit minus
+                // the (k+1)-th (the values of ranks k - 1 and k)
+                float a = -INFINITY, b = -INFINITY;
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    if (lane + 32 * q < E) {
+                        if (rk[q] == k - 1) a = v[q];
+                        if (rk[q] == k) b = v[q];
+                    }
+                }
+#pragma unroll
+                for (int o = 16; o; o >>= 1) {
+                    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+                    b = fmaxf(b, __shfl_xor_sync(0xffffffffu, b, o));
+                }
+                if (lane == 0) p.dbg_margin[(size_t)l * p.M + m] = k < E ? a - b : INFINITY;
+            }
 #pragma unroll
             for (int q = 0; q < 2; ++q) {
                 const int e = lane + 32 * q;
@@ -1501,6 +1519,16 @@ __device__ __forceinline__ bool route(Ctx& c, int l) {
 #pragma unroll
             for (int i = 0; i < MAX_E / 32; ++i)
                 if (lane + 32 * i == bi) v[i] = -INFINITY;
+        }
+        if (!PROD && blockIdx.x == 0 && p.dbg_margin) {
+            // router margin: the k-th selected logit minus the largest one left
+            float bv = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < MAX_E / 32; ++i)
+                if (lane + 32 * i < E) bv = fmaxf(bv, v[i]);
+#pragma unroll
+            for (int o = 16; o; o >>= 1) bv = fmaxf(bv, __shfl_xor_sync(0xffffffffu, bv, o));
+            if (lane == 0) p.dbg_margin[(size_t)l * p.M + m] = k < E ? sel[k - 1] - bv : INFINITY;
         }
         if (lane == 0) {
             // renormalised top-k probabilities = softmax over the selected logits

@@ -2,9 +2,9 @@
 
 Every number comes from the shared input generator (`synth`): weights are
 bf16 draws of N(0, 0.02) (RMSNorm gains 1 + N(0, 0.02)), pre-filled KV entries
-bf16 N(0, 1), token ids uniform. Tensors are generated directly in device
-memory by the generator's CUDA implementation, then handed to mk_load_weights
-/ mk_kv_write -- the same public calls a user with real weights makes.
+bf16 N(0, 1), token ids uniform. Weights are generated in device memory by the
+library itself (mk_load_synthetic); KV entries by the generator's CUDA
+implementation, then handed to mk_kv_write.
 """
 from __future__ import annotations
 
@@ -16,26 +16,10 @@ import synth
 from . import KVCache, Model, make_config
 
 
-def load_synthetic(cfg, max_batch, max_tokens_per_seq, max_ctx, seed=None, device="cuda"):
-    """Build the model of workload `cfg` from the generator and load it with mk_load_weights."""
+def load_synthetic(cfg, max_batch, max_tokens_per_seq, max_ctx, seed=None):
+    """The model of workload `cfg` with the generator's seeded weights (mk_load_synthetic)."""
     seed = cfg["seed"] if seed is None else seed
-    specs = list(synth.weight_tensors(cfg))
-    offs, total = [], 0
-    for (_, _, _, r, c, _, _) in specs:
-        offs.append(total)
-        total += (r * c + 127) // 128 * 128  # 256-byte aligned
-    buf = torch.empty(total, dtype=torch.int16, device=device)
-    stream = torch.cuda.current_stream().cuda_stream
-    base = buf.data_ptr()
-    table = []
-    for (kind, layer, expert, r, c, sigma, mean), o in zip(specs, offs):
-        synth.fill_bf16_cuda(base + 2 * o, r * c, seed, synth.tensor_id(kind, layer, expert), sigma, mean, 0, stream)
-        table.append((kind, layer, expert, base + 2 * o))
-    conf = make_config(cfg, max_batch, max_tokens_per_seq, max_ctx)
-    model = Model(conf, table)
-    del buf
-    torch.cuda.empty_cache()
-    return model
+    return Model.synthetic(make_config(cfg, max_batch, max_tokens_per_seq, max_ctx), seed)
 
 
 def kv_row(cfg) -> int:

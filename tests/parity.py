@@ -40,7 +40,7 @@ def run_gpu(cfg, B, T, steps, ctx, positions_fn=None, tokens_fn=None, block_tabl
         res = dict(tokens=np.array(tok), positions=np.array(pos),
                    logits=logits.cpu().numpy().astype(np.float64).reshape(B, T, -1))
         if cfg["n_routed_experts"]:
-            res["route_idx"], res["route_w"] = model.routing(B * T)
+            res["route_idx"], res["route_w"], res["route_margin"] = model.routing(B * T)
         if want_accept:
             res["accept"] = acc.cpu().numpy()
         out.append(res)
@@ -89,6 +89,8 @@ def compare(cfg, gpu_steps, ora_steps, B, T, seqs=None):
     exempt = set()
     flips = 0
     worst_max, sums, count = 0.0, 0.0, 0
+    # router margins: the GPU's own (from mk_debug_routing) next to the oracle's
+    mdiff, mmin_gpu, mmin_ora = 0.0, np.inf, np.inf
     for si, (g, o) in enumerate(zip(gpu_steps, ora_steps)):
         for i, b in enumerate(seqs):
             if b in exempt:
@@ -107,6 +109,10 @@ def compare(cfg, gpu_steps, ora_steps, B, T, seqs=None):
                             exempt.add(b)
                             flips += 1
                             break
+                        gm, om = float(g["route_margin"][l, mg]), float(o["route_margin"][l, mo])
+                        if np.isfinite(om):
+                            mdiff = max(mdiff, abs(gm - om))
+                            mmin_gpu, mmin_ora = min(mmin_gpu, gm), min(mmin_ora, om)
                         gw = dict(zip(g["route_idx"][l, mg].tolist(), g["route_w"][l, mg].tolist()))
                         ow = dict(zip(o["route_idx"][l, mo].tolist(), o["route_w"][l, mo].tolist()))
                         for e in gs:
@@ -125,7 +131,10 @@ def compare(cfg, gpu_steps, ora_steps, B, T, seqs=None):
     assert count > 0, "every sequence was exempted"
     assert worst_max <= MAX_ABS, f"logits max-abs {worst_max:.3e} > {MAX_ABS}"
     assert mean <= MEAN_ABS, f"logits mean-abs {mean:.3e} > {MEAN_ABS}"
-    return dict(max_abs=worst_max, mean_abs=mean, exempt=len(exempt), flips=flips, compared=count)
+    rep = dict(max_abs=worst_max, mean_abs=mean, exempt=len(exempt), flips=flips, compared=count)
+    if moe:
+        rep.update(margin_maxdiff=mdiff, margin_min_gpu=mmin_gpu, margin_min_oracle=mmin_ora)
+    return rep
 
 
 def _check_accept(g, o, b, i, T):

@@ -77,3 +77,29 @@ def test_missing_and_duplicate_tensors_are_reported():
 @pytest.mark.skipif(have_gpu(), reason="checks the no-GPU error path")
 def test_no_device_gives_cuda_error_not_crash():
     assert _bad(configs.TINY) in (mk.ERR_CUDA, mk.ERR_INVALID_ARG)
+
+
+@pytest.mark.parametrize("fault,code", [("oom", mk.ERR_OOM), ("bad_arg", mk.ERR_INVALID_ARG)])
+def test_injected_host_faults_are_reported(monkeypatch, fault, code):
+    # MK_FAULT makes the library report the failure before it touches the
+    # device, so the caller's error handling can be exercised anywhere
+    monkeypatch.setenv("MK_FAULT", fault)
+    c = mk.make_config(configs.TINY, 1, 1, 128)
+    out = ctypes.c_void_p()
+    w = (mk.Weight * 1)(mk.Weight(1, -1, 0, 0, 8))
+    assert mk.lib().mk_load_weights(ctypes.byref(c), w, 1, None, ctypes.byref(out)) == code
+    assert b"MK_FAULT=" + fault.encode() in mk.lib().mk_last_error()
+    assert not out.value
+    if fault == "oom":
+        assert mk.lib().mk_load_synthetic(ctypes.byref(c), 0, None, ctypes.byref(out)) == mk.ERR_OOM
+        assert b"MK_FAULT=oom" in mk.lib().mk_last_error()
+    monkeypatch.delenv("MK_FAULT")
+    assert mk.lib().mk_load_weights(ctypes.byref(c), w, 1, None, ctypes.byref(out)) != code or code != mk.ERR_OOM
+
+
+def test_debug_entry_points_reject_bad_handles():
+    L = mk.lib()
+    assert L.mk_load_synthetic(None, 0, None, None) == mk.ERR_INVALID_ARG
+    assert L.mk_debug_routing(None, None, None, None, None) == mk.ERR_INVALID_ARG
+    assert L.mk_debug_scratch_read(None, 0, 0, None, None) == mk.ERR_INVALID_ARG
+    assert L.mk_decode_step_noalloc(None, None, None, None, 1, 1, None, None, None) == mk.ERR_INVALID_ARG

@@ -20,7 +20,7 @@ def _run(cfg, B, T, steps, ctx, lazy=False, **kw):
     g, _ = parity.run_gpu(cfg, B, T, steps, ctx, **kw)
     o = parity.run_oracle(cfg, g, ctx, B, T, lazy=lazy)
     rep = parity.compare(cfg, g, o, B, T)
-    print(cfg["name"], B, T, rep)
+    print(cfg["name"], cfg["n_layers"], "layers", B, T, rep)
     return g, o, rep
 
 
@@ -103,3 +103,110 @@ def test_separate_router_stage(monkeypatch, name, B):
     monkeypatch.setenv("MK_ROUTER_STAGE", "1")
     cfg = configs.scaled(configs.ALL[name], n_layers=2)
     _run(cfg, B, 1, 1, cfg["ctx"])
+
+
+@pytest.mark.parametrize("B", [4, 8])
+def test_deep_batched(B):
+    # the deep model's batched path (MLA with B query rows per head, the
+    # router folded into the output projection, shared expert in token groups
+    # of 4, routed units over their own tokens) at the full 8192-position context
+    cfg = configs.scaled(configs.DEEP, n_layers=2)
+    _run(cfg, B, 1, 1, cfg["ctx"])
+
+
+def test_deep_full_depth_batch1():
+    # one decode step of all 92 layers (the configuration the throughput is
+    # quoted on) against the fp64 oracle, whose layer weights are generated on
+    # first use and released after the layer
+    cfg = configs.DEEP
+    _, _, rep = _run(cfg, 1, 1, 1, cfg["ctx"], lazy=True)
+    print(f"deep 92 layers, batch 1, ctx 8192: logits max-abs {rep['max_abs']:.3e} "
+          f"mean-abs {rep['mean_abs']:.3e}, router margin max |gpu - oracle| {rep['margin_maxdiff']:.3e}")
+
+
+def test_verify_step_with_planted_drafts():
+    # drafts are the oracle's own greedy continuation with one error planted
+    # at a known draft index per sequence (or none), so the acceptance lengths
+    # 1..7 are all exercised and compared with the oracle's
+    import oracle
+    cfg = configs.scaled(configs.VERIFY, n_layers=2)
+    B, T, ctx = 8, 7, 2000
+    V = cfg["vocab"]
+    first = parity_tokens(cfg, B)
+    # greedy continuation of every sequence, one oracle step per token
+    om = oracle.Model(cfg)
+    okv = oracle.KV(om, B, ctx + T + 1)
+    for l in range(cfg["n_layers"]):
+        for b in range(B):
+            okv.write(l, b, 0, parity._prefill_rows(cfg, l, b, ctx))
+    tok = first.copy()
+    greedy = np.zeros((B, T - 1), dtype=np.int32)
+    for i in range(T - 1):
+        lg = oracle.decode(om, okv, tok[:, None], np.full(B, ctx + i, dtype=np.int32))["logits"][:, 0]
+        tok = lg.argmax(1).astype(np.int32)
+        greedy[:, i] = tok
+    okv.close()
+    om.close()
+    err_at = [0, 1, 2, 3, 4, 5, 6, 0]  # draft index (1..6) made wrong, 0: none
+    block = np.concatenate([first[:, None], greedy], axis=1)
+    for b, j in enumerate(err_at):
+        if j:
+            block[b, j] = (block[b, j] + 1) % V
+    expect = np.array([j if j else T for j in err_at], dtype=np.int32)
+    g, o, rep = _run(cfg, B, T, 1, ctx, want_accept=True, tokens_fn=lambda s: block)
+    acc_g, acc_o = g[0]["accept"], o[0]["accept"]
+    print("planted accept", expect.tolist(), "gpu", acc_g.tolist(), "oracle", acc_o.tolist())
+    assert np.array_equal(acc_o, expect)
+    # the GPU's acceptance equals the planted one for every sequence whose
+    # argmax decisions are clear: at each row the acceptance reads, the
+    # oracle's top-2 logit gap exceeds twice the GPU's largest logit error of
+    # that row (parity.compare applies the fixed 4e-2 gap rule on top)
+    lg_g, lg_o = g[0]["logits"], o[0]["logits"]
+    clear = 0
+    for b in range(B):
+        rows = range(min(int(expect[b]), T - 1))
+        ok = True
+        for i in rows:
+            srt = np.sort(lg_o[b, i])[::-1]
+            if srt[0] - srt[1] <= 2 * np.abs(lg_g[b, i] - lg_o[b, i]).max():
+                ok = False
+        if ok:
+            clear += 1
+            assert acc_g[b] == expect[b], (b, acc_g[b], expect[b])
+    assert clear >= B - 2, f"only {clear} of {B} sequences had clear argmax decisions"
+
+
+def parity_tokens(cfg, B):
+    from moe_decode_megakernel_02_gb300 import workload
+    return workload.tokens(cfg, 0, B, 1)[:, 0].astype(np.int32)
+
+
+def test_ring_slots_of_the_loaded_build():
+    # the suite also runs against the 2-slot ring build (MK_LIB, see below):
+    # the library this process loaded reports its own ring depth
+    import os
+    import moe_decode_megakernel_02_gb300 as mk
+    from moe_decode_megakernel_02_gb300 import workload
+    model = workload.load_synthetic(configs.TINY, max_batch=1, max_tokens_per_seq=1, max_ctx=80)
+    want = 2 if os.environ.get("MK_LIB", "").endswith("libmk_nslot2.so") else 3
+    assert model.info().ring_slots == want
+
+
+def test_two_slot_ring_build_parity():
+    # a shrunken ring (2 slots instead of 3) changes every producer/consumer
+    # interleaving; the same parity cases must pass with that build
+    import os
+    import subprocess
+    import sys
+    import moe_decode_megakernel_02_gb300 as mk
+    if os.environ.get("MK_LIB"):
+        pytest.skip("already running against another build")
+    assert os.path.exists(mk.LIB_NSLOT2), "libmk_nslot2.so is not built"
+    env = dict(os.environ, MK_LIB=mk.LIB_NSLOT2)
+    sel = ("ring_slots_of_the_loaded_build or tiny_sixteen or mid_batched or deep_reduced_layers or "
+           "verify_step_reduced or deep_batched")
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-m", "gpu", "-k", sel, __file__],
+                       env=env, cwd=os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                       capture_output=True, text=True, timeout=1200)
+    print(r.stdout[-2000:])
+    assert r.returncode == 0, r.stdout[-4000:] + r.stderr[-2000:]

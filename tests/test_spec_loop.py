@@ -4,9 +4,9 @@ CPU: the loop's bookkeeping against a stand-in model whose greedy token is a
 known function of (token, position) and whose acceptance follows the verify
 step's rule; the emitted tokens must equal plain greedy decoding whatever the
 drafts, and positions advance by the accept lengths.
-GPU: the loop over the real verify step must reproduce plain one-token greedy
-decoding of the same model and cache, with the accept lengths the planted
-draft errors imply.
+GPU: the loop over the CUDA verify step must reproduce the oracle's plain
+one-token greedy decoding of the same model and cache, with the accept lengths
+the planted draft errors imply.
 """
 import numpy as np
 import pytest
@@ -172,11 +172,13 @@ def test_loop_over_the_oracle_verify_step_decodes_greedily():
 
 
 @pytest.mark.gpu
-def test_verify_loop_matches_plain_greedy_decoding():
+def test_verify_loop_matches_the_oracles_greedy_decoding():
     import time
+    import oracle
     import moe_decode_megakernel_02_gb300 as mk
     from moe_decode_megakernel_02_gb300 import workload
     from synth import configs
+    import parity
 
     cfg = configs.scaled(configs.VERIFY, n_layers=2)
     B, T, ctx, N = 2, 7, 300, 30
@@ -185,25 +187,27 @@ def test_verify_loop_matches_plain_greedy_decoding():
     first = workload.tokens(cfg, 0, B, 1)[:, 0].astype(np.int32)
     pos0 = np.full(B, ctx, dtype=np.int32)
 
-    # plain greedy: one token per step
-    kv = mk.KVCache(model, B, ctx + 64)
-    workload.prefill(kv, cfg, ctx)
-    logits = torch.empty((B, V), dtype=torch.float32, device="cuda")
+    # reference: the oracle's plain greedy decoding, one token per step
+    om = oracle.Model(cfg)
+    okv = oracle.KV(om, B, ctx + 64)
+    for l in range(cfg["n_layers"]):
+        for b in range(B):
+            okv.write(l, b, 0, parity._prefill_rows(cfg, l, b, ctx))
     tok, pos = first.copy(), pos0.copy()
     ref, gap = [[] for _ in range(B)], [[] for _ in range(B)]
     for _ in range(N):
-        model.decode_step(kv, torch.from_numpy(tok[:, None].copy()).cuda(), torch.from_numpy(pos).cuda(), logits)
-        model.check()
-        top = torch.topk(logits, 2, dim=1)
-        nxt = top.indices[:, 0].cpu().numpy().astype(np.int32)
-        g = (top.values[:, 0] - top.values[:, 1]).cpu().numpy()
+        lg = oracle.decode(om, okv, tok[:, None], pos)["logits"][:, 0]
+        srt = np.sort(lg, axis=1)
+        nxt = lg.argmax(1).astype(np.int32)
         for b in range(B):
             ref[b].append(int(nxt[b]))
-            gap[b].append(float(g[b]))
+            gap[b].append(float(srt[b, -1] - srt[b, -2]))
         tok, pos = nxt, pos + 1
-    kv.close()
+    okv.close()
+    om.close()
 
-    # speculative loop on a fresh cache, drafts = the greedy tokens with planted errors
+    # the speculative loop over the CUDA verify step, drafts = the oracle's
+    # greedy tokens with planted errors
     kv = mk.KVCache(model, B, ctx + 64)
     workload.prefill(kv, cfg, ctx)
     wrong = {3, 4, 12, 20}
@@ -217,12 +221,20 @@ def test_verify_loop_matches_plain_greedy_decoding():
     acc = np.array(loop.accepts)
     print(f"spec loop: {steps} steps, accept per step {acc[:, 0].tolist()}, "
           f"{acc.sum() / dt:.0f} tokens/s with host bookkeeping")
+    first_tie = []
     for b in range(B):
-        # the same tokens as plain greedy decoding; the two may part only where
-        # the plain run's top two logits are within rounding of each other
+        # the GPU loop emits the oracle's greedy tokens; the two may part only
+        # at a token whose top-two oracle logits are within the logit
+        # tolerance of each other (after that the contexts differ)
         n = min(len(loop.emitted[b]), N)
         i = next((i for i in range(n) if loop.emitted[b][i] != ref[b][i]), n)
-        assert i == n or gap[b][i] < 1e-3, (b, i, gap[b][i])
-    # accept lengths implied by the planted errors (before any near-tie): drafts 0..5 with 3 wrong -> 4,
+        assert i == n or gap[b][i] <= 2 * parity.MAX_ABS, (b, i, gap[b][i])
+        first_tie.append(next((j for j in range(N) if gap[b][j] <= 2 * parity.MAX_ABS), N))
+    # accept lengths implied by the planted errors: drafts 0..5 with 3 wrong -> 4,
     # then drafts 4..9 with 4 wrong -> 1, then 5..10 -> 7, then 12..17 with 12 wrong -> 1
-    assert acc[:4, 0].tolist() == [4, 1, 7, 1]
+    # (checked as far as sequence 0's greedy decisions are clear)
+    expect = [4, 1, 7, 1]
+    done = [0, 4, 5, 12, 13]
+    for s_, a in enumerate(expect):
+        if done[s_ + 1] + 1 <= first_tie[0]:
+            assert acc[s_, 0] == a, (s_, acc[:, 0].tolist())
