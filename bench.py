@@ -193,7 +193,8 @@ def cpu_baseline(cfg, B, T, ctx, sample_layers=23, steps=3):
     """Time the oracle (one thread pinned to one core, fp32 accumulation as the
     step is defined) on `sample_layers` layers of the workload and scale to
     the full layer count. Weights and cache are generated before timing (with
-    every core); each timed step decodes the next position."""
+    every core); each timed step decodes the next position with its own
+    token ids."""
     import oracle
     import synth
     sub = configs.scaled(cfg, n_layers=min(sample_layers, cfg["n_layers"]))
@@ -212,8 +213,13 @@ def cpu_baseline(cfg, B, T, ctx, sample_layers=23, steps=3):
     try:
         for i in range(steps):
             t = synth.tokens(cfg["seed"], i + 1, B, T, cfg["vocab"])
+            pos = [ctx + (i + 1) * T] * B
+            # the step's routed experts are generated on first use: run it
+            # once untimed, then time the same step (it rewrites the same
+            # cache rows with the same values)
+            oracle.decode(m, kv, t, pos, precision=32)
             t0 = time.perf_counter()
-            oracle.decode(m, kv, t, [ctx + (i + 1) * T] * B, precision=32)
+            oracle.decode(m, kv, t, pos, precision=32)
             times.append(time.perf_counter() - t0)
     finally:
         os.sched_setaffinity(0, set(cores))
@@ -244,19 +250,23 @@ def run_reference(args, cfg, B, T, ctx, ws, rank):
     print(json.dumps(line), flush=True)
 
 
-def measure(model, kv, cfg, Bm, T, ctx, K, W, ws, stream, with_clocks, local, want_accept=False):
+def measure(model, kv, cfg, Bm, T, ctx, K, W, ws, stream, with_clocks, local, want_accept=False,
+            entry="decode_step"):
     """W warm-up steps, then K timed steps (CUDA events on the launch stream),
     each at the next position(s) with its own token ids; then the same K steps
     replayed untimed to read each one's routing (for its algorithmic bytes);
-    then K end-to-end steps through the public call with host buffers."""
+    then K end-to-end steps through the public call with host buffers.
+    `entry`: decode_step (one launch per step) or decode_step_unfused (one
+    launch per stage, the comparison path)."""
     import torch
+    step = getattr(model, entry)
     V = cfg["vocab"]
     toks = [torch.from_numpy(workload_tokens(cfg, i, Bm, T)).cuda() for i in range(W + K)]
     pos_list = [torch.full((Bm,), ctx + i * T, dtype=torch.int32, device="cuda") for i in range(W + K)]
     logits = torch.empty((Bm * T, V), dtype=torch.float32, device="cuda")
     acc = torch.zeros(Bm, dtype=torch.int32, device="cuda") if want_accept else None
     for i in range(W):
-        model.decode_step(kv, toks[i], pos_list[i], logits, acc)
+        step(kv, toks[i], pos_list[i], logits, acc)
     model.check()
     barrier(ws)
     clk = Clocks(local) if with_clocks else None
@@ -267,7 +277,7 @@ def measure(model, kv, cfg, Bm, T, ctx, K, W, ws, stream, with_clocks, local, wa
     torch.cuda.synchronize()
     start.record(stream)
     for i in range(W, W + K):
-        model.decode_step(kv, toks[i], pos_list[i], logits, acc, stream=stream)
+        step(kv, toks[i], pos_list[i], logits, acc, stream=stream)
     end.record(stream)
     torch.cuda.synchronize()
     ms = start.elapsed_time(end) / K
@@ -279,7 +289,7 @@ def measure(model, kv, cfg, Bm, T, ctx, K, W, ws, stream, with_clocks, local, wa
     # the timed steps again, untimed, for their routing and acceptance
     nbytes, accepted = [], []
     for i in range(W, W + K):
-        model.decode_step(kv, toks[i], pos_list[i], logits, acc)
+        step(kv, toks[i], pos_list[i], logits, acc)
         idx = model.routing(Bm * T)[0] if cfg["n_routed_experts"] else None
         nbytes.append(algorithmic_bytes(cfg, Bm, T, [ctx + i * T] * Bm, idx))
         if want_accept:
@@ -300,7 +310,7 @@ def measure(model, kv, cfg, Bm, T, ctx, K, W, ws, stream, with_clocks, local, wa
     for i in range(K):
         tok_d.copy_(tok_h[i], non_blocking=True)
         pos_d.copy_(pos_h[i], non_blocking=True)
-        model.decode_step(kv, tok_d, pos_d, logits, acc)
+        step(kv, tok_d, pos_d, logits, acc)
         out_h.copy_(logits, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize()
@@ -386,6 +396,12 @@ def main():
     for Bm in deep_batches:
         r = measure(model, kv, cfg, Bm, T, ctx, K, W, ws, stream, False, local)
         extra[f"{cfg['name']}_b{Bm}"] = extra_line(cfg, r, Bm, T)
+    if args.extra == "all":
+        # the same step as one launch per stage (CUDA graph, programmatic
+        # dependent launch): what the single launch buys on this GPU
+        for Bm in sorted({B, 8}):
+            r = measure(model, kv, cfg, Bm, T, ctx, K, W, ws, stream, False, local, entry="decode_step_unfused")
+            extra[f"{cfg['name']}_b{Bm}_unfused"] = extra_line(cfg, r, Bm, T)
     del kv, model
     torch.cuda.empty_cache()
     if args.extra == "all" and not args.layers and args.config == "deep":

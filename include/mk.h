@@ -175,6 +175,27 @@ int mk_kv_read(const mk_kv* kv, int32_t layer, int32_t seq, int32_t pos0, int32_
 int mk_decode_step(mk_model* m, mk_kv* kv, const int32_t* tokens, const int32_t* positions, int32_t batch,
                    int32_t T, float* logits, int32_t* accept, void* stream);
 
+/* The same step as mk_decode_step, run as one kernel launch per stage
+ * instead of one launch for the whole step: the comparison point for what a
+ * single launch buys. The pages contrast a decode step of hundreds of small
+ * kernels, whose boundaries stall the weight stream, with one fused program
+ * (myzaker article, section on fusing hundreds of small kernels into one
+ * program; tanhow.com translation of the Inferact blog, paragraph on kernel
+ * boundaries, CUDA Graphs and programmatic dependent launch). Here each
+ * stage (per layer: the attention projections, attention, its combine, the
+ * output projection, the router, the experts; then the LM head) is its own
+ * launch of the same kernel code, ordered by the stream instead of by
+ * dependency counters, so no stage's weights move before the previous
+ * stage has finished; the launches are replayed from a CUDA graph (captured
+ * on the first call of each shape: kv, batch, T, logits and accept buffers)
+ * with programmatic dependent launch between them. Same arguments, results
+ * and error reporting as mk_decode_step; token ids and positions are copied
+ * into the model's own buffers first (so the graph does not depend on
+ * them). The first call of a shape captures into a private stream and must
+ * not itself be made while `stream` is being captured. */
+int mk_decode_step_unfused(mk_model* m, mk_kv* kv, const int32_t* tokens, const int32_t* positions, int32_t batch,
+                           int32_t T, float* logits, int32_t* accept, void* stream);
+
 /* mk_decode_step without any allocation on the call path. The pages have no
  * counterpart of this entry point: it is for callers that may not allocate
  * device memory while they run -- code inside a host framework that owns a

@@ -23,7 +23,8 @@ HEADER = os.path.join(_ROOT, "include", "mk.h")
 OK, ERR_INVALID_ARG, ERR_OOM, ERR_CUDA, ERR_UNSUPPORTED, ERR_TIMEOUT, ERR_STATE = 0, -1, -2, -3, -4, -5, -6
 ATTN_GQA, ATTN_MLA = 0, 1
 EXPORTS = ("mk_load_weights", "mk_load_synthetic", "mk_alloc_kv", "mk_kv_set_block_table", "mk_kv_pages_per_seq",
-           "mk_kv_write", "mk_kv_read", "mk_decode_step", "mk_decode_step_noalloc", "mk_step_status",
+           "mk_kv_write", "mk_kv_read", "mk_decode_step", "mk_decode_step_unfused", "mk_decode_step_noalloc",
+           "mk_step_status",
            "mk_debug_routing", "mk_debug_scratch_read", "mk_last_argmax", "mk_model_info", "mk_trace_read", "mk_free",
            "mk_last_error")
 TRACE_CAP = 8192
@@ -89,6 +90,7 @@ def lib():
         L.mk_kv_read.argtypes = [P, I32, I32, I32, I32, P, P]
         L.mk_decode_step.argtypes = [P, P, P, P, I32, I32, P, P, P]
         L.mk_decode_step_noalloc.argtypes = [P, P, P, P, I32, I32, P, P, P]
+        L.mk_decode_step_unfused.argtypes = [P, P, P, P, I32, I32, P, P, P]
         L.mk_step_status.argtypes = [P, P]
         L.mk_debug_routing.argtypes = [P, P, P, P, P]
         L.mk_debug_scratch_read.argtypes = [P, ctypes.c_int64, ctypes.c_int64, P, P]
@@ -99,7 +101,8 @@ def lib():
         L.mk_free.restype = None
         L.mk_last_error.restype = ctypes.c_char_p
         for f in ("mk_load_weights", "mk_load_synthetic", "mk_alloc_kv", "mk_kv_set_block_table", "mk_kv_write",
-                  "mk_kv_read", "mk_decode_step", "mk_decode_step_noalloc", "mk_step_status", "mk_debug_routing",
+                  "mk_kv_read", "mk_decode_step", "mk_decode_step_unfused", "mk_decode_step_noalloc", "mk_step_status",
+                  "mk_debug_routing",
                   "mk_debug_scratch_read", "mk_last_argmax", "mk_model_info", "mk_trace_read"):
             getattr(L, f).restype = ctypes.c_int
         _lib = L
@@ -156,6 +159,13 @@ class Model:
         _check(lib().mk_decode_step(self.h, kv.h, tokens.data_ptr(), positions.data_ptr(), B, T,
                                     logits.data_ptr(), None if accept is None else accept.data_ptr(),
                                     _stream(stream)))
+
+    def decode_step_unfused(self, kv, tokens, positions, logits, accept=None, stream=None):
+        """decode_step as one kernel launch per stage (replayed from a CUDA graph): the comparison path."""
+        B, T = tokens.shape
+        _check(lib().mk_decode_step_unfused(self.h, kv.h, tokens.data_ptr(), positions.data_ptr(), B, T,
+                                            logits.data_ptr(), None if accept is None else accept.data_ptr(),
+                                            _stream(stream)))
 
     def decode_step_noalloc(self, kv, tokens, positions, logits, accept=None, stream=None):
         """decode_step with the step's scratch in the library's static device

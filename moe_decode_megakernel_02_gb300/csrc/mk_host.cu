@@ -76,6 +76,11 @@ struct mk_model {
     float* dbg_margin = nullptr;
     int last_M = 0;
     bool last_noalloc = false;  // the last step ran in the static scratch (its routing is not in dbg_*)
+    // one launch per stage (mk_decode_step_unfused): token ids and positions
+    // are copied into these, and a graph of the launches is kept per shape
+    int* u_tok = nullptr;
+    int* u_pos = nullptr;
+    std::map<std::tuple<const void*, int, int, const void*, const void*>, cudaGraphExec_t> graphs;
     const int* last_amax = nullptr;  // argmax of the last step's rows (steps given an accept buffer)
     uint64_t steps = 0;
     uint64_t serial = 0;  // distinct per loaded model in this process
@@ -424,6 +429,7 @@ int mk_load_weights(const mk_config* cfg, const mk_weight* table, int32_t n, voi
     const size_t s_dbgi = D.E ? stake((size_t)L * Mx * D.k * 4) : 0;
     const size_t s_dbgw = D.E ? stake((size_t)L * Mx * D.k * 4) : 0;
     const size_t s_dbgm = D.E ? stake((size_t)L * Mx * 4) : 0;
+    const size_t s_utok = stake(Mx * 4), s_upos = stake((size_t)cfg->max_batch * 4);
     const int rope_dim = D.gqa ? D.hd : D.rd;
     const int npos = cfg->max_ctx + cfg->max_tokens_per_seq;
     const size_t s_rope = stake((size_t)npos * (rope_dim / 2) * 8);
@@ -676,6 +682,8 @@ int mk_load_weights(const mk_config* cfg, const mk_weight* table, int32_t n, voi
         m->dbg_w = reinterpret_cast<float*>(S + s_dbgw);
         m->dbg_margin = reinterpret_cast<float*>(S + s_dbgm);
     }
+    m->u_tok = reinterpret_cast<int*>(S + s_utok);
+    m->u_pos = reinterpret_cast<int*>(S + s_upos);
     CK(cudaStreamSynchronize(s));
     *out = m;
     return MK_OK;
@@ -832,8 +840,10 @@ static void step_router(const mk_model* m, mk::Params& P) {
     ffn_split(m, P.M, P.rfuse, P.gs, P.gr);
 }
 
-int mk_decode_step(mk_model* m, mk_kv* kv, const int32_t* tokens, const int32_t* positions, int32_t batch,
-                   int32_t T, float* logits, int32_t* accept, void* stream) {
+// the step's parameters (everything but the launch-specific fields), after
+// the argument checks every decode entry point shares
+static int step_params(mk_model* m, mk_kv* kv, const int32_t* tokens, const int32_t* positions, int32_t batch,
+                       int32_t T, float* logits, int32_t* accept, mk::Params& P) {
     if (!m || m->magic != MODEL_MAGIC) return fail(MK_ERR_INVALID_ARG, "bad model handle");
     if (!kv || kv->magic != KV_MAGIC) return fail(MK_ERR_INVALID_ARG, "bad kv handle");
     if (kv->m != m) return fail(MK_ERR_STATE, "kv cache belongs to another model");
@@ -842,7 +852,7 @@ int mk_decode_step(mk_model* m, mk_kv* kv, const int32_t* tokens, const int32_t*
     if (T < 1 || T > m->cfg.max_tokens_per_seq) return fail(MK_ERR_INVALID_ARG, "T %d out of range", T);
     if (accept && T < 2) return fail(MK_ERR_INVALID_ARG, "accept needs T > 1");
     if (fault("bad_arg")) return fail(MK_ERR_INVALID_ARG, "arguments rejected (injected by MK_FAULT=bad_arg)");
-    mk::Params P = m->base;
+    P = m->base;
     P.page_elems = (long long)kv->page_elems;
     P.pps = kv->pps;
     P.btab = kv->btab;
@@ -856,7 +866,6 @@ int mk_decode_step(mk_model* m, mk_kv* kv, const int32_t* tokens, const int32_t*
     P.T = T;
     P.M = batch * T;
     step_router(m, P);
-    P.stall = getenv("MK_TEST_STALL") != nullptr;
     P.logits = logits;
     P.accept = accept;
     P.lm.dst = logits;
@@ -864,15 +873,120 @@ int mk_decode_step(mk_model* m, mk_kv* kv, const int32_t* tokens, const int32_t*
         P.zptr[P.nz] = logits;
         P.zn[P.nz++] = (long long)P.M * P.V;
     }
-    P.parity = (int)(m->steps & 1);
     P.dbg_idx = m->dbg_idx;
     P.dbg_w = m->dbg_w;
     P.dbg_margin = m->dbg_margin;
+    return MK_OK;
+}
+
+int mk_decode_step(mk_model* m, mk_kv* kv, const int32_t* tokens, const int32_t* positions, int32_t batch,
+                   int32_t T, float* logits, int32_t* accept, void* stream) {
+    mk::Params P;
+    if (const int rc = step_params(m, kv, tokens, positions, batch, T, logits, accept, P)) return rc;
+    P.stall = getenv("MK_TEST_STALL") != nullptr;
+    P.parity = (int)(m->steps & 1);
     cudaStream_t s = (cudaStream_t)stream;
     void* args[] = {&P};
     CK(cudaLaunchCooperativeKernel((const void*)mk::megakernel, dim3(m->G), dim3(mk::NTHREADS), args,
                                    mk::SMEM_TOTAL, s));
     m->steps++;
+    m->last_M = P.M;
+    m->last_noalloc = false;
+    m->last_amax = accept ? P.amax : nullptr;
+    return MK_OK;
+}
+
+// the launches of one step run as one launch per stage: (staged, first, end)
+// program positions; stages the model or this step does not have are left
+// out, and stages that read only the same earlier results share a launch
+static std::vector<std::tuple<int, int, int>> stage_windows(const mk_model* m, const mk::Params& P) {
+    using namespace mk;
+    std::vector<std::tuple<int, int, int>> w;
+    w.emplace_back(2, 0, 0);  // set-up: embedding, accumulators zeroed
+    const int L = P.L;
+    const bool mla = P.attn == 1;
+    auto win = [&](int l, int a, int b) { w.emplace_back(1, prog_index(P, l, a), prog_index(P, l, b)); };
+    for (int l = 0; l < L; ++l) {
+        win(l, S_A, S_A + 1);
+        if (mla) {
+            win(l, S_QB, S_APP + 1);  // the latent append reads only A's output
+            win(l, S_QLAT, S_QLAT + 1);
+        }
+        win(l, S_ATTN, S_ATTN + 1);
+        win(l, S_COMB, S_COMB + 1);
+        if (mla) win(l, S_UV, S_UV + 1);
+        win(l, S_O, S_O + 1);
+        const bool router = P.E > 0 && !P.rfuse;
+        if (router || P.carry) win(l, S_ROUTER, S_CARRY + 1);  // both read only O's output
+        win(l, S_FFN, S_FFN + 1);
+    }
+    w.emplace_back(1, prog_index(P, L, S_LM), prog_index(P, L, S_LM + 1));
+    if (P.accept) {  // acceptance reads every row's argmax: a launch of its own
+        w.emplace_back(1, prog_index(P, L, S_AMAX), prog_index(P, L, S_AMAX + 1));
+        w.emplace_back(1, prog_index(P, L, S_ACCEPT), prog_index(P, L, S_ACCEPT + 1));
+    }
+    (void)m;
+    return w;
+}
+
+int mk_decode_step_unfused(mk_model* m, mk_kv* kv, const int32_t* tokens, const int32_t* positions, int32_t batch,
+                           int32_t T, float* logits, int32_t* accept, void* stream) {
+    mk::Params P;
+    if (const int rc = step_params(m, kv, tokens, positions, batch, T, logits, accept, P)) return rc;
+    cudaStream_t s = (cudaStream_t)stream;
+    // the graph reads the token ids and positions from the model's own
+    // buffers, so one graph serves every call of the same shape
+    CK(cudaMemcpyAsync(m->u_tok, tokens, (size_t)P.M * 4, cudaMemcpyDefault, s));
+    CK(cudaMemcpyAsync(m->u_pos, positions, (size_t)batch * 4, cudaMemcpyDefault, s));
+    P.tokens = m->u_tok;
+    P.pos = m->u_pos;
+    P.trace = nullptr;
+    P.trace_n = nullptr;
+    P.trace_items = 0;
+    P.parity = 0;
+    const auto key = std::make_tuple((const void*)kv, batch, T, (const void*)logits, (const void*)accept);
+    auto it = m->graphs.find(key);
+    if (it == m->graphs.end()) {
+        cudaStream_t cs;
+        CK(cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking));
+        cudaGraph_t g = nullptr;
+        CK(cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal));
+        int rc = MK_OK;
+        for (const auto& wdw : stage_windows(m, P)) {
+            mk::Params Q = P;
+            Q.staged = std::get<0>(wdw);
+            Q.st_lo = std::get<1>(wdw);
+            Q.st_hi = std::get<2>(wdw);
+            cudaLaunchConfig_t lc = {};
+            lc.gridDim = dim3(m->G);
+            lc.blockDim = dim3(mk::NTHREADS);
+            lc.dynamicSmemBytes = mk::SMEM_TOTAL;
+            lc.stream = cs;
+            cudaLaunchAttribute at[1];
+            at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            at[0].val.programmaticStreamSerializationAllowed = 1;
+            lc.attrs = at;
+            lc.numAttrs = 1;
+            const cudaError_t e = cudaLaunchKernelEx(&lc, mk::megakernel, Q);
+            if (e != cudaSuccess) {
+                rc = fail(MK_ERR_CUDA, "staged launch: %s", cudaGetErrorString(e));
+                break;
+            }
+        }
+        const cudaError_t ee = cudaStreamEndCapture(cs, &g);
+        cudaStreamDestroy(cs);
+        if (rc) {
+            if (g) cudaGraphDestroy(g);
+            return rc;
+        }
+        if (ee != cudaSuccess) return fail(MK_ERR_CUDA, "stage graph capture: %s", cudaGetErrorString(ee));
+        cudaGraphExec_t ex = nullptr;
+        const cudaError_t ie = cudaGraphInstantiate(&ex, g, 0);
+        cudaGraphDestroy(g);
+        if (ie != cudaSuccess) return fail(MK_ERR_CUDA, "stage graph instantiate: %s", cudaGetErrorString(ie));
+        it = m->graphs.emplace(key, ex).first;
+    }
+    CK(cudaGraphLaunch(it->second, s));
     m->last_M = P.M;
     m->last_noalloc = false;
     m->last_amax = accept ? P.amax : nullptr;
@@ -955,6 +1069,7 @@ void mk_free(void* h) {
     } else if (magic == MODEL_MAGIC) {
         mk_model* m = static_cast<mk_model*>(h);
         m->magic = 0;
+        for (auto& g : m->graphs) cudaGraphExecDestroy(g.second);
         cudaFree(m->wblob);
         cudaFree(m->sblob);
         cudaFree(m->d_layers);

@@ -136,7 +136,7 @@ __device__ bool cwait(Ctx& c, unsigned where) {
 // release, which is cumulative over them)
 __device__ void csignal(Ctx& c, int layer, int which, unsigned n) {
     cbar();
-    if (threadIdx.x == 0 && n) red_release(ctr_of(c.p, layer, which), n);
+    if (threadIdx.x == 0 && n && !c.p.staged) red_release(ctr_of(c.p, layer, which), n);
     if (*(volatile int*)&c.ms.abort) c.dead = true;
 }
 
@@ -279,31 +279,75 @@ __device__ __noinline__ void stage_input(Ctx& c, const Gemv& g, const float* src
         stage_input_small(c, g, src, g.in_kind == IN_RMS ? 0 : grp_off, k0, m0, ms);
         return;
     }
+    if (g.in_kind == IN_COPY || (g.in_kind == IN_RMS && g.n_kc == 1)) {
+        // several tokens' rows: every 16-byte piece is in flight at once
+        // (one L2 round trip instead of one per loop iteration), then the
+        // RMSNorm, if any, works on the copy in shared memory
+        const int off = g.in_kind == IN_RMS ? 0 : grp_off;
+        for (int i = tid * 4; i < total; i += NCT * 4) {
+            const int t = i / Kc, k = i - t * Kc;
+            cp_async16(xs + i, src + (size_t)(m0 + t) * g.src_stride + off + k0 + k);
+        }
+        cp_async_wait_all();
+        cbar();
+        if (g.in_kind == IN_COPY) return;
+        // c.ms.rms[] was zeroed by restage() before its leading barrier; a
+        // warp's 128 consecutive floats never straddle a row (rows are
+        // multiples of 128 floats), so `t` changes uniformly in the warp
+        float* acc = c.ms.rms;
+        float part = 0.f;
+        int cur = -1;
+        for (int i = tid * 4; i < total; i += NCT * 4) {
+            const int t = i / Kc;
+            const float4 v = *reinterpret_cast<const float4*>(xs + i);
+            if (t != cur) {
+                if (cur >= 0) {
+#pragma unroll
+                    for (int o = 16; o; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+                    if (lane == 0) atomicAdd(&acc[cur], part);
+                }
+                part = 0.f;
+                cur = t;
+            }
+            part = fmaf(v.x, v.x, part);
+            part = fmaf(v.y, v.y, part);
+            part = fmaf(v.z, v.z, part);
+            part = fmaf(v.w, v.w, part);
+        }
+        if (cur >= 0) {
+#pragma unroll
+            for (int o = 16; o; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+            if (lane == 0) atomicAdd(&acc[cur], part);
+        }
+        cbar();
+        const float invK = 1.0f / (float)g.K;
+#pragma unroll 4
+        for (int i = tid * 4; i < total; i += NCT * 4) {
+            const int t = i / Kc, k = i - t * Kc;
+            const float r = 1.0f / sqrtf(acc[t] * invK + p.eps);
+            const uint2 gw = __ldg(reinterpret_cast<const uint2*>(g.gain + k));
+            float4 o = *reinterpret_cast<const float4*>(xs + i);
+            o.x = o.x * bf_lo(gw.x) * r;
+            o.y = o.y * bf_hi(gw.x) * r;
+            o.z = o.z * bf_lo(gw.y) * r;
+            o.w = o.w * bf_hi(gw.y) * r;
+            *reinterpret_cast<float4*>(xs + i) = o;
+        }
+        return;
+    }
     if (g.in_kind == IN_RMS) {
         // c.ms.rms[] was zeroed by restage() before its leading barrier.
-        // Whole row staged (one K panel): one pass loads activations and
-        // gains together, stores x*gain and accumulates the sum of squares;
-        // the second pass only scales by 1/rms. Split panels: the sum of
-        // squares runs over the whole row first.
+        // Split panels (the K panel is part of the row): the sum of squares
+        // runs over the whole row first, then the panel is scaled.
         float* acc = c.ms.rms;
-        const bool whole = g.n_kc == 1;
         const int rowlen = g.K, tot = ms * rowlen;
         const uint16_t* gain = g.gain;
         float part = 0.f;
         int cur = -1;
 #pragma unroll 4
         for (int i = tid * 4; i < tot; i += NCT * 4) {
-            const int t = i / rowlen, k = i - t * rowlen;
-            const float4 v = __ldcg(reinterpret_cast<const float4*>(src + (size_t)(m0 + t) * g.src_stride + k));
-            if (whole) {
-                const uint2 gw = __ldg(reinterpret_cast<const uint2*>(gain + k));
-                float4 o;
-                o.x = v.x * bf_lo(gw.x);
-                o.y = v.y * bf_hi(gw.x);
-                o.z = v.z * bf_lo(gw.y);
-                o.w = v.w * bf_hi(gw.y);
-                *reinterpret_cast<float4*>(xs + i) = o;
-            }
+            const int t = i / rowlen;
+            const float4 v = __ldcg(reinterpret_cast<const float4*>(src + (size_t)(m0 + t) * g.src_stride + i - t * rowlen));
             // a warp's 128 consecutive floats never straddle a row (rows are
             // multiples of 128 floats), so `t` changes uniformly in the warp
             if (t != cur) {
@@ -331,29 +375,14 @@ __device__ __noinline__ void stage_input(Ctx& c, const Gemv& g, const float* src
         for (int i = tid * 4; i < total; i += NCT * 4) {
             const int t = i / Kc, k = i - t * Kc;
             const float r = 1.0f / sqrtf(acc[t] * invK + p.eps);
+            const float4 v = __ldcg(reinterpret_cast<const float4*>(src + (size_t)(m0 + t) * g.src_stride + k0 + k));
+            const uint2 gw = __ldg(reinterpret_cast<const uint2*>(gain + k0 + k));
             float4 o;
-            if (whole) {
-                o = *reinterpret_cast<const float4*>(xs + i);
-                o.x *= r;
-                o.y *= r;
-                o.z *= r;
-                o.w *= r;
-            } else {
-                const float4 v = __ldcg(reinterpret_cast<const float4*>(src + (size_t)(m0 + t) * g.src_stride + k0 + k));
-                const uint2 gw = __ldg(reinterpret_cast<const uint2*>(gain + k0 + k));
-                o.x = v.x * bf_lo(gw.x) * r;
-                o.y = v.y * bf_hi(gw.x) * r;
-                o.z = v.z * bf_lo(gw.y) * r;
-                o.w = v.w * bf_hi(gw.y) * r;
-            }
+            o.x = v.x * bf_lo(gw.x) * r;
+            o.y = v.y * bf_hi(gw.x) * r;
+            o.z = v.z * bf_lo(gw.y) * r;
+            o.w = v.w * bf_hi(gw.y) * r;
             *reinterpret_cast<float4*>(xs + i) = o;
-        }
-    } else if (g.in_kind == IN_COPY) {
-#pragma unroll 4
-        for (int i = tid * 4; i < total; i += NCT * 4) {
-            const int t = i / Kc, k = i - t * Kc;
-            *reinterpret_cast<float4*>(xs + i) =
-                __ldcg(reinterpret_cast<const float4*>(src + (size_t)(m0 + t) * g.src_stride + grp_off + k0 + k));
         }
     } else {  // IN_SWIGLU: h = silu(gate) * up
 #pragma unroll 4
@@ -2357,10 +2386,15 @@ __device__ __noinline__ bool init_phase(Ctx& c) {
             return false;
         }
     }
+    // one launch per stage: only the set-up launch initialises the step
+    if (p.staged == 1) return !c.dead;
     const size_t gtid = (size_t)blockIdx.x * NCT + tid, gstride = (size_t)p.G * NCT;
     // counters of the other parity are used by the next step: clear them now
-    unsigned* other = p.ctr + (size_t)(p.parity ^ 1) * (p.L + 1) * NCTR;
-    for (size_t i = gtid; i < (size_t)(p.L + 1) * NCTR; i += gstride) other[i] = 0u;
+    // (one launch per stage uses no counters and leaves them as they are)
+    if (!p.staged) {
+        unsigned* other = p.ctr + (size_t)(p.parity ^ 1) * (p.L + 1) * NCTR;
+        for (size_t i = gtid; i < (size_t)(p.L + 1) * NCTR; i += gstride) other[i] = 0u;
+    }
     for (int z = 0; z < p.nz; ++z)
         for (size_t i = gtid; i < (size_t)p.zn[z]; i += gstride) p.zptr[z][i] = 0.f;
     float* x0 = p.layers[0].x;
@@ -2883,6 +2917,12 @@ enum StageId {
     S_NLAYER, S_LM = S_NLAYER, S_AMAX, S_ACCEPT, S_END
 };
 
+// position of (layer, stage) in the program: layer stages l * S_NLAYER + st,
+// then the head's stages from L * S_NLAYER on
+__host__ __device__ __forceinline__ int prog_index(const Params& p, int l, int st) {
+    return l * S_NLAYER + (l < p.L ? st : st - S_LM);
+}
+
 template <bool PROD>
 __device__ __noinline__ bool exec_stage(Ctx& c) {
     const Params& p = c.p;
@@ -2891,6 +2931,7 @@ __device__ __noinline__ bool exec_stage(Ctx& c) {
     }
     const int l = c.pl, st = c.pst;
     if (st == S_END) return false;
+    if (p.staged && prog_index(p, l, st) >= p.st_hi) return false;
     {
         int nl = l, nst = st + 1;
         if (l < p.L && nst == S_NLAYER) {
@@ -3128,15 +3169,40 @@ __global__ void __launch_bounds__(NTHREADS, 1) megakernel(const __grid_constant_
     if ((threadIdx.x & 31) == 0) new (cx) Ctx(*reinterpret_cast<const Params*>(smem + SMEM_PARAMS), smem);
     __syncwarp();
     Ctx& c = *cx;
-    if (threadIdx.x >= NCT) {
-        if (prod_check(c.p))
-            while (exec_stage<true>(c)) {
+    if (p.staged) {
+        // one launch per stage: the previous launch's results must be visible
+        // before this one reads anything it wrote (programmatic dependent
+        // launch lets this launch's set-up above overlap the previous one's
+        // tail); then start at the window's first stage with that layer's
+        // descriptors in place
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+        if (p.staged == 1) {
+            int l = p.st_lo / S_NLAYER, st = p.st_lo - l * S_NLAYER;
+            if (l >= p.L) {
+                l = p.L;
+                st = p.st_lo - p.L * S_NLAYER + S_LM;
             }
-        else
+            c.set_pos(l, st);
+            if (l < p.L && st != S_A) {
+                if (threadIdx.x >= NCT)
+                    load_layer<true>(c, l);
+                else
+                    load_layer<false>(c, l);
+            }
+        }
+    }
+    if (threadIdx.x >= NCT) {
+        if (prod_check(c.p)) {
+            if (p.staged != 2)
+                while (exec_stage<true>(c)) {
+                }
+        } else {
             c.dead = true;
+        }
         if (c.dead) prod_drain(c);
     } else {
-        if (init_phase(c))
+        if (init_phase(c) && p.staged != 2)
             while (exec_stage<false>(c)) {
             }
     }

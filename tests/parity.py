@@ -16,7 +16,9 @@ MEAN_ABS = 2e-3
 
 
 def run_gpu(cfg, B, T, steps, ctx, positions_fn=None, tokens_fn=None, block_table=None, want_accept=False,
-            max_ctx=None):
+            max_ctx=None, entry="decode_step"):
+    """`entry`: the Model method that runs the step (decode_step: one launch;
+    decode_step_unfused: one launch per stage)."""
     import torch
 
     import moe_decode_megakernel_02_gb300 as mk
@@ -34,8 +36,8 @@ def run_gpu(cfg, B, T, steps, ctx, positions_fn=None, tokens_fn=None, block_tabl
     for s in range(steps):
         tok = tokens_fn(s) if tokens_fn else workload.tokens(cfg, s, B, T)
         pos = positions_fn(s) if positions_fn else np.full(B, ctx + s * T, dtype=np.int32)
-        model.decode_step(kv, torch.from_numpy(np.ascontiguousarray(tok, dtype=np.int32)).cuda(),
-                          torch.from_numpy(np.ascontiguousarray(pos, dtype=np.int32)).cuda(), logits, acc)
+        getattr(model, entry)(kv, torch.from_numpy(np.ascontiguousarray(tok, dtype=np.int32)).cuda(),
+                              torch.from_numpy(np.ascontiguousarray(pos, dtype=np.int32)).cuda(), logits, acc)
         model.check()
         res = dict(tokens=np.array(tok), positions=np.array(pos),
                    logits=logits.cpu().numpy().astype(np.float64).reshape(B, T, -1))

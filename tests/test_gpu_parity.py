@@ -210,3 +210,15 @@ def test_two_slot_ring_build_parity():
                        capture_output=True, text=True, timeout=1200)
     print(r.stdout[-2000:])
     assert r.returncode == 0, r.stdout[-4000:] + r.stderr[-2000:]
+
+
+@pytest.mark.parametrize("name,B,T,steps", [("tiny", 1, 1, 3), ("mid", 4, 1, 1), ("deep", 2, 1, 2),
+                                            ("verify", 8, 7, 1), ("dense", 1, 1, 1)])
+def test_unfused_one_launch_per_stage(name, B, T, steps):
+    # the comparison path: the same stages, each its own launch (a CUDA graph
+    # replayed per step), ordered by the stream instead of counters
+    cfg = configs.ALL[name]
+    if name != "tiny":
+        cfg = configs.scaled(cfg, n_layers=2)
+    ctx = min(cfg["ctx"], 2000)
+    _run(cfg, B, T, steps, ctx, entry="decode_step_unfused", want_accept=T > 1)
