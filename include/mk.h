@@ -122,7 +122,11 @@ typedef struct mk_info {
  * router logits of their rows, and the step has no separate router stage.
  * With the environment variable MK_ROUTER_STAGE=1 set at this call, the
  * model always keeps the separate router stage (the schedule used
- * otherwise); results agree within rounding. */
+ * otherwise); results agree within rounding. Likewise, for MLA models and
+ * steps of at most 16 tokens, the CTAs of the query up-projection also apply
+ * the absorbed key projection, and the CTAs that merge the attention splits
+ * also apply the value up-projection; MK_QLAT_STAGE=1 and MK_UV_STAGE=1 keep
+ * those as stages of their own. */
 int mk_load_weights(const mk_config* cfg, const mk_weight* table, int32_t n, void* stream, mk_model** out);
 
 /* mk_load_weights over seeded synthetic weights generated in device memory:

@@ -112,6 +112,8 @@ struct Layer {
     Gemv g[NG];
     Ffn ffn;
     const uint16_t* kv_norm;  // MLA latent RMSNorm gain
+    const uint16_t* uk;       // MLA: W_uk per head [H][nope][kl] (the absorbed query folded into QB)
+    const uint16_t* uvq;      // MLA: W_uv per head and latent quarter [H][4][vd][kl/4] (UV folded into COMB)
     const float* a;           // GQA: q|k|v   MLA: c_q | latent | k_rope   [M][a_stride]
     const float* q;           // MLA: q_b output [M][H*(nope+rope)]
     const float* qlat;        // MLA: absorbed queries [M][H*kl]
@@ -164,6 +166,8 @@ struct Params {
     // the stream, so no dependency counter is waited on or signalled.
     int staged, st_lo, st_hi;
     int rfuse;                      // router logits accumulated by the output projection's CTAs (no router stage)
+    int qfuse;                      // MLA: the absorbed query computed by the QB CTAs (no QLAT stage)
+    int ufuse;                      // MLA: the value up-projection computed by the combine CTAs (no UV stage)
     float* racc;                    // their accumulators [L][ROUTER_COPIES][M][router_row(E)], zero at step start
     float* ubuf;                    // per CTA: expert-unit gate/up and hidden values when shared memory is short
     long long ubuf_stride;          // floats per CTA
@@ -207,6 +211,11 @@ struct Misc {
     // units, which take only the tokens routed to the expert)
     uint8_t gt[MAX_M];
     int gm;
+    // 0: staging row = token id (all tokens staged, or a consecutive range);
+    // otherwise a key of the token map (routed expert + 1, or 1024 + first
+    // token of a shared-expert token group) and staging row i holds the
+    // map's token gt[m0 + i] (the map's tokens gathered, m0 the first staged)
+    int gather;
     long long tdbg[4];              // trace: clock64 marks of the expert-unit gate/up GEMV
     int abort;
     int n_slots, p_nslots;
@@ -424,6 +433,15 @@ __device__ __forceinline__ void my_range_sub(int n, int c0, int gc, int& lo, int
 }
 
 __device__ __forceinline__ int gemv_items(const Gemv& g) { return g.n_rb * g.n_kc; }
+
+// tokens per work item of the shared expert (M tokens, FFN input in n_kc K
+// panels of Kc): 4 when every token's input fits the staging area at once,
+// as many as fit when it does not (each group gathered), else all
+__host__ __device__ __forceinline__ int shared_group(int M, int n_kc, int Kc) {
+    if (M <= 1 || n_kc != 1) return M < 1 ? 1 : M;
+    if (M * Kc <= STAGE_FLOATS) return M > 4 ? 4 : M;
+    return STAGE_FLOATS / Kc;
+}
 
 // attention splits: units = prefix chunks + 1 tail unit (the new positions)
 __device__ __forceinline__ int gqa_target(const Params& p) {

@@ -68,6 +68,8 @@ struct mk_model {
     mk::Layer* d_layers = nullptr;
     mk::Params base;  // everything except the per-step fields
     bool rfuse_ok;    // the router can be folded into the output projection
+    bool qfuse_ok;    // MLA: the absorbed query can be computed by the QB CTAs
+    bool ufuse_ok;    // MLA: the value up-projection can be computed by the combine CTAs
     unsigned* ctr = nullptr;
     size_t ctr_n = 0;
     unsigned* status = nullptr;
@@ -256,6 +258,22 @@ __global__ void transpose_heads(const uint16_t* __restrict__ in, uint16_t* __res
     }
 }
 
+// W_uv per head and latent quarter, j-major: out[h][q][j][v] = W_uv[h][v][128 q + j]
+// (from the canonical [H*(nope+vd)][kl] W_ukv, whose head h holds its W_uk
+// rows, then its W_uv rows)
+__global__ void pack_uv_quarters(uint16_t* __restrict__ out, const uint16_t* __restrict__ wukv, int H, int nope,
+                                 int vd, int kl) {
+    const size_t n = (size_t)H * vd * kl, per_h = (size_t)vd * kl, per_q = (size_t)128 * vd;
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+        const int h = (int)(i / per_h);
+        const size_t r = i - h * per_h;
+        const int q = (int)(r / per_q);
+        const size_t r2 = r - q * per_q;
+        const int j = (int)(r2 / vd), v = (int)(r2 - (size_t)j * vd);
+        out[i] = wukv[((size_t)h * (nope + vd) + nope + v) * kl + (size_t)q * 128 + j];
+    }
+}
+
 __global__ void kv_scatter(uint16_t* pool, const int* btab, int pps, size_t page_elems, int gqa, int Hkv, int hd,
                            int kl, int rd, int seq, int pos0, int n, int row, uint16_t* rows, int to_cache) {
     const size_t total = (size_t)n * row;
@@ -358,7 +376,7 @@ int mk_load_weights(const mk_config* cfg, const mk_weight* table, int32_t n, voi
 
     // ---- packed weight layout ----
     const int L = D.L, d = D.d;
-    struct Off { size_t a, qn, kvn, uq, ukT, uv, o, router, gu, down, shgu, shdown, an, fn; };
+    struct Off { size_t a, qn, kvn, uq, ukT, uk, uv, uvq, o, router, gu, down, shgu, shdown, an, fn; };
     std::vector<Off> lo(L);
     size_t cur = 0;
     auto take = [&](size_t elems) { size_t o = cur; cur += align256(elems * 2) / 2; return o; };
@@ -373,6 +391,8 @@ int mk_load_weights(const mk_config* cfg, const mk_weight* table, int32_t n, voi
             o.kvn = take(D.kl);
             o.uq = take((size_t)D.Hq * D.qh * D.ql);
             o.ukT = take((size_t)D.Hq * D.kl * D.nope);
+            o.uk = take((size_t)D.Hq * D.nope * D.kl);
+            o.uvq = take((size_t)D.Hq * D.vd * D.kl);
             o.uv = take((size_t)D.Hq * D.vd * D.kl);
         }
         o.o = take((size_t)d * D.o_in);
@@ -495,6 +515,10 @@ int mk_load_weights(const mk_config* cfg, const mk_weight* table, int32_t n, voi
             CK(cudaMemcpyAsync(tmp, p, (size_t)D.Hq * (D.nope + D.vd) * D.kl * 2, cudaMemcpyDefault, s));
             transpose_heads<<<512, 256, 0, s>>>(tmp, W + o.ukT, D.Hq, D.nope, D.nope + D.vd, D.kl);
             CK(cudaGetLastError());
+            CK(cudaMemcpy2DAsync(W + o.uk, (size_t)D.nope * D.kl * 2, tmp, (size_t)(D.nope + D.vd) * D.kl * 2,
+                                 (size_t)D.nope * D.kl * 2, D.Hq, cudaMemcpyDeviceToDevice, s));
+            pack_uv_quarters<<<512, 256, 0, s>>>(W + o.uvq, tmp, D.Hq, D.nope, D.vd, D.kl);
+            CK(cudaGetLastError());
             CK(cudaMemcpy2DAsync(W + o.uv, (size_t)D.vd * D.kl * 2, tmp + (size_t)D.nope * D.kl,
                                  (size_t)(D.nope + D.vd) * D.kl * 2, (size_t)D.vd * D.kl * 2, D.Hq,
                                  cudaMemcpyDeviceToDevice, s));
@@ -575,6 +599,8 @@ int mk_load_weights(const mk_config* cfg, const mk_weight* table, int32_t n, voi
             Ld.qlat = qlat;
             Ld.olat = olat;
             Ld.kv_norm = W + o.kvn;
+            Ld.uk = W + o.uk;
+            Ld.uvq = W + o.uvq;
             make_gemv(Ld.g[mk::G_QB], W + o.uq, D.Hq * D.qh, D.ql, mk::IN_RMS, a, D.a_rows, W + o.qn, mk::OUT_STORE,
                       q, D.Hq * D.qh);
             make_gemv(Ld.g[mk::G_QLAT], W + o.ukT, D.Hq * D.kl, D.nope, mk::IN_COPY, q, D.Hq * D.qh, nullptr,
@@ -669,6 +695,22 @@ int mk_load_weights(const mk_config* cfg, const mk_weight* table, int32_t n, voi
                       (2 * per_cta * go.R + mk::router_row(D.E)) * Mx <= mk::STAGE_FLOATS && !(ev && atoi(ev) > 0);
         P.rfuse = 0;  // per step
         P.racc = D.E ? F(s_racc) : nullptr;
+    }
+    // the absorbed query folded into QB: QB tiles of 16 rows that never
+    // straddle a head's nope and rope rows, one K panel, and every CTA with
+    // an item of A (those CTAs clear q_lat before QB adds into it)
+    if (!D.gqa) {
+        const mk::Gemv& gq = m->layers[0].g[mk::G_QB];
+        const char* ev = getenv("MK_QLAT_STAGE");
+        m->qfuse_ok = gq.n_kc == 1 && gq.R == 16 && D.nope % gq.R == 0 && D.qh % gq.R == 0 &&
+                      gemv_items_host(m->layers[0].g[mk::G_A]) >= m->G && !(ev && atoi(ev) > 0);
+        // the value up-projection folded into the combine: a slab of 128
+        // latent dimensions x vd fits a ring slot, two values per thread
+        const char* eu = getenv("MK_UV_STAGE");
+        m->ufuse_ok = D.vd % 2 == 0 && D.vd <= 128 && 128 * D.vd * 2 <= mk::SLOT_BYTES &&
+                      gemv_items_host(m->layers[0].g[mk::G_A]) >= m->G && !(eu && atoi(eu) > 0);
+    } else {
+        m->qfuse_ok = m->ufuse_ok = false;
     }
     P.nz = nz;  // logits (split-K head) are added per step in mk_decode_step
     m->ctr = reinterpret_cast<unsigned*>(S + s_ctr);
@@ -814,14 +856,14 @@ static void ffn_split(const mk_model* m, int M, bool rfuse, int& gs, int& gr) {
     // a unit's time grows with its token count (the weights stream once, the
     // arithmetic is per token): about 1 + 0.8 (t - 1) tile times for t tokens.
     // A routed expert's units take only its own tokens (M k / distinct on
-    // average) and the shared expert's run per group of 4 tokens when all
-    // tokens' input is staged in one K panel.
+    // average) when its input is one K panel, and the shared expert's run
+    // once per token group (mk::shared_group).
     const auto cost = [](double t) { return 1.0 + 0.8 * (t - 1.0); };
     const double uniq = D.E * (1.0 - std::pow(1.0 - (double)D.k / D.E, (double)M));
-    const bool stage_all = M > 1 && L0.ffn.n_kc == 1 && M * L0.ffn.Kc <= mk::STAGE_FLOATS;
-    const int ntg = M > 4 && stage_all ? (M + 3) / 4 : 1;
-    const double us = L0.ffn.k[1].nu * ntg * cost(ntg > 1 ? M / (double)ntg : M);
-    const double ur = uniq * L0.ffn.k[0].nu * cost(stage_all ? M * D.k / uniq : M);
+    const int tgs = mk::shared_group(M, L0.ffn.n_kc, L0.ffn.Kc);
+    const int ntg = (M + tgs - 1) / tgs;
+    const double us = L0.ffn.k[1].nu * ntg * cost(M / (double)ntg);
+    const double ur = uniq * L0.ffn.k[0].nu * cost(M > 1 && L0.ffn.n_kc == 1 ? M * D.k / uniq : M);
     const int avail = m->G - gr;
     gs = (int)std::lround(avail * us / (us + ur));
     if (gs < 1) gs = 1;
@@ -876,6 +918,11 @@ static int step_params(mk_model* m, mk_kv* kv, const int32_t* tokens, const int3
     P.dbg_idx = m->dbg_idx;
     P.dbg_w = m->dbg_w;
     P.dbg_margin = m->dbg_margin;
+    // every token's c_q staged at once, one tile's outputs per thread
+    P.qfuse = m->qfuse_ok && P.M * P.ql <= mk::STAGE_FLOATS && P.M * m->layers[0].g[mk::G_QB].R <= mk::NCT;
+    // the combine's items are per token: each reads its 32 KB slab of W_uv,
+    // so for many tokens the separate stage (W_uv read once) is cheaper
+    P.ufuse = m->ufuse_ok && P.M <= 16;
     return MK_OK;
 }
 
@@ -910,11 +957,11 @@ static std::vector<std::tuple<int, int, int>> stage_windows(const mk_model* m, c
         win(l, S_A, S_A + 1);
         if (mla) {
             win(l, S_QB, S_APP + 1);  // the latent append reads only A's output
-            win(l, S_QLAT, S_QLAT + 1);
+            if (!P.qfuse) win(l, S_QLAT, S_QLAT + 1);
         }
         win(l, S_ATTN, S_ATTN + 1);
         win(l, S_COMB, S_COMB + 1);
-        if (mla) win(l, S_UV, S_UV + 1);
+        if (mla && !P.ufuse) win(l, S_UV, S_UV + 1);
         win(l, S_O, S_O + 1);
         const bool router = P.E > 0 && !P.rfuse;
         if (router || P.carry) win(l, S_ROUTER, S_CARRY + 1);  // both read only O's output

@@ -35,7 +35,7 @@ struct alignas(16) Ctx {
     // what the staging buffer currently holds
     const void* sk_src;
     const void* sk_gain;
-    int sk_off, sk_kc, sk_m0, sk_kind;
+    int sk_off, sk_kc, sk_m0, sk_kind, sk_gather;
     int issued;  // producer: ring fills issued
     long long t_start;
     unsigned cur_code;  // trace: stage being run
@@ -49,7 +49,7 @@ struct alignas(16) Ctx {
         pr.phase = 0;
         sk_src = nullptr;
         sk_gain = nullptr;
-        sk_off = sk_kc = sk_m0 = sk_kind = -1;
+        sk_off = sk_kc = sk_m0 = sk_kind = sk_gather = -1;
         issued = 0;
         pl = pst = 0;
         n_down = n_shdown = n_carry = 0;
@@ -195,6 +195,13 @@ __device__ __forceinline__ void trace_rec_any(Ctx& c, unsigned code, unsigned n,
 
 // =============================================================== GEMV ====
 
+// the global token row staged at staging row t (first staged entry m0)
+__device__ __forceinline__ int staged_token(const Misc& ms, int m0, int t) {
+    return ms.gather ? (int)ms.gt[m0 + t] : m0 + t;
+}
+// the staging row of token-map entry i when entries [0, ...) are staged
+__device__ __forceinline__ int staging_row(const Misc& ms, int i) { return ms.gather ? i : (int)ms.gt[i]; }
+
 // fill stage[t][0..Kc) with f(input) for tokens m0 .. m0+ms-1
 // small inputs (at most two 8-float chunks per thread, K panel a multiple
 // of 256 so a warp's chunks belong to one token): every global load is
@@ -219,7 +226,7 @@ __device__ __forceinline__ void stage_input_small(Ctx& c, const Gemv& g, const f
         va[q] = vb[q] = make_float4(0.f, 0.f, 0.f, 0.f);
         gw[q] = make_uint4(0u, 0u, 0u, 0u);
         if (ok[q]) {
-            const float* r = src + (size_t)(m0 + t) * stride + grp_off + k0 + k;
+            const float* r = src + (size_t)staged_token(c.ms, m0, t) * stride + grp_off + k0 + k;
             va[q] = __ldcg(reinterpret_cast<const float4*>(r));
             vb[q] = __ldcg(reinterpret_cast<const float4*>(r + 4));
             if (kind == IN_RMS) {
@@ -286,7 +293,7 @@ __device__ __noinline__ void stage_input(Ctx& c, const Gemv& g, const float* src
         const int off = g.in_kind == IN_RMS ? 0 : grp_off;
         for (int i = tid * 4; i < total; i += NCT * 4) {
             const int t = i / Kc, k = i - t * Kc;
-            cp_async16(xs + i, src + (size_t)(m0 + t) * g.src_stride + off + k0 + k);
+            cp_async16(xs + i, src + (size_t)staged_token(c.ms, m0, t) * g.src_stride + off + k0 + k);
         }
         cp_async_wait_all();
         cbar();
@@ -347,7 +354,8 @@ __device__ __noinline__ void stage_input(Ctx& c, const Gemv& g, const float* src
 #pragma unroll 4
         for (int i = tid * 4; i < tot; i += NCT * 4) {
             const int t = i / rowlen;
-            const float4 v = __ldcg(reinterpret_cast<const float4*>(src + (size_t)(m0 + t) * g.src_stride + i - t * rowlen));
+            const float4 v = __ldcg(
+                reinterpret_cast<const float4*>(src + (size_t)staged_token(c.ms, m0, t) * g.src_stride + i - t * rowlen));
             // a warp's 128 consecutive floats never straddle a row (rows are
             // multiples of 128 floats), so `t` changes uniformly in the warp
             if (t != cur) {
@@ -375,7 +383,8 @@ __device__ __noinline__ void stage_input(Ctx& c, const Gemv& g, const float* src
         for (int i = tid * 4; i < total; i += NCT * 4) {
             const int t = i / Kc, k = i - t * Kc;
             const float r = 1.0f / sqrtf(acc[t] * invK + p.eps);
-            const float4 v = __ldcg(reinterpret_cast<const float4*>(src + (size_t)(m0 + t) * g.src_stride + k0 + k));
+            const float4 v =
+                __ldcg(reinterpret_cast<const float4*>(src + (size_t)staged_token(c.ms, m0, t) * g.src_stride + k0 + k));
             const uint2 gw = __ldg(reinterpret_cast<const uint2*>(gain + k0 + k));
             float4 o;
             o.x = v.x * bf_lo(gw.x) * r;
@@ -388,7 +397,7 @@ __device__ __noinline__ void stage_input(Ctx& c, const Gemv& g, const float* src
 #pragma unroll 4
         for (int i = tid * 4; i < total; i += NCT * 4) {
             const int t = i / Kc, k = i - t * Kc;
-            const float* r = src + (size_t)(m0 + t) * g.src_stride + k0 + k;
+            const float* r = src + (size_t)staged_token(c.ms, m0, t) * g.src_stride + k0 + k;
             float4 gv = __ldcg(reinterpret_cast<const float4*>(r));
             float4 uv = __ldcg(reinterpret_cast<const float4*>(r + g.sw_off));
             float4 o;
@@ -484,7 +493,8 @@ __device__ void gemv_warp_tile(Ctx& c, const Gemv& g, const uint8_t* tile, int n
     // staged row of token mbase + m: the staging holds tokens from mbase - mt0 on
     int xrow[MTc];
 #pragma unroll
-    for (int m = 0; m < MTc; ++m) xrow[m] = m < mcount ? (int)c.ms.gt[mbase + m] - (mbase - mt0) : mt0 + m;
+    for (int m = 0; m < MTc; ++m)
+        xrow[m] = m < mcount && !c.ms.gather ? (int)c.ms.gt[mbase + m] - (mbase - mt0) : mt0 + m;
     if (NC >= 32) {
         const int JC = NC >> 5;
         for (int r = 0; r < RWv; r += 4) {
@@ -569,7 +579,7 @@ __device__ void gemv_warp_tile(Ctx& c, const Gemv& g, const uint8_t* tile, int n
 __device__ __forceinline__ bool restage(Ctx& c, const Gemv& g, const float* src, int grp_off, int kc, int m0,
                                         int ms) {
     if (c.sk_src == src && c.sk_off == grp_off && c.sk_kc == kc && c.sk_m0 == m0 && c.sk_kind == g.in_kind &&
-        c.sk_gain == g.gain)
+        c.sk_gain == g.gain && c.sk_gather == c.ms.gather)
         return false;
     // nobody reads the RMS accumulators between stagings: zero them before
     // the barrier that ends every use of the previous contents
@@ -583,6 +593,7 @@ __device__ __forceinline__ bool restage(Ctx& c, const Gemv& g, const float* src,
     c.sk_m0 = m0;
     c.sk_kind = g.in_kind;
     c.sk_gain = g.gain;
+    c.sk_gather = c.ms.gather;
     return true;
 }
 
@@ -713,7 +724,7 @@ __device__ __forceinline__ void gemv_range_ks(Ctx& c, const Gemv& g, int slot, i
 #pragma unroll
                         for (int m = 0; m < MR; ++m) {
                             const bool ok = act && mb + m < M;
-                            const float* xp = xs + (size_t)(ok ? ms.gt[mb + m] : 0) * Kc + chunk * 8;
+                            const float* xp = xs + (size_t)(ok ? staging_row(ms, mb + m) : 0) * Kc + chunk * 8;
                             xa[m] = ok ? *reinterpret_cast<const float4*>(xp) : make_float4(0.f, 0.f, 0.f, 0.f);
                             xb[m] = ok ? *reinterpret_cast<const float4*>(xp + 4) : make_float4(0.f, 0.f, 0.f, 0.f);
                         }
@@ -913,12 +924,12 @@ __device__ __forceinline__ void gemv_range_rx(Ctx& c, const Gemv& g, int slot, i
         const int jend = run_end(j, j_hi, n_rb, rb0, R, grp_rows, g0);
         if (p.trace_items == 1 && threadIdx.x == 0) ms.tdbg[1] = clock64();
         const long long ta = p.trace_items ? gtimer() : 0;
-        restage(c, g, src, g0 * grp_stride, kc0, 0, p.M);
+        restage(c, g, src, g0 * grp_stride, kc0, 0, ms.gather ? ms.gm : p.M);
         const long long tb = p.trace_items ? gtimer() : 0;
         long long tc = tb;
         const int ch0 = wide ? lane : (lane & 15);
         const auto load_x = [&](int tk) {
-            const float* xt = xs + (size_t)ms.gt[tk] * g.Kc;
+            const float* xt = xs + (size_t)staging_row(ms, tk) * g.Kc;
 #pragma unroll
             for (int q = 0; q < NX; ++q) {
                 const float* xp = xt + (ch0 + 32 * q) * 8;
@@ -1322,8 +1333,107 @@ __device__ __noinline__ void cons_mm(Ctx& c, int l, const Gemv& g, int sig, int 
     const long long t1 = gtimer();
     cons_gemv(c, g, 0, -1, lo, hi);
     if (sig == C_O && c.p.rfuse && !c.dead) router_part(c, l, g, lo, hi);
+    if (sig == C_A && (c.p.qfuse || c.p.ufuse)) {
+        // buffers of layer l that later stages add into with reductions: the
+        // QB CTAs' absorbed queries (q_lat), the combine CTAs' value
+        // up-projection (o); every CTA (each has A items) clears its share
+        // before signalling A
+        const int gt = (int)blockIdx.x * NCT + ctid(), gs = c.p.G * NCT;
+        if (c.p.qfuse) {
+            float4* q = reinterpret_cast<float4*>(const_cast<float*>(c.layer().qlat));
+            const int n4 = c.p.M * MLA_H * MLA_KL / 4;
+            for (int i = gt; i < n4; i += gs) q[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        if (c.p.ufuse) {
+            float4* o = reinterpret_cast<float4*>(c.layer().o);
+            const int n4 = c.p.M * MLA_H * c.p.vd / 4;
+            for (int i = gt; i < n4; i += gs) o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    }
     csignal(c, l, sig, (unsigned)(hi - lo));
     trace_rec(c, ((unsigned)sig << 16) | (unsigned)l, (unsigned)(hi - lo), t0, t1);
+}
+
+// ---- the absorbed query folded into QB (MLA, all tokens' c_q staged) ----
+// q_lat[h] = q_nope[h] . W_uk[h] is a sum over the 128 nope dimensions of
+// head h. A QB tile of R nope rows of head h (R = 16) yields q_nope for those
+// dimensions; the CTA multiplies them at once by the same R rows of W_uk[h]
+// (a slab of R x 512, streamed into the ring right after the tile) and adds
+// the product into q_lat with vector reductions. q_lat is cleared by the A
+// stage, so the attention waits only for QB: one dependent stage fewer.
+__device__ __noinline__ void qb_fused_cons(Ctx& c, int l, int lo, int hi) {
+    const Params& p = c.p;
+    c.cur_code = ((unsigned)C_QB << 16) | (unsigned)l;
+    const long long t0 = gtimer();
+    cwait(c, 0x1000u | (unsigned)(l << 16) | (unsigned)C_QB);
+    const long long t1 = gtimer();
+    const Layer& Ld = c.layer();
+    const Gemv& g = Ld.g[G_QB];
+    const int M = p.M, qh = p.nope + p.rd, R = g.R, tid = ctid();
+    float* qv = c.red();  // [M][R] this tile's outputs
+    // every warp runs every iteration and every barrier (a warp that saw an
+    // abort skips the work, not the barriers: its copy of `dead` may differ
+    // from the other warps')
+    for (int j = lo; j < hi; ++j) {
+        cons_gemv(c, g, 0, -1, j, j + 1);
+        const int r0 = j * R, h = r0 / qh, i0 = r0 - h * qh;
+        if (i0 >= p.nope) continue;  // rope rows: the attention reads them from q
+        cbar();                      // every warp's outputs of the tile are written
+        if (tid < M * R) qv[tid] = __ldcg(g.dst + (size_t)(tid / R) * g.dst_stride + r0 + tid % R);
+        cbar();
+        const uint8_t* slab = c.dead ? nullptr : cons_wait(p, c.smem, c.ms, c.cr);
+        if (slab) {
+            // thread: latent columns 2 tid, 2 tid + 1 (512 = 2 NCT)
+            const uint32_t* W = reinterpret_cast<const uint32_t*>(slab) + tid;
+            float* ql = const_cast<float*>(Ld.qlat) + (size_t)h * MLA_KL + 2 * tid;
+            for (int m = 0; m < M; ++m) {
+                float a0 = 0.f, a1 = 0.f;
+#pragma unroll 4
+                for (int r = 0; r < R; ++r) {
+                    const uint32_t w = W[(size_t)r * (MLA_KL / 2)];
+                    const float x = qv[m * R + r];
+                    a0 = fmaf(x, bf_lo(w), a0);
+                    a1 = fmaf(x, bf_hi(w), a1);
+                }
+                asm volatile("red.relaxed.gpu.global.add.v2.f32 [%0], {%1, %2};" ::"l"(ql + (size_t)m * MLA_H * MLA_KL),
+                             "f"(a0), "f"(a1)
+                             : "memory");
+            }
+        }
+        cons_release(c.ms, c.cr);  // every warp's ring state advances alike
+        if (*(volatile int*)&c.ms.abort) c.dead = true;
+    }
+    csignal(c, l, C_QB, (unsigned)(hi - lo));
+    trace_rec(c, ((unsigned)C_QB << 16) | (unsigned)l, (unsigned)(hi - lo), t0, t1);
+}
+
+// producer side: each QB tile, and after a tile of nope rows its W_uk slab
+__device__ __noinline__ void qb_fused_prod(Ctx& c, int lo, int hi) {
+    const Params& p = c.p;
+    const Layer& Ld = c.layer();
+    const Gemv& g = Ld.g[G_QB];
+    const int qh = p.nope + p.rd, R = g.R;
+    for (int j = lo; j < hi && !c.dead; ++j) {
+        prod_gemv(c, g, -1, j, j + 1);
+        const int r0 = j * R, h = r0 / qh, i0 = r0 - h * qh;
+        if (c.dead || i0 >= p.nope) continue;
+        const unsigned bytes = (unsigned)R * MLA_KL * 2u;
+        int ok = 1;
+        if ((threadIdx.x & 31) == 0) {
+            uint8_t* dst = prod_begin(p, c.smem, c.ms, c.pr, bytes);
+            if (dst)
+                bulk_g2s(dst, Ld.uk + ((size_t)h * p.nope + i0) * MLA_KL, bytes, &c.ms.full[c.pr.slot]);
+            else
+                ok = 0;
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) {
+            c.dead = true;
+            return;
+        }
+        c.bump_issued();
+        prod_next(c.pr);
+    }
 }
 
 // ============================================================ routing ====
@@ -2236,13 +2346,67 @@ __device__ __forceinline__ void cons_comb(Ctx& c, int l, int i) {
         *reinterpret_cast<float4*>(c.red() + warp * 128 + lane * 4) = acc;
     }
     cbar();
+    const bool uv = p.attn == 1 && p.ufuse;
+    float* xl = c.stage();  // fused value up-projection: this item's 128 latent values
     for (int e = tid; e < D; e += NCT) {
         float v = 0.f;
 #pragma unroll
         for (int w2 = 0; w2 < NCW; ++w2) v += c.red()[w2 * 128 + e];
-        out[e] = v;
+        if (uv)
+            xl[e] = v;
+        else
+            out[e] = v;
     }
     cbar();
+    if (uv) {
+        // o[m][h][v] += sum_j olat[m][h][d0 + j] W_uv[h][v][d0 + j] over this
+        // item's 128 latent dimensions j: the slab W_uv[h] (quarter d0 / 128)
+        // is stored j-major [128 j][vd v]; thread: values v = 2 vp, 2 vp + 1
+        // against j in [32 jq, 32 jq + 32), added into o with a reduction
+        c.sk_src = nullptr;  // the staging area no longer holds a GEMV input
+        const uint8_t* slab = c.dead ? nullptr : cons_wait(p, c.smem, c.ms, c.cr);
+        const int vp = tid & 63, jq = tid >> 6, m = i / (MLA_H * 4), h = (i >> 2) & (MLA_H - 1);
+        if (slab && 2 * vp < p.vd) {
+            const uint32_t* W = reinterpret_cast<const uint32_t*>(slab) + vp;
+            float a0 = 0.f, a1 = 0.f;
+#pragma unroll 8
+            for (int j = 32 * jq; j < 32 * jq + 32; ++j) {
+                const uint32_t w = W[(size_t)j * (p.vd / 2)];
+                a0 = fmaf(xl[j], bf_lo(w), a0);
+                a1 = fmaf(xl[j], bf_hi(w), a1);
+            }
+            float* o = Ld.o + (size_t)m * MLA_H * p.vd + h * p.vd + 2 * vp;
+            asm volatile("red.relaxed.gpu.global.add.v2.f32 [%0], {%1, %2};" ::"l"(o), "f"(a0), "f"(a1) : "memory");
+        }
+        cons_release(c.ms, c.cr);  // every warp's ring state advances alike
+        cbar();                    // xl is free for the next item
+    }
+}
+
+// producer side of the combine with the value up-projection folded in: the
+// W_uv slab of each item (head, latent quarter)
+__device__ __noinline__ void comb_prod(Ctx& c, int lo, int hi) {
+    const Params& p = c.p;
+    const Layer& Ld = c.layer();
+    const unsigned bytes = 128u * (unsigned)p.vd * 2u;
+    for (int i = lo; i < hi && !c.dead; ++i) {
+        const int h = (i >> 2) & (MLA_H - 1), q = i & 3;
+        int ok = 1;
+        if ((threadIdx.x & 31) == 0) {
+            uint8_t* dst = prod_begin(p, c.smem, c.ms, c.pr, bytes);
+            if (dst)
+                bulk_g2s(dst, Ld.uvq + (size_t)(h * 4 + q) * 128 * p.vd, bytes, &c.ms.full[c.pr.slot]);
+            else
+                ok = 0;
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) {
+            c.dead = true;
+            return;
+        }
+        c.bump_issued();
+        prod_next(c.pr);
+    }
 }
 
 __device__ __noinline__ void comb_cons(Ctx& c, int l, int lo, int hi) {
@@ -2422,7 +2586,8 @@ __device__ bool prod_check(const Params& p) {
 __device__ __noinline__ void prefetch_attn_mla(Ctx& c, int l) {
     const Params& p = c.p;
     const Layer& Ld = c.layer();
-    const long long ahead = (long long)gemv_items(Ld.g[G_A]) + gemv_items(Ld.g[G_QB]) + p.M + gemv_items(Ld.g[G_QLAT]);
+    const long long ahead = (long long)gemv_items(Ld.g[G_A]) + gemv_items(Ld.g[G_QB]) + p.M +
+                            (p.qfuse ? 0 : gemv_items(Ld.g[G_QLAT]));
     int lo, hi;
     my_range(p, attn_items(p), (int)((c.off + ahead) % p.G), lo, hi);
     const int lane = threadIdx.x & 31;
@@ -2609,11 +2774,15 @@ __device__ __noinline__ void unit_seg_cons(Ctx& c, int l, int kind, int expert, 
     const long long tu0 = p.trace_items ? gtimer() : 0;
     if (p.trace_items && tid == 0) trace_rec(c, 0x80000000u | (((unsigned)C_DOWN + 5) << 16) | (unsigned)l, 0u, tue, tu0);
     // the tokens of this expert: a routed expert takes only the tokens routed
-    // to it when every token's input is staged in one K panel (the routed
-    // CTAs stage it before routing), otherwise all tokens, weight 0 or not;
-    // the shared expert takes tokens [m_lo, m_hi)
+    // to it when its input is one K panel -- read from the staging area when
+    // every token's input is staged there (the routed CTAs stage it before
+    // routing), else its own tokens are gathered into the staging area --
+    // and otherwise all tokens, weight 0 or not; the shared expert takes
+    // tokens [m_lo, m_hi), gathered when not every token's input is staged
     if (tid < 32) {
-        const bool compact = expert >= 0 && p.M > 1 && Ld.ffn.n_kc == 1 && p.M * Ld.ffn.Kc <= STAGE_FLOATS;
+        const bool one_panel = p.M > 1 && Ld.ffn.n_kc == 1;
+        const bool all_staged = one_panel && p.M * Ld.ffn.Kc <= STAGE_FLOATS;
+        const bool compact = expert >= 0 && one_panel;
         const int lane = tid;
         float w[2];
         bool sel[2];
@@ -2634,7 +2803,12 @@ __device__ __noinline__ void unit_seg_cons(Ctx& c, int l, int kind, int expert, 
                 c.ms.uw[pos[q]] = w[q];
             }
         }
-        if (lane == 0) c.ms.gm = __popc(b0) + __popc(b1);
+        if (lane == 0) {
+            c.ms.gm = __popc(b0) + __popc(b1);
+            c.ms.gather = one_panel && !all_staged && (expert >= 0 || m_hi - m_lo < p.M)
+                              ? (expert >= 0 ? expert + 1 : 1024 + m_lo)
+                              : 0;
+        }
     }
     cbar();
     const int M = c.ms.gm;
@@ -2810,11 +2984,13 @@ __device__ __noinline__ void ffn_stage(Ctx& c, int l) {
     const long long t0 = gtimer();
     c.cur_code = ((unsigned)C_DOWN << 16) | (unsigned)l;
     int done = 0;
-    // more than 4 tokens, all staged in one K panel: the shared expert's
-    // units run once per group of 4 tokens (work items unit x group, for more
-    // CTAs and the register GEMV path)
+    // the shared expert's units run once per group of tokens (work items
+    // unit x group): groups of 4 when every token's input is staged in one K
+    // panel (more CTAs, and the register GEMV path); groups as large as the
+    // staging area holds when not (each group's tokens gathered there)
     const bool stage_all = p.M > 1 && Ld.ffn.n_kc == 1 && p.M * Ld.ffn.Kc <= STAGE_FLOATS;
-    const int ntg = p.M > 4 && stage_all ? (p.M + 3) / 4 : 1;
+    const int tgs = shared_group(p.M, Ld.ffn.n_kc, Ld.ffn.Kc);
+    const int ntg = (p.M + tgs - 1) / tgs;
     if ((int)blockIdx.x < p.gs) {
         if (p.has_sh) {
             const int nu = Ld.ffn.k[1].nu;
@@ -2822,17 +2998,18 @@ __device__ __noinline__ void ffn_stage(Ctx& c, int l) {
             my_range_sub(nu * ntg, 0, p.gs, lo, hi);
             if (lo < hi) {
                 if constexpr (!PROD) {
-                    if (ntg > 1 && threadIdx.x == 0) unit_gemv(p, Ld, c.ms.ug, 1, -1, 0, 1, c.red() + RED_FLOATS / 2);
+                    const bool pre = ntg > 1 && stage_all;
+                    if (pre && threadIdx.x == 0) unit_gemv(p, Ld, c.ms.ug, 1, -1, 0, 1, c.red() + RED_FLOATS / 2);
                     set_deps(c, deps1(l, C_O, (unsigned)gemv_items(Ld.g[G_O])));
                     cwait(c, 0x1100u | (unsigned)(l << 16));
-                    if (ntg > 1) restage(c, c.ms.ug, Ld.x, 0, 0, 0, p.M);
+                    if (pre) restage(c, c.ms.ug, Ld.x, 0, 0, 0, p.M);
                 }
                 for (int i = lo; i < hi && !(PROD && c.dead);) {
                     const int tg = i / nu, iend = min(hi, (tg + 1) * nu);
                     if constexpr (PROD) {
                         unit_seg_prod(c, 1, -1, i - tg * nu, iend - tg * nu);
                     } else {
-                        const int m0 = ntg > 1 ? 4 * tg : 0, m1 = ntg > 1 ? min(p.M, m0 + 4) : p.M;
+                        const int m0 = tg * tgs, m1 = min(p.M, m0 + tgs);
                         unit_seg_cons(c, l, 1, -1, i - tg * nu, iend - tg * nu, m0, m1);
                     }
                     i = iend;
@@ -2884,7 +3061,10 @@ __device__ __noinline__ void ffn_stage(Ctx& c, int l) {
         // back to all tokens in order for the stages that follow (their
         // readers pass a barrier first)
         if (threadIdx.x < MAX_M) c.ms.gt[threadIdx.x] = (uint8_t)threadIdx.x;
-        if (threadIdx.x == 0) c.ms.gm = p.M;
+        if (threadIdx.x == 0) {
+            c.ms.gm = p.M;
+            c.ms.gather = 0;
+        }
         trace_rec(c, ((unsigned)C_DOWN << 16) | (unsigned)l, (unsigned)done, t0, t0);
     }
 }
@@ -2973,6 +3153,20 @@ __device__ __noinline__ bool exec_stage(Ctx& c) {
             }
             case S_QB:
                 if (!mla) return true;
+                if (p.qfuse) {
+                    const int n = gemv_items(Ld.g[G_QB]);
+                    int lo, hi;
+                    my_range(p, n, c.off, lo, hi);
+                    c.advance(n);
+                    if (lo >= hi) return true;
+                    if constexpr (PROD) {
+                        qb_fused_prod(c, lo, hi);
+                    } else {
+                        set_deps(c, deps1(l, C_A, (unsigned)gemv_items(Ld.g[G_A])));
+                        qb_fused_cons(c, l, lo, hi);
+                    }
+                    return true;
+                }
                 g = &Ld.g[G_QB];
                 deps = deps1(l, C_A, (unsigned)gemv_items(Ld.g[G_A]));
                 sig = C_QB;
@@ -2989,7 +3183,7 @@ __device__ __noinline__ bool exec_stage(Ctx& c) {
                 return true;
             }
             case S_QLAT:
-                if (!mla) return true;
+                if (!mla || p.qfuse) return true;
                 g = &Ld.g[G_QLAT];
                 deps = deps1(l, C_QB, (unsigned)gemv_items(Ld.g[G_QB]));
                 sig = C_QLAT;
@@ -3006,7 +3200,8 @@ __device__ __noinline__ bool exec_stage(Ctx& c) {
                     Deps da;
                     if (mla) {
                         da.n = 2;
-                        da.d[0] = {l, C_QLAT, (unsigned)gemv_items(Ld.g[G_QLAT])};
+                        da.d[0] = p.qfuse ? Dep{l, C_QB, (unsigned)gemv_items(Ld.g[G_QB])}
+                                          : Dep{l, C_QLAT, (unsigned)gemv_items(Ld.g[G_QLAT])};
                         da.d[1] = {l, C_APP, (unsigned)p.M};
                     } else {
                         da = deps1(l, C_A, (unsigned)gemv_items(Ld.g[G_A]));
@@ -3021,21 +3216,26 @@ __device__ __noinline__ bool exec_stage(Ctx& c) {
                 int lo, hi;
                 my_range(p, n, c.off, lo, hi);
                 c.advance(n);
-                if (!PROD && lo < hi) {
-                    set_deps(c, deps1(l, C_ATTN, (unsigned)attn_items(p)));
-                    comb_cons(c, l, lo, hi);
+                if (lo < hi) {
+                    if constexpr (PROD) {
+                        if (mla && p.ufuse) comb_prod(c, lo, hi);
+                    } else {
+                        set_deps(c, deps1(l, C_ATTN, (unsigned)attn_items(p)));
+                        comb_cons(c, l, lo, hi);
+                    }
                 }
                 return true;
             }
             case S_UV:
-                if (!mla) return true;
+                if (!mla || p.ufuse) return true;
                 g = &Ld.g[G_UV];
                 deps = deps1(l, C_COMB, (unsigned)comb_items(p));
                 sig = C_UV;
                 break;
             case S_O:
                 g = &Ld.g[G_O];
-                deps = mla ? deps1(l, C_UV, (unsigned)gemv_items(Ld.g[G_UV])) : deps1(l, C_COMB, (unsigned)comb_items(p));
+                deps = mla && !p.ufuse ? deps1(l, C_UV, (unsigned)gemv_items(Ld.g[G_UV]))
+                                       : deps1(l, C_COMB, (unsigned)comb_items(p));
                 sig = C_O;
                 break;
             // the router runs on its own CTAs [G - gr, G): the routed units
@@ -3152,6 +3352,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) megakernel(const __grid_constant_
         ms.n_slots = ms.p_nslots = 0;
         for (int i = 0; i < MAX_M; ++i) ms.gt[i] = (uint8_t)i;
         ms.gm = p.M;
+        ms.gather = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     {

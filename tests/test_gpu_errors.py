@@ -95,7 +95,9 @@ def test_trace_covers_every_stage_of_every_layer(monkeypatch, name, B):
             seen.add((code & 0xFFFF, tracing.stage_name(code)))
     L = cfg["n_layers"]
     mla = cfg["attn_kind"] == 1
-    want = ["A", "ATTN", "COMB", "O", "FFN", "ROUTE"] + (["QB", "APP", "QLAT", "UV"] if mla else [])
+    # (MLA: the absorbed-query and value up-projection stages, QLAT and UV,
+    # run on their own only when they are not folded into QB and the combine)
+    want = ["A", "ATTN", "COMB", "O", "FFN", "ROUTE"] + (["QB", "APP"] if mla else [])
     if B == 1:
         want.append("ROUTER")  # steps of two or more tokens fold the router into O
     for l in range(L):

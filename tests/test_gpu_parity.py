@@ -222,3 +222,15 @@ def test_unfused_one_launch_per_stage(name, B, T, steps):
         cfg = configs.scaled(cfg, n_layers=2)
     ctx = min(cfg["ctx"], 2000)
     _run(cfg, B, T, steps, ctx, entry="decode_step_unfused", want_accept=T > 1)
+
+
+@pytest.mark.parametrize("B", [1, 3])
+def test_deep_separate_absorbed_query_and_value_stages(monkeypatch, B):
+    # the schedule in which the absorbed query (QLAT) and the value
+    # up-projection (UV) are stages of their own (used when the tokens' inputs
+    # do not fit the staging area at once); by default, for few tokens, the
+    # QB CTAs and the combine CTAs compute them
+    monkeypatch.setenv("MK_QLAT_STAGE", "1")
+    monkeypatch.setenv("MK_UV_STAGE", "1")
+    cfg = configs.scaled(configs.DEEP, n_layers=2)
+    _run(cfg, B, 1, 2, cfg["ctx"])
