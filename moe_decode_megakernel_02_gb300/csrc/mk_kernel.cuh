@@ -1186,8 +1186,14 @@ __device__ __forceinline__ void prefetch_tiles(const Gemv& g, int expert, int lo
     }
 }
 
-constexpr int PF_TILES = 8;  // L2 prefetch distance beyond the ring, in tiles
-constexpr int UNIT_PF_BYTES = 640 * 1024;  // expert units: L2 prefetch up front, per CTA
+#ifndef MK_PF_TILES
+#define MK_PF_TILES 8
+#endif
+#ifndef MK_UNIT_PF_BYTES
+#define MK_UNIT_PF_BYTES (640 * 1024)
+#endif
+constexpr int PF_TILES = MK_PF_TILES;            // L2 prefetch distance beyond the ring, in tiles
+constexpr int UNIT_PF_BYTES = MK_UNIT_PF_BYTES;  // expert units: L2 prefetch up front, per CTA
 
 __device__ __noinline__ void prod_gemv(Ctx& c, const Gemv& g, int expert, int lo, int hi) {
     const uint16_t* W = g.W + (expert >= 0 ? (size_t)expert * g.w_estride : 0);
@@ -1370,17 +1376,28 @@ __device__ __noinline__ void qb_fused_cons(Ctx& c, int l, int lo, int hi) {
     const Layer& Ld = c.layer();
     const Gemv& g = Ld.g[G_QB];
     const int M = p.M, qh = p.nope + p.rd, R = g.R, tid = ctid();
-    float* qv = c.red();  // [M][R] this tile's outputs
+    // [M][R] a nope tile's outputs, in the upper half of the reduction area
+    // (the split-K GEMV uses the lower half)
+    float* qv = c.red() + RED_FLOATS / 2;
     // every warp runs every iteration and every barrier (a warp that saw an
     // abort skips the work, not the barriers: its copy of `dead` may differ
     // from the other warps')
     for (int j = lo; j < hi; ++j) {
-        cons_gemv(c, g, 0, -1, j, j + 1);
         const int r0 = j * R, h = r0 / qh, i0 = r0 - h * qh;
-        if (i0 >= p.nope) continue;  // rope rows: the attention reads them from q
-        cbar();                      // every warp's outputs of the tile are written
-        if (tid < M * R) qv[tid] = __ldcg(g.dst + (size_t)(tid / R) * g.dst_stride + r0 + tid % R);
+        if (i0 >= p.nope) {  // rope rows: the attention reads them from q
+            cons_gemv(c, g, 0, -1, j, j + 1);
+            continue;
+        }
+        // nope rows: the same GEMV with its outputs going to qv (only this
+        // CTA reads them)
+        if (tid == 0) {
+            c.ms.ug = g;
+            c.ms.ug.dst = qv - r0;
+            c.ms.ug.dst_stride = R;
+        }
         cbar();
+        cons_gemv(c, c.ms.ug, 0, -1, j, j + 1);
+        cbar();  // every warp's outputs of the tile are in qv
         const uint8_t* slab = c.dead ? nullptr : cons_wait(p, c.smem, c.ms, c.cr);
         if (slab) {
             // thread: latent columns 2 tid, 2 tid + 1 (512 = 2 NCT)
@@ -2720,8 +2737,23 @@ __device__ __forceinline__ void unit_gemv(const Params& p, const Layer& Ld, Gemv
     ug.dst2 = nullptr;
 }
 
-// one thread's rows of a down tile (nr rows x F), one token, hidden values
-// of the unit in registers
+// add v (this lane's row of 4 consecutive rows held by lanes 4i .. 4i+3 of
+// the warp) into dst + row with one vector reduction per 4 rows: the
+// residual rows receive every unit's down output, and 4-wide reductions
+// cut the operations the L2 performs on those few lines by 4
+__device__ __forceinline__ void red4_rows(float* dst, int row, bool ok, float v) {
+    const float v1 = __shfl_down_sync(0xffffffffu, v, 1);
+    const float v2 = __shfl_down_sync(0xffffffffu, v, 2);
+    const float v3 = __shfl_down_sync(0xffffffffu, v, 3);
+    if (ok && (threadIdx.x & 3) == 0)
+        asm volatile("red.relaxed.gpu.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst + row), "f"(v), "f"(v1),
+                     "f"(v2), "f"(v3)
+                     : "memory");
+}
+
+// one thread's rows of a down tile (nr rows x F, nr a multiple of 8), one
+// token, hidden values of the unit in registers; a warp takes 32 consecutive
+// rows at a time
 template <int F8>
 __device__ __forceinline__ void down_rows1(const uint8_t* tile, int nr, const float* hu, float w, float* xo) {
     float4 ha[F8], hb[F8];
@@ -2731,35 +2763,42 @@ __device__ __forceinline__ void down_rows1(const uint8_t* tile, int nr, const fl
         hb[q] = *reinterpret_cast<const float4*>(hu + 8 * q + 4);
     }
     const uint4* T4 = reinterpret_cast<const uint4*>(tile);
-    for (int r = ctid(); r < nr; r += NCT) {
+    const int lane = threadIdx.x & 31;
+    for (int rb = (ctid() >> 5) * 32; rb < nr; rb += NCT) {
+        const int r = rb + lane;
         float a = 0.f, b = 0.f;
+        if (r < nr) {
 #pragma unroll
-        for (int q = 0; q < F8; ++q) fma8v2(a, b, T4[(size_t)r * F8 + q], ha[q], hb[q]);
-        atomicAdd(xo + r, w * (a + b));
+            for (int q = 0; q < F8; ++q) fma8v2(a, b, T4[(size_t)r * F8 + q], ha[q], hb[q]);
+        }
+        red4_rows(xo, r, r < nr, w * (a + b));
     }
 }
 
-// one thread's rows of a down tile (nr rows x F), several tokens: the row's
-// weights in registers, token i's hidden values at hu + i hstride, its
-// output row gt[i] of xo (stride d), scaled by its routing weight
+// one thread's rows of a down tile (nr rows x F, nr a multiple of 8),
+// several tokens: the row's weights in registers, token i's hidden values at
+// hu + i hstride, its output row gt[i] of xo (stride d), scaled by its
+// routing weight
 template <int F8>
 __device__ __forceinline__ void down_rowsM(const uint8_t* tile, int nr, const float* hu, int hstride, int M,
                                            const Misc& ms, float* xo, int d) {
     const uint4* T4 = reinterpret_cast<const uint4*>(tile);
-    for (int r = ctid(); r < nr; r += NCT) {
+    const int lane = threadIdx.x & 31;
+    for (int rb = (ctid() >> 5) * 32; rb < nr; rb += NCT) {
+        const int r = rb + lane;
         uint4 w[F8];
 #pragma unroll
-        for (int q = 0; q < F8; ++q) w[q] = T4[(size_t)r * F8 + q];
+        for (int q = 0; q < F8; ++q) w[q] = r < nr ? T4[(size_t)r * F8 + q] : make_uint4(0u, 0u, 0u, 0u);
         for (int i = 0; i < M; ++i) {
             const float wt = ms.uw[i];
-            if (wt == 0.f) continue;
+            if (wt == 0.f) continue;  // uniform: every lane reads the same entry
             const float* hi = hu + (size_t)i * hstride;
             float a = 0.f, b = 0.f;
 #pragma unroll
             for (int q = 0; q < F8; ++q)
                 fma8v2(a, b, w[q], *reinterpret_cast<const float4*>(hi + 8 * q),
                        *reinterpret_cast<const float4*>(hi + 8 * q + 4));
-            atomicAdd(xo + (size_t)ms.gt[i] * d + r, wt * (a + b));
+            red4_rows(xo + (size_t)ms.gt[i] * d, r, r < nr, wt * (a + b));
         }
     }
 }
