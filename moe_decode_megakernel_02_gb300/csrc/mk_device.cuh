@@ -35,13 +35,17 @@ constexpr int NTHREADS = NCT + 32;        // + one producer warp
 #define MK_NSLOT 3
 #endif
 #ifndef MK_STAGE_BYTES
-#define MK_STAGE_BYTES 65536
+#define MK_STAGE_BYTES 66048
 #endif
 constexpr int NSLOT = MK_NSLOT;           // ring slots
 constexpr int SLOT_BYTES = 37888;         // one MLA chunk (32 padded latent rows + rope rows)
 constexpr int TILE_MAX = 32768;           // GEMV weight tile
 constexpr int STAGE_BYTES = MK_STAGE_BYTES;  // activation / query staging
 constexpr int STAGE_FLOATS = STAGE_BYTES / 4;
+// staged input rows are Kc + 8 floats apart: a tensor-core fragment load
+// (8 token rows, 2 floats each) then touches every bank once per half warp
+__host__ __device__ constexpr int stage_stride(int Kc) { return Kc + 8; }
+__host__ __device__ constexpr bool stage_fits(int M, int Kc) { return M * stage_stride(Kc) <= STAGE_FLOATS; }
 constexpr int RED_FLOATS = 1024;
 constexpr int MT = 4;                     // tokens per register group in the GEMV
 constexpr int MAX_M = 64;                 // batch * tokens per step
@@ -439,8 +443,8 @@ __device__ __forceinline__ int gemv_items(const Gemv& g) { return g.n_rb * g.n_k
 // as many as fit when it does not (each group gathered), else all
 __host__ __device__ __forceinline__ int shared_group(int M, int n_kc, int Kc) {
     if (M <= 1 || n_kc != 1) return M < 1 ? 1 : M;
-    if (M * Kc <= STAGE_FLOATS) return M > 4 ? 4 : M;
-    return STAGE_FLOATS / Kc;
+    if (stage_fits(M, Kc)) return M > 4 ? 4 : M;
+    return STAGE_FLOATS / stage_stride(Kc);
 }
 
 // attention splits: units = prefix chunks + 1 tail unit (the new positions)

@@ -919,7 +919,7 @@ static int step_params(mk_model* m, mk_kv* kv, const int32_t* tokens, const int3
     P.dbg_w = m->dbg_w;
     P.dbg_margin = m->dbg_margin;
     // every token's c_q staged at once, one tile's outputs per thread
-    P.qfuse = m->qfuse_ok && P.M * P.ql <= mk::STAGE_FLOATS && P.M * m->layers[0].g[mk::G_QB].R <= mk::NCT;
+    P.qfuse = m->qfuse_ok && mk::stage_fits(P.M, P.ql) && P.M * m->layers[0].g[mk::G_QB].R <= mk::NCT;
     // the combine's items are per token: each reads its 32 KB slab of W_uv,
     // so for many tokens the separate stage (W_uv read once) is cheaper
     P.ufuse = m->ufuse_ok && P.M <= 16;

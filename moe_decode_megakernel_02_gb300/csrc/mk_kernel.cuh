@@ -271,9 +271,10 @@ __device__ __forceinline__ void stage_input_small(Ctx& c, const Gemv& g, const f
 #pragma unroll
     for (int q = 0; q < 2; ++q) {
         if (!ok[q]) continue;
-        const int i = (tid + q * NCT) * 8;
-        *reinterpret_cast<float4*>(xs + i) = va[q];
-        *reinterpret_cast<float4*>(xs + i + 4) = vb[q];
+        const int i = (tid + q * NCT) * 8, t = i / Kc;
+        float* d = xs + t * stage_stride(Kc) + (i - t * Kc);
+        *reinterpret_cast<float4*>(d) = va[q];
+        *reinterpret_cast<float4*>(d + 4) = vb[q];
     }
 }
 
@@ -291,9 +292,10 @@ __device__ __noinline__ void stage_input(Ctx& c, const Gemv& g, const float* src
         // (one L2 round trip instead of one per loop iteration), then the
         // RMSNorm, if any, works on the copy in shared memory
         const int off = g.in_kind == IN_RMS ? 0 : grp_off;
+        const int SS = stage_stride(Kc);
         for (int i = tid * 4; i < total; i += NCT * 4) {
             const int t = i / Kc, k = i - t * Kc;
-            cp_async16(xs + i, src + (size_t)staged_token(c.ms, m0, t) * g.src_stride + off + k0 + k);
+            cp_async16(xs + t * SS + k, src + (size_t)staged_token(c.ms, m0, t) * g.src_stride + off + k0 + k);
         }
         cp_async_wait_all();
         cbar();
@@ -306,7 +308,7 @@ __device__ __noinline__ void stage_input(Ctx& c, const Gemv& g, const float* src
         int cur = -1;
         for (int i = tid * 4; i < total; i += NCT * 4) {
             const int t = i / Kc;
-            const float4 v = *reinterpret_cast<const float4*>(xs + i);
+            const float4 v = *reinterpret_cast<const float4*>(xs + t * SS + (i - t * Kc));
             if (t != cur) {
                 if (cur >= 0) {
 #pragma unroll
@@ -333,12 +335,13 @@ __device__ __noinline__ void stage_input(Ctx& c, const Gemv& g, const float* src
             const int t = i / Kc, k = i - t * Kc;
             const float r = 1.0f / sqrtf(acc[t] * invK + p.eps);
             const uint2 gw = __ldg(reinterpret_cast<const uint2*>(g.gain + k));
-            float4 o = *reinterpret_cast<const float4*>(xs + i);
+            float4* xp = reinterpret_cast<float4*>(xs + t * SS + k);
+            float4 o = *xp;
             o.x = o.x * bf_lo(gw.x) * r;
             o.y = o.y * bf_hi(gw.x) * r;
             o.z = o.z * bf_lo(gw.y) * r;
             o.w = o.w * bf_hi(gw.y) * r;
-            *reinterpret_cast<float4*>(xs + i) = o;
+            *xp = o;
         }
         return;
     }
@@ -391,7 +394,7 @@ __device__ __noinline__ void stage_input(Ctx& c, const Gemv& g, const float* src
             o.y = v.y * bf_hi(gw.x) * r;
             o.z = v.z * bf_lo(gw.y) * r;
             o.w = v.w * bf_hi(gw.y) * r;
-            *reinterpret_cast<float4*>(xs + i) = o;
+            *reinterpret_cast<float4*>(xs + t * stage_stride(Kc) + k) = o;
         }
     } else {  // IN_SWIGLU: h = silu(gate) * up
 #pragma unroll 4
@@ -405,9 +408,16 @@ __device__ __noinline__ void stage_input(Ctx& c, const Gemv& g, const float* src
             o.y = silu(gv.y) * uv.y;
             o.z = silu(gv.z) * uv.z;
             o.w = silu(gv.w) * uv.w;
-            *reinterpret_cast<float4*>(xs + i) = o;
+            *reinterpret_cast<float4*>(xs + t * stage_stride(Kc) + k) = o;
         }
     }
+}
+
+// token m was routed to `expert` (its weight may still round to zero)
+__device__ __forceinline__ bool routed_to(const Misc& ms, int m, int expert, int k) {
+    for (int j = 0; j < k; ++j)
+        if (ms.ridx[m][j] == expert) return true;
+    return false;
 }
 
 __device__ __forceinline__ float route_weight(const Misc& ms, int m, int expert, int k) {
@@ -509,8 +519,8 @@ __device__ void gemv_warp_tile(Ctx& c, const Gemv& g, const uint8_t* tile, int n
                 float xv[MTc][8];
 #pragma unroll
                 for (int m = 0; m < MTc; ++m) {
-                    const float4 a = *reinterpret_cast<const float4*>(xs + (size_t)xrow[m] * Kc + ch * 8);
-                    const float4 b = *reinterpret_cast<const float4*>(xs + (size_t)xrow[m] * Kc + ch * 8 + 4);
+                    const float4 a = *reinterpret_cast<const float4*>(xs + (size_t)xrow[m] * stage_stride(Kc) + ch * 8);
+                    const float4 b = *reinterpret_cast<const float4*>(xs + (size_t)xrow[m] * stage_stride(Kc) + ch * 8 + 4);
                     xv[m][0] = a.x; xv[m][1] = a.y; xv[m][2] = a.z; xv[m][3] = a.w;
                     xv[m][4] = b.x; xv[m][5] = b.y; xv[m][6] = b.z; xv[m][7] = b.w;
                 }
@@ -554,8 +564,8 @@ __device__ void gemv_warp_tile(Ctx& c, const Gemv& g, const uint8_t* tile, int n
 #pragma unroll
             for (int m = 0; m < MTc; ++m) {
                 float xv[8];
-                const float4 a = *reinterpret_cast<const float4*>(xs + (size_t)xrow[m] * Kc + ch * 8);
-                const float4 b = *reinterpret_cast<const float4*>(xs + (size_t)xrow[m] * Kc + ch * 8 + 4);
+                const float4 a = *reinterpret_cast<const float4*>(xs + (size_t)xrow[m] * stage_stride(Kc) + ch * 8);
+                const float4 b = *reinterpret_cast<const float4*>(xs + (size_t)xrow[m] * stage_stride(Kc) + ch * 8 + 4);
                 xv[0] = a.x; xv[1] = a.y; xv[2] = a.z; xv[3] = a.w;
                 xv[4] = b.x; xv[5] = b.y; xv[6] = b.z; xv[7] = b.w;
                 acc[m] = 0.f;
@@ -724,7 +734,7 @@ __device__ __forceinline__ void gemv_range_ks(Ctx& c, const Gemv& g, int slot, i
 #pragma unroll
                         for (int m = 0; m < MR; ++m) {
                             const bool ok = act && mb + m < M;
-                            const float* xp = xs + (size_t)(ok ? staging_row(ms, mb + m) : 0) * Kc + chunk * 8;
+                            const float* xp = xs + (size_t)(ok ? staging_row(ms, mb + m) : 0) * stage_stride(Kc) + chunk * 8;
                             xa[m] = ok ? *reinterpret_cast<const float4*>(xp) : make_float4(0.f, 0.f, 0.f, 0.f);
                             xb[m] = ok ? *reinterpret_cast<const float4*>(xp + 4) : make_float4(0.f, 0.f, 0.f, 0.f);
                         }
@@ -929,7 +939,7 @@ __device__ __forceinline__ void gemv_range_rx(Ctx& c, const Gemv& g, int slot, i
         long long tc = tb;
         const int ch0 = wide ? lane : (lane & 15);
         const auto load_x = [&](int tk) {
-            const float* xt = xs + (size_t)staging_row(ms, tk) * g.Kc;
+            const float* xt = xs + (size_t)staging_row(ms, tk) * stage_stride(g.Kc);
 #pragma unroll
             for (int q = 0; q < NX; ++q) {
                 const float* xp = xt + (ch0 + 32 * q) * 8;
@@ -1094,7 +1104,7 @@ __device__ __forceinline__ void gemv_range_rx(Ctx& c, const Gemv& g, int slot, i
 __device__ __forceinline__ void gemv_range_smem(Ctx& c, const Gemv& g, int slot, int expert, int j_lo, int j_hi) {
     const Params& p = c.p;
     const float* src = g.src + (size_t)slot * g.src_sstride;
-    const int cap = STAGE_FLOATS / g.Kc;
+    const int cap = STAGE_FLOATS / stage_stride(g.Kc);
     const int M = c.ms.gm;
     for (int j = j_lo; j < j_hi; ++j) {
         const int kc = j / g.n_rb, rb = j - kc * g.n_rb;
@@ -1126,6 +1136,145 @@ __device__ __forceinline__ void gemv_range_smem(Ctx& c, const Gemv& g, int slot,
     }
 }
 
+// ---- tensor-core GEMV (2 to 8 tokens, K panels of 2048 or 1024) ----
+// Per tile of R = 8 NG rows: out[token][row] = sum_k x[token][k] W[row][k] as
+// mma.sync m16n8k16 (bf16 in, fp32 accumulate) with the tokens as the 16
+// rows of A (at most 8 used) and 8 weight rows as the 8 columns of B. Warps
+// split the tile into NG row groups x 8/NG K slices of 256: 16 k-steps per
+// warp. Per k-step a lane converts its two pairs of staged input values into
+// bf16 hi + lo fragments (x = hi + lo keeps ~16 mantissa bits; two MMAs per
+// k-step; fragments are rebuilt per tile: kept for the whole run they would
+// not fit the registers and spill to the stack). The producer copies
+// these tiles row by row into rows Kc*2 + 16 bytes apart, so a warp's B
+// fragment loads (8 rows x 4 lanes) touch 32 distinct banks. The warp frees
+// the slot right after its MMAs, then the 8 warps' partial sums meet in the
+// reduction area.
+__device__ __forceinline__ bool mma_gemv(int ntok, const Gemv& g) {
+    return ntok >= 2 && ntok <= 8 && (g.Kc == 2048 || g.Kc == 1024) && g.R * g.Kc * 2 == TILE_MAX &&
+           g.out_kind != OUT_SCALED;
+}
+__device__ __forceinline__ uint32_t bf2_pack(float a, float b) {  // a: lower k index, low half
+    const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+template <int NG>
+__device__ __forceinline__ void gemv_range_mma(Ctx& c, const Gemv& g, int slot, int j_lo, int j_hi) {
+    const Params& p = c.p;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, tid = threadIdx.x;
+    const int gq = lane >> 2, t4 = lane & 3;
+    constexpr int WK = NCW / NG, KS = 16;  // warps per row group, k-steps per warp
+    const int ngw = warp / WK, kbase = (warp % WK) * KS * 16;
+    const int M = c.ms.gm, Kc = g.Kc, SS = stage_stride(Kc), pitch = Kc * 2 + 16, R = g.R;
+    const int n_rb = g.n_rb, N = g.N, grp_rows = g.grp_rows, grp_stride = g.grp_stride;
+    const int out_kind = g.out_kind, n_kc = g.n_kc, dst_stride = g.dst_stride;
+    float* const dst = g.dst + (size_t)slot * g.dst_sstride;
+    float* const dst2 = g.dst2;
+    const float* src = g.src + (size_t)slot * g.src_sstride;
+    Misc& ms = c.ms;
+    uint8_t* const ring = c.smem + SMEM_RING;
+    const float* const xs = c.stage();
+    float* const part = c.red();  // [warp][token 8][row 8] partial sums (lower half of the area)
+    CRing cr = c.cr;
+    bool dead = c.dead, timed_out = false;
+    int j = j_lo;
+    while (j < j_hi) {
+        const int kc0 = j / n_rb, rb0 = j - kc0 * n_rb;
+        const int g0 = grp_rows ? (rb0 * R) / grp_rows : 0;
+        const int jend = run_end(j, j_hi, n_rb, rb0, R, grp_rows, g0);
+        const long long ta = p.trace_items ? gtimer() : 0;
+        restage(c, g, src, g0 * grp_stride, kc0, 0, ms.gather ? ms.gm : p.M);
+        const long long tb = p.trace_items ? gtimer() : 0;
+        long long tc = tb;
+        // this warp's input: token gq (tokens >= M contribute zeros), k = kbase + 16 s + 2 t4 (+8)
+        const bool xok = gq < M;
+        const float* xr = xs + (size_t)(xok ? staging_row(ms, gq) : 0) * SS + kbase + 2 * t4;
+        const int jrun = j;
+        for (; j < jend; ++j) {
+            const int r0 = (rb0 + (j - jrun)) * R, nr = min(R, N - r0);
+            const uint8_t* tile = nullptr;
+            if (!dead) {
+                if (spin_wait(p, &ms.full[cr.slot], cr.phase))
+                    tile = ring + cr.slot * SLOT_BYTES;
+                else
+                    dead = timed_out = true;
+            }
+            if (p.trace_items && j == jrun) tc = gtimer();
+            float hsum[4] = {0.f, 0.f, 0.f, 0.f}, lsum[4] = {0.f, 0.f, 0.f, 0.f};
+            if (tile) {
+                const uint8_t* tr = tile + (size_t)(ngw * 8 + gq) * pitch + (size_t)kbase * 2 + 4 * t4;
+#pragma unroll 4
+                for (int s2 = 0; s2 < KS; ++s2) {
+                    const uint32_t b0 = *reinterpret_cast<const uint32_t*>(tr + 32 * s2);
+                    const uint32_t b1 = *reinterpret_cast<const uint32_t*>(tr + 32 * s2 + 16);
+                    const float2 u = xok ? *reinterpret_cast<const float2*>(xr + 16 * s2) : make_float2(0.f, 0.f);
+                    const float2 v = xok ? *reinterpret_cast<const float2*>(xr + 16 * s2 + 8) : make_float2(0.f, 0.f);
+                    const uint32_t h0 = bf2_pack(u.x, u.y), h1 = bf2_pack(v.x, v.y);
+                    const uint32_t a_h[4] = {h0, 0u, h1, 0u};
+                    const uint32_t a_l[4] = {bf2_pack(u.x - bf_lo(h0), u.y - bf_hi(h0)), 0u,
+                                             bf2_pack(v.x - bf_lo(h1), v.y - bf_hi(h1)), 0u};
+                    mma_bf16(hsum, a_h, b0, b1);
+                    mma_bf16(lsum, a_l, b0, b1);
+                }
+            }
+            // the warp has read its part of the tile: hand the slot back
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ms.empty[cr.slot]);
+            if (++cr.slot == NSLOT) {
+                cr.slot = 0;
+                cr.phase ^= 1u;
+            }
+            // token gq, rows 2 t4 and 2 t4 + 1 of this warp's row group
+            *reinterpret_cast<float2*>(part + (warp * 8 + gq) * 8 + 2 * t4) =
+                make_float2(hsum[0] + lsum[0], hsum[1] + lsum[1]);
+            cbar();
+            if (tile) {
+                for (int t = tid; t < M * R; t += NCT) {
+                    const int m = t / R, r = t - m * R;
+                    if (r >= nr) continue;
+                    const int ng = r >> 3, rr = r & 7;
+                    float y = 0.f;
+#pragma unroll
+                    for (int k = 0; k < WK; ++k) y += part[((ng * WK + k) * 8 + m) * 8 + rr];
+                    const int row = r0 + r;
+                    float* d = dst + (size_t)m * dst_stride + row;
+                    if (out_kind == OUT_STORE) {
+                        if (n_kc == 1)
+                            *d = y;
+                        else
+                            atomicAdd(d, y);
+                    } else if (out_kind == OUT_RESID) {
+                        if (n_kc == 1) {
+                            const float nv = __ldcg(d) + y;
+                            *d = nv;
+                            dst2[(size_t)m * dst_stride + row] = nv;
+                        } else {
+                            atomicAdd(d, y);
+                        }
+                    } else {  // OUT_ACC
+                        *d += y;
+                    }
+                }
+            }
+            cbar();  // the partials have been read
+        }
+        if (p.trace_items && threadIdx.x == 0) trace_rec(c, 0x80000000u | c.cur_code, (unsigned)(tb - ta), ta, tc);
+    }
+    if (timed_out) {
+        ms.abort = 1;
+        raise_status(p, ST_TIMEOUT, 0x230u);
+    }
+    c.set_ring(cr);
+    if (dead) c.dead = true;
+}
+
+__device__ __noinline__ void gemv_mma(Ctx& c, const Gemv& g, int slot, int j_lo, int j_hi) {
+    if (g.Kc == 2048)
+        gemv_range_mma<1>(c, g, slot, j_lo, j_hi);
+    else
+        gemv_range_mma<2>(c, g, slot, j_lo, j_hi);
+}
+
 // consumer: GEMV work items [j_lo, j_hi) of one slot, two or more tokens:
 // split-K path when every token's K panel is staged at once, shared-memory
 // path otherwise. A function of
@@ -1136,7 +1285,7 @@ __device__ __noinline__ void gemv_multi(Ctx& c, const Gemv& g, int slot, int exp
     const bool narrow = g.Kc == 128 || g.Kc == 768;  // row slices of 16 / 12 chunks
     // split K (input in registers for the whole run, two tokens at a time)
     // when every token's K panel is staged at once
-    const bool ks = M >= 2 && nks > 0 && g.R <= (8 / nks) * (narrow ? 16 : 8) && M * g.Kc <= STAGE_FLOATS;
+    const bool ks = M >= 2 && nks > 0 && g.R <= (8 / nks) * (narrow ? 16 : 8) && stage_fits(M, g.Kc);
     if (!ks)
         gemv_range_smem(c, g, slot, expert, j_lo, j_hi);
     else if (narrow)
@@ -1153,7 +1302,9 @@ __device__ __noinline__ void cons_gemv(Ctx& c, const Gemv& g, int slot, int expe
     // K panels of 2048 and 1024: the register path also for 2 to 4 tokens
     // (each tile once per token)
     const bool mt = M >= 2 && M <= 4 && g.out_kind != OUT_SCALED;
-    if (M == 1 && Kc == 2048)
+    if (mma_gemv(M, g))
+        gemv_mma(c, g, slot, j_lo, j_hi);
+    else if (M == 1 && Kc == 2048)
         gemv_range_rx<8>(c, g, slot, expert, j_lo, j_hi);
     else if (mt && Kc == 2048)
         gemv_range_rx<8, true>(c, g, slot, expert, j_lo, j_hi);
@@ -1195,7 +1346,11 @@ __device__ __forceinline__ void prefetch_tiles(const Gemv& g, int expert, int lo
 constexpr int PF_TILES = MK_PF_TILES;            // L2 prefetch distance beyond the ring, in tiles
 constexpr int UNIT_PF_BYTES = MK_UNIT_PF_BYTES;  // expert units: L2 prefetch up front, per CTA
 
-__device__ __noinline__ void prod_gemv(Ctx& c, const Gemv& g, int expert, int lo, int hi) {
+// producer: bulk-load the weight tiles of items [lo, hi) (one slot); tiles a
+// tensor-core GEMV of `ntok` tokens reads (mma_gemv) are copied row by row
+// into rows Kc*2 + 16 bytes apart. All descriptor fields and the ring state
+// live in registers for the loop.
+__device__ __noinline__ void prod_gemv(Ctx& c, const Gemv& g, int expert, int lo, int hi, int ntok) {
     const uint16_t* W = g.W + (expert >= 0 ? (size_t)expert * g.w_estride : 0);
     const int n_rb = g.n_rb, R = g.R, N = g.N, Kc = g.Kc;
     const Params& p = c.p;
@@ -1203,7 +1358,9 @@ __device__ __noinline__ void prod_gemv(Ctx& c, const Gemv& g, int expert, int lo
     uint8_t* ring = c.smem + SMEM_RING;
     PRing pr = c.pr;
     int issued = c.issued;
-    const bool leader = (threadIdx.x & 31) == 0;
+    const int lane = threadIdx.x & 31;
+    const bool leader = lane == 0;
+    const bool pad = mma_gemv(ntok, g);
     const unsigned long long pol = l2_evict_first();
     // panel / row block of item j and of item j + PF_TILES, advanced per item;
     // the window's first tiles go towards L2 after the first copy is issued
@@ -1229,7 +1386,7 @@ __device__ __noinline__ void prod_gemv(Ctx& c, const Gemv& g, int expert, int lo
         if (leader) {
             if (spin_wait(p, &ms.empty[pr.slot], pr.phase ^ 1u)) {
                 mbar_expect_tx(&ms.full[pr.slot], bytes);
-                bulk_g2s_pol(ring + pr.slot * SLOT_BYTES, src, bytes, &ms.full[pr.slot], pol);
+                if (!pad) bulk_g2s_pol(ring + pr.slot * SLOT_BYTES, src, bytes, &ms.full[pr.slot], pol);
             } else {
                 ok = 0;
             }
@@ -1240,6 +1397,10 @@ __device__ __noinline__ void prod_gemv(Ctx& c, const Gemv& g, int expert, int lo
             c.dead = true;
             break;
         }
+        if (pad && lane < nr)  // nr <= 16 rows (tiles of 16 KB-per-row halves)
+            bulk_g2s_pol(ring + pr.slot * SLOT_BYTES + (size_t)lane * (Kc * 2 + 16), src + (size_t)lane * Kc,
+                         (unsigned)Kc * 2u, &ms.full[pr.slot], pol);
+        __syncwarp();
         ++issued;
         prod_next(pr);
         if (j == lo) prefetch_tiles(g, expert, lo + 1, min(hi, lo + PF_TILES));
@@ -1431,7 +1592,7 @@ __device__ __noinline__ void qb_fused_prod(Ctx& c, int lo, int hi) {
     const Gemv& g = Ld.g[G_QB];
     const int qh = p.nope + p.rd, R = g.R;
     for (int j = lo; j < hi && !c.dead; ++j) {
-        prod_gemv(c, g, -1, j, j + 1);
+        prod_gemv(c, g, -1, j, j + 1, p.M);
         const int r0 = j * R, h = r0 / qh, i0 = r0 - h * qh;
         if (c.dead || i0 >= p.nope) continue;
         const unsigned bytes = (unsigned)R * MLA_KL * 2u;
@@ -2678,7 +2839,9 @@ __device__ __forceinline__ void load_layer(Ctx& c, int l) {
 }
 
 // ======================================================= producer leaves ====
-__device__ __noinline__ void prod_plain(Ctx& c, const Gemv& g, int lo, int hi) { prod_gemv(c, g, -1, lo, hi); }
+__device__ __noinline__ void prod_plain(Ctx& c, const Gemv& g, int lo, int hi) {
+    prod_gemv(c, g, -1, lo, hi, c.p.M);
+}
 
 // attention chunks of items [lo, hi) into the ring
 __device__ __noinline__ void prod_attn(Ctx& c, int l, int lo, int hi) {
@@ -2820,7 +2983,7 @@ __device__ __noinline__ void unit_seg_cons(Ctx& c, int l, int kind, int expert, 
     // tokens [m_lo, m_hi), gathered when not every token's input is staged
     if (tid < 32) {
         const bool one_panel = p.M > 1 && Ld.ffn.n_kc == 1;
-        const bool all_staged = one_panel && p.M * Ld.ffn.Kc <= STAGE_FLOATS;
+        const bool all_staged = one_panel && stage_fits(p.M, Ld.ffn.Kc);
         const bool compact = expert >= 0 && one_panel;
         const int lane = tid;
         float w[2];
@@ -2830,7 +2993,9 @@ __device__ __noinline__ void unit_seg_cons(Ctx& c, int l, int kind, int expert, 
             const int m = lane + 32 * q;
             const bool in = expert < 0 ? m >= m_lo && m < m_hi : m < p.M;
             w[q] = in ? (expert < 0 ? 1.0f : route_weight(c.ms, m, expert, p.topk)) : 0.f;
-            sel[q] = in && (!compact || w[q] != 0.f);
+            // (the producer streams this unit's tiles for the same number of
+            // tokens: the routing count, tokens of weight 0 included)
+            sel[q] = in && (!compact || routed_to(c.ms, m, expert, p.topk));
         }
         const unsigned b0 = __ballot_sync(0xffffffffu, sel[0]), b1 = __ballot_sync(0xffffffffu, sel[1]);
         const unsigned lt = (1u << lane) - 1u;
@@ -2939,7 +3104,7 @@ __device__ __noinline__ void unit_seg_cons(Ctx& c, int l, int kind, int expert, 
 }
 
 // producer: the segment's tiles into the ring (and, first, towards L2)
-__device__ __noinline__ void unit_seg_prod(Ctx& c, int kind, int expert, int u0, int u1) {
+__device__ __noinline__ void unit_seg_prod(Ctx& c, int kind, int expert, int u0, int u1, int ntok) {
     const Params& p = c.p;
     const Layer& Ld = c.layer();
     const FfnKind& K = Ld.ffn.k[kind];
@@ -2952,7 +3117,7 @@ __device__ __noinline__ void unit_seg_prod(Ctx& c, int kind, int expert, int u0,
     // the first ring-full of gate/up tiles is requested before the L2
     // prefetch of the rest of the segment, which would queue ahead of it
     const int first = min(NSLOT, (u1 - u0) * rpu);
-    prod_gemv(c, c.ms.pug, -1, u0 * rpu, u0 * rpu + first);
+    prod_gemv(c, c.ms.pug, -1, u0 * rpu, u0 * rpu + first, ntok);
     // then the L2 prefetch of the segment's first units (per K panel their
     // gate/up rows are contiguous, and so are their down blocks; pieces of at
     // most 64 KB, one lane each). Only about UNIT_PF_BYTES per CTA up front:
@@ -2974,7 +3139,7 @@ __device__ __noinline__ void unit_seg_prod(Ctx& c, int kind, int expert, int u0,
         for (size_t o = (size_t)lane * piece; o < n; o += 32 * piece) l2_prefetch(b + o, (unsigned)(min(piece, n - o) * 2));
     }
     for (int kc = 0; kc < Ld.ffn.n_kc && !c.dead; ++kc)
-        prod_gemv(c, c.ms.pug, -1, kc * n_rb + u0 * rpu + (kc == 0 ? first : 0), kc * n_rb + u1 * rpu);
+        prod_gemv(c, c.ms.pug, -1, kc * n_rb + u0 * rpu + (kc == 0 ? first : 0), kc * n_rb + u1 * rpu, ntok);
     Misc& ms = c.ms;
     uint8_t* ring = c.smem + SMEM_RING;
     PRing pr = c.pr;
@@ -3027,7 +3192,7 @@ __device__ __noinline__ void ffn_stage(Ctx& c, int l) {
     // unit x group): groups of 4 when every token's input is staged in one K
     // panel (more CTAs, and the register GEMV path); groups as large as the
     // staging area holds when not (each group's tokens gathered there)
-    const bool stage_all = p.M > 1 && Ld.ffn.n_kc == 1 && p.M * Ld.ffn.Kc <= STAGE_FLOATS;
+    const bool stage_all = p.M > 1 && Ld.ffn.n_kc == 1 && stage_fits(p.M, Ld.ffn.Kc);
     const int tgs = shared_group(p.M, Ld.ffn.n_kc, Ld.ffn.Kc);
     const int ntg = (p.M + tgs - 1) / tgs;
     if ((int)blockIdx.x < p.gs) {
@@ -3045,12 +3210,11 @@ __device__ __noinline__ void ffn_stage(Ctx& c, int l) {
                 }
                 for (int i = lo; i < hi && !(PROD && c.dead);) {
                     const int tg = i / nu, iend = min(hi, (tg + 1) * nu);
-                    if constexpr (PROD) {
-                        unit_seg_prod(c, 1, -1, i - tg * nu, iend - tg * nu);
-                    } else {
-                        const int m0 = tg * tgs, m1 = min(p.M, m0 + tgs);
+                    const int m0 = tg * tgs, m1 = min(p.M, m0 + tgs);
+                    if constexpr (PROD)
+                        unit_seg_prod(c, 1, -1, i - tg * nu, iend - tg * nu, m1 - m0);
+                    else
                         unit_seg_cons(c, l, 1, -1, i - tg * nu, iend - tg * nu, m0, m1);
-                    }
                     i = iend;
                 }
                 done += hi - lo;
@@ -3068,7 +3232,7 @@ __device__ __noinline__ void ffn_stage(Ctx& c, int l) {
             if (threadIdx.x == 0) unit_gemv(p, Ld, c.ms.ug, 0, 0, 0, 1, c.red() + RED_FLOATS / 2);
             set_deps(c, deps1(l, C_O, (unsigned)gemv_items(Ld.g[G_O])));
             cwait(c, 0x1200u | (unsigned)(l << 16));
-            if (p.M * Ld.ffn.Kc <= STAGE_FLOATS) restage(c, c.ms.ug, Ld.x, 0, 0, 0, p.M);
+            if (stage_fits(p.M, Ld.ffn.Kc)) restage(c, c.ms.ug, Ld.x, 0, 0, 0, p.M);
         }
         const long long tr0 = p.trace_items ? gtimer() : 0;
         if (!route<PROD>(c, l) && PROD) {
@@ -3086,7 +3250,8 @@ __device__ __noinline__ void ffn_stage(Ctx& c, int l) {
         for (int i = lo; i < hi && !(PROD && c.dead);) {
             const int s2 = i / K.nu, iend = min(hi, (s2 + 1) * K.nu);
             if constexpr (PROD)
-                unit_seg_prod(c, 0, slot_e[s2], i - s2 * K.nu, iend - s2 * K.nu);
+                unit_seg_prod(c, 0, slot_e[s2], i - s2 * K.nu, iend - s2 * K.nu,
+                              p.M > 1 && Ld.ffn.n_kc == 1 ? (int)c.ms.p_used[slot_e[s2]] : p.M);
             else
                 unit_seg_cons(c, l, 0, slot_e[s2], i - s2 * K.nu, iend - s2 * K.nu, 0, p.M);
             i = iend;
