@@ -453,7 +453,12 @@ __device__ __forceinline__ int gqa_target(const Params& p) {
     return t < 1 ? 1 : t;
 }
 __device__ __forceinline__ int mla_target(const Params& p) {
-    int t = p.G / (p.B * p.T);
+    // splits per query row: one item per CTA; when that leaves CTAs idle
+    // (B T does not divide the grid well), about three items per CTA
+    const int rows = p.B * p.T;
+    int t = p.G / rows;
+    if (t < 4 && t * rows < p.G - p.G / 8) t = (3 * p.G) / rows;
+    t = t > p.s_max ? p.s_max : t;
     return t < 1 ? 1 : t;
 }
 __device__ __forceinline__ int nch_of(const Params& p, int b, int ch) { return (p.pos[b] + ch - 1) / ch; }

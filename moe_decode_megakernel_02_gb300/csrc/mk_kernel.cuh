@@ -2980,7 +2980,9 @@ __device__ __noinline__ void unit_seg_cons(Ctx& c, int l, int kind, int expert, 
     // every token's input is staged there (the routed CTAs stage it before
     // routing), else its own tokens are gathered into the staging area --
     // and otherwise all tokens, weight 0 or not; the shared expert takes
-    // tokens [m_lo, m_hi), gathered when not every token's input is staged
+    // tokens [m_lo, m_hi), gathered when not every token's input is staged.
+    // A routed expert with more tokens than the staging area holds runs once
+    // per group: entries [m_lo, m_hi) of its list of tokens.
     if (tid < 32) {
         const bool one_panel = p.M > 1 && Ld.ffn.n_kc == 1;
         const bool all_staged = one_panel && stage_fits(p.M, Ld.ffn.Kc);
@@ -2997,8 +2999,15 @@ __device__ __noinline__ void unit_seg_cons(Ctx& c, int l, int kind, int expert, 
             // tokens: the routing count, tokens of weight 0 included)
             sel[q] = in && (!compact || routed_to(c.ms, m, expert, p.topk));
         }
-        const unsigned b0 = __ballot_sync(0xffffffffu, sel[0]), b1 = __ballot_sync(0xffffffffu, sel[1]);
+        unsigned b0 = __ballot_sync(0xffffffffu, sel[0]), b1 = __ballot_sync(0xffffffffu, sel[1]);
         const unsigned lt = (1u << lane) - 1u;
+        if (compact) {  // this group's entries of the expert's token list
+            const int q0 = __popc(b0 & lt), q1 = __popc(b0) + __popc(b1 & lt);
+            sel[0] = sel[0] && q0 >= m_lo && q0 < m_hi;
+            sel[1] = sel[1] && q1 >= m_lo && q1 < m_hi;
+            b0 = __ballot_sync(0xffffffffu, sel[0]);
+            b1 = __ballot_sync(0xffffffffu, sel[1]);
+        }
         const int pos[2] = {__popc(b0 & lt), __popc(b0) + __popc(b1 & lt)};
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
@@ -3009,8 +3018,9 @@ __device__ __noinline__ void unit_seg_cons(Ctx& c, int l, int kind, int expert, 
         }
         if (lane == 0) {
             c.ms.gm = __popc(b0) + __popc(b1);
+            // a key per token list: routed expert and group, or shared group
             c.ms.gather = one_panel && !all_staged && (expert >= 0 || m_hi - m_lo < p.M)
-                              ? (expert >= 0 ? expert + 1 : 1024 + m_lo)
+                              ? (expert >= 0 ? 1 + expert + 256 * m_lo : (1 << 24) + m_lo)
                               : 0;
         }
     }
@@ -3247,14 +3257,25 @@ __device__ __noinline__ void ffn_stage(Ctx& c, int l) {
         int lo, hi;
         routed_range(PROD ? c.ms.p_used : c.ms.used, slot_e, nslots, K.nu, (int)blockIdx.x - p.gs,
                      p.G - p.gs - p.gr, lo, hi);
-        for (int i = lo; i < hi && !(PROD && c.dead);) {
-            const int s2 = i / K.nu, iend = min(hi, (s2 + 1) * K.nu);
+        // a routed expert's units take its own tokens (one K panel), in groups
+        // of as many as the staging area holds when not all tokens fit it
+        // (g0: the group's first entry of the expert's token list)
+        for (int i = lo, g0 = 0; i < hi && !(PROD && c.dead);) {
+            const int s2 = i / K.nu, iend = min(hi, (s2 + 1) * K.nu), e = slot_e[s2];
+            const bool one_panel = p.M > 1 && Ld.ffn.n_kc == 1;
+            const int cnt = one_panel ? (int)(PROD ? c.ms.p_used[e] : c.ms.used[e]) : p.M;
+            const int cap = one_panel && !stage_fits(p.M, Ld.ffn.Kc) ? STAGE_FLOATS / stage_stride(Ld.ffn.Kc) : MAX_M;
+            const int g1 = min(cnt, g0 + cap);
             if constexpr (PROD)
-                unit_seg_prod(c, 0, slot_e[s2], i - s2 * K.nu, iend - s2 * K.nu,
-                              p.M > 1 && Ld.ffn.n_kc == 1 ? (int)c.ms.p_used[slot_e[s2]] : p.M);
+                unit_seg_prod(c, 0, e, i - s2 * K.nu, iend - s2 * K.nu, one_panel ? g1 - g0 : p.M);
             else
-                unit_seg_cons(c, l, 0, slot_e[s2], i - s2 * K.nu, iend - s2 * K.nu, 0, p.M);
-            i = iend;
+                unit_seg_cons(c, l, 0, e, i - s2 * K.nu, iend - s2 * K.nu, g0, g1);
+            if (g1 < cnt) {
+                g0 = g1;
+            } else {
+                g0 = 0;
+                i = iend;
+            }
         }
         done = hi - lo;
     }
