@@ -159,10 +159,10 @@ struct Params {
     float* logits;
     int* accept;
     int* amax;
-    float* zptr[6];
-    long long zn[6];                // floats to zero at the start of the step
+    float* zptr[10];
+    long long zn[10];               // floats to zero at the start of the step
     int nz, carry;                  // carry: residual copied by items (split-K output projection)
-    int gs, gr;                     // CTAs [0, gs): shared expert, [G-gr, G): router, between: routed experts
+    int gs, gr;                     // CTAs [0, gs): shared expert, [gs, G): routed experts ([G-gr, G) first run the router)
     int stall;                      // testing: CTA 0 first waits on a counter nothing signals (ends in a timeout)
     // one launch per stage (the unfused comparison path): 0 = the whole step
     // in this launch; 1 = program positions [st_lo, st_hi) only, 2 = the

@@ -180,11 +180,22 @@ int validate(const mk_config* c) {
 
 int gemv_items_host(const mk::Gemv& g) { return g.n_rb * g.n_kc; }
 
-void make_gemv(mk::Gemv& g, const uint16_t* W, int N, int K, int in_kind, const float* src, int src_stride,
-               const uint16_t* gain, int out_kind, float* dst, int dst_stride, float* dst2 = nullptr) {
-    std::memset(&g, 0, sizeof g);
+// K panel of a matrix with K columns: the whole row up to 2048, else the
+// largest of 1024 / 512 / 256 dividing K; narrower (down to 256) while Mx
+// tokens' staged input rows would not fit the staging area at once (models
+// loaded for many tokens per step: their stages then stage each panel once
+// per run of items instead of re-staging token chunks for every tile)
+int panel_width(int K, int Mx) {
     int Kc = K;
     if (K > 2048) Kc = K % 1024 == 0 ? 1024 : (K % 512 == 0 ? 512 : 256);
+    while (Kc > 256 && !mk::stage_fits(Mx, Kc) && K % (Kc / 2) == 0) Kc /= 2;
+    return Kc;
+}
+
+void make_gemv(mk::Gemv& g, const uint16_t* W, int N, int K, int in_kind, const float* src, int src_stride,
+               const uint16_t* gain, int out_kind, float* dst, int dst_stride, int Mx, float* dst2 = nullptr) {
+    std::memset(&g, 0, sizeof g);
+    const int Kc = panel_width(K, Mx);
     int R = (mk::TILE_MAX / (2 * Kc)) / 8 * 8;
     if (R > N) R = N;
     g.W = W;
@@ -474,7 +485,7 @@ int mk_load_weights(const mk_config* cfg, const mk_weight* table, int32_t n, voi
     } while (0)
 #define PACK(dst, N, K, row0, src, rows)                                                              \
     do {                                                                                              \
-        const int Kc_ = (K) > 2048 ? ((K) % 1024 == 0 ? 1024 : ((K) % 512 == 0 ? 512 : 256)) : (K); \
+        const int Kc_ = panel_width((K), (int)Mx);                                                      \
         if ((r = pack_rows(dst, N, K, Kc_, row0, src, rows, (size_t)(K) * 2, s))) return bail(r);     \
     } while (0)
     NEED(MK_W_EMBED, -1, 0);
@@ -590,7 +601,7 @@ int mk_load_weights(const mk_config* cfg, const mk_weight* table, int32_t n, voi
         Ld.a = a;
         Ld.a_stride = D.a_rows;
         Ld.o = ob;
-        make_gemv(Ld.g[mk::G_A], W + o.a, D.a_rows, d, mk::IN_RMS, x, d, W + o.an, mk::OUT_STORE, a, D.a_rows);
+        make_gemv(Ld.g[mk::G_A], W + o.a, D.a_rows, d, mk::IN_RMS, x, d, W + o.an, mk::OUT_STORE, a, D.a_rows, Mxi);
         if (!D.gqa) {
             float* q = F(s_q) + (size_t)l * Mx * D.Hq * D.qh;
             float* qlat = F(s_qlat) + (size_t)l * Mx * D.Hq * D.kl;
@@ -602,17 +613,17 @@ int mk_load_weights(const mk_config* cfg, const mk_weight* table, int32_t n, voi
             Ld.uk = W + o.uk;
             Ld.uvq = W + o.uvq;
             make_gemv(Ld.g[mk::G_QB], W + o.uq, D.Hq * D.qh, D.ql, mk::IN_RMS, a, D.a_rows, W + o.qn, mk::OUT_STORE,
-                      q, D.Hq * D.qh);
+                      q, D.Hq * D.qh, Mxi);
             make_gemv(Ld.g[mk::G_QLAT], W + o.ukT, D.Hq * D.kl, D.nope, mk::IN_COPY, q, D.Hq * D.qh, nullptr,
-                      mk::OUT_STORE, qlat, D.Hq * D.kl);
+                      mk::OUT_STORE, qlat, D.Hq * D.kl, Mxi);
             Ld.g[mk::G_QLAT].grp_rows = D.kl;
             Ld.g[mk::G_QLAT].grp_stride = D.qh;
             make_gemv(Ld.g[mk::G_UV], W + o.uv, D.Hq * D.vd, D.kl, mk::IN_COPY, olat, D.Hq * D.kl, nullptr,
-                      mk::OUT_STORE, ob, D.Hq * D.vd);
+                      mk::OUT_STORE, ob, D.Hq * D.vd, Mxi);
             Ld.g[mk::G_UV].grp_rows = D.vd;
             Ld.g[mk::G_UV].grp_stride = D.kl;
         }
-        make_gemv(Ld.g[mk::G_O], W + o.o, d, D.o_in, mk::IN_COPY, ob, D.o_in, nullptr, mk::OUT_RESID, x, d, xn);
+        make_gemv(Ld.g[mk::G_O], W + o.o, d, D.o_in, mk::IN_COPY, ob, D.o_in, nullptr, mk::OUT_RESID, x, d, Mxi, xn);
         Ld.ffn.gain = W + o.fn;
         auto set_kind = [&](mk::FfnKind& K, int Fi, const uint16_t* gu, const uint16_t* dn) {
             K.gu = gu;
@@ -633,7 +644,7 @@ int mk_load_weights(const mk_config* cfg, const mk_weight* table, int32_t n, voi
             float* rlog = F(s_rlog) + (size_t)l * Mx * mk::router_row(D.E);
             Ld.rlog = rlog;
             make_gemv(Ld.g[mk::G_ROUTER], W + o.router, D.E, d, mk::IN_RMS, x, d, W + o.fn, mk::OUT_STORE, rlog,
-                      mk::router_row(D.E));
+                      mk::router_row(D.E), Mxi);
             set_kind(Ld.ffn.k[0], D.ffn, W + o.gu, W + o.down);
         }
         if (D.sh) set_kind(Ld.ffn.k[1], D.sffn, W + o.shgu, W + o.shdown);
@@ -653,7 +664,7 @@ int mk_load_weights(const mk_config* cfg, const mk_weight* table, int32_t n, voi
     P.layers = m->d_layers;
     P.embed = W + off_embed;
     make_gemv(P.lm, W + off_lm, D.V, d, mk::IN_RMS, F(s_x) + (size_t)L * Mx * d, d, W + off_fn, mk::OUT_STORE,
-              nullptr, D.V);
+              nullptr, D.V, (int)Mx);
     P.rope = reinterpret_cast<const float2*>(S + s_rope);
     P.rope_half = rope_dim / 2;
     P.rope_npos = npos;
@@ -681,6 +692,25 @@ int mk_load_weights(const mk_config* cfg, const mk_weight* table, int32_t n, voi
     if (P.carry) {
         P.zptr[nz] = F(s_x) + (size_t)Mx * d;
         P.zn[nz++] = (long long)L * Mx * d;
+    }
+    // outputs of the other projections that split K into panels
+    if (!D.gqa && m->layers[0].g[mk::G_QB].n_kc > 1) {
+        P.zptr[nz] = F(s_q);
+        P.zn[nz++] = (long long)L * Mx * D.Hq * D.qh;
+    }
+    if (!D.gqa && (m->layers[0].g[mk::G_QLAT].n_kc > 1 || m->layers[0].g[mk::G_UV].n_kc > 1)) {
+        if (m->layers[0].g[mk::G_QLAT].n_kc > 1) {
+            P.zptr[nz] = F(s_qlat);
+            P.zn[nz++] = (long long)L * Mx * D.Hq * D.kl;
+        }
+        if (m->layers[0].g[mk::G_UV].n_kc > 1) {
+            P.zptr[nz] = F(s_o);
+            P.zn[nz++] = (long long)L * Mx * D.o_in;
+        }
+    }
+    if (D.E && m->layers[0].g[mk::G_ROUTER].n_kc > 1) {
+        P.zptr[nz] = F(s_rlog);
+        P.zn[nz++] = (long long)L * Mx * mk::router_row(D.E);
     }
     // the router folded into the output projection: possible when that
     // projection has one K panel (its rows are final in the CTA that computes
@@ -837,10 +867,11 @@ int mk_kv_read(const mk_kv* kv, int32_t layer, int32_t seq, int32_t pos0, int32_
     return kv_copy(kv, layer, seq, pos0, n, rows, stream, 0);
 }
 
-// FFN CTA groups: gr CTAs run the router (one per router tile), gs CTAs the
-// shared expert's units, the rest the routed experts' units; gs follows the
-// two kinds' expected work, the routed unit count taken as the expected
-// number of distinct experts of M tokens picking top_k of E uniformly at random
+// FFN CTA groups: gr CTAs run the router (one per router tile) and then,
+// with the CTAs from gs on, the routed experts' units; CTAs [0, gs) run the
+// shared expert's units; gs follows the two kinds' expected work, the routed
+// unit count taken as the expected number of distinct experts of M tokens
+// picking top_k of E uniformly at random
 static void ffn_split(const mk_model* m, int M, bool rfuse, int& gs, int& gr) {
     const Dims D = dims_of(m->cfg);
     const mk::Layer& L0 = m->layers[0];
@@ -864,7 +895,7 @@ static void ffn_split(const mk_model* m, int M, bool rfuse, int& gs, int& gr) {
     const int ntg = (M + tgs - 1) / tgs;
     const double us = L0.ffn.k[1].nu * ntg * cost(M / (double)ntg);
     const double ur = uniq * L0.ffn.k[0].nu * cost(M > 1 && L0.ffn.n_kc == 1 ? M * D.k / uniq : M);
-    const int avail = m->G - gr;
+    const int avail = m->G;  // the router CTAs also take routed units after their router tile
     gs = (int)std::lround(avail * us / (us + ur));
     if (gs < 1) gs = 1;
     if (gs > avail - 1) gs = avail - 1;

@@ -354,26 +354,37 @@ __device__ __noinline__ void stage_input(Ctx& c, const Gemv& g, const float* src
         const uint16_t* gain = g.gain;
         float part = 0.f;
         int cur = -1;
-#pragma unroll 4
-        for (int i = tid * 4; i < tot; i += NCT * 4) {
-            const int t = i / rowlen;
-            const float4 v = __ldcg(
-                reinterpret_cast<const float4*>(src + (size_t)staged_token(c.ms, m0, t) * g.src_stride + i - t * rowlen));
-            // a warp's 128 consecutive floats never straddle a row (rows are
-            // multiples of 128 floats), so `t` changes uniformly in the warp
-            if (t != cur) {
-                if (cur >= 0) {
+        // 4 loads per thread in flight per round trip (the rows were written
+        // by other SMs moments ago: every load goes to L2)
+        for (int i0 = tid * 4; i0 < tot; i0 += NCT * 4 * 4) {
+            float4 v[4];
 #pragma unroll
-                    for (int o = 16; o; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
-                    if (lane == 0) atomicAdd(&acc[cur], part);
-                }
-                part = 0.f;
-                cur = t;
+            for (int u = 0; u < 4; ++u) {
+                const int i = i0 + u * NCT * 4, t = i / rowlen;
+                v[u] = i < tot ? __ldcg(reinterpret_cast<const float4*>(
+                                     src + (size_t)staged_token(c.ms, m0, t) * g.src_stride + i - t * rowlen))
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
             }
-            part = fmaf(v.x, v.x, part);
-            part = fmaf(v.y, v.y, part);
-            part = fmaf(v.z, v.z, part);
-            part = fmaf(v.w, v.w, part);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int i = i0 + u * NCT * 4, t = i / rowlen;
+                if (i >= tot) break;  // uniform in the warp
+                // a warp's 128 consecutive floats never straddle a row (rows are
+                // multiples of 128 floats), so `t` changes uniformly in the warp
+                if (t != cur) {
+                    if (cur >= 0) {
+#pragma unroll
+                        for (int o = 16; o; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+                        if (lane == 0) atomicAdd(&acc[cur], part);
+                    }
+                    part = 0.f;
+                    cur = t;
+                }
+                part = fmaf(v[u].x, v[u].x, part);
+                part = fmaf(v[u].y, v[u].y, part);
+                part = fmaf(v[u].z, v[u].z, part);
+                part = fmaf(v[u].w, v[u].w, part);
+            }
         }
         if (cur >= 0) {
 #pragma unroll
@@ -1149,9 +1160,14 @@ __device__ __forceinline__ void gemv_range_smem(Ctx& c, const Gemv& g, int slot,
 // fragment loads (8 rows x 4 lanes) touch 32 distinct banks. The warp frees
 // the slot right after its MMAs, then the 8 warps' partial sums meet in the
 // reduction area.
+// tensor-core tiles: 2 to 8 tokens on K panels of 2048 / 1024 (R = 8 / 16
+// rows), 2 to 64 tokens on K panels of 256 (R = 64 rows, the panels of models
+// loaded for many tokens per step, gemv_range_mma_wide)
+__device__ __forceinline__ bool mma_wide(const Gemv& g) { return g.Kc == 256 && g.R == 64; }
 __device__ __forceinline__ bool mma_gemv(int ntok, const Gemv& g) {
-    return ntok >= 2 && ntok <= 8 && (g.Kc == 2048 || g.Kc == 1024) && g.R * g.Kc * 2 == TILE_MAX &&
-           g.out_kind != OUT_SCALED;
+    if (ntok < 2 || g.out_kind == OUT_SCALED) return false;
+    if (mma_wide(g)) return ntok <= MAX_M;
+    return ntok <= 8 && (g.Kc == 2048 || g.Kc == 1024) && g.R * g.Kc * 2 == TILE_MAX;
 }
 __device__ __forceinline__ uint32_t bf2_pack(float a, float b) {  // a: lower k index, low half
     const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
@@ -1268,8 +1284,123 @@ __device__ __forceinline__ void gemv_range_mma(Ctx& c, const Gemv& g, int slot, 
     if (dead) c.dead = true;
 }
 
+// ---- tensor-core GEMV on K panels of 256 (64 rows per tile, up to 64 tokens) ----
+// Each warp owns 8 rows and the whole panel (16 k-steps of mma.sync
+// m16n8k16), the tokens in blocks of 16 (A's rows g and g + 8), so a warp's
+// sums are final: no partials and no CTA barrier per tile. The B fragments
+// (weights, rows 16 bytes apart as in gemv_range_mma) are read once per token
+// block; the input fragments come from the staging area as there.
+__device__ __forceinline__ void gemv_range_mma_wide(Ctx& c, const Gemv& g, int slot, int j_lo, int j_hi) {
+    const Params& p = c.p;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int gq = lane >> 2, t4 = lane & 3;
+    const int M = c.ms.gm, Kc = g.Kc, SS = stage_stride(Kc), pitch = Kc * 2 + 16, R = g.R;
+    const int n_rb = g.n_rb, N = g.N, grp_rows = g.grp_rows, grp_stride = g.grp_stride;
+    const int out_kind = g.out_kind, n_kc = g.n_kc, dst_stride = g.dst_stride;
+    float* const dst = g.dst + (size_t)slot * g.dst_sstride;
+    float* const dst2 = g.dst2;
+    const float* src = g.src + (size_t)slot * g.src_sstride;
+    Misc& ms = c.ms;
+    uint8_t* const ring = c.smem + SMEM_RING;
+    const float* const xs = c.stage();
+    CRing cr = c.cr;
+    bool dead = c.dead, timed_out = false;
+    int j = j_lo;
+    while (j < j_hi) {
+        const int kc0 = j / n_rb, rb0 = j - kc0 * n_rb;
+        const int g0 = grp_rows ? (rb0 * R) / grp_rows : 0;
+        const int jend = run_end(j, j_hi, n_rb, rb0, R, grp_rows, g0);
+        const long long ta = p.trace_items ? gtimer() : 0;
+        restage(c, g, src, g0 * grp_stride, kc0, 0, ms.gather ? ms.gm : p.M);
+        const long long tb = p.trace_items ? gtimer() : 0;
+        long long tc = tb;
+        const int jrun = j;
+        for (; j < jend; ++j) {
+            const int r0 = (rb0 + (j - jrun)) * R, nr = min(R, N - r0);
+            const uint8_t* tile = nullptr;
+            if (!dead) {
+                if (spin_wait(p, &ms.full[cr.slot], cr.phase))
+                    tile = ring + cr.slot * SLOT_BYTES;
+                else
+                    dead = timed_out = true;
+            }
+            if (p.trace_items && j == jrun) tc = gtimer();
+            if (tile) {
+                const uint8_t* tr = tile + (size_t)(warp * 8 + gq) * pitch + 4 * t4;
+                const int row = r0 + warp * 8 + 2 * t4;  // this lane's output rows: row, row + 1
+                for (int mb = 0; mb < M; mb += 16) {
+                    const int t0 = mb + gq, t1 = t0 + 8;
+                    const bool ok0 = t0 < M, ok1 = t1 < M;
+                    const float* x0 = xs + (size_t)(ok0 ? staging_row(ms, t0) : 0) * SS + 2 * t4;
+                    const float* x1 = xs + (size_t)(ok1 ? staging_row(ms, t1) : 0) * SS + 2 * t4;
+                    float hs[4] = {0.f, 0.f, 0.f, 0.f}, ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+                    for (int s2 = 0; s2 < 16; ++s2) {
+                        const uint32_t b0 = *reinterpret_cast<const uint32_t*>(tr + 32 * s2);
+                        const uint32_t b1 = *reinterpret_cast<const uint32_t*>(tr + 32 * s2 + 16);
+                        const float2 z = make_float2(0.f, 0.f);
+                        const float2 u0 = ok0 ? *reinterpret_cast<const float2*>(x0 + 16 * s2) : z;
+                        const float2 v0 = ok0 ? *reinterpret_cast<const float2*>(x0 + 16 * s2 + 8) : z;
+                        const float2 u1 = ok1 ? *reinterpret_cast<const float2*>(x1 + 16 * s2) : z;
+                        const float2 v1 = ok1 ? *reinterpret_cast<const float2*>(x1 + 16 * s2 + 8) : z;
+                        const uint32_t hu0 = bf2_pack(u0.x, u0.y), hu1 = bf2_pack(u1.x, u1.y);
+                        const uint32_t hv0 = bf2_pack(v0.x, v0.y), hv1 = bf2_pack(v1.x, v1.y);
+                        const uint32_t a_h[4] = {hu0, hu1, hv0, hv1};
+                        const uint32_t a_l[4] = {bf2_pack(u0.x - bf_lo(hu0), u0.y - bf_hi(hu0)),
+                                                 bf2_pack(u1.x - bf_lo(hu1), u1.y - bf_hi(hu1)),
+                                                 bf2_pack(v0.x - bf_lo(hv0), v0.y - bf_hi(hv0)),
+                                                 bf2_pack(v1.x - bf_lo(hv1), v1.y - bf_hi(hv1))};
+                        mma_bf16(hs, a_h, b0, b1);
+                        mma_bf16(ls, a_l, b0, b1);
+                    }
+                    // hs[0..1]: token t0, rows row and row + 1; hs[2..3]: token t1
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int m = q < 2 ? t0 : t1, rr = row + (q & 1);
+                        if ((q < 2 ? ok0 : ok1) && rr - r0 < nr) {
+                            const float y = hs[q] + ls[q];
+                            float* d = dst + (size_t)m * dst_stride + rr;
+                            if (out_kind == OUT_STORE) {
+                                if (n_kc == 1)
+                                    *d = y;
+                                else
+                                    atomicAdd(d, y);
+                            } else if (out_kind == OUT_RESID) {
+                                if (n_kc == 1) {
+                                    const float nv = __ldcg(d) + y;
+                                    *d = nv;
+                                    dst2[(size_t)m * dst_stride + rr] = nv;
+                                } else {
+                                    atomicAdd(d, y);
+                                }
+                            } else {  // OUT_ACC
+                                *d += y;
+                            }
+                        }
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ms.empty[cr.slot]);
+            if (++cr.slot == NSLOT) {
+                cr.slot = 0;
+                cr.phase ^= 1u;
+            }
+        }
+        if (p.trace_items && threadIdx.x == 0) trace_rec(c, 0x80000000u | c.cur_code, (unsigned)(tb - ta), ta, tc);
+    }
+    if (timed_out) {
+        ms.abort = 1;
+        raise_status(p, ST_TIMEOUT, 0x240u);
+    }
+    c.set_ring(cr);
+    if (dead) c.dead = true;
+}
+
 __device__ __noinline__ void gemv_mma(Ctx& c, const Gemv& g, int slot, int j_lo, int j_hi) {
-    if (g.Kc == 2048)
+    if (mma_wide(g))
+        gemv_range_mma_wide(c, g, slot, j_lo, j_hi);
+    else if (g.Kc == 2048)
         gemv_range_mma<1>(c, g, slot, j_lo, j_hi);
     else
         gemv_range_mma<2>(c, g, slot, j_lo, j_hi);
@@ -1397,9 +1528,10 @@ __device__ __noinline__ void prod_gemv(Ctx& c, const Gemv& g, int expert, int lo
             c.dead = true;
             break;
         }
-        if (pad && lane < nr)  // nr <= 16 rows (tiles of 16 KB-per-row halves)
-            bulk_g2s_pol(ring + pr.slot * SLOT_BYTES + (size_t)lane * (Kc * 2 + 16), src + (size_t)lane * Kc,
-                         (unsigned)Kc * 2u, &ms.full[pr.slot], pol);
+        if (pad)  // one copy per row (nr <= 64 rows: at most two per lane)
+            for (int r = lane; r < nr; r += 32)
+                bulk_g2s_pol(ring + pr.slot * SLOT_BYTES + (size_t)r * (Kc * 2 + 16), src + (size_t)r * Kc,
+                             (unsigned)Kc * 2u, &ms.full[pr.slot], pol);
         __syncwarp();
         ++issued;
         prod_next(pr);
@@ -3255,8 +3387,9 @@ __device__ __noinline__ void ffn_stage(Ctx& c, int l) {
         const int nslots = PROD ? c.ms.p_nslots : c.ms.n_slots;
         const uint8_t* slot_e = PROD ? c.ms.p_slot_e : c.ms.slot_e;
         int lo, hi;
-        routed_range(PROD ? c.ms.p_used : c.ms.used, slot_e, nslots, K.nu, (int)blockIdx.x - p.gs,
-                     p.G - p.gs - p.gr, lo, hi);
+        // (the router CTAs take routed units too once their router tile is done)
+        routed_range(PROD ? c.ms.p_used : c.ms.used, slot_e, nslots, K.nu, (int)blockIdx.x - p.gs, p.G - p.gs, lo,
+                     hi);
         // a routed expert's units take its own tokens (one K panel), in groups
         // of as many as the staging area holds when not all tokens fit it
         // (g0: the group's first entry of the expert's token list)
