@@ -212,8 +212,7 @@ int mk_decode_step_unfused(mk_model* m, mk_kv* kv, const int32_t* tokens, const 
  * step scratch (mk_info.scratch_bytes plus about 1.3 KB per layer) does not
  * fit, or that has more than 128 layers, is rejected with
  * MK_ERR_UNSUPPORTED. The first call on each device looks up the array's
- * device address (set-up): make that first call before any stream capture
- * begins. All calls share the array, which keeps the last call's contents;
+ * device address. All calls share the array, which keeps the last call's contents;
  * each call clears what must start at zero (dependency counters, status
  * word) and, when another model used the array last, copies in the model's
  * constant tables (RoPE angles, a zero page). Calls that overlap on the GPU

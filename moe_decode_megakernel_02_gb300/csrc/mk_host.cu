@@ -530,9 +530,14 @@ int mk_load_weights(const mk_config* cfg, const mk_weight* table, int32_t n, voi
                                  (size_t)D.nope * D.kl * 2, D.Hq, cudaMemcpyDeviceToDevice, s));
             pack_uv_quarters<<<512, 256, 0, s>>>(W + o.uvq, tmp, D.Hq, D.nope, D.vd, D.kl);
             CK(cudaGetLastError());
-            CK(cudaMemcpy2DAsync(W + o.uv, (size_t)D.vd * D.kl * 2, tmp + (size_t)D.nope * D.kl,
-                                 (size_t)(D.nope + D.vd) * D.kl * 2, (size_t)D.vd * D.kl * 2, D.Hq,
-                                 cudaMemcpyDeviceToDevice, s));
+            // W_uv, head by head, into the K-panel layout of its GEMV (kv_lora
+            // 512 splits into two panels of 256 on models loaded for many
+            // tokens per step)
+            for (int h = 0; h < D.Hq; ++h)
+                if ((r = pack_rows(W + o.uv, D.Hq * D.vd, D.kl, panel_width(D.kl, (int)Mx), h * D.vd,
+                                   tmp + (size_t)h * (D.nope + D.vd) * D.kl + (size_t)D.nope * D.kl, D.vd,
+                                   (size_t)D.kl * 2, s)))
+                    return bail(r);
         }
         NEED(MK_W_WO, l, 0);
         PACK(W + o.o, d, D.o_in, 0, p, d);
