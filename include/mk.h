@@ -282,8 +282,12 @@ int mk_model_info(const mk_model* m, mk_info* out);
  * `stream`. Errors: STATE when tracing is off. */
 int mk_trace_read(mk_model* m, void* recs_out, int64_t bytes, int32_t* counts_out, void* stream);
 
-/* Free a model or a KV cache (NULL is a no-op). A KV cache must be freed
- * before its model. */
+/* Free a model or a KV cache (NULL is a no-op). Either may be freed first:
+ * a model freed while KV caches of it are alive releases its device memory
+ * at once and rejects every later call; its caches keep their own memory
+ * (mk_kv_read, mk_kv_write and mk_free still work on them) and the model's
+ * small host record, which they read for its dimensions, is deleted with
+ * the last of them. */
 void mk_free(void* handle);
 
 const char* mk_last_error(void);

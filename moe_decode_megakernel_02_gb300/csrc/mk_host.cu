@@ -86,7 +86,11 @@ struct mk_model {
     const int* last_amax = nullptr;  // argmax of the last step's rows (steps given an accept buffer)
     uint64_t steps = 0;
     uint64_t serial = 0;  // distinct per loaded model in this process
+    // KV caches of this model not yet freed; a model freed while some are
+    // alive gives up its device memory at once and its host record (which
+    // the caches still read for their dimensions) when the last one goes
     int live_kv = 0;
+    bool released = false;
 };
 
 struct mk_kv {
@@ -1147,16 +1151,24 @@ void mk_free(void* h) {
         kv->magic = 0;
         cudaFree(kv->pool);
         cudaFree(kv->btab);
-        if (kv->m) kv->m->live_kv--;
+        mk_model* m = kv->m;
         delete kv;
+        if (m && --m->live_kv == 0 && m->released) delete m;
     } else if (magic == MODEL_MAGIC) {
         mk_model* m = static_cast<mk_model*>(h);
         m->magic = 0;
         for (auto& g : m->graphs) cudaGraphExecDestroy(g.second);
+        m->graphs.clear();
         cudaFree(m->wblob);
         cudaFree(m->sblob);
         cudaFree(m->d_layers);
-        delete m;
+        m->wblob = nullptr;
+        m->sblob = nullptr;
+        m->d_layers = nullptr;
+        if (m->live_kv > 0)
+            m->released = true;  // deleted with its last KV cache
+        else
+            delete m;
     }
 }
 

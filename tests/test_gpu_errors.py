@@ -107,3 +107,36 @@ def test_trace_covers_every_stage_of_every_layer(monkeypatch, name, B):
     summ = tracing.summary(per_cta, L)
     assert summ["layer_us"] is not None and summ["layer_us"] > 0
     print(name, B, "layer us", summ["layer_us"], "stage spans", summ["stage_span_us"])
+
+
+@pytest.mark.parametrize("model_first", [True, False])
+def test_model_and_caches_free_in_either_order(model_first):
+    # a model freed while its caches are alive (as happens when the garbage
+    # collector finalises a cycle holding both) gives up its device memory
+    # at once; the caches keep working on their own memory and the model's
+    # host record goes with the last of them -- no write into freed memory
+    import ctypes
+    import gc
+    import moe_decode_megakernel_02_gb300 as mk
+    from moe_decode_megakernel_02_gb300 import workload
+    cfg = configs.TINY
+    ctx = 40
+    model = workload.load_synthetic(cfg, max_batch=2, max_tokens_per_seq=1, max_ctx=ctx + 8)
+    kv1, kv2 = mk.KVCache(model, 2, ctx + 8), mk.KVCache(model, 2, ctx + 8)
+    workload.prefill(kv1, cfg, ctx)
+    rows = kv1.read(0, 1, 0, ctx)
+    if model_first:
+        model.close()
+        assert np.array_equal(kv1.read(0, 1, 0, ctx), rows)  # the cache's own memory is intact
+        kv1.close()
+        kv2.close()
+    else:
+        kv2.close()
+        kv1.close()
+        model.close()
+    # freed chunks are consolidated and handed out again: corrupted heap
+    # metadata would abort the process here
+    gc.collect()
+    junk = [bytearray(n) for n in (24, 48, 96, 200, 1000, 5000) for _ in range(200)]
+    del junk
+    ctypes.CDLL("libc.so.6").malloc_trim(0)
