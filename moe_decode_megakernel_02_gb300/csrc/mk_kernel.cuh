@@ -3074,26 +3074,67 @@ __device__ __forceinline__ void down_rows1(const uint8_t* tile, int nr, const fl
 // several tokens: the row's weights in registers, token i's hidden values at
 // hu + i hstride, its output row gt[i] of xo (stride d), scaled by its
 // routing weight
-template <int F8>
-__device__ __forceinline__ void down_rowsM(const uint8_t* tile, int nr, const float* hu, int hstride, int M,
-                                           const Misc& ms, float* xo, int d) {
-    const uint4* T4 = reinterpret_cast<const uint4*>(tile);
-    const int lane = threadIdx.x & 31;
-    for (int rb = (ctid() >> 5) * 32; rb < nr; rb += NCT) {
-        const int r = rb + lane;
-        uint4 w[F8];
+// down columns of one unit for two or more tokens on the tensor cores:
+// out[token][row] = sum_f W[row][f] h[token][f] with mma.sync m16n8k16 --
+// the tokens are A's 16 rows (their hidden values split into bf16 hi + lo,
+// two MMAs, as for the activations of the gate/up tiles), 8 rows of the
+// tile are B's 8 columns and K is the unit's F (F / 16 k-steps). A lane's
+// results are two adjacent rows of one token: one 8-byte reduction into
+// that token's residual row, scaled by its routing weight. Warp w takes the
+// groups of 8 rows w, w + 8, ...; the tile's rows are F * 2 bytes apart in
+// the ring slot (the B loads of 8 rows x 4 lanes meet two-way bank conflicts
+// at F = 48).
+template <int F>
+__device__ __forceinline__ void down_mma(const uint8_t* tile, int nr, const float* hu, int hstride, int M,
+                                         const Misc& ms, float* xo, int d) {
+    constexpr int KS = F / 16;
+    const int lane = threadIdx.x & 31, warp = ctid() >> 5, g = lane >> 2, t4 = lane & 3;
+    for (int mb = 0; mb < M; mb += 16) {
+        const int t0 = mb + g, t1 = t0 + 8;
+        const bool ok0 = t0 < M, ok1 = t1 < M;
+        uint32_t ah[KS][4], al[KS][4];
 #pragma unroll
-        for (int q = 0; q < F8; ++q) w[q] = r < nr ? T4[(size_t)r * F8 + q] : make_uint4(0u, 0u, 0u, 0u);
-        for (int i = 0; i < M; ++i) {
-            const float wt = ms.uw[i];
-            if (wt == 0.f) continue;  // uniform: every lane reads the same entry
-            const float* hi = hu + (size_t)i * hstride;
-            float a = 0.f, b = 0.f;
+        for (int s2 = 0; s2 < KS; ++s2) {
+            const float2 z = make_float2(0.f, 0.f);
+            const float* h0 = hu + (size_t)(ok0 ? t0 : 0) * hstride + 16 * s2 + 2 * t4;
+            const float* h1 = hu + (size_t)(ok1 ? t1 : 0) * hstride + 16 * s2 + 2 * t4;
+            const float2 u0 = ok0 ? *reinterpret_cast<const float2*>(h0) : z;
+            const float2 v0 = ok0 ? *reinterpret_cast<const float2*>(h0 + 8) : z;
+            const float2 u1 = ok1 ? *reinterpret_cast<const float2*>(h1) : z;
+            const float2 v1 = ok1 ? *reinterpret_cast<const float2*>(h1 + 8) : z;
+            ah[s2][0] = bf2_pack(u0.x, u0.y);
+            ah[s2][1] = bf2_pack(u1.x, u1.y);
+            ah[s2][2] = bf2_pack(v0.x, v0.y);
+            ah[s2][3] = bf2_pack(v1.x, v1.y);
+            al[s2][0] = bf2_pack(u0.x - bf_lo(ah[s2][0]), u0.y - bf_hi(ah[s2][0]));
+            al[s2][1] = bf2_pack(u1.x - bf_lo(ah[s2][1]), u1.y - bf_hi(ah[s2][1]));
+            al[s2][2] = bf2_pack(v0.x - bf_lo(ah[s2][2]), v0.y - bf_hi(ah[s2][2]));
+            al[s2][3] = bf2_pack(v1.x - bf_lo(ah[s2][3]), v1.y - bf_hi(ah[s2][3]));
+        }
+        const float w0 = ok0 ? ms.uw[t0] : 0.f, w1 = ok1 ? ms.uw[t1] : 0.f;
+        float* const x0 = xo + (size_t)(ok0 ? ms.gt[t0] : 0) * d;
+        float* const x1 = xo + (size_t)(ok1 ? ms.gt[t1] : 0) * d;
+        // nr is a multiple of 8 (d and the tile height are): every group of
+        // 8 rows is whole
+        for (int n0 = warp * 8; n0 < nr; n0 += NCW * 8) {
+            const uint8_t* br = tile + (size_t)(n0 + g) * (F * 2) + 4 * t4;
+            float c4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int q = 0; q < F8; ++q)
-                fma8v2(a, b, w[q], *reinterpret_cast<const float4*>(hi + 8 * q),
-                       *reinterpret_cast<const float4*>(hi + 8 * q + 4));
-            red4_rows(xo + (size_t)ms.gt[i] * d, r, r < nr, wt * (a + b));
+            for (int s2 = 0; s2 < KS; ++s2) {
+                const uint32_t b0 = *reinterpret_cast<const uint32_t*>(br + 32 * s2);
+                const uint32_t b1 = *reinterpret_cast<const uint32_t*>(br + 32 * s2 + 16);
+                mma_bf16(c4, ah[s2], b0, b1);
+                mma_bf16(c4, al[s2], b0, b1);
+            }
+            const int row = n0 + 2 * t4;
+            if (w0 != 0.f)
+                asm volatile("red.relaxed.gpu.global.add.v2.f32 [%0], {%1, %2};" ::"l"(x0 + row), "f"(w0 * c4[0]),
+                             "f"(w0 * c4[1])
+                             : "memory");
+            if (w1 != 0.f)
+                asm volatile("red.relaxed.gpu.global.add.v2.f32 [%0], {%1, %2};" ::"l"(x1 + row), "f"(w1 * c4[2]),
+                             "f"(w1 * c4[3])
+                             : "memory");
         }
     }
 }
@@ -3218,10 +3259,10 @@ __device__ __noinline__ void unit_seg_cons(Ctx& c, int l, int kind, int expert, 
                 } else {
                     float* xo = Ld.xn + r0;
                     const float* hu = h + uu * F;
-                    if (F == 64) down_rowsM<8>(tile, nr, hu, n * F, M, ms, xo, d);
-                    else if (F == 48) down_rowsM<6>(tile, nr, hu, n * F, M, ms, xo, d);
-                    else if (F == 32) down_rowsM<4>(tile, nr, hu, n * F, M, ms, xo, d);
-                    else down_rowsM<2>(tile, nr, hu, n * F, M, ms, xo, d);
+                    if (F == 64) down_mma<64>(tile, nr, hu, n * F, M, ms, xo, d);
+                    else if (F == 48) down_mma<48>(tile, nr, hu, n * F, M, ms, xo, d);
+                    else if (F == 32) down_mma<32>(tile, nr, hu, n * F, M, ms, xo, d);
+                    else down_mma<16>(tile, nr, hu, n * F, M, ms, xo, d);
                 }
             }
             __syncwarp();
