@@ -61,11 +61,15 @@ constexpr int MLA_CH = 32;                // positions per MLA chunk (half a pag
 constexpr int PAGE = 64;
 // MLA: 16 heads, latent 512, rope 64 (checked on the host)
 constexpr int MLA_H = 16, MLA_KL = 512, MLA_RD = 64, MLA_D = MLA_KL + MLA_RD;
-constexpr int MLA_QS = 584;               // padded smem row strides (bf16 elements)
-constexpr int MLA_CS = 520;
-constexpr int MLA_RS = 72;
-constexpr int MLA_CHUNK_BYTES = MLA_CH * MLA_CS * 2 + MLA_CH * MLA_RS * 2;
-static_assert(MLA_CHUNK_BYTES <= SLOT_BYTES, "MLA chunk must fit a slot");
+constexpr int MLA_QS = 584;               // padded smem row stride of the queries (bf16 elements)
+// an MLA chunk in shared memory: 9 boxes of MLA_CH positions x 64 bf16 (128
+// bytes a row) -- the latent's 8 column blocks, then the rope -- each in the
+// 128-byte swizzled order of the bulk tensor copy that fills it (the 16-byte
+// piece j of a row sits at piece j ^ bits 7..9 of the row's address)
+constexpr int MLA_BOX = MLA_CH * 128;
+constexpr int MLA_TILE_BYTES = 9 * MLA_BOX;
+static_assert(MLA_TILE_BYTES <= SLOT_BYTES, "MLA chunk must fit a slot");
+static_assert(SLOT_BYTES % 1024 == 0, "ring slots keep the 1024-byte alignment of the swizzled boxes");
 
 enum InKind { IN_COPY = 0, IN_RMS = 1, IN_SWIGLU = 2 };
 enum OutKind { OUT_STORE = 0, OUT_RESID = 1, OUT_SCALED = 2, OUT_ACC = 3 };  // OUT_ACC: += into a CTA-private buffer
@@ -148,7 +152,11 @@ struct Params {
     int pps;                        // pages per sequence
     const int* btab;                // [kv_batch][pps]
     int kv_cap, kv_batch;           // positions per sequence, sequences in the cache
-    const uint16_t* zeros;          // >= 2 KB of zero bytes (fills unused chunk rows)
+    const uint16_t* zeros;          // >= 2 KB of zero bytes
+    // MLA caches: two tensor maps (CUtensorMap, 128 bytes each) in device
+    // memory -- the latent [L][pages][64 rows][512] and the rope [L][pages]
+    // [64 rows][64] of the pool, boxes of 32 rows x 64 bf16, 128-byte swizzle
+    const void* kv_tmaps;
     uint16_t* newlat;               // MLA new latents [MAX_M][576] bf16
     float* part;                    // attention partials: unnormalised O rows
     float* part_ml;                 // attention partials: (running max, sum) per row
@@ -346,6 +354,26 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], 
         "{%0,%1,%2,%3};\n"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// one box of a 4-D tensor map into shared memory, completing on `bar`
+__device__ __forceinline__ void tma_load_4d(void* dst, const void* tmap, int x, int y, int z, int w,
+                                            unsigned long long* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, "
+        "%5}], [%6];" ::"r"(su32(dst)),
+        "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(w), "r"(su32(bar))
+        : "memory");
+}
+// the byte of the 16-byte piece holding bf16 element (row, k) of an MLA
+// chunk whose boxes start at `base`, `bb` bytes apart (swizzled as above)
+__device__ __forceinline__ const uint8_t* mla_piece(const uint8_t* base, int bb, int row, int k) {
+    const uint8_t* r = base + (k >> 6) * bb + row * 128;
+    return r + ((((unsigned)k >> 3 & 7u) ^ (su32(r) >> 7 & 7u)) << 4);
+}
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const void* p) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(su32(p)));
 }
 __device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], const void* p) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"

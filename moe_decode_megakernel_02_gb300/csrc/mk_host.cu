@@ -1,5 +1,6 @@
 // mk_host.cu -- C ABI of the decode megakernel (include/mk.h): validation,
 // weight packing, scratch layout, paged KV cache and the cooperative launch.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -100,6 +101,7 @@ struct mk_kv {
     size_t page_elems, layer_elems;
     uint16_t* pool = nullptr;
     int* btab = nullptr;
+    void* tmaps = nullptr;  // MLA: the latent and rope tensor maps of the pool (device memory)
     std::vector<int> h_btab;
 };
 
@@ -783,6 +785,50 @@ int mk_model_info(const mk_model* m, mk_info* out) {
     return MK_OK;
 }
 
+// the two tensor maps of an MLA cache's pool (pages of 64 rows x 512 latent
+// values, then 64 rows x 64 rope values, bf16): 4-D views [L][pages][64][512]
+// and [L][pages][64][64] whose boxes of 32 rows x 64 values are the attention
+// chunks' pieces, copied in the 128-byte swizzled order
+static int mla_tensor_maps(mk_kv* kv, int L) {
+    using Encode = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+    static Encode encode = nullptr;
+    if (!encode) {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || !fn) {
+            cudaGetLastError();
+            return fail(MK_ERR_CUDA, "kv: the driver has no cuTensorMapEncodeTiled");
+        }
+        encode = reinterpret_cast<Encode>(fn);
+    }
+    const cuuint64_t pages = kv->layer_elems / kv->page_elems;
+    alignas(64) CUtensorMap maps[2];
+    const cuuint32_t box[4] = {64, (cuuint32_t)mk::MLA_CH, 1, 1}, one[4] = {1, 1, 1, 1};
+    const cuuint64_t dl[4] = {(cuuint64_t)mk::MLA_KL, (cuuint64_t)mk::PAGE, pages, (cuuint64_t)L};
+    const cuuint64_t dr[4] = {(cuuint64_t)mk::MLA_RD, (cuuint64_t)mk::PAGE, pages, (cuuint64_t)L};
+    const cuuint64_t sl[3] = {(cuuint64_t)mk::MLA_KL * 2, kv->page_elems * 2, kv->layer_elems * 2};
+    const cuuint64_t sr[3] = {(cuuint64_t)mk::MLA_RD * 2, kv->page_elems * 2, kv->layer_elems * 2};
+    CUresult r = encode(&maps[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, kv->pool, dl, sl, box, one,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r == CUDA_SUCCESS)
+        r = encode(&maps[1], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, kv->pool + (size_t)mk::PAGE * mk::MLA_KL, dr, sr,
+                   box, one, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(MK_ERR_CUDA, "kv: cuTensorMapEncodeTiled failed (%d)", (int)r);
+    static_assert(sizeof(CUtensorMap) == 128, "tensor maps are 128 bytes");
+    if (cudaMalloc(&kv->tmaps, sizeof maps) != cudaSuccess) {
+        cudaGetLastError();
+        return fail(MK_ERR_OOM, "kv: tensor maps");
+    }
+    CK(cudaMemcpy(kv->tmaps, maps, sizeof maps, cudaMemcpyHostToDevice));
+    return MK_OK;
+}
+
 int mk_alloc_kv(const mk_model* m, int32_t batch, int32_t max_ctx, mk_kv** out) {
     if (!out) return fail(MK_ERR_INVALID_ARG, "out is NULL");
     *out = nullptr;
@@ -816,6 +862,15 @@ int mk_alloc_kv(const mk_model* m, int32_t batch, int32_t max_ctx, mk_kv** out) 
         return fail(MK_ERR_OOM, "kv block table");
     }
     CK(cudaMemset(kv->pool, 0, bytes));
+    if (!D.gqa) {
+        if (const int rc = mla_tensor_maps(kv, D.L)) {
+            cudaFree(kv->pool);
+            cudaFree(kv->btab);
+            if (kv->tmaps) cudaFree(kv->tmaps);
+            delete kv;
+            return rc;
+        }
+    }
     kv->h_btab.resize(pages);
     for (int b = 0; b < batch; ++b)
         for (int j = 0; j < kv->pps; ++j) kv->h_btab[(size_t)b * kv->pps + j] = j * batch + b;
@@ -942,6 +997,7 @@ static int step_params(mk_model* m, mk_kv* kv, const int32_t* tokens, const int3
     P.kv_batch = kv->batch;
     P.kv_pool = kv->pool;
     P.kv_layer_elems = (long long)kv->layer_elems;
+    P.kv_tmaps = kv->tmaps;
     P.tokens = tokens;
     P.pos = positions;
     P.B = batch;
@@ -1151,6 +1207,7 @@ void mk_free(void* h) {
         kv->magic = 0;
         cudaFree(kv->pool);
         cudaFree(kv->btab);
+        if (kv->tmaps) cudaFree(kv->tmaps);
         mk_model* m = kv->m;
         delete kv;
         if (m && --m->live_kv == 0 && m->released) delete m;
@@ -1321,6 +1378,7 @@ extern "C" int mk_decode_step_noalloc(mk_model* m, mk_kv* kv, const int32_t* tok
     P.kv_batch = kv->batch;
     P.kv_pool = kv->pool;
     P.kv_layer_elems = (long long)kv->layer_elems;
+    P.kv_tmaps = kv->tmaps;
     P.tokens = tokens;
     P.pos = positions;
     P.B = batch;

@@ -2276,8 +2276,7 @@ struct MlaSmem {
     float* mst;      // [16] running max
     float* lst;      // [16] running sum
     float* cst;      // [16] correction of this chunk
-    uint16_t* tc;    // tail latent rows [16][MLA_CS]
-    uint16_t* tr;    // tail rope rows [16][MLA_RS]
+    uint8_t* tk;     // the step's new positions: 16 rows in 9 swizzled boxes of 2 KB
 };
 __device__ __forceinline__ MlaSmem mla_smem(float* stage) {
     MlaSmem s;
@@ -2290,37 +2289,58 @@ __device__ __forceinline__ MlaSmem mla_smem(float* stage) {
     s.mst = reinterpret_cast<float*>(b + 42752 + 16 * 40 * 2);                    // 44032
     s.lst = s.mst + 16;
     s.cst = s.lst + 16;
-    s.tc = reinterpret_cast<uint16_t*>(b + 44032 + 192);                          // 44224
-    s.tr = reinterpret_cast<uint16_t*>(b + 44224 + 16 * MLA_CS * 2);              // 60864
+    s.tk = b + 44288;                                                             // .. 62720
     return s;
 }
 
 __device__ __forceinline__ uint32_t lds32(const uint16_t* p) { return *reinterpret_cast<const uint32_t*>(p); }
 
-__device__ __forceinline__ void mla_chunk(const MlaSmem& S, const uint16_t* ck, const uint16_t* kr, int NR, int nvalid,
-                          float (&acc)[8][4]) {
+// kb: the chunk's 9 swizzled boxes, bb bytes apart (a ring slot: boxes of
+// MLA_CH rows; the step's new positions: 16 rows); rows from nvalid on are
+// not positions of the sequence
+template <int NR>
+__device__ __forceinline__ void mla_chunk(const MlaSmem& S, const uint8_t* kb, int bb, int nvalid,
+                                          float (&acc)[8][4]) {
     const int tid = ctid(), lane = tid & 31, warp = tid >> 5, g = lane >> 2, t4 = lane & 3;
     // ---- scores S[16][NR] = Q . KV^T ----
-    const int NT = NR / 8, KS = 8 / NT, nt = warp % NT, ks = warp / NT;
-    const int steps = 36 / KS;
-    float sacc[4] = {0.f, 0.f, 0.f, 0.f};
+    // warp = (column block nt of 8 rows, K slice ks); the K slice's k-steps
+    // fully unrolled over four accumulators (hi / lo parts x even / odd
+    // steps: four MMA chains instead of one); the query fragments by
+    // ldmatrix from the padded rows (lane l addresses row l & 15, columns
+    // + (l >> 4) * 8)
+    constexpr int NT = NR / 8, KS = 8 / NT, STEPS = 36 / KS;
+    const int nt = warp % NT, ks = warp / NT;
+    float sa[4][4] = {};
     const int n = nt * 8 + g;
-    for (int kk = ks * steps; kk < (ks + 1) * steps; ++kk) {
-        const int k0 = kk * 16;
+    // this lane's chunk row: its pieces are swizzled by bits 7..9 of the row's
+    // address, the same in every box (boxes are multiples of 1024 bytes apart)
+    const uint8_t* const rowp = kb + n * 128 + 4 * t4;
+    const unsigned sw = (su32(kb + n * 128) >> 7) & 7u;
+    const uint16_t* const qh = S.qhi + (lane & 15) * MLA_QS + (lane >> 4) * 8;
+    const uint16_t* const ql = S.qlo + (lane & 15) * MLA_QS + (lane >> 4) * 8;
+    const auto step = [&](int i, float (&shi)[4], float (&slo)[4]) {
+        const int k0 = (ks * STEPS + i) * 16;
         uint32_t ah[4], al[4];
-        ah[0] = lds32(S.qhi + g * MLA_QS + k0 + 2 * t4);
-        ah[1] = lds32(S.qhi + (g + 8) * MLA_QS + k0 + 2 * t4);
-        ah[2] = lds32(S.qhi + g * MLA_QS + k0 + 8 + 2 * t4);
-        ah[3] = lds32(S.qhi + (g + 8) * MLA_QS + k0 + 8 + 2 * t4);
-        al[0] = lds32(S.qlo + g * MLA_QS + k0 + 2 * t4);
-        al[1] = lds32(S.qlo + (g + 8) * MLA_QS + k0 + 2 * t4);
-        al[2] = lds32(S.qlo + g * MLA_QS + k0 + 8 + 2 * t4);
-        al[3] = lds32(S.qlo + (g + 8) * MLA_QS + k0 + 8 + 2 * t4);
-        const uint16_t* br = k0 < MLA_KL ? (ck + n * MLA_CS + k0) : (kr + n * MLA_RS + (k0 - MLA_KL));
-        const uint32_t b0 = lds32(br + 2 * t4), b1 = lds32(br + 8 + 2 * t4);
-        mma_bf16(sacc, ah, b0, b1);
-        mma_bf16(sacc, al, b0, b1);
+        ldsm_x4(ah, qh + k0);
+        ldsm_x4(al, ql + k0);
+        // (k0 is a multiple of 16: elements k0 + 2 t4 and k0 + 8 + 2 t4 are in
+        // the neighbouring 16-byte pieces j0 and j0 + 1 of the row)
+        const uint8_t* const bp = rowp + (k0 >> 6) * bb;
+        const unsigned j0 = ((unsigned)k0 >> 3) & 7u;
+        const uint32_t b0 = *reinterpret_cast<const uint32_t*>(bp + ((j0 ^ sw) << 4));
+        const uint32_t b1 = *reinterpret_cast<const uint32_t*>(bp + (((j0 + 1u) ^ sw) << 4));
+        mma_bf16(shi, ah, b0, b1);
+        mma_bf16(slo, al, b0, b1);
+    };
+#pragma unroll 3
+    for (int i = 0; i + 1 < STEPS; i += 2) {
+        step(i, sa[0], sa[1]);
+        step(i + 1, sa[2], sa[3]);
     }
+    if (STEPS & 1) step(STEPS - 1, sa[0], sa[1]);
+    float sacc[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) sacc[q] = (sa[0][q] + sa[1][q]) + (sa[2][q] + sa[3][q]);
     {
         float* sp = S.spart + (size_t)ks * 16 * NR;
         sp[g * NR + nt * 8 + 2 * t4] = sacc[0];
@@ -2348,9 +2368,9 @@ __device__ __forceinline__ void mla_chunk(const MlaSmem& S, const uint16_t* ck, 
         const float mn = fmaxf(mold, mc);
         float corr = 1.f, p0 = 0.f, p1 = 0.f;
         if (mn != -INFINITY) {
-            corr = mold == -INFINITY ? 0.f : expf(mold - mn);
-            p0 = s0 == -INFINITY ? 0.f : expf(s0 - mn);
-            p1 = s1 == -INFINITY ? 0.f : expf(s1 - mn);
+            corr = mold == -INFINITY ? 0.f : __expf(mold - mn);
+            p0 = s0 == -INFINITY ? 0.f : __expf(s0 - mn);
+            p1 = s1 == -INFINITY ? 0.f : __expf(s1 - mn);
         }
         float ps = p0 + p1;
 #pragma unroll
@@ -2360,6 +2380,16 @@ __device__ __forceinline__ void mla_chunk(const MlaSmem& S, const uint16_t* ck, 
             S.mst[h] = mn;
             S.lst[h] = S.lst[h] * corr + ps;
             S.cst[h] = corr;
+        }
+        // rows past the sequence's end came with the chunk's half page (their
+        // probabilities are 0): zero their latent values so that P.V stays finite
+        if (nvalid < NR) {
+            const int nb = (NR - nvalid) * 8;  // 16-byte pieces per box
+            for (int i = tid; i < 8 * nb; i += NCT) {
+                const int bx = i / nb, rem = i - bx * nb;
+                *reinterpret_cast<uint4*>(const_cast<uint8_t*>(kb) + bx * bb + (nvalid + (rem >> 3)) * 128 +
+                                          (rem & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
+            }
         }
         const uint16_t h0 = f2bf(p0), h1 = f2bf(p1);
         S.phi[h * 40 + l16] = h0;
@@ -2380,21 +2410,21 @@ __device__ __forceinline__ void mla_chunk(const MlaSmem& S, const uint16_t* ck, 
             acc[j][2] *= c1;
             acc[j][3] *= c1;
         }
+        // rows kp + (lane & 15): bits 7..9 of their addresses do not depend on
+        // kp (a multiple of 16 rows, 2048 bytes)
+        const unsigned swv = (su32(kb + (lane & 15) * 128) >> 7) & 7u;
+#pragma unroll
         for (int kp = 0; kp < NR; kp += 16) {
+            // probabilities [16 heads][positions kp..kp+15] by ldmatrix (rows of
+            // 80 bytes: the 8 rows of a matrix hit distinct banks)
             uint32_t ah[4], al[4];
-            ah[0] = lds32(S.phi + g * 40 + kp + 2 * t4);
-            ah[1] = lds32(S.phi + (g + 8) * 40 + kp + 2 * t4);
-            ah[2] = lds32(S.phi + g * 40 + kp + 8 + 2 * t4);
-            ah[3] = lds32(S.phi + (g + 8) * 40 + kp + 8 + 2 * t4);
-            al[0] = lds32(S.plo + g * 40 + kp + 2 * t4);
-            al[1] = lds32(S.plo + (g + 8) * 40 + kp + 2 * t4);
-            al[2] = lds32(S.plo + g * 40 + kp + 8 + 2 * t4);
-            al[3] = lds32(S.plo + (g + 8) * 40 + kp + 8 + 2 * t4);
+            ldsm_x4(ah, S.phi + (lane & 15) * 40 + kp + (lane >> 4) * 8);
+            ldsm_x4(al, S.plo + (lane & 15) * 40 + kp + (lane >> 4) * 8);
 #pragma unroll
             for (int np = 0; np < 4; ++np) {
-                const int n0 = warp * 64 + np * 16;
-                uint32_t r[4];
-                ldsm_x4_t(r, ck + (size_t)(kp + (lane & 15)) * MLA_CS + n0 + (lane >> 4) * 8);
+                uint32_t r[4];  // columns warp * 64 + np * 16 (+ 8): box `warp`, pieces 2 np, 2 np + 1
+                ldsm_x4_t(r, kb + warp * bb + (kp + (lane & 15)) * 128 +
+                                 (((unsigned)(2 * np + (lane >> 4)) ^ swv) << 4));
                 mma_bf16(acc[2 * np], ah, r[0], r[1]);
                 mma_bf16(acc[2 * np], al, r[0], r[1]);
                 mma_bf16(acc[2 * np + 1], ah, r[2], r[3]);
@@ -2455,14 +2485,13 @@ __device__ __forceinline__ void cons_attn_mla(Ctx& c, int l, const AttnItem& it)
         S.lst[tid] = 0.f;
     }
     if (tail) {
-        // the new positions 0..T-1 of this step; token t sees 0..t
-        for (int i = tid; i < 16 * MLA_D; i += NCT) {
-            const int r = i / MLA_D, e = i - r * MLA_D;
-            const uint16_t v = r <= t ? p.newlat[(size_t)(b * p.T + r) * MLA_D + e] : (uint16_t)0;
-            if (e < MLA_KL)
-                S.tc[r * MLA_CS + e] = v;
-            else
-                S.tr[r * MLA_RS + (e - MLA_KL)] = v;
+        // the new positions 0..T-1 of this step (token t sees 0..t), 16 bytes
+        // at a time into the layout of a ring chunk with 16-row boxes
+        for (int i = tid; i < 16 * (MLA_D / 8); i += NCT) {
+            const int r = i / (MLA_D / 8), k = (i - r * (MLA_D / 8)) * 8;
+            const uint4 v = r <= t ? *reinterpret_cast<const uint4*>(p.newlat + (size_t)(b * p.T + r) * MLA_D + k)
+                                   : make_uint4(0u, 0u, 0u, 0u);
+            *reinterpret_cast<uint4*>(const_cast<uint8_t*>(mla_piece(S.tk, 16 * 128, r, k))) = v;
         }
     }
     cbar();
@@ -2475,15 +2504,13 @@ __device__ __forceinline__ void cons_attn_mla(Ctx& c, int l, const AttnItem& it)
         const bool ring_chunk = u < it.nch;
         const uint8_t* tile = nullptr;
         if (ring_chunk && !c.dead) tile = cons_wait(p, c.smem, c.ms, c.cr);
-        const uint16_t* ck = ring_chunk ? reinterpret_cast<const uint16_t*>(tile) : S.tc;
-        const uint16_t* kr = ring_chunk ? reinterpret_cast<const uint16_t*>(tile + MLA_CH * MLA_CS * 2) : S.tr;
-        const int NR = ring_chunk ? MLA_CH : 16;
-        const int nvalid = ring_chunk ? min(MLA_CH, p.pos[b] - u * MLA_CH) : t + 1;
         if (ring_chunk && !tile) {
             cbar();
             cbar();
+        } else if (ring_chunk) {
+            mla_chunk<MLA_CH>(S, tile, MLA_BOX, min(MLA_CH, p.pos[b] - u * MLA_CH), acc);
         } else {
-            mla_chunk(S, ck, kr, NR, nvalid, acc);
+            mla_chunk<16>(S, S.tk, 16 * 128, t + 1, acc);  // boxes of 16 rows
         }
         if (ring_chunk) cons_release(c.ms, c.cr);
     }
@@ -2507,30 +2534,28 @@ __device__ __forceinline__ void cons_attn_mla(Ctx& c, int l, const AttnItem& it)
 // rows past the valid positions are filled from a zero buffer
 __device__ __noinline__ void prod_mla_chunk(Ctx& c, int l, int b, int u) {
     const Params& p = c.p;
-    const int lane = threadIdx.x & 31;
-    const int nvalid = min(MLA_CH, p.pos[b] - u * MLA_CH);
-    const unsigned bytes = MLA_CH * (MLA_KL * 2 + MLA_RD * 2);
-    uint8_t* dst = nullptr;
-    unsigned long long dptr = 0;
-    if (lane == 0) {
-        dst = prod_begin(p, c.smem, c.ms, c.pr, bytes);
-        dptr = (unsigned long long)dst;
+    int ok = 1;
+    if ((threadIdx.x & 31) == 0) {
+        // 9 bulk tensor copies: the latent's 8 column blocks and the rope of
+        // the chunk's 32 rows (half a page); rows past the sequence's end
+        // come along and are zeroed by the consumers
+        uint8_t* dst = prod_begin(p, c.smem, c.ms, c.pr, MLA_TILE_BYTES);
+        if (dst) {
+            const int page = p.btab[b * p.pps + (u * MLA_CH) / PAGE], r0 = (u * MLA_CH) % PAGE;
+            const uint8_t* tm = static_cast<const uint8_t*>(p.kv_tmaps);
+            unsigned long long* bar = &c.ms.full[c.pr.slot];
+#pragma unroll 1
+            for (int j = 0; j < 8; ++j) tma_load_4d(dst + j * MLA_BOX, tm, 64 * j, r0, page, l, bar);
+            tma_load_4d(dst + 8 * MLA_BOX, tm + 128, 0, r0, page, l, bar);
+        } else {
+            ok = 0;
+        }
     }
-    dptr = __shfl_sync(0xffffffffu, dptr, 0);
-    if (!dptr) {
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (!ok) {
         c.dead = true;
         return;
     }
-    dst = reinterpret_cast<uint8_t*>(dptr);
-    const uint16_t* pg = page_ptr(p, (p.kv_pool + (size_t)l * p.kv_layer_elems), b, (u * MLA_CH) / PAGE);
-    const int r0 = (u * MLA_CH) % PAGE;
-    // lane r copies latent row r and rope row r
-    const int r = lane;
-    const uint16_t* srcc = r < nvalid ? pg + (size_t)(r0 + r) * MLA_KL : p.zeros;
-    const uint16_t* srcr = r < nvalid ? pg + (size_t)PAGE * MLA_KL + (size_t)(r0 + r) * MLA_RD : p.zeros;
-    bulk_g2s(dst + (size_t)r * MLA_CS * 2, srcc, MLA_KL * 2, &c.ms.full[c.pr.slot]);
-    bulk_g2s(dst + (size_t)MLA_CH * MLA_CS * 2 + (size_t)r * MLA_RS * 2, srcr, MLA_RD * 2, &c.ms.full[c.pr.slot]);
-    __syncwarp();
     c.bump_issued();
     prod_next(c.pr);
 }
@@ -3738,7 +3763,7 @@ __device__ void prod_drain(Ctx& c) {
 }
 
 __global__ void __launch_bounds__(NTHREADS, 1) megakernel(const __grid_constant__ Params p) {
-    extern __shared__ __align__(128) uint8_t smem[];
+    extern __shared__ __align__(1024) uint8_t smem[];  // 1024: the swizzled MLA boxes of the ring
     Misc& ms = *reinterpret_cast<Misc*>(smem + SMEM_MISC);
     if (threadIdx.x == 0) {
         for (int i = 0; i < NSLOT; ++i) {

@@ -79,14 +79,17 @@ def test_dense_reduced_layers():
     _run(cfg, 8, 1, 1, cfg["ctx"])
 
 
-def test_paged_cache_with_permuted_block_table():
-    cfg = configs.scaled(configs.MID, n_layers=2)
+@pytest.mark.parametrize("name,T", [("mid", 1), ("deep", 3)])
+def test_paged_cache_with_permuted_block_table(name, T):
+    # pages in a random order: GQA chunks are copied from their page's
+    # address, MLA chunks by tensor-map coordinates (page index, half page)
+    cfg = configs.scaled(configs.ALL[name], n_layers=2)
     rng = np.random.default_rng(3)
 
     def table(pps, B=2):
         return rng.permutation(B * pps).astype(np.int32).reshape(B, pps)
 
-    _run(cfg, 2, 1, 2, 700, block_table=table)
+    _run(cfg, 2, T, 2, 700, block_table=table, want_accept=T > 1)
 
 
 def test_verify_step_reduced_layers():
