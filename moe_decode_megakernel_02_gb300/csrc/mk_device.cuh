@@ -72,7 +72,9 @@ static_assert(MLA_TILE_BYTES <= SLOT_BYTES, "MLA chunk must fit a slot");
 static_assert(SLOT_BYTES % 1024 == 0, "ring slots keep the 1024-byte alignment of the swizzled boxes");
 
 enum InKind { IN_COPY = 0, IN_RMS = 1, IN_SWIGLU = 2 };
-enum OutKind { OUT_STORE = 0, OUT_RESID = 1, OUT_SCALED = 2, OUT_ACC = 3 };  // OUT_ACC: += into a CTA-private buffer
+// OUT_ACC: += into a CTA-private buffer; OUT_ADD: every warp adds its share
+// (a K slice) atomically into a zeroed CTA-private buffer, no barrier per tile
+enum OutKind { OUT_STORE = 0, OUT_RESID = 1, OUT_SCALED = 2, OUT_ACC = 3, OUT_ADD = 4 };
 enum StatusCode { ST_OK = 0, ST_INVALID = 1, ST_TIMEOUT = 5 };
 
 // A matrix-vector stage: out[m][row] (+)= W[row, :] . f(in)[m, :]

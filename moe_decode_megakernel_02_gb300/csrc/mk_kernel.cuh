@@ -1240,6 +1240,15 @@ __device__ __forceinline__ void gemv_range_mma(Ctx& c, const Gemv& g, int slot, 
                 cr.slot = 0;
                 cr.phase ^= 1u;
             }
+            if (out_kind == OUT_ADD) {  // (uniform) the warp's K slice straight into the buffer
+                const int row = r0 + ngw * 8 + 2 * t4;
+                if (tile && xok && row - r0 < nr) {
+                    float* d = dst + (size_t)gq * dst_stride + row;
+                    atomicAdd(d, hsum[0] + lsum[0]);
+                    atomicAdd(d + 1, hsum[1] + lsum[1]);
+                }
+                continue;
+            }
             // token gq, rows 2 t4 and 2 t4 + 1 of this warp's row group
             *reinterpret_cast<float2*>(part + (warp * 8 + gq) * 8 + 2 * t4) =
                 make_float2(hsum[0] + lsum[0], hsum[1] + lsum[1]);
@@ -3226,9 +3235,14 @@ __device__ __noinline__ void unit_seg_cons(Ctx& c, int l, int kind, int expert, 
     const int M = c.ms.gm;
     float* hs = unit_buf(c, 3 * F * n * M);
     float* h = hs + (size_t)rows * M;
-    if (Ld.ffn.n_kc > 1)
+    // two or more tokens on the tensor cores: the warps' K slices add into
+    // the zeroed buffer (OUT_ADD) instead of meeting at two barriers per tile
+    if (Ld.ffn.n_kc > 1 || M >= 2)
         for (int i = tid; i < rows * M; i += NCT) hs[i] = 0.f;
-    if (tid == 0) unit_gemv(p, Ld, c.ms.ug, kind, expert, u0, u1, hs);
+    if (tid == 0) {
+        unit_gemv(p, Ld, c.ms.ug, kind, expert, u0, u1, hs);
+        if (M >= 2 && mma_gemv(M, c.ms.ug)) c.ms.ug.out_kind = OUT_ADD;
+    }
     cbar();
     const long long tz = p.trace_items ? gtimer() : 0;
     const long long cz = clock64();
@@ -3247,7 +3261,10 @@ __device__ __noinline__ void unit_seg_cons(Ctx& c, int l, int kind, int expert, 
     for (int i = tid; i < F * n * M; i += NCT) {
         const int m = i / (F * n), rem = i - m * F * n, uu = rem / F, f = rem - uu * F;
         const float* g = hs + (size_t)m * rows + uu * 2 * F;
-        h[i] = silu(g[f]) * g[F + f];
+        // (from L2 when the buffer is in global memory: the atomic additions
+        // of OUT_ADD bypass this SM's L1)
+        const float gv = __isShared(g) ? g[f] : __ldcg(g + f), uv = __isShared(g) ? g[F + f] : __ldcg(g + F + f);
+        h[i] = silu(gv) * uv;
     }
     cbar();
     // down columns of each unit: tiles of Rd rows x F from the ring
