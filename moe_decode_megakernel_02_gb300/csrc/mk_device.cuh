@@ -137,7 +137,7 @@ struct Layer {
 
 // counters per layer (and one extra "layer" L for the head)
 enum { C_A = 0, C_QB, C_APP, C_QLAT, C_ATTN, C_COMB, C_UV, C_O, C_ROUTER, C_SHGU, C_CARRY, C_SHDOWN, C_DOWN,
-       C_INIT, C_LM, C_AMAX, C_GU0, NCTR = C_GU0 + MAX_E };
+       C_INIT, C_LM, C_AMAX, C_NRM0, C_NRM1, C_NRM2, C_GU0, NCTR = C_GU0 + MAX_E };
 
 struct Params {
     int L, d, V, attn, Hq, Hkv, hd, ql, kl, nope, rd, vd, E, topk, has_sh, ffn, sffn;
@@ -183,6 +183,11 @@ struct Params {
     int qfuse;                      // MLA: the absorbed query computed by the QB CTAs (no QLAT stage)
     int ufuse;                      // MLA: the value up-projection computed by the combine CTAs (no UV stage)
     float* racc;                    // their accumulators [L][ROUTER_COPIES][M][router_row(E)], zero at step start
+    // sums of squares of the rows of RMSNorm inputs whose K panels are parts
+    // of the row, summed once per stage by its CTAs (several tokens):
+    // [L + 1][3 sites: A or LM, QB, router][rss_mx], zero at step start
+    float* rss;
+    int rss_mx;
     float* ubuf;                    // per CTA: expert-unit gate/up and hidden values when shared memory is short
     long long ubuf_stride;          // floats per CTA
     unsigned* ctr;                  // [2][L+1][NCTR]

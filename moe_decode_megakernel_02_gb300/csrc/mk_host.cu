@@ -459,6 +459,7 @@ int mk_load_weights(const mk_config* cfg, const mk_weight* table, int32_t n, voi
     const size_t s_trace_n = tracing ? stake((size_t)m->G * 4) : 0;
     const size_t s_newlat = stake(Mx * mk::MLA_D * 2);
     const size_t s_amax = stake(Mx * 4);
+    const size_t s_rss = stake((size_t)(L + 1) * 3 * Mx * 4);  // row sums of squares of split-panel norms
     const size_t s_zero = stake(4096);
     const size_t ctr_n = (size_t)2 * (L + 1) * mk::NCTR;
     const size_t s_ctr = stake(ctr_n * 4);
@@ -723,6 +724,10 @@ int mk_load_weights(const mk_config* cfg, const mk_weight* table, int32_t n, voi
         P.zptr[nz] = F(s_rlog);
         P.zn[nz++] = (long long)L * Mx * mk::router_row(D.E);
     }
+    P.rss = F(s_rss);
+    P.rss_mx = (int)Mx;
+    P.zptr[nz] = P.rss;
+    P.zn[nz++] = (long long)(L + 1) * 3 * Mx;
     // the router folded into the output projection: possible when that
     // projection has one K panel (its rows are final in the CTA that computes
     // them) and a CTA's rows of every token (twice) and its logit sums fit
@@ -753,7 +758,9 @@ int mk_load_weights(const mk_config* cfg, const mk_weight* table, int32_t n, voi
     } else {
         m->qfuse_ok = m->ufuse_ok = false;
     }
-    P.nz = nz;  // logits (split-K head) are added per step in mk_decode_step
+    // logits (split-K head) and the router accumulators are added per step
+    static_assert(sizeof(P.zptr) / sizeof(P.zptr[0]) >= 9, "zero list: 7 buffers here + 2 per step");
+    P.nz = nz;
     m->ctr = reinterpret_cast<unsigned*>(S + s_ctr);
     m->ctr_n = ctr_n;
     m->status = reinterpret_cast<unsigned*>(S + s_status);
@@ -1362,6 +1369,7 @@ extern "C" int mk_decode_step_noalloc(mk_model* m, mk_kv* kv, const int32_t* tok
     P.amax = r(P.amax);
     P.ubuf = r(P.ubuf);
     P.racc = r(P.racc);
+    P.rss = r(P.rss);
     for (int z = 0; z < P.nz; ++z) P.zptr[z] = r(P.zptr[z]);
     P.ctr = r(P.ctr);
     P.status = r(P.status);

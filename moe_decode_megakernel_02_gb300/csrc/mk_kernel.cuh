@@ -35,6 +35,8 @@ struct alignas(16) Ctx {
     // what the staging buffer currently holds
     const void* sk_src;
     const void* sk_gain;
+    const void* rms_src;  // c.ms.rms holds the whole rows' sums of squares of this input
+    int st_rank, st_np;   // plain GEMV stage: this CTA's rank among the np CTAs that have items
     int sk_off, sk_kc, sk_m0, sk_kind, sk_gather;
     int issued;  // producer: ring fills issued
     long long t_start;
@@ -49,6 +51,7 @@ struct alignas(16) Ctx {
         pr.phase = 0;
         sk_src = nullptr;
         sk_gain = nullptr;
+        rms_src = nullptr;
         sk_off = sk_kc = sk_m0 = sk_kind = sk_gather = -1;
         issued = 0;
         pl = pst = 0;
@@ -350,7 +353,7 @@ __device__ __noinline__ void stage_input(Ctx& c, const Gemv& g, const float* src
         // Split panels (the K panel is part of the row): the sum of squares
         // runs over the whole row first, then the panel is scaled.
         float* acc = c.ms.rms;
-        const int rowlen = g.K, tot = ms * rowlen;
+        const int rowlen = g.K, tot = c.rms_src == src ? 0 : ms * rowlen;  // (0: summed by the stage's CTAs)
         const uint16_t* gain = g.gain;
         float part = 0.f;
         int cur = -1;
@@ -604,7 +607,7 @@ __device__ __forceinline__ bool restage(Ctx& c, const Gemv& g, const float* src,
         return false;
     // nobody reads the RMS accumulators between stagings: zero them before
     // the barrier that ends every use of the previous contents
-    if (g.in_kind == IN_RMS && ctid() < ms) c.ms.rms[ctid()] = 0.f;
+    if (g.in_kind == IN_RMS && ctid() < ms && c.rms_src != src) c.ms.rms[ctid()] = 0.f;
     cbar();
     stage_input(c, g, src, grp_off, kc, m0, ms);
     cbar();
@@ -1634,12 +1637,52 @@ __device__ __noinline__ void router_part(Ctx& c, int l, const Gemv& go, int lo, 
 // consumer side of a GEMV stage: items [lo, hi) of g after the deps set by
 // set_deps, then signal `sig` (the GEMV code, cons_gemv, is shared with the
 // expert units).
+// RMSNorm input whose K panels are parts of the row, several tokens: the
+// stage's np CTAs (this one has rank `rank`) each sum the squares of one
+// slice of the M x K input (128-float blocks, a few KB), add them into the
+// step's per-row accumulators and meet at a counter; every CTA then holds
+// the whole rows' sums and stages only its panels (instead of every CTA
+// reading every row: 458 KB at 56 tokens x 2048)
+__device__ __noinline__ void rms_prepass(Ctx& c, int l, const Gemv& g, int sig, int rank, int np) {
+    const Params& p = c.p;
+    const int site = sig == C_QB ? 1 : (sig == C_ROUTER ? 2 : 0);
+    float* const acc = p.rss + ((size_t)l * 3 + site) * p.rss_mx;
+    const int tid = ctid(), lane = tid & 31, warp = tid >> 5, K = g.K;
+    const int nb = (p.M * K) >> 7, b0 = (int)((long long)rank * nb / np), b1 = (int)((long long)(rank + 1) * nb / np);
+    for (int b = b0 + warp; b < b1; b += NCW) {
+        const int i = (b << 7) + lane * 4, t = i / K;  // a block lies in one row (K is a multiple of 128)
+        const float4 v = __ldcg(reinterpret_cast<const float4*>(g.src + (size_t)t * g.src_stride + (i - t * K)));
+        float part = v.x * v.x;
+        part = fmaf(v.y, v.y, part);
+        part = fmaf(v.z, v.z, part);
+        part = fmaf(v.w, v.w, part);
+#pragma unroll
+        for (int o = 16; o; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+        if (lane == 0) atomicAdd(acc + t, part);
+    }
+    // every CTA's additions are done before its arrival (the barrier orders the
+    // other threads' atomics before thread 0's release, which is cumulative)
+    cbar();
+    unsigned* const arr = ctr_of(p, l, C_NRM0 + site);
+    if (threadIdx.x == 0 && !c.dead) {
+        red_release(arr, 1u);
+        if (!wait_ge(p, arr, (unsigned)np, 0x1500u | (unsigned)(l << 16) | (unsigned)site)) c.ms.abort = 1;
+    }
+    cbar();
+    if (*(volatile int*)&c.ms.abort) c.dead = true;
+    if (tid < p.M) c.ms.rms[tid] = __ldcg(acc + tid);
+    c.rms_src = g.src;  // (each warp's own state; restage's barrier orders the rms values)
+}
+
 __device__ __noinline__ void cons_mm(Ctx& c, int l, const Gemv& g, int sig, int lo, int hi) {
     c.cur_code = ((unsigned)sig << 16) | (unsigned)l;
     const long long t0 = gtimer();
     cwait(c, 0x1000u | (unsigned)(l << 16) | (unsigned)sig);
     const long long t1 = gtimer();
+    const bool pre = c.p.rss && !c.p.staged && g.in_kind == IN_RMS && g.n_kc > 1 && c.p.M >= 2 && !c.dead;
+    if (pre) rms_prepass(c, l, g, sig, c.st_rank, c.st_np);
     cons_gemv(c, g, 0, -1, lo, hi);
+    c.rms_src = nullptr;
     if (sig == C_O && c.p.rfuse && !c.dead) router_part(c, l, g, lo, hi);
     if (sig == C_A && (c.p.qfuse || c.p.ufuse)) {
         // buffers of layer l that later stages add into with reductions: the
@@ -3738,20 +3781,29 @@ __device__ __noinline__ bool exec_stage(Ctx& c) {
                 return true;
         }
     }
-    // plain GEMV stage
+    // plain GEMV stage (rank among the np CTAs that have items: for the
+    // norm sums of split-panel inputs)
     const int n = gemv_items(*g);
-    int lo, hi;
+    int lo, hi, rank, np;
     if (gc > 0) {
         my_range_sub(n, c0, gc, lo, hi);
+        np = min(n, gc);
+        rank = n >= gc ? (int)blockIdx.x - c0 : lo;
     } else {
+        int v = (int)blockIdx.x + c.off;
+        if (v >= p.G) v -= p.G;
         my_range(p, n, c.off, lo, hi);
         c.advance(n);
+        np = min(n, p.G);
+        rank = n >= p.G ? v : lo;
     }
     if (lo >= hi) return true;
     if constexpr (PROD) {
         if (!c.dead) prod_plain(c, *g, lo, hi);
     } else {
         set_deps(c, deps);
+        c.st_rank = rank;
+        c.st_np = np;
         cons_mm(c, ls, *g, sig, lo, hi);
     }
     return true;
