@@ -227,14 +227,26 @@ int mk_decode_step_noalloc(mk_model* m, mk_kv* kv, const int32_t* tokens, const 
 
 /* Fault injection on the host (testing the caller's error handling; the GPU
  * is never made to fault): while the environment variable MK_FAULT is
- *   "oom"     mk_load_weights, mk_load_synthetic and mk_alloc_kv fail with
- *             MK_ERR_OOM before they allocate anything;
- *   "bad_arg" mk_load_weights, mk_decode_step and mk_decode_step_noalloc
- *             reject their arguments with MK_ERR_INVALID_ARG.
- * Each failure sets mk_last_error() to a message naming MK_FAULT. */
+ *   "oom"         mk_load_weights, mk_load_synthetic and mk_alloc_kv fail
+ *                 with MK_ERR_OOM before they allocate anything;
+ *   "bad_arg"     mk_load_weights, mk_decode_step and mk_decode_step_noalloc
+ *                 reject their arguments with MK_ERR_INVALID_ARG;
+ *   "skip_signal" mk_decode_step launches a step in which no CTA signals
+ *                 the completion of layer 0's first projection: the
+ *                 stages that read it wait until the wait limit (MK_WAIT_NS)
+ *                 and the step reports MK_ERR_TIMEOUT through mk_step_status.
+ * Each host failure sets mk_last_error() to a message naming MK_FAULT.
+ *
+ * Debug mode: with MK_DEBUG=1 when the model is loaded, every CTA writes a
+ * 16-byte pattern into the unused end of each shared-memory ring slot and
+ * after its input staging area at the start of a step and compares it when
+ * it leaves, and the expert units check that every entry of their token map
+ * is a token of the step. A failed check reports MK_ERR_STATE through
+ * mk_step_status (with the place in mk_last_error()); nothing traps. */
 
 /* Synchronise `stream` and return the device status of the last step
- * (MK_OK, MK_ERR_TIMEOUT, MK_ERR_INVALID_ARG). A failed status resets the
+ * (MK_OK, MK_ERR_TIMEOUT, MK_ERR_INVALID_ARG, or MK_ERR_STATE for a failed
+ * debug-mode check). A failed status resets the
  * model's device state so the next step can run.
  * Every wait inside the step (on another CTA's progress or on a copy into
  * shared memory) gives up after the limit set by the environment variable

@@ -68,14 +68,17 @@ constexpr int MLA_QS = 584;               // padded smem row stride of the queri
 // piece j of a row sits at piece j ^ bits 7..9 of the row's address)
 constexpr int MLA_BOX = MLA_CH * 128;
 constexpr int MLA_TILE_BYTES = 9 * MLA_BOX;
-static_assert(MLA_TILE_BYTES <= SLOT_BYTES, "MLA chunk must fit a slot");
+static_assert(MLA_TILE_BYTES <= SLOT_BYTES - 16, "MLA chunk must fit a slot (and leave its debug canary alone)");
+static_assert(64 * (256 * 2 + 16) <= SLOT_BYTES - 16 && 16 * (1024 * 2 + 16) <= SLOT_BYTES - 16 &&
+                  8 * (2048 * 2 + 16) <= SLOT_BYTES - 16,
+              "padded tensor-core tiles leave the slot's debug canary alone");
 static_assert(SLOT_BYTES % 1024 == 0, "ring slots keep the 1024-byte alignment of the swizzled boxes");
 
 enum InKind { IN_COPY = 0, IN_RMS = 1, IN_SWIGLU = 2 };
 // OUT_ACC: += into a CTA-private buffer; OUT_ADD: every warp adds its share
 // (a K slice) atomically into a zeroed CTA-private buffer, no barrier per tile
 enum OutKind { OUT_STORE = 0, OUT_RESID = 1, OUT_SCALED = 2, OUT_ACC = 3, OUT_ADD = 4 };
-enum StatusCode { ST_OK = 0, ST_INVALID = 1, ST_TIMEOUT = 5 };
+enum StatusCode { ST_OK = 0, ST_INVALID = 1, ST_TIMEOUT = 5, ST_DEBUG = 6 };
 
 // A matrix-vector stage: out[m][row] (+)= W[row, :] . f(in)[m, :]
 // W is packed [n_kc][N][Kc] (K-panels; n_kc == 1 is plain row-major).
@@ -174,6 +177,8 @@ struct Params {
     int nz, carry;                  // carry: residual copied by items (split-K output projection)
     int gs, gr;                     // CTAs [0, gs): shared expert, [gs, G): routed experts ([G-gr, G) first run the router)
     int stall;                      // testing: CTA 0 first waits on a counter nothing signals (ends in a timeout)
+    int skip_sig;                   // testing: 1 + the stage whose layer-0 signal CTA 0 leaves out (0: none)
+    int debug;                      // shared-memory canaries and token-map checks (ST_DEBUG on a failure)
     // one launch per stage (the unfused comparison path): 0 = the whole step
     // in this launch; 1 = program positions [st_lo, st_hi) only, 2 = the
     // step's set-up only (embedding, buffers zeroed). Launches are ordered by
@@ -250,7 +255,10 @@ struct Misc {
 };
 constexpr int SMEM_RING = 0;
 constexpr int SMEM_STAGE = NSLOT * SLOT_BYTES;
-constexpr int SMEM_RED = SMEM_STAGE + STAGE_BYTES;
+// 16 bytes between the staging area and the reduction area: a canary in
+// debug mode (checked when the CTA leaves)
+constexpr int SMEM_CANARY = SMEM_STAGE + STAGE_BYTES;
+constexpr int SMEM_RED = SMEM_CANARY + 16;
 constexpr int SMEM_MISC = SMEM_RED + RED_FLOATS * 4;
 constexpr int SMEM_CTX = (SMEM_MISC + (int)sizeof(Misc) + 15) & ~15;
 constexpr int CTX_BYTES = 160;  // per warp (checked against sizeof(Ctx))

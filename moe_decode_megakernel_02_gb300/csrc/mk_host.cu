@@ -767,6 +767,7 @@ int mk_load_weights(const mk_config* cfg, const mk_weight* table, int32_t n, voi
     P.ctr = m->ctr;
     P.status = m->status;
     P.timeout_ns = wait_ns();
+    P.debug = getenv("MK_DEBUG") && atoi(getenv("MK_DEBUG")) > 0;
     if (D.E) {
         m->dbg_idx = reinterpret_cast<int*>(S + s_dbgi);
         m->dbg_w = reinterpret_cast<float*>(S + s_dbgw);
@@ -1034,6 +1035,7 @@ int mk_decode_step(mk_model* m, mk_kv* kv, const int32_t* tokens, const int32_t*
     mk::Params P;
     if (const int rc = step_params(m, kv, tokens, positions, batch, T, logits, accept, P)) return rc;
     P.stall = getenv("MK_TEST_STALL") != nullptr;
+    P.skip_sig = fault("skip_signal") ? 1 + mk::C_A : 0;
     P.parity = (int)(m->steps & 1);
     cudaStream_t s = (cudaStream_t)stream;
     void* args[] = {&P};
@@ -1159,6 +1161,8 @@ int mk_step_status(mk_model* m, void* stream) {
         return fail(MK_ERR_TIMEOUT, "device wait timed out (where=0x%x, cta=%u)", st[2], st[3]);
     if (st[0] == mk::ST_INVALID)
         return fail(MK_ERR_INVALID_ARG, "token id or position out of range for this step");
+    if (st[0] == mk::ST_DEBUG)
+        return fail(MK_ERR_STATE, "debug check failed (MK_DEBUG; where=0x%x, cta=%u)", st[2], st[3]);
     return fail(MK_ERR_CUDA, "device status %u", st[0]);
 }
 
@@ -1415,5 +1419,7 @@ extern "C" int mk_decode_step_noalloc(mk_model* m, mk_kv* kv, const int32_t* tok
     if (st[0] == mk::ST_TIMEOUT)
         return fail(MK_ERR_TIMEOUT, "device wait timed out (where=0x%x, cta=%u)", st[2], st[3]);
     if (st[0] == mk::ST_INVALID) return fail(MK_ERR_INVALID_ARG, "token id or position out of range for this step");
+    if (st[0] == mk::ST_DEBUG)
+        return fail(MK_ERR_STATE, "debug check failed (MK_DEBUG; where=0x%x, cta=%u)", st[2], st[3]);
     return fail(MK_ERR_CUDA, "device status %u", st[0]);
 }

@@ -139,7 +139,10 @@ __device__ bool cwait(Ctx& c, unsigned where) {
 // release, which is cumulative over them)
 __device__ void csignal(Ctx& c, int layer, int which, unsigned n) {
     cbar();
-    if (threadIdx.x == 0 && n && !c.p.staged) red_release(ctr_of(c.p, layer, which), n);
+    // (MK_FAULT=skip_signal: the CTAs leave out their releases of one stage
+    // of layer 0, so that stage's readers run into their wait limit)
+    const bool skip = c.p.skip_sig && layer == 0 && which == c.p.skip_sig - 1;
+    if (threadIdx.x == 0 && n && !c.p.staged && !skip) red_release(ctr_of(c.p, layer, which), n);
     if (*(volatile int*)&c.ms.abort) c.dead = true;
 }
 
@@ -2909,9 +2912,26 @@ __device__ __noinline__ void argmax_cons(Ctx& c, int lo, int hi) {
 }
 
 // ====================================================== init (consumers) ====
+// debug mode: 16 bytes at the end of every ring slot (no copy reaches
+// them: the largest, an MLA chunk, ends 1 KB earlier) and after the staging
+// area hold a pattern written at entry and compared when the CTA leaves
+__device__ __noinline__ void debug_canaries(const Params& p, uint8_t* smem, bool check) {
+    const uint4 pat = make_uint4(0x6d6b4341u, 0x4e415259u, blockIdx.x, 0x5a5a5a5au);
+    for (int s2 = 0; s2 <= NSLOT; ++s2) {
+        uint4* w = reinterpret_cast<uint4*>(smem + (s2 < NSLOT ? SMEM_RING + (s2 + 1) * SLOT_BYTES - 16 : SMEM_CANARY));
+        if (!check) {
+            *w = pat;
+        } else {
+            const uint4 v = *w;
+            if (v.x != pat.x || v.y != pat.y || v.z != pat.z || v.w != pat.w) raise_status(p, ST_DEBUG, 0x9100u + s2);
+        }
+    }
+}
+
 __device__ __noinline__ bool init_phase(Ctx& c) {
     const Params& p = c.p;
     const int tid = ctid();
+    if (p.debug && tid == 0) debug_canaries(p, c.smem, false);
     // every CTA checks the step's inputs itself (all reach the same verdict)
     if (tid == 0) {
         int bad = 0;
@@ -3266,8 +3286,15 @@ __device__ __noinline__ void unit_seg_cons(Ctx& c, int l, int kind, int expert, 
                 c.ms.uw[pos[q]] = w[q];
             }
         }
+        __syncwarp();
         if (lane == 0) {
             c.ms.gm = __popc(b0) + __popc(b1);
+            if (p.debug)  // every entry of the token map is a token of the step
+                for (int i = 0; i < c.ms.gm; ++i)
+                    if (c.ms.gt[i] >= p.M) {
+                        raise_status(p, ST_DEBUG, 0x9300u);
+                        c.ms.abort = 1;
+                    }
             // a key per token list: routed expert and group, or shared group
             c.ms.gather = one_panel && !all_staged && (expert >= 0 || m_hi - m_lo < p.M)
                               ? (expert >= 0 ? 1 + expert + 256 * m_lo : (1 << 24) + m_lo)
@@ -3594,8 +3621,12 @@ __device__ __noinline__ bool exec_stage(Ctx& c) {
         if (c.dead) return false;
     }
     const int l = c.pl, st = c.pst;
-    if (st == S_END) return false;
-    if (p.staged && prog_index(p, l, st) >= p.st_hi) return false;
+    if (st == S_END || (p.staged && prog_index(p, l, st) >= p.st_hi)) {
+        // the consumers' last stage ended at a barrier: every slot they read
+        // was filled and released
+        if (!PROD && p.debug && threadIdx.x == 0) debug_canaries(p, c.smem, true);
+        return false;
+    }
     {
         int nl = l, nst = st + 1;
         if (l < p.L && nst == S_NLAYER) {
@@ -3830,6 +3861,7 @@ __device__ void prod_drain(Ctx& c) {
         }
     }
 }
+
 
 __global__ void __launch_bounds__(NTHREADS, 1) megakernel(const __grid_constant__ Params p) {
     extern __shared__ __align__(1024) uint8_t smem[];  // 1024: the swizzled MLA boxes of the ring

@@ -140,3 +140,20 @@ def test_model_and_caches_free_in_either_order(model_first):
     junk = [bytearray(n) for n in (24, 48, 96, 200, 1000, 5000) for _ in range(200)]
     del junk
     ctypes.CDLL("libc.so.6").malloc_trim(0)
+
+
+@pytest.mark.parametrize("name,B,T", [("deep", 2, 1), ("verify", 8, 7), ("dense", 8, 1)])
+def test_debug_mode_checks_pass_and_parity_holds(monkeypatch, name, B, T):
+    # MK_DEBUG=1: shared-memory canaries at the end of every ring slot and
+    # after the staging area (written when a CTA starts, compared when it
+    # leaves) and the expert units' token-map check; a clean step reports
+    # MK_OK and still matches the oracle (the deep and verify cases stream
+    # MLA chunks, 64-row tensor-core tiles and expert down tiles through
+    # the ring; dense B 8 the split-panel norm inputs)
+    monkeypatch.setenv("MK_DEBUG", "1")
+    cfg = configs.scaled(configs.ALL[name], n_layers=2)
+    ctx = min(cfg["ctx"], 2000)
+    g, _ = parity.run_gpu(cfg, B, T, 1, ctx, want_accept=T > 1)
+    o = parity.run_oracle(cfg, g, ctx, B, T)
+    rep = parity.compare(cfg, g, o, B, T)
+    print(name, B, T, "debug mode", rep)
