@@ -36,12 +36,16 @@ class Cfg(ctypes.Structure):
         "n_q_heads", "n_kv_heads", "head_dim",
         "q_lora_rank", "kv_lora_rank", "qk_nope_dim", "qk_rope_dim", "v_head_dim",
         "n_routed_experts", "top_k", "n_shared_experts", "ffn_dim", "shared_ffn_dim")] + [
-        ("rms_eps", ctypes.c_float), ("rope_theta", ctypes.c_float)]
+        ("rms_eps", ctypes.c_float), ("rope_theta", ctypes.c_float), ("expert_format", ctypes.c_int32)]
+
+# expert_format values: every weight bf16, or MXFP8 expert weights
+BF16, MXFP8 = 0, 1
 
 
 def cfg_struct(cfg) -> Cfg:
-    vals = [int(cfg[f]) for f, t in Cfg._fields_ if t is ctypes.c_int32]
-    return Cfg(*vals, float(cfg["rms_eps"]), float(cfg["rope_theta"]))
+    vals = {f: int(cfg[f]) for f, t in Cfg._fields_ if t is ctypes.c_int32 and f != "expert_format"}
+    return Cfg(**vals, rms_eps=float(cfg["rms_eps"]), rope_theta=float(cfg["rope_theta"]),
+               expert_format=int(cfg.get("expert_format", BF16)))
 
 
 _lib = None
@@ -83,6 +87,10 @@ def lib():
         L.oracle_topk.argtypes = [P, I32, I32, P, P, P]
         L.oracle_silu.argtypes = [ctypes.c_double]
         L.oracle_silu.restype = ctypes.c_double
+        L.oracle_e4m3_value.argtypes = [ctypes.c_uint8]
+        L.oracle_e4m3_value.restype = ctypes.c_double
+        L.oracle_mx_dequant.argtypes = [P, P, I32, I32, P]
+        L.oracle_mx_dequant.restype = None
         L.oracle_attend.argtypes = [P, P, P, I32, I32, ctypes.c_double, P]
         _lib = L
     return _lib
@@ -232,4 +240,18 @@ def attend(q, K_u16, V_u16, scale):
     n, hd = K.shape
     out = np.empty(hd, dtype=np.float64)
     lib().oracle_attend(q.ctypes.data, K.ctypes.data, V.ctypes.data, n, hd, scale, out.ctypes.data)
+    return out
+
+
+def e4m3_value(code: int) -> float:
+    """Value of an FP8 E4M3 code (the oracle's decoder)."""
+    return float(lib().oracle_e4m3_value(code))
+
+
+def mx_dequant(codes_u8, scales_u8, rows: int, cols: int) -> np.ndarray:
+    """MX dequantisation of E4M3 codes [rows, cols] with E8M0 scales [rows, cols/32] (fp64)."""
+    q = np.ascontiguousarray(codes_u8, dtype=np.uint8).reshape(rows, cols)
+    sc = np.ascontiguousarray(scales_u8, dtype=np.uint8).reshape(rows, cols // 32)
+    out = np.empty((rows, cols))
+    lib().oracle_mx_dequant(q.ctypes.data, sc.ctypes.data, rows, cols, out.ctypes.data)
     return out

@@ -75,6 +75,31 @@ template <class T> T bf(uint16_t h) { return (T)bf16_to_double(h); }
 
 }  // namespace
 
+/* Value of an FP8 E4M3 code, from the format's definition (OCP "Microscaling
+ * Formats (MX) Specification" v1.0, the E4M3 element type): sign bit, 4
+ * exponent bits of bias 7, 3 mantissa bits; exponent field 0 holds the
+ * subnormals m * 2^-9; 0x7F and 0xFF are NaN; there are no infinities. */
+double oracle_e4m3_value(uint8_t code) {
+    const int s = code >> 7, e = (code >> 3) & 15, m = code & 7;
+    if (e == 15 && m == 7) return std::numeric_limits<double>::quiet_NaN();
+    const double v = e == 0 ? std::ldexp((double)m, -9) : std::ldexp(8.0 + m, e - 10);
+    return s ? -v : v;
+}
+
+/* MX dequantisation (same specification): element j of row r is its E4M3
+ * value times 2^(E - 127), E the E8M0 scale byte of its block of 32
+ * consecutive elements of the row (scale 0xFF is NaN). codes [rows, cols],
+ * scales [rows, cols / 32], out [rows, cols]. */
+void oracle_mx_dequant(const uint8_t* codes, const uint8_t* scales, int32_t rows, int32_t cols, double* out) {
+    const int32_t nb = cols / 32;
+    for (int32_t r = 0; r < rows; ++r)
+        for (int32_t j = 0; j < cols; ++j) {
+            const uint8_t E = scales[(size_t)r * nb + j / 32];
+            const double x = oracle_e4m3_value(codes[(size_t)r * cols + j]);
+            out[(size_t)r * cols + j] = E == 0xFF ? std::numeric_limits<double>::quiet_NaN() : std::ldexp(x, (int)E - 127);
+        }
+}
+
 struct oracle_model {
     oracle_cfg c;
     synth_dims d;
@@ -105,6 +130,11 @@ synth_dims dims_of(const oracle_cfg& c) {
     return d;
 }
 
+bool is_expert_kind(int kind) {
+    return kind == SYNTH_GATE || kind == SYNTH_UP || kind == SYNTH_DOWN || kind == SYNTH_SH_GATE ||
+           kind == SYNTH_SH_UP || kind == SYNTH_SH_DOWN;
+}
+
 const uint16_t* tensor(oracle_model* m, int kind, int layer, int expert) {
     TKey k(kind, layer, expert);
     auto it = m->w.find(k);
@@ -113,8 +143,20 @@ const uint16_t* tensor(oracle_model* m, int kind, int layer, int expert) {
     float sigma, mean;
     if (synth_weight_spec(&m->d, kind, &rows, &cols, &sigma, &mean) != 0) return nullptr;
     std::vector<uint16_t> v((size_t)rows * cols);
-    synth_fill_bf16(v.data(), v.size(), m->seed, synth_tensor_id(kind, layer, expert), sigma, mean, 0,
-                    m->gen_threads);
+    if (m->c.expert_format == 1 && is_expert_kind(kind)) {
+        /* MXFP8 expert weights: the generator's E4M3 codes and E8M0 block
+         * scales, dequantised; every value (at most 4 significant bits, scale
+         * 2^-10 or 2^-9) is a bf16 number, so the bf16 store holds it exactly */
+        std::vector<uint8_t> q((size_t)rows * cols), sc((size_t)rows * (cols / SYNTH_MX_BLOCK));
+        synth_fill_e4m3(q.data(), q.size(), m->seed, synth_tensor_id(kind, layer, expert), 0, m->gen_threads);
+        synth_fill_e8m0(sc.data(), sc.size(), m->seed, synth_tensor_id(kind + 6, layer, expert), 0);
+        std::vector<double> deq(q.size());
+        oracle_mx_dequant(q.data(), sc.data(), rows, cols, deq.data());
+        for (size_t i = 0; i < deq.size(); ++i) v[i] = to_bf16(deq[i]);
+    } else {
+        synth_fill_bf16(v.data(), v.size(), m->seed, synth_tensor_id(kind, layer, expert), sigma, mean, 0,
+                        m->gen_threads);
+    }
     auto& slot = m->w[k];
     slot.swap(v);
     return slot.data();
@@ -550,6 +592,10 @@ bool cfg_ok(const oracle_cfg* c) {
     if (c->n_routed_experts < 0 || (c->n_routed_experts > 0 && (c->top_k < 1 || c->top_k > c->n_routed_experts)))
         return false;
     if (c->n_shared_experts < 0 || c->n_shared_experts > 1) return false;
+    if (c->expert_format != 0 && c->expert_format != 1) return false;
+    if (c->expert_format == 1 && (c->d_model % SYNTH_MX_BLOCK || c->ffn_dim % SYNTH_MX_BLOCK ||
+                                  c->shared_ffn_dim % SYNTH_MX_BLOCK))
+        return false;
     return true;
 }
 

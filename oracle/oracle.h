@@ -39,6 +39,9 @@ typedef struct oracle_cfg {
     int32_t q_lora_rank, kv_lora_rank, qk_nope_dim, qk_rope_dim, v_head_dim;
     int32_t n_routed_experts, top_k, n_shared_experts, ffn_dim, shared_ffn_dim;
     float rms_eps, rope_theta;
+    /* 0: every weight bf16; 1: routed and shared expert weights MXFP8 (the
+     * generator's E4M3 codes and E8M0 block scales, dequantised exactly) */
+    int32_t expert_format;
 } oracle_cfg;
 
 typedef struct oracle_model oracle_model;
@@ -87,6 +90,8 @@ int oracle_full_recompute(oracle_model* m, const int32_t* tokens, int32_t B, int
                           double* logits);
 
 /* Building blocks, exposed for pinning (all fp64 unless stated). */
+double oracle_e4m3_value(uint8_t code);
+void oracle_mx_dequant(const uint8_t* codes, const uint8_t* scales, int32_t rows, int32_t cols, double* out);
 void oracle_rmsnorm(const double* x, const uint16_t* gain, int32_t n, double eps, double* out);
 void oracle_rope(double* x, int32_t dim, int32_t pos, double theta);
 void oracle_softmax(const double* x, int32_t n, double* out);

@@ -25,7 +25,15 @@ EMBED, LM_HEAD, FINAL_NORM, ATTN_NORM, FFN_NORM = 1, 2, 3, 4, 5
 WQ, WK, WV, WO = 6, 7, 8, 9
 WDQ, Q_NORM, WUQ, WDKV, KV_NORM, WUKV = 10, 11, 12, 13, 14, 15
 ROUTER, GATE, UP, DOWN, SH_GATE, SH_UP, SH_DOWN = 16, 17, 18, 19, 20, 21, 22
+GATE_SCALE, UP_SCALE, DOWN_SCALE, SH_GATE_SCALE, SH_UP_SCALE, SH_DOWN_SCALE = 23, 24, 25, 26, 27, 28
 KV_K, KV_V, KV_LATENT, TOKENS = 40, 41, 42, 43
+
+# MXFP8 expert weights: E4M3 codes of sigma-16 draws, one E8M0 scale per 32
+# elements of a row (synth.h); the scale kind of a code kind is kind + 6
+F8_SIGMA = 16.0
+MX_BLOCK = 32
+F8_KINDS = (GATE, UP, DOWN, SH_GATE, SH_UP, SH_DOWN)
+SCALE_OF = {k: k + 6 for k in F8_KINDS}
 
 GLOBAL_KINDS = (EMBED, LM_HEAD, FINAL_NORM)
 LAYER_KINDS = (ATTN_NORM, FFN_NORM, WQ, WK, WV, WO, WDQ, Q_NORM, WUQ, WDKV, KV_NORM, WUKV,
@@ -89,6 +97,14 @@ def _load_host():
         lib.synth_key.restype = ctypes.c_uint64
         lib.synth_scale_const.argtypes = [ctypes.c_float]
         lib.synth_scale_const.restype = ctypes.c_float
+        lib.synth_e4m3_rne.argtypes = [ctypes.c_float]
+        lib.synth_e4m3_rne.restype = ctypes.c_uint8
+        lib.synth_fill_e4m3.argtypes = [ctypes.c_void_p, ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint64,
+                                        ctypes.c_uint64, ctypes.c_int]
+        lib.synth_fill_e4m3.restype = None
+        lib.synth_fill_e8m0.argtypes = [ctypes.c_void_p, ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint64,
+                                        ctypes.c_uint64]
+        lib.synth_fill_e8m0.restype = None
         _host = lib
     return _host
 
@@ -102,6 +118,10 @@ def _load_cuda():
         lib.synth_fill_bf16_cuda.argtypes = [ctypes.c_void_p, ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint64,
                                              ctypes.c_float, ctypes.c_float, ctypes.c_uint64, ctypes.c_void_p]
         lib.synth_fill_bf16_cuda.restype = ctypes.c_int
+        for fn in (lib.synth_fill_e4m3_cuda, lib.synth_fill_e8m0_cuda):
+            fn.argtypes = [ctypes.c_void_p, ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint64,
+                           ctypes.c_void_p]
+            fn.restype = ctypes.c_int
         _cuda = lib
     return _cuda
 
@@ -146,6 +166,35 @@ def fill_bf16_cuda(dev_ptr: int, n: int, seed: int, tid: int, sigma: float, mean
     rc = _load_cuda().synth_fill_bf16_cuda(dev_ptr, n, seed, tid, sigma, mean, index0, stream)
     if rc != 0:
         raise RuntimeError(f"synth_fill_bf16_cuda failed with CUDA error {rc}")
+
+
+def e4m3_rne(f: float) -> int:
+    """The generator's fp32 -> FP8 E4M3 rounding (nearest, ties to even, saturating)."""
+    return int(_load_host().synth_e4m3_rne(f))
+
+
+def fill_e4m3_host(n: int, seed: int, tid: int, index0: int = 0) -> np.ndarray:
+    out = np.empty(n, dtype=np.uint8)
+    _load_host().synth_fill_e4m3(out.ctypes.data, n, seed, tid, index0, 1)
+    return out
+
+
+def fill_e8m0_host(n: int, seed: int, tid: int, index0: int = 0) -> np.ndarray:
+    out = np.empty(n, dtype=np.uint8)
+    _load_host().synth_fill_e8m0(out.ctypes.data, n, seed, tid, index0)
+    return out
+
+
+def fill_e4m3_cuda(dev_ptr: int, n: int, seed: int, tid: int, index0: int = 0, stream: int = 0) -> None:
+    rc = _load_cuda().synth_fill_e4m3_cuda(dev_ptr, n, seed, tid, index0, stream)
+    if rc != 0:
+        raise RuntimeError(f"synth_fill_e4m3_cuda failed with CUDA error {rc}")
+
+
+def fill_e8m0_cuda(dev_ptr: int, n: int, seed: int, tid: int, index0: int = 0, stream: int = 0) -> None:
+    rc = _load_cuda().synth_fill_e8m0_cuda(dev_ptr, n, seed, tid, index0, stream)
+    if rc != 0:
+        raise RuntimeError(f"synth_fill_e8m0_cuda failed with CUDA error {rc}")
 
 
 def token(seed: int, step: int, b: int, t: int, vocab: int) -> int:

@@ -28,6 +28,20 @@
  *                   rounded to bf16 with round-to-nearest-even.
  *   token(seed, step, b, t, V): draw(key(seed, TOKENS id), step*2^20 + b*2^10 + t) mod V
  *
+ * MXFP8 expert weights (the microscaling format of the OCP "Microscaling
+ * Formats (MX) Specification" v1.0: each block of 32 consecutive elements of
+ * a row shares one E8M0 scale byte E, value 2^(E-127); the elements are FP8
+ * E4M3 codes -- sign, 4 exponent bits of bias 7, 3 mantissa bits, subnormals
+ * of quantum 2^-9, largest finite 448, codes 0x7F/0xFF NaN, no infinities):
+ *   code(i)   = e4m3_rne(normal(key, i) with sigma 16): the same normal draw
+ *               as a bf16 weight, rounded to E4M3 (nearest, ties to even;
+ *               |value| >= 464 saturates to 448, NaN gives 0x7F) instead of
+ *               bf16. |16 N| <= 96, so no draw saturates.
+ *   scale(b)  = 117 + (draw(key(seed, scale tensor id), b) & 1): 2^-10 or
+ *               2^-9, block b = row * (cols / 32) + column / 32.
+ * The elements are then about N(0, 0.016..0.031), the bf16 recipe's scale.
+ * The scale tensors have kinds of their own (GATE_SCALE .. SH_DOWN_SCALE).
+ *
  * Recipe (the reading of "weights bf16 N(0, 0.02)" and "KV bf16 N(0, 1)"):
  * matrices and embeddings sigma = 0.02, mean 0; RMSNorm gains sigma = 0.02,
  * mean 1; pre-filled KV entries sigma = 1, mean 0. KV entries are indexed
@@ -54,6 +68,9 @@ enum synth_kind {
     /* MoE */
     SYNTH_ROUTER = 16, SYNTH_GATE = 17, SYNTH_UP = 18, SYNTH_DOWN = 19,
     SYNTH_SH_GATE = 20, SYNTH_SH_UP = 21, SYNTH_SH_DOWN = 22,
+    /* E8M0 block scales of the MXFP8 expert weights (kind of the codes + 6) */
+    SYNTH_GATE_SCALE = 23, SYNTH_UP_SCALE = 24, SYNTH_DOWN_SCALE = 25,
+    SYNTH_SH_GATE_SCALE = 26, SYNTH_SH_UP_SCALE = 27, SYNTH_SH_DOWN_SCALE = 28,
     /* non-weight streams */
     SYNTH_KV_K = 40, SYNTH_KV_V = 41, SYNTH_KV_LATENT = 42, SYNTH_TOKENS = 43
 };
@@ -82,6 +99,15 @@ void synth_fill_bf16(uint16_t* out, uint64_t n, uint64_t seed, uint64_t tensor_i
                      float sigma, float mean, uint64_t index0, int threads);
 
 int32_t synth_token(uint64_t seed, int64_t step, int32_t b, int32_t t, int32_t vocab);
+
+#define SYNTH_F8_SIGMA 16.0f      /* sigma of the normal draws behind E4M3 codes */
+#define SYNTH_MX_BLOCK 32         /* elements per E8M0 scale */
+/* fp32 -> FP8 E4M3 code, round to nearest even, saturating (see above) */
+uint8_t synth_e4m3_rne(float f);
+/* E4M3 codes of elements index0 .. index0+n-1 of tensor `tensor_id` */
+void synth_fill_e4m3(uint8_t* out, uint64_t n, uint64_t seed, uint64_t tensor_id, uint64_t index0, int threads);
+/* E8M0 scale bytes of blocks index0 .. index0+n-1 of scale tensor `tensor_id` */
+void synth_fill_e8m0(uint8_t* out, uint64_t n, uint64_t seed, uint64_t tensor_id, uint64_t index0);
 
 /* shape and scale of weight tensor (kind, layer, expert) under the recipe.
  * returns 0 and fills rows/cols/sigma/mean if the tensor exists for these

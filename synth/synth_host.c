@@ -48,6 +48,42 @@ uint16_t synth_bf16_rne(float f) {
     return (uint16_t)(u >> 16);
 }
 
+uint8_t synth_e4m3_rne(float f) {
+    uint32_t u;
+    memcpy(&u, &f, 4);
+    const uint8_t sign = (uint8_t)((u >> 24) & 0x80u);
+    const uint32_t a = u & 0x7fffffffu;
+    if (a > 0x7f800000u) return 0x7f;                 /* NaN */
+    if (a >= 0x43e80000u) return (uint8_t)(sign | 0x7e); /* |f| >= 464: saturate to 448 */
+    if (a >= 0x3c800000u) {                           /* |f| >= 2^-6: normal E4M3 */
+        const uint32_t r = a + 0x7ffffu + ((a >> 20) & 1u); /* keep 3 of 23 mantissa bits, ties to even */
+        const uint32_t e = (r >> 23) - 127u + 7u, m = (r >> 20) & 7u;
+        return (uint8_t)(sign | (e << 3) | m);
+    }
+    /* subnormal E4M3: multiples of 2^-9 (8 of them give the smallest normal) */
+    float x, fa;
+    memcpy(&fa, &a, 4);
+    x = fa * 512.0f;                                  /* exact: a power-of-two scaling */
+    uint32_t n = (uint32_t)x;
+    const float fr = x - (float)n;                    /* exact: x < 8 */
+    if (fr > 0.5f || (fr == 0.5f && (n & 1u))) ++n;
+    return (uint8_t)(sign | n);
+}
+
+void synth_fill_e4m3(uint8_t* out, uint64_t n, uint64_t seed, uint64_t tensor_id, uint64_t index0, int threads) {
+    /* the bf16 fill's normal draws, one fp32 value at a time (no threads
+     * needed at the sizes the CPU side generates) */
+    (void)threads;
+    const uint64_t key = synth_key(seed, tensor_id);
+    const float c = synth_scale_const(SYNTH_F8_SIGMA);
+    for (uint64_t i = 0; i < n; ++i) out[i] = synth_e4m3_rne(synth_normal_f32(key, index0 + i, c, 0.0f));
+}
+
+void synth_fill_e8m0(uint8_t* out, uint64_t n, uint64_t seed, uint64_t tensor_id, uint64_t index0) {
+    const uint64_t key = synth_key(seed, tensor_id);
+    for (uint64_t i = 0; i < n; ++i) out[i] = (uint8_t)(117u + (uint32_t)(synth_draw(key, index0 + i) & 1u));
+}
+
 typedef struct {
     uint16_t* out;
     uint64_t lo, hi, key, index0;
@@ -125,6 +161,12 @@ int synth_weight_spec(const synth_dims* d, int32_t kind, int32_t* rows, int32_t*
     case SYNTH_DOWN: if (!moe) return -1; r = d->d_model; c = d->ffn_dim; break;
     case SYNTH_SH_GATE: case SYNTH_SH_UP: if (!sh) return -1; r = d->shared_ffn_dim; c = d->d_model; break;
     case SYNTH_SH_DOWN: if (!sh) return -1; r = d->d_model; c = d->shared_ffn_dim; break;
+    case SYNTH_GATE_SCALE: case SYNTH_UP_SCALE: case SYNTH_DOWN_SCALE:
+    case SYNTH_SH_GATE_SCALE: case SYNTH_SH_UP_SCALE: case SYNTH_SH_DOWN_SCALE:
+        /* one E8M0 byte per block of 32 elements of the code tensor's rows */
+        if (synth_weight_spec(d, kind - 6, &r, &c, 0, 0) != 0 || c % SYNTH_MX_BLOCK) return -1;
+        c /= SYNTH_MX_BLOCK;
+        break;
     default: return -1;
     }
     if (rows) *rows = r;

@@ -141,3 +141,80 @@ def test_router_folded_into_output_rows_equals_norm_then_matmul():
     assert np.allclose(folded, plain, rtol=1e-12, atol=1e-12)
     # top-k unchanged by the common positive scale
     assert np.array_equal(oracle.topk(folded, 8)[0], oracle.topk(tot[:E], 8)[0])
+
+
+def test_e4m3_value_against_torch_and_closed_forms():
+    # every code against torch's float8_e4m3fn decoding (a library routine
+    # the oracle does not use), plus values fixed by the format's definition
+    import torch
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    mine = np.array([oracle.e4m3_value(int(c)) for c in codes])
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(mine), nan) and set(np.flatnonzero(nan)) == {0x7F, 0xFF}
+    assert np.array_equal(mine[~nan], ref[~nan])
+    assert oracle.e4m3_value(0x7E) == 448.0 and oracle.e4m3_value(0x01) == 2.0 ** -9
+    assert oracle.e4m3_value(0x38) == 1.0 and oracle.e4m3_value(0xC0) == -2.0
+
+
+def test_mx_dequant_blocks_and_scales():
+    # element (r, j) = value(code) * 2^(E[r, j // 32] - 127): built here from
+    # torch's decoding and numpy's ldexp with the scales repeated per block;
+    # a wrong block index, bias or row stride breaks the comparison
+    import torch
+    rng = np.random.default_rng(8)
+    rows, cols = 5, 96
+    q = rng.integers(0, 256, (rows, cols), dtype=np.uint8)
+    q[(q & 0x7F) == 0x7F] = 0x3A  # no NaN codes
+    sc = rng.integers(100, 140, (rows, cols // 32), dtype=np.uint8)
+    dec = torch.from_numpy(q).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    ref = np.ldexp(dec, np.repeat(sc.astype(np.int64) - 127, 32, axis=1))
+    assert np.array_equal(oracle.mx_dequant(q, sc, rows, cols), ref)
+    # scale byte 127 is the identity
+    one = np.full((rows, cols // 32), 127, dtype=np.uint8)
+    assert np.array_equal(oracle.mx_dequant(q, one, rows, cols), dec)
+
+
+def _tiny_mx():
+    from synth import configs
+    return configs.scaled(configs.TINY, n_layers=1, expert_format=oracle.MXFP8)
+
+
+def test_mxfp8_model_expert_weights_are_the_dequantised_codes():
+    # the MXFP8 model's expert tensors equal the generator's codes decoded by
+    # torch and scaled by 2^(E - 127), exactly (as bf16 bits); every other
+    # tensor is the bf16 model's
+    import torch
+    from synth import configs
+    cfg = _tiny_mx()
+    mx, bf = oracle.Model(cfg), oracle.Model(configs.scaled(cfg, expert_format=oracle.BF16))
+    for kind, layer, e in [(synth.GATE, 0, 0), (synth.UP, 0, 5), (synth.DOWN, 0, 7), (synth.SH_DOWN, 0, 0)]:
+        r, c, _, _ = synth.weight_spec(cfg, kind)
+        q = synth.fill_e4m3_host(r * c, cfg["seed"], synth.tensor_id(kind, layer, e))
+        sc = synth.fill_e8m0_host(r * c // 32, cfg["seed"], synth.tensor_id(synth.SCALE_OF[kind], layer, e))
+        dec = torch.from_numpy(q).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+        want = np.ldexp(dec, np.repeat(sc.astype(np.int64) - 127, 32))
+        got = synth.bf16_to_f32(mx.get_tensor(kind, layer, e)).astype(np.float64)
+        assert np.array_equal(got, want)
+    for kind in (synth.WQ, synth.WO, synth.ROUTER, synth.FFN_NORM):
+        assert np.array_equal(mx.get_tensor(kind, 0, 0), bf.get_tensor(kind, 0, 0))
+
+
+def test_mxfp8_model_is_the_bf16_model_with_those_weights():
+    # a decode step of the MXFP8 model equals, bit for bit, the bf16 model's
+    # step once its expert tensors are set to the MXFP8 model's values: the
+    # format changes the weights and nothing else
+    from synth import configs
+    cfg = _tiny_mx()
+    mx, bf = oracle.Model(cfg), oracle.Model(configs.scaled(cfg, expert_format=oracle.BF16))
+    for kind in (synth.SH_GATE, synth.SH_UP, synth.SH_DOWN):
+        bf.set_tensor(kind, 0, 0, mx.get_tensor(kind, 0, 0))
+    for e in range(cfg["n_routed_experts"]):
+        for kind in (synth.GATE, synth.UP, synth.DOWN):
+            bf.set_tensor(kind, 0, e, mx.get_tensor(kind, 0, e))
+    outs = []
+    for m in (mx, bf):
+        kv = oracle.KV(m, 1, 40)
+        kv.prefill(cfg["seed"], 32)
+        outs.append(oracle.decode(m, kv, np.array([[7]], dtype=np.int32), [32])["logits"])
+    assert np.array_equal(outs[0], outs[1])
