@@ -53,10 +53,11 @@ def workload_name(cfg, B, T, ctx):
 
 
 def algorithmic_bytes(cfg, B, T, positions, route_idx=None):
-    """bf16 bytes the step must move: every non-routed weight, the union of
-    the routed experts actually selected (per layer), the LM head, B*T
-    embedding rows, the cached KV read (positions before the step) and the KV
-    written for the new positions."""
+    """Bytes the step must move: every non-routed weight, the union of the
+    routed experts actually selected (per layer), the LM head, B*T embedding
+    rows, the cached KV read (positions before the step) and the KV written
+    for the new positions; 2 bytes per element, and for MXFP8 expert weights
+    1 + 1/32 (a code, and a scale byte per 32 codes)."""
     d, L, V = cfg["d_model"], cfg["n_layers"], cfg["vocab"]
     per = 2 * d
     if cfg["attn_kind"] == 0:
@@ -71,16 +72,18 @@ def algorithmic_bytes(cfg, B, T, positions, route_idx=None):
     E = cfg["n_routed_experts"]
     if E:
         per += E * d
+    ex = 0  # expert weight elements
     if cfg["n_shared_experts"]:
-        per += 3 * d * cfg["shared_ffn_dim"]
+        ex += L * 3 * d * cfg["shared_ffn_dim"]
     elems = L * per + V * d + d + B * T * d
     if E:
         expert = 3 * d * cfg["ffn_dim"]
         for l in range(L):
-            elems += len(set(np.asarray(route_idx[l]).ravel().tolist())) * expert
+            ex += len(set(np.asarray(route_idx[l]).ravel().tolist())) * expert
     kv_read = sum(int(p) for p in positions) * row * L
     kv_write = B * T * row * L
-    return 2 * (elems + kv_read + kv_write)
+    ex_bytes = ex * 33 // 32 if cfg.get("expert_format", 0) == 1 else 2 * ex
+    return 2 * (elems + kv_read + kv_write) + ex_bytes
 
 
 class Clocks:
@@ -420,6 +423,15 @@ def main():
                 extra[f"{name}_b{Bm}"] = extra_line(c, r, Bm, 1)
             del kv, model
             torch.cuda.empty_cache()
+        # the deep model with MXFP8 expert weights, batch 1 (a different
+        # model: its experts hold other values; bytes counted at 1 + 1/32 per
+        # expert weight)
+        c = configs.DEEP_MXFP8
+        model, kv = load(c, 1, 1)
+        r = measure(model, kv, c, 1, 1, c["ctx"], K, W, ws, stream, False, local)
+        extra["deep_mxfp8_b1"] = extra_line(c, r, 1, 1)
+        del kv, model
+        torch.cuda.empty_cache()
     if rank != 0:
         return
     ms = main_r["ms"]

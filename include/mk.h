@@ -70,7 +70,23 @@ typedef struct mk_config {
     int32_t n_routed_experts, top_k, n_shared_experts, ffn_dim, shared_ffn_dim;
     int32_t max_batch, max_tokens_per_seq, max_ctx, kv_page_size;
     float rms_eps, rope_theta;
+    int32_t expert_format;  /* mk_expert_format: how routed and shared expert weights are stored */
 } mk_config;
+
+/* Expert weight formats.
+ *  MK_EXPERT_BF16  every weight bf16 (the default).
+ *  MK_EXPERT_MXFP8 the gate, up and down weights of the routed and shared
+ *      experts in the MXFP8 format of the OCP "Microscaling Formats (MX)
+ *      Specification" v1.0: FP8 E4M3 elements (sign, 4 exponent bits of bias
+ *      7, 3 mantissa bits, subnormals) with one E8M0 scale byte E (value
+ *      2^(E-127)) per block of 32 consecutive elements of a row; the weight is
+ *      element x scale. About half the bytes of bf16 experts (1 + 1/32 bytes
+ *      per weight). The kernel takes the dequantised values exactly; scale
+ *      byte 0xFF (NaN in the format) is not supported.
+ *      Supported for one token per step (max_batch * max_tokens_per_seq = 1),
+ *      d_model 512, 1024 or 2048, ffn_dim and shared_ffn_dim multiples of 64;
+ *      other shapes give MK_ERR_UNSUPPORTED at load. */
+enum mk_expert_format { MK_EXPERT_BF16 = 0, MK_EXPERT_MXFP8 = 1 };
 
 /* Weight kinds. Canonical layouts are row-major [rows, cols] bf16:
  *  EMBED, LM_HEAD [vocab, d]; *_NORM gains [n];
@@ -80,18 +96,25 @@ typedef struct mk_config {
  *       then k_rope rows), KV_NORM [kv_lora], WUKV [H*(nope+v), kv_lora]
  *       (per head: W_uk rows then W_uv rows), WO [d, H*v];
  *  MoE: ROUTER [E, d]; per expert GATE/UP [ffn, d], DOWN [d, ffn];
- *  shared expert: SH_GATE/SH_UP [sffn, d], SH_DOWN [d, sffn]. */
+ *  shared expert: SH_GATE/SH_UP [sffn, d], SH_DOWN [d, sffn].
+ * With expert_format MK_EXPERT_MXFP8, GATE, UP, DOWN, SH_GATE, SH_UP and
+ * SH_DOWN hold one E4M3 code byte per element (same shapes), and the *_SCALE
+ * kinds their E8M0 scale bytes, [rows, cols / 32] (block b of row r scales
+ * elements 32 b .. 32 b + 31 of that row). */
 enum mk_weight_kind {
     MK_W_EMBED = 1, MK_W_LM_HEAD = 2, MK_W_FINAL_NORM = 3, MK_W_ATTN_NORM = 4, MK_W_FFN_NORM = 5,
     MK_W_WQ = 6, MK_W_WK = 7, MK_W_WV = 8, MK_W_WO = 9,
     MK_W_WDQ = 10, MK_W_Q_NORM = 11, MK_W_WUQ = 12, MK_W_WDKV = 13, MK_W_KV_NORM = 14, MK_W_WUKV = 15,
     MK_W_ROUTER = 16, MK_W_GATE = 17, MK_W_UP = 18, MK_W_DOWN = 19,
-    MK_W_SH_GATE = 20, MK_W_SH_UP = 21, MK_W_SH_DOWN = 22
+    MK_W_SH_GATE = 20, MK_W_SH_UP = 21, MK_W_SH_DOWN = 22,
+    MK_W_GATE_SCALE = 23, MK_W_UP_SCALE = 24, MK_W_DOWN_SCALE = 25,
+    MK_W_SH_GATE_SCALE = 26, MK_W_SH_UP_SCALE = 27, MK_W_SH_DOWN_SCALE = 28
 };
 
 /* One entry of the weight table: layer = -1 for EMBED/LM_HEAD/FINAL_NORM,
- * expert = routed expert index (0 otherwise); data = bf16 bits in the
- * canonical layout, host or device memory, only read during the call. */
+ * expert = routed expert index (0 otherwise); data = bf16 bits (or MXFP8
+ * code / scale bytes) in the canonical layout, host or device memory, only
+ * read during the call. */
 typedef struct mk_weight {
     int32_t kind, layer, expert, reserved;
     const void* data;
@@ -140,7 +163,10 @@ int mk_load_weights(const mk_config* cfg, const mk_weight* table, int32_t n, voi
  * size of mk_info.weight_bytes). Errors as mk_load_weights. Synchronises
  * `stream`. The pages use trained weights; the synthetic model stands in for
  * them with the stated shapes (workload descriptions of the deep MoE model:
- * bf16 weights drawn from N(0, 0.02)). */
+ * bf16 weights drawn from N(0, 0.02)). With expert_format MK_EXPERT_MXFP8
+ * the expert weights are the generator's E4M3 codes (the same normal draws
+ * with sigma 16, rounded to E4M3 nearest even) and E8M0 block scales (117 or
+ * 118: 2^-10 or 2^-9). */
 int mk_load_synthetic(const mk_config* cfg, uint64_t seed, void* stream, mk_model** out);
 
 /* Paged KV cache for `batch` sequences of up to `max_ctx` positions each

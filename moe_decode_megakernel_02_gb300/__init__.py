@@ -22,6 +22,7 @@ HEADER = os.path.join(_ROOT, "include", "mk.h")
 
 OK, ERR_INVALID_ARG, ERR_OOM, ERR_CUDA, ERR_UNSUPPORTED, ERR_TIMEOUT, ERR_STATE = 0, -1, -2, -3, -4, -5, -6
 ATTN_GQA, ATTN_MLA = 0, 1
+EXPERT_BF16, EXPERT_MXFP8 = 0, 1  # mk_config.expert_format
 EXPORTS = ("mk_load_weights", "mk_load_synthetic", "mk_alloc_kv", "mk_kv_set_block_table", "mk_kv_pages_per_seq",
            "mk_kv_write", "mk_kv_read", "mk_decode_step", "mk_decode_step_unfused", "mk_decode_step_noalloc",
            "mk_step_status",
@@ -49,7 +50,7 @@ class Config(ctypes.Structure):
         "q_lora_rank", "kv_lora_rank", "qk_nope_dim", "qk_rope_dim", "v_head_dim",
         "n_routed_experts", "top_k", "n_shared_experts", "ffn_dim", "shared_ffn_dim",
         "max_batch", "max_tokens_per_seq", "max_ctx", "kv_page_size")] + [
-        ("rms_eps", ctypes.c_float), ("rope_theta", ctypes.c_float)]
+        ("rms_eps", ctypes.c_float), ("rope_theta", ctypes.c_float), ("expert_format", ctypes.c_int32)]
 
 
 class Weight(ctypes.Structure):

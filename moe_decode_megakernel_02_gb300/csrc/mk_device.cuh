@@ -109,11 +109,17 @@ enum { G_A = 0, G_QB, G_QLAT, G_UV, G_O, G_ROUTER, NG };
 // CTA needs to add the unit's share of the expert output to the residual:
 // no exchange between CTAs inside the FFN.
 struct FfnKind {
-    const uint16_t* gu;       // [n_kc][2*Fi][Kc], rows unit-major
-    const uint16_t* dn;       // [nu][d][F]
+    const uint16_t* gu;       // [n_kc][2*Fi][Kc], rows unit-major (bf16 experts)
+    const uint16_t* dn;       // [nu][d][F] (bf16 experts)
     long long gu_es, dn_es;   // elements between routed experts
     int Fi, F, nu;            // intermediate width, unit width, units per expert
     int R, Rd;                // gate/up rows per tile, down rows per tile
+    // MXFP8 experts (gu, dn null): tiles of E4M3 codes, each followed by its
+    // rows' E8M0 block scales (one per 32 codes of a row)
+    const uint8_t* qgu;       // [2Fi/R] tiles: R rows x Kc codes, then R x Kc/32 scales (rows unit-major)
+    const uint8_t* qdn;       // [nu][d/Rd] tiles: Rd rows x F codes, then Rd x F/32 scales
+    long long qgu_es, qdn_es; // bytes between routed experts
+    int qtb_gu, qtb_dn;       // bytes per gate/up tile, per down tile
 };
 struct Ffn {
     FfnKind k[2];             // [0] routed experts, [1] shared expert
@@ -177,8 +183,9 @@ struct Params {
     int nz, carry;                  // carry: residual copied by items (split-K output projection)
     int gs, gr;                     // CTAs [0, gs): shared expert, [gs, G): routed experts ([G-gr, G) first run the router)
     int stall;                      // testing: CTA 0 first waits on a counter nothing signals (ends in a timeout)
-    int skip_sig;                   // testing: 1 + the stage whose layer-0 signal CTA 0 leaves out (0: none)
+    int skip_sig;                   // testing: 1 + the stage whose layer-0 signals the CTAs leave out (0: none)
     int debug;                      // shared-memory canaries and token-map checks (ST_DEBUG on a failure)
+    int f8;                         // MXFP8 expert weights (one token per step)
     // one launch per stage (the unfused comparison path): 0 = the whole step
     // in this launch; 1 = program positions [st_lo, st_hi) only, 2 = the
     // step's set-up only (embedding, buffers zeroed). Launches are ordered by

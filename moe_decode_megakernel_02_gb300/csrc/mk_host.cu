@@ -110,6 +110,7 @@ namespace {
 struct Dims {
     int L, d, V, gqa, Hq, Hkv, hd, ql, kl, nope, rd, vd, E, k, sh, ffn, sffn, Mx;
     int a_rows, o_in, qh;
+    int f8;  // MXFP8 expert weights
 };
 
 Dims dims_of(const mk_config& c) {
@@ -122,6 +123,7 @@ Dims dims_of(const mk_config& c) {
     d.qh = d.nope + d.rd;
     d.a_rows = d.gqa ? (d.Hq + 2 * d.Hkv) * d.hd : d.ql + d.kl + d.rd;
     d.o_in = d.gqa ? d.Hq * d.hd : d.Hq * d.vd;
+    d.f8 = c.expert_format == MK_EXPERT_MXFP8;
     return d;
 }
 
@@ -144,6 +146,26 @@ void unit_geometry(int d, int F, int& Kc, int& R, int& Rd) {
     while (R > 8 && (2 * F) % R) R -= 8;
     Rd = mk::SLOT_BYTES / (2 * F) / 128 * 128;  // down tiles fill a ring slot
     if (Rd > d) Rd = d;
+}
+
+// MXFP8 experts: units 64 wide (two 32-code scale blocks of a down row);
+// gate/up tiles of R = 32768 / d whole rows (one K panel: 32 KB of codes)
+// followed by their scales; down tiles of Rd rows x 64 codes (32 KB, at most
+// d rows) followed by theirs
+struct F8Geom {
+    int F, R, Rd, tb_gu, tb_dn;
+    size_t gu_bytes, dn_bytes;  // per expert
+};
+F8Geom f8_geometry(int d, int Fi) {
+    F8Geom g;
+    g.F = 64;
+    g.R = 32768 / d;
+    g.Rd = std::min(d, 32768 / g.F);
+    g.tb_gu = g.R * d + g.R * (d / 32);
+    g.tb_dn = g.Rd * g.F + g.Rd * (g.F / 32);
+    g.gu_bytes = (size_t)(2 * Fi / g.R) * g.tb_gu;
+    g.dn_bytes = (size_t)(Fi / g.F) * (d / g.Rd) * g.tb_dn;
+    return g;
 }
 
 int validate(const mk_config* c) {
@@ -181,6 +203,15 @@ int validate(const mk_config* c) {
     if (d.E && !unit_width(d.ffn, d.d)) return fail(MK_ERR_UNSUPPORTED, "ffn_dim must be a multiple of 16");
     if (d.sh && !unit_width(d.sffn, d.d)) return fail(MK_ERR_UNSUPPORTED, "shared_ffn_dim must be a multiple of 16");
     if (d.V % 8) return fail(MK_ERR_UNSUPPORTED, "vocab must be a multiple of 8");
+    if (c->expert_format != MK_EXPERT_BF16 && c->expert_format != MK_EXPERT_MXFP8)
+        return fail(MK_ERR_INVALID_ARG, "expert_format");
+    if (d.f8) {
+        if (d.Mx != 1) return fail(MK_ERR_UNSUPPORTED, "MXFP8 experts: one token per step (max_batch * max_tokens_per_seq = 1)");
+        if (d.d != 512 && d.d != 1024 && d.d != 2048) return fail(MK_ERR_UNSUPPORTED, "MXFP8 experts: d_model 512, 1024 or 2048");
+        if ((d.E && d.ffn % 64) || (d.sh && d.sffn % 64))
+            return fail(MK_ERR_UNSUPPORTED, "MXFP8 experts: ffn_dim and shared_ffn_dim multiples of 64");
+        static_assert(32768 + 1024 <= mk::SLOT_BYTES - 16, "an MXFP8 tile fits a ring slot");
+    }
     return MK_OK;
 }
 
@@ -247,6 +278,54 @@ __global__ void pack_gu_units(uint16_t* __restrict__ dst, const uint16_t* __rest
         const int u = row / (2 * F), j = row - u * 2 * F;
         const uint16_t* src = j < F ? gate + (size_t)(u * F + j) * d : up + (size_t)(u * F + j - F) * d;
         *reinterpret_cast<uint4*>(dst + e) = *reinterpret_cast<const uint4*>(src + (size_t)kc * Kc + k);
+    }
+}
+
+// MXFP8 gate/up tiles: tile t holds unit-major rows t R .. t R + R - 1 (row
+// 2F u + j is gate row uF + j for j < F, else up row uF + j - F): their d
+// codes each, then their d / 32 scale bytes each. One work item per 16-byte
+// chunk of codes or per scale byte.
+__global__ void pack_gu_f8(uint8_t* __restrict__ dst, const uint8_t* __restrict__ gq, const uint8_t* __restrict__ uq,
+                           const uint8_t* __restrict__ gs, const uint8_t* __restrict__ us, int Fi, int d, int F, int R,
+                           int tb) {
+    const int cpr = d / 16 + d / 32;
+    const size_t n = (size_t)2 * Fi * cpr;
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+        const int row = (int)(i / cpr), k = (int)(i - (size_t)row * cpr);
+        const int u = row / (2 * F), j = row - u * 2 * F;
+        const bool gate = j < F;
+        const int sr = gate ? u * F + j : u * F + j - F;
+        const int t = row / R, rr = row - t * R;
+        uint8_t* tile = dst + (size_t)t * tb;
+        if (k < d / 16) {
+            *reinterpret_cast<uint4*>(tile + (size_t)rr * d + 16 * k) =
+                *reinterpret_cast<const uint4*>((gate ? gq : uq) + (size_t)sr * d + 16 * k);
+        } else {
+            const int kk = k - d / 16;
+            tile[(size_t)R * d + rr * (d / 32) + kk] = (gate ? gs : us)[(size_t)sr * (d / 32) + kk];
+        }
+    }
+}
+
+// MXFP8 down tiles: unit u, tile t: rows t Rd .. t Rd + Rd - 1 of the down
+// matrix, their codes [uF, uF + F) each, then those codes' F / 32 scales each
+__global__ void pack_dn_f8(uint8_t* __restrict__ dst, const uint8_t* __restrict__ q, const uint8_t* __restrict__ sc,
+                           int Fi, int d, int F, int Rd, int tb) {
+    const int nt = d / Rd, nu = Fi / F, cpr = F / 16 + F / 32;
+    const size_t n = (size_t)nu * d * cpr;
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+        const size_t rid = i / cpr;
+        const int k = (int)(i - rid * cpr);
+        const int u = (int)(rid / d), r = (int)(rid - (size_t)u * d);
+        const int t = r / Rd, rr = r - t * Rd;
+        uint8_t* tile = dst + ((size_t)u * nt + t) * tb;
+        if (k < F / 16) {
+            *reinterpret_cast<uint4*>(tile + (size_t)rr * F + 16 * k) =
+                *reinterpret_cast<const uint4*>(q + (size_t)r * Fi + (size_t)u * F + 16 * k);
+        } else {
+            const int kk = k - F / 16;
+            tile[(size_t)Rd * F + rr * (F / 32) + kk] = sc[(size_t)r * (Fi / 32) + u * (F / 32) + kk];
+        }
     }
 }
 
@@ -413,14 +492,15 @@ int mk_load_weights(const mk_config* cfg, const mk_weight* table, int32_t n, voi
             o.uv = take((size_t)D.Hq * D.vd * D.kl);
         }
         o.o = take((size_t)d * D.o_in);
+        // (MXFP8 experts: bytes of tiles, counted in 2-byte elements)
         if (D.E) {
             o.router = take((size_t)D.E * d);
-            o.gu = take((size_t)D.E * 2 * D.ffn * d);
-            o.down = take((size_t)D.E * d * D.ffn);
+            o.gu = take(D.f8 ? D.E * f8_geometry(d, D.ffn).gu_bytes / 2 : (size_t)D.E * 2 * D.ffn * d);
+            o.down = take(D.f8 ? D.E * f8_geometry(d, D.ffn).dn_bytes / 2 : (size_t)D.E * d * D.ffn);
         }
         if (D.sh) {
-            o.shgu = take((size_t)2 * D.sffn * d);
-            o.shdown = take((size_t)d * D.sffn);
+            o.shgu = take(D.f8 ? f8_geometry(d, D.sffn).gu_bytes / 2 : (size_t)2 * D.sffn * d);
+            o.shdown = take(D.f8 ? f8_geometry(d, D.sffn).dn_bytes / 2 : (size_t)d * D.sffn);
         }
     }
     m->wbytes = cur * 2;
@@ -552,6 +632,25 @@ int mk_load_weights(const mk_config* cfg, const mk_weight* table, int32_t n, voi
         // unit layout
         auto pack_expert = [&](int kgate, int kup, int kdown, int e, int Fi, uint16_t* gu, uint16_t* dn) -> int {
             const size_t n = (size_t)Fi * d;
+            if (D.f8) {
+                // codes of gate, up, down, then their scales, into the staging
+                // buffer (6 n bytes hold them), then into the tiles
+                uint8_t* b = reinterpret_cast<uint8_t*>(etmp);
+                const int kinds[6] = {kgate, kup, kdown, kgate + 6, kup + 6, kdown + 6};
+                const size_t offs[6] = {0, n, 2 * n, 3 * n, 3 * n + n / 32, 3 * n + 2 * n / 32};
+                for (int i = 0; i < 6; ++i) {
+                    if ((r = need(kinds[i], l, e, &p))) return r;
+                    CK(cudaMemcpyAsync(b + offs[i], p, i < 3 ? n : n / 32, cudaMemcpyDefault, s));
+                }
+                const F8Geom g = f8_geometry(d, Fi);
+                pack_gu_f8<<<1024, 256, 0, s>>>(reinterpret_cast<uint8_t*>(gu), b, b + n, b + 3 * n, b + 3 * n + n / 32,
+                                               Fi, d, g.F, g.R, g.tb_gu);
+                CK(cudaGetLastError());
+                pack_dn_f8<<<1024, 256, 0, s>>>(reinterpret_cast<uint8_t*>(dn), b + 2 * n, b + 3 * n + 2 * n / 32, Fi, d,
+                                               g.F, g.Rd, g.tb_dn);
+                CK(cudaGetLastError());
+                return MK_OK;
+            }
             const int F = unit_width(Fi, d);
             int Kc, R, Rd;
             unit_geometry(d, F, Kc, R, Rd);
@@ -570,9 +669,11 @@ int mk_load_weights(const mk_config* cfg, const mk_weight* table, int32_t n, voi
         if (D.E) {
             NEED(MK_W_ROUTER, l, 0);
             PACK(W + o.router, D.E, d, 0, p, D.E);
+            const size_t gu_es = D.f8 ? f8_geometry(d, D.ffn).gu_bytes / 2 : (size_t)2 * D.ffn * d;
+            const size_t dn_es = D.f8 ? f8_geometry(d, D.ffn).dn_bytes / 2 : (size_t)d * D.ffn;
             for (int e = 0; e < D.E; ++e)
-                if ((r = pack_expert(MK_W_GATE, MK_W_UP, MK_W_DOWN, e, D.ffn, W + o.gu + (size_t)e * 2 * D.ffn * d,
-                                     W + o.down + (size_t)e * d * D.ffn)))
+                if ((r = pack_expert(MK_W_GATE, MK_W_UP, MK_W_DOWN, e, D.ffn, W + o.gu + (size_t)e * gu_es,
+                                     W + o.down + (size_t)e * dn_es)))
                     return bail(r);
         }
         if (D.sh && (r = pack_expert(MK_W_SH_GATE, MK_W_SH_UP, MK_W_SH_DOWN, 0, D.sffn, W + o.shgu, W + o.shdown)))
@@ -638,6 +739,23 @@ int mk_load_weights(const mk_config* cfg, const mk_weight* table, int32_t n, voi
         make_gemv(Ld.g[mk::G_O], W + o.o, d, D.o_in, mk::IN_COPY, ob, D.o_in, nullptr, mk::OUT_RESID, x, d, Mxi, xn);
         Ld.ffn.gain = W + o.fn;
         auto set_kind = [&](mk::FfnKind& K, int Fi, const uint16_t* gu, const uint16_t* dn) {
+            if (D.f8) {
+                const F8Geom g = f8_geometry(d, Fi);
+                K.qgu = reinterpret_cast<const uint8_t*>(gu);
+                K.qdn = reinterpret_cast<const uint8_t*>(dn);
+                K.qgu_es = (long long)g.gu_bytes;
+                K.qdn_es = (long long)g.dn_bytes;
+                K.qtb_gu = g.tb_gu;
+                K.qtb_dn = g.tb_dn;
+                K.Fi = Fi;
+                K.F = g.F;
+                K.nu = Fi / g.F;
+                K.R = g.R;
+                K.Rd = g.Rd;
+                Ld.ffn.Kc = d;
+                Ld.ffn.n_kc = 1;
+                return;
+            }
             K.gu = gu;
             K.dn = dn;
             K.gu_es = (long long)2 * Fi * d;
@@ -670,6 +788,7 @@ int mk_load_weights(const mk_config* cfg, const mk_weight* table, int32_t n, voi
     P.L = L; P.d = d; P.V = D.V; P.attn = D.gqa ? 0 : 1; P.Hq = D.Hq; P.Hkv = D.Hkv; P.hd = D.hd;
     P.ql = D.ql; P.kl = D.kl; P.nope = D.nope; P.rd = D.rd; P.vd = D.vd; P.E = D.E; P.topk = D.k;
     P.has_sh = D.sh; P.ffn = D.ffn; P.sffn = D.sffn;
+    P.f8 = D.f8;
     P.eps = cfg->rms_eps;
     P.attn_scale = D.gqa ? (float)(1.0 / std::sqrt((double)D.hd)) : (float)(1.0 / std::sqrt((double)D.qh));
     P.G = m->G;

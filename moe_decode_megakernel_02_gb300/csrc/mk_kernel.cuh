@@ -3236,6 +3236,138 @@ __device__ __forceinline__ void down_mma(const uint8_t* tile, int nr, const floa
     }
 }
 
+// ---- MXFP8 expert weights (one token per step) ----
+// Two E4M3 codes become two fp16 values with one conversion instruction
+// (cvt.rn.f16x2.e4m3x2; every E4M3 value, subnormals included, is an fp16
+// number, so the conversion is exact), then fp32. A block's partial sum times
+// 2^(E - 127) is the sum of (code value x 2^(E - 127)) x input.
+__device__ __forceinline__ float2 f8_pair(uint32_t w16) {
+    uint32_t h;
+    asm("{ .reg .b16 t; cvt.u16.u32 t, %1; cvt.rn.f16x2.e4m3x2 %0, t; }" : "=r"(h) : "r"(w16));
+    float lo, hi;
+    asm("{ .reg .b16 a, b; mov.b32 {a, b}, %2; cvt.f32.f16 %0, a; cvt.f32.f16 %1, b; }" : "=f"(lo), "=f"(hi) : "r"(h));
+    return make_float2(lo, hi);
+}
+// 2^(E - 127) for an E8M0 scale byte E (E = 0: 2^-127, a float subnormal;
+// 0xFF, NaN in the format, is not supported and reads as infinity)
+__device__ __forceinline__ float f8_scale(uint32_t E) { return E ? __uint_as_float(E << 23) : __uint_as_float(0x400000u); }
+
+// sum of 16 codes (one 16-byte chunk) times 16 inputs
+__device__ __forceinline__ float f8_dot16(const uint4 u, const float4 (&x)[4]) {
+    float a = 0.f, b = 0.f;
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const float2 p0 = f8_pair(w[q] & 0xffffu), p1 = f8_pair(w[q] >> 16);
+        a = fmaf(p0.x, x[q].x, a);
+        b = fmaf(p0.y, x[q].y, b);
+        a = fmaf(p1.x, x[q].z, a);
+        b = fmaf(p1.y, x[q].w, b);
+    }
+    return a + b;
+}
+
+// gate/up tiles [j_lo, j_hi) of one unit segment, one token: a tile is
+// R = 64 / NQ rows of the K = 512 NQ codes each (then their scales); lane
+// chunk q of a row holds codes 16 (lane + 32 q) .. + 15, all inside one
+// 32-code block; warp w takes rows RB w .. RB w + RB - 1 (RB = R / 8) and
+// one transposed reduction gives the RB sums. Row r of tile j lands at
+// hs[(j - j_lo) R + r].
+template <int NQ>
+__device__ __forceinline__ void gu_f8(Ctx& c, int j_lo, int j_hi, float* hs) {
+    constexpr int RB = 8 / NQ, KC = 512 * NQ, R = 8 * RB;
+    const Params& p = c.p;
+    Misc& ms = c.ms;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    uint8_t* const ring = c.smem + SMEM_RING;
+    const float* xt = c.stage() + (size_t)staging_row(ms, 0) * stage_stride(KC);
+    float4 x[NQ][4];
+#pragma unroll
+    for (int q = 0; q < NQ; ++q)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) x[q][i] = *reinterpret_cast<const float4*>(xt + 16 * (lane + 32 * q) + 4 * i);
+    CRing cr = c.cr;
+    bool dead = c.dead, timed_out = false;
+    for (int j = j_lo; j < j_hi; ++j) {
+        const uint8_t* tile = nullptr;
+        if (!dead) {
+            if (spin_wait(p, &ms.full[cr.slot], cr.phase))
+                tile = ring + cr.slot * SLOT_BYTES;
+            else
+                dead = timed_out = true;
+        }
+        if (tile) {
+            const uint8_t* sc = tile + R * KC;
+            float v[RB];
+#pragma unroll
+            for (int b = 0; b < RB; ++b) {
+                const int r = warp * RB + b;
+                const uint4* row = reinterpret_cast<const uint4*>(tile + (size_t)r * KC) + lane;
+                float acc = 0.f;
+#pragma unroll
+                for (int q = 0; q < NQ; ++q)
+                    acc = fmaf(f8_dot16(row[32 * q], x[q]), f8_scale(sc[r * (KC / 32) + ((lane + 32 * q) >> 1)]), acc);
+                v[b] = acc;
+            }
+            const int b = rx_reduce<RB>(v);
+            if ((lane & (32 / RB - 1)) == 0) hs[(j - j_lo) * R + warp * RB + b] = v[0];
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ms.empty[cr.slot]);
+        if (++cr.slot == NSLOT) {
+            cr.slot = 0;
+            cr.phase ^= 1u;
+        }
+    }
+    if (timed_out) {
+        ms.abort = 1;
+        raise_status(p, ST_TIMEOUT, 0x230u);
+    }
+    c.set_ring(cr);
+    if (dead) c.dead = true;
+}
+
+// one thread's rows of an MXFP8 down tile (nr rows x F codes, then nr x F/32
+// scales; FQ = F / 16 chunks per row), one token, the unit's F hidden values
+// in registers; a warp takes 32 consecutive rows at a time
+template <int FQ>
+__device__ __forceinline__ void down_f8(const uint8_t* tile, int nr, const float* hu, float w, float* xo) {
+    constexpr int F = 16 * FQ;
+    float4 hx[FQ][4];
+#pragma unroll
+    for (int q = 0; q < FQ; ++q)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) hx[q][i] = *reinterpret_cast<const float4*>(hu + 16 * q + 4 * i);
+    const uint8_t* sc = tile + (size_t)nr * F;
+    const int lane = threadIdx.x & 31;
+    for (int rb = (ctid() >> 5) * 32; rb < nr; rb += NCT) {
+        const int r = rb + lane;
+        float a = 0.f;
+        if (r < nr) {
+            const uint4* row = reinterpret_cast<const uint4*>(tile + (size_t)r * F);
+#pragma unroll
+            for (int q = 0; q < FQ; ++q) a = fmaf(f8_dot16(row[q], hx[q]), f8_scale(sc[r * (F / 32) + q / 2]), a);
+        }
+        red4_rows(xo, r, r < nr, w * a);
+    }
+}
+
+// MXFP8 gate/up tiles [j_lo, j_hi) of a unit segment (one K panel, one
+// token): the input is staged once (the routed CTAs staged it already), then
+// the tiles
+__device__ __noinline__ void unit_gu_f8(Ctx& c, int j_lo, int j_hi, float* hs) {
+    restage(c, c.ms.ug, c.ms.ug.src, 0, 0, 0, c.ms.gather ? c.ms.gm : c.p.M);
+    const int Kc = c.layer().ffn.Kc;
+    if (Kc == 2048) gu_f8<4>(c, j_lo, j_hi, hs);
+    else if (Kc == 1024) gu_f8<2>(c, j_lo, j_hi, hs);
+    else gu_f8<1>(c, j_lo, j_hi, hs);
+}
+
+// one MXFP8 down tile, one token (units 64 wide)
+__device__ __noinline__ void unit_down_f8(const uint8_t* tile, int nr, const float* hu, float w, float* xo) {
+    down_f8<4>(tile, nr, hu, w, xo);
+}
+
 __device__ __noinline__ void unit_seg_cons(Ctx& c, int l, int kind, int expert, int u0, int u1, int m_lo, int m_hi) {
     const Params& p = c.p;
     const Layer& Ld = c.layer();
@@ -3317,7 +3449,12 @@ __device__ __noinline__ void unit_seg_cons(Ctx& c, int l, int kind, int expert, 
     const long long tz = p.trace_items ? gtimer() : 0;
     const long long cz = clock64();
     const int n_rb = 2 * K.Fi / K.R, rpu = 2 * F / K.R;
-    for (int kc = 0; kc < Ld.ffn.n_kc; ++kc) cons_gemv(c, c.ms.ug, 0, -1, kc * n_rb + u0 * rpu, kc * n_rb + u1 * rpu);
+    if (p.f8) {
+        unit_gu_f8(c, u0 * rpu, u1 * rpu, hs);
+    } else {
+        for (int kc = 0; kc < Ld.ffn.n_kc; ++kc)
+            cons_gemv(c, c.ms.ug, 0, -1, kc * n_rb + u0 * rpu, kc * n_rb + u1 * rpu);
+    }
     const long long tg = p.trace_items ? gtimer() : 0;
     const long long cg = clock64();
     // clock cycles: entry of the GEMV, its run start, its run end, return
@@ -3362,7 +3499,9 @@ __device__ __noinline__ void unit_seg_cons(Ctx& c, int l, int kind, int expert, 
                     const float* hu = h + uu * F;
                     float* xo = Ld.xn + (size_t)ms.gt[0] * d + r0;
                     const float w = ms.uw[0];
-                    if (w != 0.f) {
+                    if (w != 0.f && p.f8) {
+                        unit_down_f8(tile, nr, hu, w, xo);
+                    } else if (w != 0.f) {
                         if (F == 64) down_rows1<8>(tile, nr, hu, w, xo);
                         else if (F == 48) down_rows1<6>(tile, nr, hu, w, xo);
                         else if (F == 32) down_rows1<4>(tile, nr, hu, w, xo);
@@ -3398,11 +3537,86 @@ __device__ __noinline__ void unit_seg_cons(Ctx& c, int l, int kind, int expert, 
     if (dead) c.dead = true;
 }
 
+// producer, MXFP8 experts: the segment's gate/up tiles, then each unit's
+// down tiles in the consumers' rotated order; whole tiles, one bulk copy each
+// (codes and scales are contiguous). L2 prefetch: once the first ring-full of
+// copies is requested (a prefetch issued before them would queue ahead of
+// them), the rest of the first units (about UNIT_PF_BYTES); then the next
+// unit's tiles a unit ahead.
+__device__ __noinline__ void unit_seg_prod_f8(Ctx& c, const FfnKind& K, int expert, int u0, int u1) {
+    const Params& p = c.p;
+    const int lane = threadIdx.x & 31;
+    const uint8_t* gu = K.qgu + (expert >= 0 ? (size_t)expert * K.qgu_es : 0);
+    const uint8_t* dn = K.qdn + (expert >= 0 ? (size_t)expert * K.qdn_es : 0);
+    const int rpu = 2 * K.F / K.R, nt = p.d / K.Rd;
+    const size_t ugu = (size_t)rpu * K.qtb_gu, udn = (size_t)nt * K.qtb_dn;  // bytes per unit
+    const int npf = min(u1 - u0, max(1, UNIT_PF_BYTES / (int)(ugu + udn)));
+    const unsigned piece = 65536;
+    Misc& ms = c.ms;
+    uint8_t* ring = c.smem + SMEM_RING;
+    PRing pr = c.pr;
+    int issued = c.issued;
+    const unsigned long long pol = l2_evict_first();
+    const int rot = (int)(blockIdx.x % (unsigned)nt);
+    // tiles of the segment: gate/up j in [0, n_gu), then down
+    const int n_gu = (u1 - u0) * rpu, n_all = n_gu + (u1 - u0) * nt, first = min(NSLOT, n_gu);
+    for (int i = 0; i < n_all && !c.dead; ++i) {
+        if (i == first) {
+            // (gate/up tiles from `first` on; the down tiles of the first units)
+            const size_t g0 = (size_t)u0 * ugu + (size_t)first * K.qtb_gu, g1 = (size_t)(u0 + npf) * ugu;
+            for (size_t o = g0 + (size_t)lane * piece; o < g1; o += 32 * (size_t)piece)
+                l2_prefetch(gu + o, (unsigned)min((size_t)piece, g1 - o));
+            for (size_t o = (size_t)lane * piece, n = (size_t)npf * udn; o < n; o += 32 * (size_t)piece)
+                l2_prefetch(dn + (size_t)u0 * udn + o, (unsigned)min((size_t)piece, n - o));
+        }
+        const uint8_t* src;
+        unsigned bytes;
+        if (i < n_gu) {
+            src = gu + (size_t)(u0 * rpu + i) * K.qtb_gu;
+            bytes = (unsigned)K.qtb_gu;
+            // the gate/up tiles of units beyond the first npf, a unit ahead
+            if (i % rpu == 0 && i / rpu + 1 < u1 - u0 && i / rpu + 1 >= npf)
+                for (size_t o = (size_t)lane * piece; o < ugu; o += 32 * (size_t)piece)
+                    l2_prefetch(gu + (size_t)(u0 + i / rpu + 1) * ugu + o, (unsigned)min((size_t)piece, ugu - o));
+        } else {
+            const int k = i - n_gu, uu = k / nt, t0 = k - uu * nt;
+            const int t = t0 + rot < nt ? t0 + rot : t0 + rot - nt;
+            src = dn + ((size_t)(u0 + uu) * nt + t) * K.qtb_dn;
+            bytes = (unsigned)K.qtb_dn;
+            if (t0 == 0 && uu + 1 < u1 - u0 && uu + 1 >= npf)
+                for (size_t o = (size_t)lane * piece; o < udn; o += 32 * (size_t)piece)
+                    l2_prefetch(dn + (size_t)(u0 + uu + 1) * udn + o, (unsigned)min((size_t)piece, udn - o));
+        }
+        int ok = 1;
+        if (lane == 0) {
+            if (spin_wait(p, &ms.empty[pr.slot], pr.phase ^ 1u)) {
+                mbar_expect_tx(&ms.full[pr.slot], bytes);
+                bulk_g2s_pol(ring + pr.slot * SLOT_BYTES, src, bytes, &ms.full[pr.slot], pol);
+            } else {
+                ok = 0;
+            }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) {
+            if (lane == 0) raise_status(p, ST_TIMEOUT, 0x130u);
+            c.dead = true;
+            break;
+        }
+        ++issued;
+        prod_next(pr);
+    }
+    c.set_pring(pr, issued);
+}
+
 // producer: the segment's tiles into the ring (and, first, towards L2)
 __device__ __noinline__ void unit_seg_prod(Ctx& c, int kind, int expert, int u0, int u1, int ntok) {
     const Params& p = c.p;
     const Layer& Ld = c.layer();
     const FfnKind& K = Ld.ffn.k[kind];
+    if (p.f8) {
+        unit_seg_prod_f8(c, K, expert, u0, u1);
+        return;
+    }
     const int F = K.F, d = p.d, lane = threadIdx.x & 31, Kc = Ld.ffn.Kc;
     const uint16_t* gu = K.gu + (expert >= 0 ? (size_t)expert * K.gu_es : 0);
     const uint16_t* dn = K.dn + (expert >= 0 ? (size_t)expert * K.dn_es : 0);

@@ -237,3 +237,33 @@ def test_deep_separate_absorbed_query_and_value_stages(monkeypatch, B):
     monkeypatch.setenv("MK_UV_STAGE", "1")
     cfg = configs.scaled(configs.DEEP, n_layers=2)
     _run(cfg, B, 1, 2, cfg["ctx"])
+
+
+# MXFP8 expert weights (one token per step): the oracle dequantises the
+# generator's E4M3 codes and E8M0 scales exactly, the kernel streams the codes
+# and scales and takes the same values; the tolerance is the bf16 model's
+# (the arithmetic is the same once the weights are read).
+# d_model 2048 (deep, mid): 16-row gate/up tiles, 4 chunks of 16 codes per
+# lane; 1024 and 512: 32- and 64-row tiles, 2 and 1 chunks (at 512 one down
+# tile per unit)
+_MX = dict(expert_format=1)
+_MX_SMALL = dict(_MX, n_layers=2, vocab=4096, n_q_heads=4, n_kv_heads=2, head_dim=128, n_routed_experts=16,
+                 top_k=4, ctx=300)
+
+
+@pytest.mark.parametrize("name,over", [
+    ("deep", dict(_MX, n_layers=3)),
+    ("mid", dict(_MX, n_layers=2)),
+    ("mid", dict(_MX_SMALL, d_model=1024, ffn_dim=512, shared_ffn_dim=256)),
+    ("mid", dict(_MX_SMALL, d_model=512, ffn_dim=256, shared_ffn_dim=128)),
+])
+def test_mxfp8_experts_batch1(name, over):
+    cfg = configs.scaled(configs.ALL[name], **over)
+    _run(cfg, 1, 1, 2, cfg["ctx"])
+
+
+def test_mxfp8_experts_full_depth_batch1():
+    cfg = configs.scaled(configs.DEEP, **_MX)
+    _, _, rep = _run(cfg, 1, 1, 1, cfg["ctx"], lazy=True)
+    print(f"deep 92 layers, MXFP8 experts, batch 1, ctx 8192: logits max-abs {rep['max_abs']:.3e} "
+          f"mean-abs {rep['mean_abs']:.3e}")
