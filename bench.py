@@ -345,7 +345,7 @@ def main():
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="mk", choices=["mk", "reference"])
-    ap.add_argument("--config", default="deep", choices=list(configs.ALL))
+    ap.add_argument("--config", default="deep", choices=list(configs.ALL) + ["deep_mxfp8"])
     ap.add_argument("--batch", type=int, default=1)
     ap.add_argument("--extra", default="all", choices=["none", "batch8", "all"],
                     help="other measurements in the same run (batch8: the deep model at batch 8 only)")
@@ -353,7 +353,9 @@ def main():
     ap.add_argument("--layers", type=int, default=0, help="override layer count (profiling runs only)")
     args = ap.parse_args()
 
-    cfg = configs.ALL[args.config]
+    cfg = configs.DEEP_MXFP8 if args.config == "deep_mxfp8" else configs.ALL[args.config]
+    if args.config == "deep_mxfp8":  # (one token per step)
+        args.extra, args.batch = "none", 1
     if args.layers:
         cfg = configs.scaled(cfg, n_layers=args.layers)
     B, T, ctx = args.batch, cfg["T"], cfg["ctx"]
