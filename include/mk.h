@@ -266,9 +266,17 @@ int mk_decode_step_noalloc(mk_model* m, mk_kv* kv, const int32_t* tokens, const 
  * Debug mode: with MK_DEBUG=1 when the model is loaded, every CTA writes a
  * 16-byte pattern into the unused end of each shared-memory ring slot and
  * after its input staging area at the start of a step and compares it when
- * it leaves, and the expert units check that every entry of their token map
- * is a token of the step. A failed check reports MK_ERR_STATE through
- * mk_step_status (with the place in mk_last_error()); nothing traps. */
+ * it leaves; the producer checks every weight-tile copy against the slot
+ * size before issuing it (an oversized one ends the step instead); the
+ * expert units check that every entry of their token map is a token of the
+ * step; and every scratch region of the model is followed by a 256-byte
+ * guard (pattern 0xA5) that mk_step_status compares after the step (and
+ * restores). A failed check reports MK_ERR_STATE through mk_step_status
+ * (with the place in mk_last_error()); nothing traps. The guards cover the
+ * model's own scratch (mk_decode_step, mk_decode_step_unfused), not the
+ * static scratch of mk_decode_step_noalloc. While MK_FAULT is
+ * "corrupt_guard", mk_step_status overwrites one guard before its check
+ * (host injection: the report path without a device fault). */
 
 /* Synchronise `stream` and return the device status of the last step
  * (MK_OK, MK_ERR_TIMEOUT, MK_ERR_INVALID_ARG, or MK_ERR_STATE for a failed

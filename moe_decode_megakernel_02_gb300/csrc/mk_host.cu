@@ -92,6 +92,9 @@ struct mk_model {
     // the caches still read for their dimensions) when the last one goes
     int live_kv = 0;
     bool released = false;
+    // MK_DEBUG: offsets of the 256-byte guards after each scratch region
+    // (pattern 0xA5, written at load, checked by mk_step_status)
+    std::vector<size_t> guards;
 };
 
 struct mk_kv {
@@ -517,7 +520,16 @@ int mk_load_weights(const mk_config* cfg, const mk_weight* table, int32_t n, voi
     const size_t Mx = D.Mx;
     const int Q8 = 8;
     size_t scur = 0;
-    auto stake = [&](size_t bytes) { size_t o = scur; scur += align256(bytes); return o; };
+    const bool dbg = getenv("MK_DEBUG") && atoi(getenv("MK_DEBUG")) > 0;
+    auto stake = [&](size_t bytes) {
+        const size_t o = scur;
+        scur += align256(bytes);
+        if (dbg) {  // a guard after the region
+            m->guards.push_back(scur);
+            scur += 256;
+        }
+        return o;
+    };
     const size_t s_x = stake((size_t)(L + 1) * Mx * d * 4);
     const size_t s_a = stake((size_t)L * Mx * D.a_rows * 4);
     const size_t s_q = D.gqa ? 0 : stake((size_t)L * Mx * D.Hq * D.qh * 4);
@@ -560,6 +572,7 @@ int mk_load_weights(const mk_config* cfg, const mk_weight* table, int32_t n, voi
         }
     }
     CK(cudaMemsetAsync(m->sblob, 0, m->sbytes, s));
+    for (size_t g : m->guards) CK(cudaMemsetAsync(m->sblob + g, 0xA5, 256, s));
     uint8_t* S = m->sblob;
     auto F = [&](size_t off) { return reinterpret_cast<float*>(S + off); };
 
@@ -1264,13 +1277,32 @@ int mk_decode_step_unfused(mk_model* m, mk_kv* kv, const int32_t* tokens, const 
     return MK_OK;
 }
 
+// MK_DEBUG: every scratch guard still holds its pattern (one overwritten is
+// restored and reported). MK_FAULT=corrupt_guard overwrites one first (host
+// injection, to test the caller's handling of the report).
+static int check_guards(mk_model* m) {
+    if (m->guards.empty()) return MK_OK;
+    if (fault("corrupt_guard")) CK(cudaMemset(m->sblob + m->guards[m->guards.size() / 2], 0, 4));
+    unsigned char b[256];
+    for (size_t i = 0; i < m->guards.size(); ++i) {
+        CK(cudaMemcpy(b, m->sblob + m->guards[i], sizeof b, cudaMemcpyDeviceToHost));
+        for (unsigned char v : b)
+            if (v != 0xA5) {
+                CK(cudaMemset(m->sblob + m->guards[i], 0xA5, 256));
+                return fail(MK_ERR_STATE, "debug check failed (MK_DEBUG; scratch guard %zu of %zu overwritten)", i,
+                            m->guards.size());
+            }
+    }
+    return MK_OK;
+}
+
 int mk_step_status(mk_model* m, void* stream) {
     if (!m || m->magic != MODEL_MAGIC) return fail(MK_ERR_INVALID_ARG, "bad model handle");
     cudaStream_t s = (cudaStream_t)stream;
     CK(cudaStreamSynchronize(s));
     unsigned st[4];
     CK(cudaMemcpy(st, m->status, sizeof st, cudaMemcpyDeviceToHost));
-    if (st[0] == 0 && st[1] == 0) return MK_OK;
+    if (st[0] == 0 && st[1] == 0) return check_guards(m);
     // reset device state so the next step starts clean
     CK(cudaMemset(m->ctr, 0, m->ctr_n * sizeof(unsigned)));
     CK(cudaMemset(m->status, 0, 64));

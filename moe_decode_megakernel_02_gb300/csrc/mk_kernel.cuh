@@ -1528,6 +1528,12 @@ __device__ __noinline__ void prod_gemv(Ctx& c, const Gemv& g, int expert, int lo
             rbp = 0;
             ++kp;
         }
+        if (p.debug && (pad ? (unsigned)nr * (Kc * 2 + 16) : bytes) > (unsigned)(SLOT_BYTES - 16)) {
+            // (debug mode: a tile that would overrun its ring slot)
+            if (leader) raise_status(p, ST_DEBUG, 0x9210u);
+            c.dead = true;
+            break;
+        }
         int ok = 1;
         if (leader) {
             if (spin_wait(p, &ms.empty[pr.slot], pr.phase ^ 1u)) {
@@ -3587,6 +3593,11 @@ __device__ __noinline__ void unit_seg_prod_f8(Ctx& c, const FfnKind& K, int expe
                 for (size_t o = (size_t)lane * piece; o < udn; o += 32 * (size_t)piece)
                     l2_prefetch(dn + (size_t)(u0 + uu + 1) * udn + o, (unsigned)min((size_t)piece, udn - o));
         }
+        if (p.debug && bytes > (unsigned)(SLOT_BYTES - 16)) {
+            if (lane == 0) raise_status(p, ST_DEBUG, 0x9230u);
+            c.dead = true;
+            break;
+        }
         int ok = 1;
         if (lane == 0) {
             if (spin_wait(p, &ms.empty[pr.slot], pr.phase ^ 1u)) {
@@ -3666,6 +3677,11 @@ __device__ __noinline__ void unit_seg_prod(Ctx& c, int kind, int expert, int u0,
             const int t = t0 + rot < nt ? t0 + rot : t0 + rot - nt;
             const int r0 = t * K.Rd, nr = min(K.Rd, d - r0);
             const unsigned bytes = (unsigned)nr * F * 2u;
+            if (p.debug && bytes > (unsigned)(SLOT_BYTES - 16)) {
+                if (lane == 0) raise_status(p, ST_DEBUG, 0x9220u);
+                c.dead = true;
+                break;
+            }
             int ok = 1;
             if (lane == 0) {
                 if (spin_wait(p, &ms.empty[pr.slot], pr.phase ^ 1u)) {

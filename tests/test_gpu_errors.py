@@ -157,3 +157,40 @@ def test_debug_mode_checks_pass_and_parity_holds(monkeypatch, name, B, T):
     o = parity.run_oracle(cfg, g, ctx, B, T)
     rep = parity.compare(cfg, g, o, B, T)
     print(name, B, T, "debug mode", rep)
+
+
+def test_debug_mode_scratch_guard_report(monkeypatch):
+    # MK_DEBUG=1: the scratch guards hold after a clean step; with
+    # MK_FAULT=corrupt_guard the host overwrites one before the check, the
+    # step reports MK_ERR_STATE naming the guard, and (the guard restored)
+    # the next step reports MK_OK and matches the oracle
+    import torch
+    import moe_decode_megakernel_02_gb300 as mk
+    from moe_decode_megakernel_02_gb300 import workload
+    import oracle
+
+    monkeypatch.setenv("MK_DEBUG", "1")
+    cfg = configs.TINY
+    ctx = cfg["ctx"]
+    model = workload.load_synthetic(cfg, max_batch=1, max_tokens_per_seq=1, max_ctx=ctx + 8)
+    kv = mk.KVCache(model, 1, ctx + 8)
+    workload.prefill(kv, cfg, ctx)
+    tok = workload.tokens(cfg, 0, 1, 1)
+    logits = torch.empty((1, cfg["vocab"]), dtype=torch.float32, device="cuda")
+    pos = torch.tensor([ctx], dtype=torch.int32, device="cuda")
+    model.decode_step(kv, torch.from_numpy(tok).cuda(), pos, logits)
+    model.check()
+    monkeypatch.setenv("MK_FAULT", "corrupt_guard")
+    model.decode_step(kv, torch.from_numpy(tok).cuda(), pos, logits)
+    with pytest.raises(mk.MKError) as e:
+        model.check()
+    assert e.value.code == mk.ERR_STATE and "scratch guard" in str(e.value)
+    monkeypatch.delenv("MK_FAULT")
+    model.decode_step(kv, torch.from_numpy(tok).cuda(), pos, logits)
+    model.check()
+    om = oracle.Model(cfg)
+    okv = oracle.KV(om, 1, ctx + 8)
+    okv.prefill(cfg["seed"], ctx)
+    ref = oracle.decode(om, okv, tok, [ctx])["logits"].reshape(1, -1)
+    err = np.abs(logits.cpu().numpy().astype(np.float64) - ref)
+    assert err.max() <= parity.MAX_ABS and err.mean() <= parity.MEAN_ABS
