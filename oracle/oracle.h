@@ -13,7 +13,10 @@
  * MLA attention over a bf16 KV cache with rotate-half RoPE, output
  * projection and residual; RMSNorm, softmax router with top-k and
  * renormalised weights, routed and shared SwiGLU experts, residual; final
- * RMSNorm and LM head. Sources: "TPU Megakernel Achieves 709 tokens/s on Kimi
+ * RMSNorm and LM head; optionally the expert weights in MXFP8 (E4M3 codes
+ * with an E8M0 scale per 32 elements of a row, the OCP "Microscaling
+ * Formats (MX) Specification" v1.0), dequantised exactly before the same
+ * plain step (the pages state no weight precision). Sources: "TPU Megakernel Achieves 709 tokens/s on Kimi
  * K3" (kongchang.com), section "The Key Innovation" (all layers are MoE
  * layers with per-layer routing) and the MoE explainer after "Cross-Layer
  * Weight Prefetching" (a router picks a few experts per token); the myzaker
