@@ -260,7 +260,9 @@ int mk_decode_step_noalloc(mk_model* m, mk_kv* kv, const int32_t* tokens, const 
  *   "skip_signal" mk_decode_step launches a step in which no CTA signals
  *                 the completion of layer 0's first projection: the
  *                 stages that read it wait until the wait limit (MK_WAIT_NS)
- *                 and the step reports MK_ERR_TIMEOUT through mk_step_status.
+ *                 and the step reports MK_ERR_TIMEOUT through mk_step_status;
+ *   "corrupt_guard" (debug mode, below) mk_step_status overwrites one scratch
+ *                 guard before checking them and reports MK_ERR_STATE.
  * Each host failure sets mk_last_error() to a message naming MK_FAULT.
  *
  * Debug mode: with MK_DEBUG=1 when the model is loaded, every CTA writes a
