@@ -288,3 +288,10 @@ def test_repeated_steps_reproduce_routing_and_logits(name, B):
         clear = r0["route_margin"] > 1e-3
         same = (np.sort(r["route_idx"], axis=-1) == np.sort(r0["route_idx"], axis=-1)).all(axis=-1)
         assert same[clear].all()
+
+
+@pytest.mark.parametrize("name", ["deep", "mid"])
+def test_mxfp8_experts_unfused(name):
+    # MXFP8 experts through the one-launch-per-stage path
+    cfg = configs.scaled(configs.ALL[name], n_layers=2, **_MX)
+    _run(cfg, 1, 1, 2, min(cfg["ctx"], 2000), entry="decode_step_unfused")

@@ -23,7 +23,7 @@ def _rows_f32(kv, layer, seq, pos, n):
     return (kv.read(layer, seq, pos, n).astype(np.uint32) << 16).view(np.float32)
 
 
-@pytest.mark.parametrize("name,B,T", [("tiny", 1, 1), ("mid", 2, 1), ("deep", 2, 2)])
+@pytest.mark.parametrize("name,B,T", [("tiny", 1, 1), ("mid", 2, 1), ("deep", 2, 2), ("deep_mxfp8", 1, 1)])
 def test_noalloc_matches_regular_entry_point(name, B, T):
     # deep, T 2: MLA (the query, absorbed-query, latent-output and new-latent
     # buffers) and the verify extras (row argmaxes, acceptance); larger
@@ -32,7 +32,7 @@ def test_noalloc_matches_regular_entry_point(name, B, T):
     import torch
     import moe_decode_megakernel_02_gb300 as mk
     from moe_decode_megakernel_02_gb300 import workload
-    cfg = configs.ALL[name]
+    cfg = configs.DEEP_MXFP8 if name == "deep_mxfp8" else configs.ALL[name]
     if name != "tiny":
         cfg = configs.scaled(cfg, n_layers=2)
     ctx = min(cfg["ctx"], 300)
