@@ -354,8 +354,8 @@ def main():
     args = ap.parse_args()
 
     cfg = configs.DEEP_MXFP8 if args.config == "deep_mxfp8" else configs.ALL[args.config]
-    if args.config == "deep_mxfp8":  # (one token per step)
-        args.extra, args.batch = "none", 1
+    if args.config == "deep_mxfp8":
+        args.extra = "none"
     if args.layers:
         cfg = configs.scaled(cfg, n_layers=args.layers)
     B, T, ctx = args.batch, cfg["T"], cfg["ctx"]
@@ -425,13 +425,14 @@ def main():
                 extra[f"{name}_b{Bm}"] = extra_line(c, r, Bm, 1)
             del kv, model
             torch.cuda.empty_cache()
-        # the deep model with MXFP8 expert weights, batch 1 (a different
-        # model: its experts hold other values; bytes counted at 1 + 1/32 per
-        # expert weight)
+        # the deep model with MXFP8 expert weights, batch 1 and 8 (a
+        # different model: its experts hold other values; bytes counted at
+        # 1 + 1/32 per expert weight)
         c = configs.DEEP_MXFP8
-        model, kv = load(c, 1, 1)
-        r = measure(model, kv, c, 1, 1, c["ctx"], K, W, ws, stream, False, local)
-        extra["deep_mxfp8_b1"] = extra_line(c, r, 1, 1)
+        model, kv = load(c, 8, 1)
+        for Bm in (1, 8):
+            r = measure(model, kv, c, Bm, 1, c["ctx"], K, W, ws, stream, False, local)
+            extra[f"deep_mxfp8_b{Bm}"] = extra_line(c, r, Bm, 1)
         del kv, model
         torch.cuda.empty_cache()
     if rank != 0:

@@ -83,9 +83,12 @@ typedef struct mk_config {
  *      element x scale. About half the bytes of bf16 experts (1 + 1/32 bytes
  *      per weight). The kernel takes the dequantised values exactly; scale
  *      byte 0xFF (NaN in the format) is not supported.
- *      Supported for one token per step (max_batch * max_tokens_per_seq = 1),
- *      d_model 512, 1024 or 2048, ffn_dim and shared_ffn_dim multiples of 64;
- *      other shapes give MK_ERR_UNSUPPORTED at load. */
+ *      Supported for d_model 512, 1024 or 2048 (one K panel per expert row),
+ *      ffn_dim and shared_ffn_dim multiples of 64, any batch and tokens per
+ *      step (each of an expert unit's tokens takes the unit's tiles in turn on
+ *      the CUDA cores; the bf16 experts' tensor-core tiles for several tokens
+ *      have no MXFP8 counterpart); other shapes give MK_ERR_UNSUPPORTED at
+ *      load. */
 enum mk_expert_format { MK_EXPERT_BF16 = 0, MK_EXPERT_MXFP8 = 1 };
 
 /* Weight kinds. Canonical layouts are row-major [rows, cols] bf16:

@@ -185,7 +185,7 @@ struct Params {
     int stall;                      // testing: CTA 0 first waits on a counter nothing signals (ends in a timeout)
     int skip_sig;                   // testing: 1 + the stage whose layer-0 signals the CTAs leave out (0: none)
     int debug;                      // shared-memory canaries and token-map checks (ST_DEBUG on a failure)
-    int f8;                         // MXFP8 expert weights (one token per step)
+    int f8;                         // MXFP8 expert weights
     // one launch per stage (the unfused comparison path): 0 = the whole step
     // in this launch; 1 = program positions [st_lo, st_hi) only, 2 = the
     // step's set-up only (embedding, buffers zeroed). Launches are ordered by

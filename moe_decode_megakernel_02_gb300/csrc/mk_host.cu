@@ -209,7 +209,6 @@ int validate(const mk_config* c) {
     if (c->expert_format != MK_EXPERT_BF16 && c->expert_format != MK_EXPERT_MXFP8)
         return fail(MK_ERR_INVALID_ARG, "expert_format");
     if (d.f8) {
-        if (d.Mx != 1) return fail(MK_ERR_UNSUPPORTED, "MXFP8 experts: one token per step (max_batch * max_tokens_per_seq = 1)");
         if (d.d != 512 && d.d != 1024 && d.d != 2048) return fail(MK_ERR_UNSUPPORTED, "MXFP8 experts: d_model 512, 1024 or 2048");
         if ((d.E && d.ffn % 64) || (d.sh && d.sffn % 64))
             return fail(MK_ERR_UNSUPPORTED, "MXFP8 experts: ffn_dim and shared_ffn_dim multiples of 64");

@@ -3242,7 +3242,7 @@ __device__ __forceinline__ void down_mma(const uint8_t* tile, int nr, const floa
     }
 }
 
-// ---- MXFP8 expert weights (one token per step) ----
+// ---- MXFP8 expert weights ----
 // Two E4M3 codes become two fp16 values with one conversion instruction
 // (cvt.rn.f16x2.e4m3x2; every E4M3 value, subnormals included, is an fp16
 // number, so the conversion is exact), then fp32. A block's partial sum times
@@ -3273,25 +3273,31 @@ __device__ __forceinline__ float f8_dot16(const uint4 u, const float4 (&x)[4]) {
     return a + b;
 }
 
-// gate/up tiles [j_lo, j_hi) of one unit segment, one token: a tile is
-// R = 64 / NQ rows of the K = 512 NQ codes each (then their scales); lane
-// chunk q of a row holds codes 16 (lane + 32 q) .. + 15, all inside one
-// 32-code block; warp w takes rows RB w .. RB w + RB - 1 (RB = R / 8) and
-// one transposed reduction gives the RB sums. Row r of tile j lands at
-// hs[(j - j_lo) R + r].
+// gate/up tiles [j_lo, j_hi) of one unit segment: a tile is R = 64 / NQ
+// rows of the K = 512 NQ codes each (then their scales); lane chunk q of a
+// row holds codes 16 (lane + 32 q) .. + 15, all inside one 32-code block;
+// warp w takes rows RB w .. RB w + RB - 1 (RB = R / 8) and one transposed
+// reduction gives the RB sums. The unit's tokens (ms.gm, their inputs
+// staged) take the tile one after the other, each input loaded into
+// registers for its pass (one token: once for the segment). Row r of tile j
+// for token i lands at hs[i rows + (j - j_lo) R + r], rows = (j_hi - j_lo) R.
 template <int NQ>
 __device__ __forceinline__ void gu_f8(Ctx& c, int j_lo, int j_hi, float* hs) {
     constexpr int RB = 8 / NQ, KC = 512 * NQ, R = 8 * RB;
     const Params& p = c.p;
     Misc& ms = c.ms;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int ntok = ms.gm, rows = (j_hi - j_lo) * R;
     uint8_t* const ring = c.smem + SMEM_RING;
-    const float* xt = c.stage() + (size_t)staging_row(ms, 0) * stage_stride(KC);
     float4 x[NQ][4];
+    const auto load_x = [&](int tk) {
+        const float* xt = c.stage() + (size_t)staging_row(ms, tk) * stage_stride(KC);
 #pragma unroll
-    for (int q = 0; q < NQ; ++q)
+        for (int q = 0; q < NQ; ++q)
 #pragma unroll
-        for (int i = 0; i < 4; ++i) x[q][i] = *reinterpret_cast<const float4*>(xt + 16 * (lane + 32 * q) + 4 * i);
+            for (int i = 0; i < 4; ++i) x[q][i] = *reinterpret_cast<const float4*>(xt + 16 * (lane + 32 * q) + 4 * i);
+    };
+    load_x(0);
     CRing cr = c.cr;
     bool dead = c.dead, timed_out = false;
     for (int j = j_lo; j < j_hi; ++j) {
@@ -3304,19 +3310,23 @@ __device__ __forceinline__ void gu_f8(Ctx& c, int j_lo, int j_hi, float* hs) {
         }
         if (tile) {
             const uint8_t* sc = tile + R * KC;
-            float v[RB];
+            for (int tk = 0; tk < ntok; ++tk) {
+                if (ntok > 1) load_x(tk);
+                float v[RB];
 #pragma unroll
-            for (int b = 0; b < RB; ++b) {
-                const int r = warp * RB + b;
-                const uint4* row = reinterpret_cast<const uint4*>(tile + (size_t)r * KC) + lane;
-                float acc = 0.f;
+                for (int b = 0; b < RB; ++b) {
+                    const int r = warp * RB + b;
+                    const uint4* row = reinterpret_cast<const uint4*>(tile + (size_t)r * KC) + lane;
+                    float acc = 0.f;
 #pragma unroll
-                for (int q = 0; q < NQ; ++q)
-                    acc = fmaf(f8_dot16(row[32 * q], x[q]), f8_scale(sc[r * (KC / 32) + ((lane + 32 * q) >> 1)]), acc);
-                v[b] = acc;
+                    for (int q = 0; q < NQ; ++q)
+                        acc = fmaf(f8_dot16(row[32 * q], x[q]), f8_scale(sc[r * (KC / 32) + ((lane + 32 * q) >> 1)]),
+                                   acc);
+                    v[b] = acc;
+                }
+                const int b = rx_reduce<RB>(v);
+                if ((lane & (32 / RB - 1)) == 0) hs[(size_t)tk * rows + (j - j_lo) * R + warp * RB + b] = v[0];
             }
-            const int b = rx_reduce<RB>(v);
-            if ((lane & (32 / RB - 1)) == 0) hs[(j - j_lo) * R + warp * RB + b] = v[0];
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&ms.empty[cr.slot]);
@@ -3358,9 +3368,9 @@ __device__ __forceinline__ void down_f8(const uint8_t* tile, int nr, const float
     }
 }
 
-// MXFP8 gate/up tiles [j_lo, j_hi) of a unit segment (one K panel, one
-// token): the input is staged once (the routed CTAs staged it already), then
-// the tiles
+// MXFP8 gate/up tiles [j_lo, j_hi) of a unit segment (one K panel): the
+// inputs are staged once (the routed CTAs may have staged them already),
+// then the tiles
 __device__ __noinline__ void unit_gu_f8(Ctx& c, int j_lo, int j_hi, float* hs) {
     restage(c, c.ms.ug, c.ms.ug.src, 0, 0, 0, c.ms.gather ? c.ms.gm : c.p.M);
     const int Kc = c.layer().ffn.Kc;
@@ -3369,9 +3379,18 @@ __device__ __noinline__ void unit_gu_f8(Ctx& c, int j_lo, int j_hi, float* hs) {
     else gu_f8<1>(c, j_lo, j_hi, hs);
 }
 
-// one MXFP8 down tile, one token (units 64 wide)
-__device__ __noinline__ void unit_down_f8(const uint8_t* tile, int nr, const float* hu, float w, float* xo) {
-    down_f8<4>(tile, nr, hu, w, xo);
+// one MXFP8 down tile (units 64 wide), once per token of the unit (the
+// CTA's token map in shared memory): token i's hidden values at hu + i n F
+// (n units of F in the segment: half the segment's gate/up rows), its
+// residual row gt[i] (xo is token 0's, rows d apart), its routing weight
+__device__ __noinline__ void unit_down_f8(const uint8_t* tile, int nr, const float* hu, float* xo, int d) {
+    extern __shared__ __align__(1024) uint8_t smem_base[];
+    const Misc& ms = *reinterpret_cast<const Misc*>(smem_base + SMEM_MISC);
+    const int M = ms.gm, hstride = ms.ug.dst_stride / 2, g0 = ms.gt[0];
+    for (int i = 0; i < M; ++i) {
+        const float w = ms.uw[i];
+        if (w != 0.f) down_f8<4>(tile, nr, hu + (size_t)i * hstride, w, xo + (ptrdiff_t)((int)ms.gt[i] - g0) * d);
+    }
 }
 
 __device__ __noinline__ void unit_seg_cons(Ctx& c, int l, int kind, int expert, int u0, int u1, int m_lo, int m_hi) {
@@ -3501,12 +3520,12 @@ __device__ __noinline__ void unit_seg_cons(Ctx& c, int l, int kind, int expert, 
                     dead = timed_out = true;
             }
             if (tile) {
-                if (M == 1) {
+                if (M == 1 || p.f8) {
                     const float* hu = h + uu * F;
                     float* xo = Ld.xn + (size_t)ms.gt[0] * d + r0;
                     const float w = ms.uw[0];
-                    if (w != 0.f && p.f8) {
-                        unit_down_f8(tile, nr, hu, w, xo);
+                    if (p.f8) {
+                        unit_down_f8(tile, nr, hu, xo, d);
                     } else if (w != 0.f) {
                         if (F == 64) down_rows1<8>(tile, nr, hu, w, xo);
                         else if (F == 48) down_rows1<6>(tile, nr, hu, w, xo);

@@ -34,8 +34,8 @@ VERIFY = dict(DEEP, name="verify", batches=(8,), T=7)
 ALL = {c["name"]: c for c in (TINY, MID, DEEP, DENSE, VERIFY)}
 
 # the deep model with MXFP8 expert weights (E4M3 codes, one E8M0 scale per 32
-# codes of a row), one token per step
-DEEP_MXFP8 = dict(DEEP, name="deep_mxfp8", expert_format=1, batches=(1,))
+# codes of a row)
+DEEP_MXFP8 = dict(DEEP, name="deep_mxfp8", expert_format=1, batches=(1, 8))
 
 
 def scaled(cfg, **over):

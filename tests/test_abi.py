@@ -106,14 +106,10 @@ def test_debug_entry_points_reject_bad_handles():
 
 
 def test_mxfp8_expert_shapes_are_checked():
-    # MXFP8 experts: one token per step, d_model 512 / 1024 / 2048; an
-    # unknown format is an argument error (all found before any device call)
+    # MXFP8 experts: d_model 512 / 1024 / 2048; an unknown format is an
+    # argument error (both found before any device call)
     mx = dict(expert_format=1)
     assert _bad(configs.TINY, **mx) == mk.ERR_UNSUPPORTED  # d_model 256
     assert b"MXFP8" in mk.lib().mk_last_error()
+    assert _bad(configs.DENSE, **mx) == mk.ERR_UNSUPPORTED  # d_model 5120
     assert _bad(configs.DEEP, expert_format=2) == mk.ERR_INVALID_ARG
-    c = mk.make_config(dict(configs.DEEP, **mx), 2, 1, 128)
-    out = ctypes.c_void_p()
-    w = (mk.Weight * 1)(mk.Weight(1, -1, 0, 0, 1))
-    assert mk.lib().mk_load_weights(ctypes.byref(c), w, 1, None, ctypes.byref(out)) == mk.ERR_UNSUPPORTED
-    assert b"one token per step" in mk.lib().mk_last_error()

@@ -239,7 +239,7 @@ def test_deep_separate_absorbed_query_and_value_stages(monkeypatch, B):
     _run(cfg, B, 1, 2, cfg["ctx"])
 
 
-# MXFP8 expert weights (one token per step): the oracle dequantises the
+# MXFP8 expert weights: the oracle dequantises the
 # generator's E4M3 codes and E8M0 scales exactly, the kernel streams the codes
 # and scales and takes the same values; the tolerance is the bf16 model's
 # (the arithmetic is the same once the weights are read).
@@ -260,6 +260,22 @@ _MX_SMALL = dict(_MX, n_layers=2, vocab=4096, n_q_heads=4, n_kv_heads=2, head_di
 def test_mxfp8_experts_batch1(name, over):
     cfg = configs.scaled(configs.ALL[name], **over)
     _run(cfg, 1, 1, 2, cfg["ctx"])
+
+
+@pytest.mark.parametrize("name,B,T,over", [
+    ("deep", 2, 1, dict(_MX, n_layers=2)),
+    ("deep", 8, 1, dict(_MX, n_layers=2)),
+    ("mid", 4, 1, dict(_MX, n_layers=2)),
+    ("mid", 3, 1, dict(_MX_SMALL, d_model=1024, ffn_dim=512, shared_ffn_dim=256)),
+    ("verify", 8, 7, dict(_MX, n_layers=2)),
+])
+def test_mxfp8_experts_several_tokens(name, B, T, over):
+    # every token of an expert unit takes the unit's tiles in turn (routed
+    # experts: the tokens routed to them, in groups the staging area holds;
+    # the shared expert: token groups); verify B 8 x T 7: 56 tokens, gathered
+    cfg = configs.scaled(configs.ALL[name], **over)
+    ctx = min(cfg["ctx"], 2000)
+    _run(cfg, B, T, 1, ctx, want_accept=T > 1)
 
 
 def test_mxfp8_experts_full_depth_batch1():
